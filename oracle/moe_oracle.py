@@ -1,0 +1,257 @@
+"""Float64 CPU oracle for the DeepSeekMoE layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The product path (the
+CUDA library and its Python binding) never calls it, and it shares no code with
+that path: no kernels, helpers, tables or constants.
+
+What it computes, and where the pages say so
+--------------------------------------------
+Sources are the five pages about the deepseek-v3-jax project:
+
+* "190行JAX复刻DeepSeek V3" (openai-hub.com), section "190行代码到底装进了什么":
+  the DeepSeekMoE layer has 16 routed experts, each token picks 4, plus one
+  always-on shared expert; the project runs *every* routed expert on *every*
+  token and zeroes the experts that were not selected.
+* Same page, section "最有价值的实验:无辅助损失均衡真的有效": after each training
+  step an over-loaded expert's routing bias goes down and an idle one's goes
+  up, with update speed gamma = 1e-3; the bias only changes *which* experts
+  are selected, never the gate value of a selected expert.
+* "DeepSeek V3 viết lại bằng 190 dòng JAX thuần" (lehuy.net), sections
+  "Những gì có trong 190 dòng code" (bias pushes routing towards idle experts
+  and changes which expert is chosen, not the expert weights) and
+  "Những gì đã được đơn giản hóa" (dense MoE: every expert on every token,
+  unselected ones zeroed; no sparse dispatch).
+
+The pages print no formulas.  The readings below are the plain ones the text
+supports (the DeepSeek-V3 technical report, which the pages summarise and list
+as a source, uses the same):
+
+1. affinity    s[t,e] = sigmoid(u[t,e]),  u = x @ W_r.T,  sigmoid(u) = 1/(1+exp(-u))
+2. selection   the k experts with the largest biased score z = s + b; ties go to
+               the lower expert index; slots ordered by descending z.  A NaN
+               score ranks below every number.
+3. gates       g[t,j] = s[t, idx[t,j]] / sum_j' s[t, idx[t,j']]   (unbiased s)
+4. experts     SwiGLU:  E(x) = W_down (silu(W_gate x) * (W_up x)),
+               silu(z) = z * sigmoid(z)
+5. output      y[t] = shared(x[t]) + sum_j g[t,j] * E_{idx[t,j]}(x[t])
+6. load        load[e] = #{(t,j) : idx[t,j] = e}
+7. bias        b_e <- fp32(b_e - fp32(gamma) * sgn(load_e - mean_load)),
+               mean_load = T*k/E, sgn(0) = 0, so that sgn(E*load_e - T*k) is an
+               exact integer comparison.
+
+``moe_forward_dense`` is the pages' own formulation (every expert on every
+token, then masked).  ``moe_forward_sparse`` evaluates only the selected
+experts; tests pin it to the dense formulation on small inputs, and it is the
+form used for sampled rows of the large workloads.
+
+Pinning: tests/test_oracle_pins.py (brute-force top-k over all subsets,
+hand-derived closed forms in tests/golden/, bias invariance, textbook
+reductions of the SwiGLU expert, permutation equivariance, dense/sparse
+agreement) and tests/test_oracle_mutations.py (planted mistakes must fail a
+pin).  Everything is float64 on the exact (bf16-rounded where the workload
+stores bf16) input values; nothing is rounded except the fp32 bias result.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=F64)
+
+
+# --------------------------------------------------------------------------
+# 1. router affinity
+# --------------------------------------------------------------------------
+def sigmoid(u: np.ndarray) -> np.ndarray:
+    """Logistic function 1/(1+exp(-u)) in float64 (reading 1 above)."""
+    u = _f64(u)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-u))
+
+
+def router_affinity(x, w_router) -> tuple[np.ndarray, np.ndarray]:
+    """u = x W_r^T and s = sigmoid(u).
+
+    x: [T, d], w_router: [E, d].  Returns (u, s), both [T, E] float64.
+    Follows "190行JAX复刻DeepSeek V3", section "190行代码到底装进了什么"
+    (a per-token, per-expert routing score) with the sigmoid reading.
+    """
+    u = _f64(x) @ _f64(w_router).T
+    return u, sigmoid(u)
+
+
+# --------------------------------------------------------------------------
+# 2. biased top-k selection
+# --------------------------------------------------------------------------
+def biased_scores(s, bias) -> np.ndarray:
+    """z = s + b (the bias enters selection only; section
+    "最有价值的实验:无辅助损失均衡真的有效")."""
+    return _f64(s) + _f64(bias)[None, :]
+
+
+def select_topk(z: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest biased scores per row, ordered by (z desc,
+    expert index asc).  NaN ranks below every number (treated as -inf).
+
+    A stable sort on -z keeps equal keys in ascending index order, which is
+    exactly the "ties go to the lower index" rule.
+    """
+    z = _f64(z)
+    key = np.where(np.isnan(z), -np.inf, z)
+    order = np.argsort(-key, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def topk_gap(z: np.ndarray, k: int) -> np.ndarray:
+    """Per-row gap between the k-th and (k+1)-th largest biased score
+    (float64).  A GPU selection may differ from the oracle's only where this
+    gap is below the tie tolerance.  For k == E the gap is +inf."""
+    z = _f64(z)
+    key = np.where(np.isnan(z), -np.inf, z)
+    srt = -np.sort(-key, axis=1)
+    if k >= z.shape[1]:
+        return np.full(z.shape[0], np.inf)
+    return srt[:, k - 1] - srt[:, k]
+
+
+# --------------------------------------------------------------------------
+# 3. gates
+# --------------------------------------------------------------------------
+def gate_weights(s: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """g[t,j] = s[t, idx[t,j]] / sum_j' s[t, idx[t,j']]  (unbiased s)."""
+    sel = np.take_along_axis(_f64(s), idx, axis=1)
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+def route(x, w_router, bias, k: int) -> dict:
+    """Router steps 1-3 for every token: u, s, z, idx, gates, gap."""
+    u, s = router_affinity(x, w_router)
+    z = biased_scores(s, bias)
+    idx = select_topk(z, k)
+    return {"u": u, "s": s, "z": z, "idx": idx,
+            "gates": gate_weights(s, idx), "gap": topk_gap(z, k)}
+
+
+# --------------------------------------------------------------------------
+# 4. SwiGLU expert
+# --------------------------------------------------------------------------
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z)."""
+    z = _f64(z)
+    return z * sigmoid(z)
+
+
+def swiglu_expert(x, w_gate, w_up, w_down) -> np.ndarray:
+    """E(x) = W_down (silu(W_gate x) * (W_up x)) applied to each row of x.
+
+    x: [n, d]; w_gate, w_up: [h, d]; w_down: [d, h].  Returns [n, d].
+    """
+    x = _f64(x)
+    a = x @ _f64(w_gate).T
+    c = x @ _f64(w_up).T
+    return (silu(a) * c) @ _f64(w_down).T
+
+
+# --------------------------------------------------------------------------
+# 5. layer output
+# --------------------------------------------------------------------------
+def moe_forward_dense(x, w_router, bias, experts, shared, k: int,
+                      idx_override=None) -> dict:
+    """The pages' formulation: every routed expert on every token, the
+    unselected ones masked to zero, plus the shared expert.
+
+    experts: (W_gate [E,h,d], W_up [E,h,d], W_down [E,d,h]);
+    shared:  (W_gate [h,d],   W_up [h,d],   W_down [d,h]).
+    idx_override (optional [T,k]) replaces the selection, e.g. to evaluate
+    the output for a tolerated near-tie flip; gates follow from it.
+    """
+    r = route(x, w_router, bias, k)
+    idx = r["idx"] if idx_override is None else np.asarray(idx_override)
+    gates = gate_weights(r["s"], idx)
+    T, E = r["s"].shape
+    mask = np.zeros((T, E), dtype=F64)
+    np.put_along_axis(mask, idx, gates, axis=1)
+    wg, wu, wd = experts
+    y = swiglu_expert(x, *shared)
+    for e in range(E):
+        y = y + mask[:, e:e + 1] * swiglu_expert(x, wg[e], wu[e], wd[e])
+    out = dict(r)
+    out.update({"idx": idx, "gates": gates, "y": y})
+    return out
+
+
+def moe_forward_sparse(x, w_router, bias, experts, shared, k: int,
+                       idx_override=None) -> dict:
+    """Same output as ``moe_forward_dense`` evaluating only the selected
+    experts of each token (what a truly sparse layer computes)."""
+    r = route(x, w_router, bias, k)
+    idx = r["idx"] if idx_override is None else np.asarray(idx_override)
+    gates = gate_weights(r["s"], idx)
+    wg, wu, wd = experts
+    y = swiglu_expert(x, *shared)
+    for t in range(idx.shape[0]):
+        for j in range(idx.shape[1]):
+            e = int(idx[t, j])
+            y[t] += gates[t, j] * swiglu_expert(x[t:t + 1], wg[e], wu[e], wd[e])[0]
+    out = dict(r)
+    out.update({"idx": idx, "gates": gates, "y": y})
+    return out
+
+
+def expert_output_rows(x_rows, idx_rows, gate_rows, get_expert, shared):
+    """Sparse output for a sample of rows, streaming one expert at a time.
+
+    x_rows [n,d]; idx_rows [n,k]; gate_rows [n,k] (float64);
+    get_expert(e) -> (W_gate [h,d], W_up [h,d], W_down [d,h]) as arrays.
+    Used for the large workloads, whose weights do not fit a float64 copy in
+    host memory: only the experts that the sampled rows selected are fetched.
+    """
+    x_rows = _f64(x_rows)
+    y = swiglu_expert(x_rows, *shared)
+    idx_rows = np.asarray(idx_rows)
+    for e in np.unique(idx_rows):
+        w = get_expert(int(e))
+        tt, jj = np.nonzero(idx_rows == e)
+        ye = swiglu_expert(x_rows[tt], *w)
+        for n in range(len(tt)):
+            y[tt[n]] += gate_rows[tt[n], jj[n]] * ye[n]
+    return y
+
+
+# --------------------------------------------------------------------------
+# 6, 7. load counts and bias update
+# --------------------------------------------------------------------------
+def load_counts(idx: np.ndarray, n_experts: int) -> np.ndarray:
+    """load[e] = number of (token, slot) pairs routed to expert e."""
+    return np.bincount(np.asarray(idx).ravel(), minlength=n_experts).astype(np.int64)
+
+
+def bias_update(bias, load, gamma: float, tk: int) -> np.ndarray:
+    """b_e <- fp32(b_e - fp32(gamma) * sgn(load_e - TK/E)), sgn(0) = 0.
+
+    sgn(load_e - TK/E) == sgn(E*load_e - TK) is taken on integers.  The
+    subtraction is done in float64 on the float32 operands (exact, since both
+    are float32 values whose exponents differ by far less than 29) and then
+    rounded once to float32, which equals the IEEE float32 subtraction.
+    """
+    bias32 = np.asarray(bias, dtype=np.float32)
+    load = np.asarray(load, dtype=np.int64)
+    n_experts = load.shape[0]
+    sgn = np.sign(n_experts * load - int(tk)).astype(F64)
+    g32 = F64(np.float32(gamma))
+    return (bias32.astype(F64) - g32 * sgn).astype(np.float32)
+
+
+def route_and_update(x, w_router, bias, k: int, gamma: float) -> dict:
+    """One route-only step: routing, load counts, updated bias."""
+    r = route(x, w_router, bias, k)
+    E = r["s"].shape[1]
+    load = load_counts(r["idx"], E)
+    r["load"] = load
+    r["bias_new"] = bias_update(bias, load, gamma, r["idx"].size)
+    return r

@@ -1,0 +1,405 @@
+"""Checks that pin the float64 oracle to things other than itself.
+
+Each ``pin_*`` takes the oracle module and raises AssertionError when the
+oracle disagrees with a value fixed by the pages or by mathematics:
+
+* hand-derived closed forms (tests/golden/*.txt, each with its citation);
+* brute force over every k-subset of experts with exact rational sums;
+* invariants: k distinct experts per token, gates summing to one, gates
+  unchanged by the bias, load counts summing to T*k;
+* textbook reductions of the SwiGLU expert (identity weights reduce it to the
+  elementwise silu(x)*x; zero up-projection gives zero);
+* equivariances that catch index and transposition mistakes (permuting
+  tokens, hidden units or experts);
+* the pages' dense formulation against the sparse one.
+
+tests/test_oracle_pins.py runs them on the real oracle, and
+tests/test_oracle_mutations.py plants mistakes in the oracle and requires at
+least one pin to fail for each.
+"""
+
+from __future__ import annotations
+
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line)
+    return rows
+
+
+def _logit(p):
+    return math.log(p / (1.0 - p))
+
+
+def _tiny_layer(rng, T, d, h, E):
+    x = rng.standard_normal((T, d))
+    w_r = rng.standard_normal((E, d)) / math.sqrt(d)
+    b = rng.uniform(-0.05, 0.05, E)
+    wg = rng.standard_normal((E, h, d)) / math.sqrt(d)
+    wu = rng.standard_normal((E, h, d)) / math.sqrt(d)
+    wd = rng.standard_normal((E, d, h)) / math.sqrt(h)
+    sh = (rng.standard_normal((h, d)) / math.sqrt(d),
+          rng.standard_normal((h, d)) / math.sqrt(d),
+          rng.standard_normal((d, h)) / math.sqrt(h))
+    return x, w_r, b, (wg, wu, wd), sh
+
+
+# ---------------------------------------------------------------- routing
+def pin_routing_golden(O):
+    rows = _read_golden("routing_closed_form.txt")
+    kv = {}
+    p, idx, gates = {}, {}, {}
+    for r in rows:
+        key, *vals = r.split()
+        if key == "p":
+            p[int(vals[0])] = [float(v) for v in vals[1:]]
+        elif key == "idx":
+            idx[int(vals[0])] = [int(v) for v in vals[1:]]
+        elif key == "gates":
+            gates[int(vals[0])] = [float(Fraction(v)) for v in vals[1:]]
+        else:
+            kv[key] = vals
+    E, k = int(kv["E"][0]), int(kv["k"][0])
+    T = len(p)
+    bias = np.array([float(v) for v in kv["bias"]])
+    x = np.eye(T)
+    w_r = np.array([[_logit(p[t][e]) for t in range(T)] for e in range(E)])
+    r = O.route(x, w_r, bias, k)
+    assert np.allclose(r["s"], np.array([p[t] for t in range(T)]), rtol=0, atol=1e-14)
+    for t in range(T):
+        assert list(r["idx"][t]) == idx[t], (t, r["idx"][t], idx[t])
+        assert np.allclose(r["gates"][t], gates[t], rtol=0, atol=1e-14)
+    load = O.load_counts(r["idx"], E)
+    assert list(load) == [int(v) for v in kv["load"]]
+    gamma = float(kv["gamma"][0])
+    sign = np.array([int(v) for v in kv["sign"]], dtype=np.float32)
+    b_new = O.bias_update(bias, load, gamma, T * k)
+    # IEEE single-precision subtraction done by numpy's float32 ALU
+    expect = np.float32(bias.astype(np.float32)) - np.float32(gamma) * sign
+    assert b_new.dtype == np.float32
+    assert np.array_equal(b_new, expect.astype(np.float32)), (b_new, expect)
+
+
+def pin_topk_bruteforce(O):
+    """The selected set maximises the exact sum of biased scores over all
+    k-subsets; among equal sums the lexicographically smallest index set wins
+    (ties go to the lower index).  Slots are ordered by descending score."""
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        E = int(rng.integers(2, 9))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        T = 6
+        if trial % 3 == 0:   # many exact ties: multiples of 1/8
+            z = rng.integers(0, 5, size=(T, E)) / 8.0
+        else:
+            z = rng.uniform(-1, 1, size=(T, E))
+        if trial % 5 == 0:   # a few NaN scores rank below every number
+            z[rng.random((T, E)) < 0.2] = np.nan
+        idx = O.select_topk(z, k)
+        assert idx.shape == (T, k)
+        for t in range(T):
+            vals = [(-math.inf if math.isnan(v) else Fraction(v)) for v in z[t]]
+
+            def total(c):
+                fin = [vals[i] for i in c if vals[i] != -math.inf]
+                ninf = sum(1 for i in c if vals[i] == -math.inf)
+                return (-ninf, sum(fin, Fraction(0)))
+            best = max(itertools.combinations(range(E), k),
+                       key=lambda c: (total(c), [-i for i in c]))
+            assert sorted(idx[t].tolist()) == list(best), (z[t], idx[t], best)
+            assert len(set(idx[t].tolist())) == k
+            for j in range(k - 1):
+                a, b = vals[idx[t, j]], vals[idx[t, j + 1]]
+                assert a > b or (a == b and idx[t, j] < idx[t, j + 1])
+
+
+def pin_gap(O):
+    """The reported k-th/(k+1)-th gap is the margin that separates the
+    selected set from the rest: nudging the best unselected score up by more
+    than it changes the selection, by less does not."""
+    rng = np.random.default_rng(5)
+    z = rng.uniform(0, 1, size=(8, 7))
+    k = 3
+    gap = O.topk_gap(z, k)
+    idx = O.select_topk(z, k)
+    for t in range(8):
+        rest = [e for e in range(7) if e not in idx[t]]
+        e_best = max(rest, key=lambda e: z[t, e])
+        assert gap[t] > 0
+        assert abs(gap[t] - (min(z[t, idx[t]]) - z[t, e_best])) < 1e-15
+        z2 = z.copy()
+        z2[t, e_best] += 1.5 * gap[t]
+        assert e_best in O.select_topk(z2, k)[t]
+        z2[t, e_best] = z[t, e_best] + 0.5 * gap[t]
+        assert e_best not in O.select_topk(z2, k)[t]
+
+
+def pin_gate_invariants(O):
+    rng = np.random.default_rng(3)
+    x, w_r, b, _, _ = _tiny_layer(rng, 40, 16, 8, 12)
+    k = 4
+    r = O.route(x, w_r, b, k)
+    s, g, idx = r["s"], r["gates"], r["idx"]
+    assert np.all((s > 0) & (s < 1))
+    # sigmoid(-u) = 1 - sigmoid(u); sigmoid(0) = 1/2
+    r_neg = O.route(-x, w_r, b, k)
+    assert np.allclose(r_neg["s"], 1.0 - s, rtol=0, atol=1e-15)
+    assert np.allclose(g.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(g > 0)
+    sel = np.take_along_axis(s, idx, axis=1)
+    # g proportional to the unbiased affinity of the selected experts
+    assert np.allclose(g / g[:, :1], sel / sel[:, :1], rtol=1e-12, atol=0)
+    # a constant shift of every bias changes nothing
+    r2 = O.route(x, w_r, b + 0.37, k)
+    assert np.array_equal(r2["idx"], idx)
+    assert np.allclose(r2["gates"], g, rtol=0, atol=1e-15)
+    # a large bias on a chosen set forces exactly that set, and the gates
+    # are that set's unbiased affinities normalised (bias invariance)
+    S = [1, 5, 7, 10]
+    b3 = b.copy()
+    b3[S] += 100.0
+    r3 = O.route(x, w_r, b3, k)
+    for t in range(x.shape[0]):
+        assert sorted(r3["idx"][t].tolist()) == S
+        u = x[t] @ w_r[S].T
+        sS = np.array([1.0 / (1.0 + math.exp(-v)) for v in u])
+        order = [S.index(e) for e in r3["idx"][t]]
+        assert np.allclose(r3["gates"][t], (sS / sS.sum())[order], rtol=0, atol=1e-14)
+    # selecting every expert: gates are s / sum(s) over all experts
+    rk = O.route(x, w_r, b, 12)
+    Gfull = np.zeros_like(s)
+    np.put_along_axis(Gfull, rk["idx"], rk["gates"], axis=1)
+    assert np.allclose(Gfull, s / s.sum(axis=1, keepdims=True), rtol=0, atol=1e-15)
+
+
+def pin_router_one_hot(O):
+    """One-hot tokens read one router column: u[t,e] = W_r[e,t]."""
+    rng = np.random.default_rng(9)
+    w_r = rng.standard_normal((6, 4))
+    u, s = O.router_affinity(np.eye(4), w_r)
+    assert np.array_equal(u, w_r.T)
+    assert np.allclose(s, [[1.0 / (1.0 + math.exp(-v)) for v in row] for row in w_r.T],
+                       rtol=0, atol=1e-16)
+    u2, _ = O.router_affinity(np.array([[2.0, 0, 0, -1.0]]), w_r)
+    assert np.allclose(u2[0], 2.0 * w_r[:, 0] - w_r[:, 3], rtol=0, atol=1e-15)
+
+
+def pin_load_counts(O):
+    rng = np.random.default_rng(4)
+    for E, k, T in [(16, 4, 50), (7, 7, 9), (5, 1, 1), (9, 2, 0)]:
+        z = rng.uniform(0, 1, size=(T, E))
+        idx = O.select_topk(z, k)
+        load = O.load_counts(idx, E)
+        assert load.shape == (E,) and load.sum() == T * k
+        for e in range(E):
+            assert load[e] == sum(int(v == e) for row in idx.tolist() for v in row)
+    idx = np.array([[3, 0], [3, 1], [2, 3]])
+    assert O.load_counts(idx, 5).tolist() == [1, 1, 1, 3, 0]
+
+
+def pin_bias_update(O):
+    g32 = np.float32(1e-3)
+    # float32(1e-3) is 0.001000000047497451305389404296875 exactly
+    assert float(g32) == 0.001000000047497451305389404296875
+    b = np.array([0.0, 0.5, -0.25, 0.0078125], dtype=np.float32)
+    # E = 4, TK = 8 -> mean 2: loads [4, 2, 1, 1] -> signs [+1, 0, -1, -1]
+    out = O.bias_update(b, np.array([4, 2, 1, 1]), 1e-3, 8)
+    expect = np.array([b[0] - g32, b[1], b[2] + g32, b[3] + g32], dtype=np.float32)
+    assert out.dtype == np.float32 and np.array_equal(out, expect), (out, expect)
+    assert out[0] == -g32 and out[1] == np.float32(0.5)
+    # non-integer mean: E = 3, TK = 4 -> mean 4/3: loads [2, 1, 1] -> [+1, -1, -1]
+    out = O.bias_update(np.zeros(3, np.float32), np.array([2, 1, 1]), 1e-3, 4)
+    assert np.array_equal(out, np.array([-g32, g32, g32], dtype=np.float32))
+    # balanced load leaves the bias unchanged (sign(0) = 0)
+    bb = np.array([0.1, -0.2, 0.3], dtype=np.float32)
+    assert np.array_equal(O.bias_update(bb, np.array([2, 2, 2]), 1e-3, 6), bb)
+    # over many steps each bias moves by at most gamma per step (+ rounding)
+    rng = np.random.default_rng(1)
+    E = 8
+    b0 = rng.uniform(-0.01, 0.01, E).astype(np.float32)
+    bt = b0.copy()
+    for step in range(50):
+        load = rng.multinomial(32, np.ones(E) / E)
+        bt = O.bias_update(bt, load, 1e-3, 32)
+        assert np.all(np.abs(bt.astype(np.float64) - b0) <= (step + 1) * 1.0000001e-3 + 1e-8)
+
+
+# ---------------------------------------------------------------- experts
+def pin_swiglu_reductions(O):
+    L3 = math.log(3.0)
+    # identity weights: E(x) = silu(x) * x elementwise
+    x = np.array([[L3, -L3, 0.0, 2.0]])
+    I4 = np.eye(4)
+    y = O.swiglu_expert(x, I4, I4, I4)
+    sig = lambda v: 1.0 / (1.0 + math.exp(-v))  # noqa: E731
+    expect = [0.75 * L3 * L3, 0.25 * L3 * L3, 0.0, 2.0 * sig(2.0) * 2.0]
+    assert np.allclose(y[0], expect, rtol=1e-15, atol=1e-15)
+    # gate row picks feature 0, up row picks feature 1, down writes to feature 2
+    wg = np.array([[1.0, 0, 0, 0]])
+    wu = np.array([[0, 1.0, 0, 0]])
+    wd = np.array([[0.0], [0.0], [3.0], [0.0]])
+    y = O.swiglu_expert(np.array([[L3, 2.0, 7.0, 9.0]]), wg, wu, wd)
+    assert np.allclose(y[0], [0, 0, 3.0 * 0.75 * L3 * 2.0, 0], rtol=1e-15, atol=1e-15)
+    # zero up projection gives zero; scaling down/up scales the output
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((5, 6))
+    wg, wu, wd = rng.standard_normal((3, 6)), rng.standard_normal((3, 6)), rng.standard_normal((6, 3))
+    assert np.array_equal(O.swiglu_expert(x, wg, 0 * wu, wd), np.zeros((5, 6)))
+    y = O.swiglu_expert(x, wg, wu, wd)
+    assert np.allclose(O.swiglu_expert(x, wg, 2.5 * wu, wd), 2.5 * y, rtol=1e-13, atol=1e-14)
+    assert np.allclose(O.swiglu_expert(x, wg, wu, -3 * wd), -3 * y, rtol=1e-13, atol=1e-14)
+    # permuting hidden units (rows of W_gate, W_up, columns of W_down) is a no-op
+    P = rng.permutation(3)
+    assert np.allclose(O.swiglu_expert(x, wg[P], wu[P], wd[:, P]), y, rtol=1e-13, atol=1e-14)
+    # permuting tokens permutes output rows
+    Q = rng.permutation(5)
+    assert np.allclose(O.swiglu_expert(x[Q], wg, wu, wd), y[Q], rtol=1e-13, atol=1e-14)
+    # rectangular shapes: d = 6, h = 3 -> output [n, d]
+    assert y.shape == (5, 6)
+    # the gate path is not symmetric in gate/up: swapping them changes the result
+    assert not np.allclose(O.swiglu_expert(x, wu, wg, wd), y)
+
+
+def pin_scalar_layer_golden(O):
+    rows = _read_golden("scalar_layer_closed_form.txt")
+    L = math.log(3.0) ** 2
+    data, cases = {}, []
+    for r in rows:
+        if r.startswith("case"):
+            parts = [p.split() for p in r.split("|")]
+            head = parts[0]
+            cases.append({
+                "k": int(head[2]), "b": [float(head[3]), float(head[4])],
+                "idx": [int(v) for v in parts[1][1:]],
+                "gates": [float(Fraction(v)) for v in parts[2][1:]],
+                "y": float(Fraction(parts[3][1])) * L,
+            })
+        else:
+            key, *vals = r.split()
+            if key == "expert":
+                data.setdefault("expert", {})[int(vals[0])] = [float(v) for v in vals[1:]]
+            else:
+                data[key] = [float(v) for v in vals]
+    x = np.array([[data["x"][0]]])
+    w_r = np.array([[data["w_router"][0]], [data["w_router"][1]]])
+    ex = data["expert"]
+    experts = (np.array([[[ex[e][0]]] for e in range(2)]),
+               np.array([[[ex[e][1]]] for e in range(2)]),
+               np.array([[[ex[e][2]]] for e in range(2)]))
+    sh = data["shared"]
+    shared = (np.array([[sh[0]]]), np.array([[sh[1]]]), np.array([[sh[2]]]))
+    for c in cases:
+        for fwd in (O.moe_forward_dense, O.moe_forward_sparse):
+            out = fwd(x, w_r, np.array(c["b"]), experts, shared, c["k"])
+            assert out["idx"][0].tolist() == c["idx"], (c, out["idx"])
+            assert np.allclose(out["gates"][0], c["gates"], rtol=0, atol=1e-14)
+            assert abs(out["y"][0, 0] - c["y"]) < 1e-13, (c, out["y"])
+
+
+def pin_layer_reductions(O):
+    rng = np.random.default_rng(8)
+    x, w_r, b, (wg, wu, wd), sh = _tiny_layer(rng, 12, 6, 4, 5)
+    # one expert selected from one: gate 1, y = shared(x) + expert(x)
+    out = O.moe_forward_dense(x, w_r[:1], b[:1], (wg[:1], wu[:1], wd[:1]), sh, 1)
+    assert np.allclose(out["gates"], 1.0, rtol=0, atol=0)
+    ident = np.eye(6)
+    out_id = O.moe_forward_dense(x, w_r[:1], b[:1], (ident[None, :, :], ident[None], ident[None]),
+                                 (ident, ident, ident), 1)
+    # both experts identity: y = 2 * silu(x) * x elementwise
+    assert np.allclose(out_id["y"], 2 * x * x / (1 + np.exp(-x)), rtol=1e-14, atol=1e-14)
+    # zero routed down-projections leave only the shared expert
+    out0 = O.moe_forward_dense(x, w_r, b, (wg, wu, 0 * wd), sh, 2)
+    only_shared = O.moe_forward_dense(x, w_r, b, (wg, wu, wd), (sh[0], sh[1], 0 * sh[2]), 2)
+    full = O.moe_forward_dense(x, w_r, b, (wg, wu, wd), sh, 2)
+    assert np.allclose(out0["y"] + only_shared["y"], full["y"], rtol=1e-13, atol=1e-14)
+    # zero shared down-projection and all experts selected: y = sum_e s_e/sum(s) E_e(x)
+    allk = O.moe_forward_dense(x, w_r, b, (wg, wu, wd), (sh[0], sh[1], 0 * sh[2]), 5)
+    s = 1.0 / (1.0 + np.exp(-(x @ w_r.T)))
+    ref = sum((s[:, e:e + 1] / s.sum(axis=1, keepdims=True)) * O.swiglu_expert(x, wg[e], wu[e], wd[e])
+              for e in range(5))
+    assert np.allclose(allk["y"], ref, rtol=1e-13, atol=1e-14)
+
+
+def pin_equivariance(O):
+    rng = np.random.default_rng(6)
+    x, w_r, b, (wg, wu, wd), sh = _tiny_layer(rng, 10, 8, 6, 7)
+    k = 3
+    base = O.moe_forward_dense(x, w_r, b, (wg, wu, wd), sh, k)
+    # permuting tokens permutes every per-token output
+    Q = rng.permutation(10)
+    o = O.moe_forward_dense(x[Q], w_r, b, (wg, wu, wd), sh, k)
+    assert np.array_equal(o["idx"], base["idx"][Q])
+    assert np.allclose(o["y"], base["y"][Q], rtol=1e-13, atol=1e-14)
+    # relabelling experts (router rows, biases and weights together) leaves
+    # y unchanged and relabels the selection
+    P = rng.permutation(7)
+    o = O.moe_forward_dense(x, w_r[P], b[P], (wg[P], wu[P], wd[P]), sh, k)
+    inv = np.argsort(P)
+    assert np.array_equal(P[o["idx"]], base["idx"])
+    assert np.array_equal(inv[base["idx"]], o["idx"])
+    assert np.allclose(o["y"], base["y"], rtol=1e-13, atol=1e-14)
+    # duplicated router rows with equal bias tie exactly; the lower index wins
+    w2 = w_r.copy()
+    w2[4] = w2[2]
+    b2 = b.copy()
+    b2[4] = b2[2]
+    b2[2] += 50.0
+    b2[4] += 50.0
+    r = O.route(x, w2, b2, 1)
+    assert np.all(r["idx"][:, 0] == 2)
+
+
+def pin_dense_sparse_agree(O):
+    rng = np.random.default_rng(7)
+    for (T, d, h, E, k) in [(9, 8, 4, 6, 2), (5, 4, 8, 3, 3), (7, 6, 6, 8, 1)]:
+        x, w_r, b, ex, sh = _tiny_layer(rng, T, d, h, E)
+        dn = O.moe_forward_dense(x, w_r, b, ex, sh, k)
+        sp = O.moe_forward_sparse(x, w_r, b, ex, sh, k)
+        assert np.array_equal(dn["idx"], sp["idx"])
+        rel = np.linalg.norm(dn["y"] - sp["y"]) / np.linalg.norm(dn["y"])
+        assert rel < 1e-12, rel
+        rows = O.expert_output_rows(x, dn["idx"], dn["gates"],
+                                    lambda e: (ex[0][e], ex[1][e], ex[2][e]), sh)
+        assert np.linalg.norm(rows - dn["y"]) / np.linalg.norm(dn["y"]) < 1e-12
+
+
+def pin_route_and_update(O):
+    rng = np.random.default_rng(12)
+    x, w_r, b, _, _ = _tiny_layer(rng, 30, 8, 4, 6)
+    r = O.route_and_update(x, w_r, b.astype(np.float32), 2, 1e-3)
+    assert r["load"].sum() == 60
+    over = r["load"] * 6 > 60
+    under = r["load"] * 6 < 60
+    bb = b.astype(np.float32)
+    assert np.all(r["bias_new"][over] < bb[over])
+    assert np.all(r["bias_new"][under] > bb[under])
+
+
+PINS = [
+    pin_routing_golden,
+    pin_topk_bruteforce,
+    pin_gap,
+    pin_gate_invariants,
+    pin_router_one_hot,
+    pin_load_counts,
+    pin_bias_update,
+    pin_swiglu_reductions,
+    pin_scalar_layer_golden,
+    pin_layer_reductions,
+    pin_equivariance,
+    pin_dense_sparse_agree,
+    pin_route_and_update,
+]

@@ -1,0 +1,207 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and require that at
+least one pin catches each of them.  This is what makes the pins a real
+check: a pin set that passes a broken oracle would not pin anything."""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from tests.oracle_pins import PINS
+
+F64 = np.float64
+
+
+def _sigmoid_flipped(u):
+    return 1.0 / (1.0 + np.exp(np.asarray(u, F64)))
+
+
+def _biased_minus(s, bias):
+    return np.asarray(s, F64) - np.asarray(bias, F64)[None, :]
+
+
+def _biased_none(s, bias):
+    return np.asarray(s, F64) + 0.0 * np.asarray(bias, F64)[None, :]
+
+
+def _topk_high_index_ties(z, k):
+    z = np.asarray(z, F64)
+    key = np.where(np.isnan(z), -np.inf, z)
+    E = z.shape[1]
+    order = np.argsort(-key[:, ::-1], axis=1, kind="stable")
+    return (E - 1 - order[:, :k]).astype(np.int64)
+
+
+def _topk_smallest(z, k):
+    z = np.asarray(z, F64)
+    return np.argsort(z, axis=1, kind="stable")[:, :k].astype(np.int64)
+
+
+def _topk_nan_first(z, k):
+    z = np.asarray(z, F64)
+    key = np.where(np.isnan(z), np.inf, z)
+    return np.argsort(-key, axis=1, kind="stable")[:, :k].astype(np.int64)
+
+
+def _topk_unordered(z, k):
+    z = np.asarray(z, F64)
+    key = np.where(np.isnan(z), -np.inf, z)
+    order = np.argsort(-key, axis=1, kind="stable")[:, :k]
+    return np.sort(order, axis=1).astype(np.int64)
+
+
+def _gates_unnormalised(s, idx):
+    return np.take_along_axis(np.asarray(s, F64), idx, axis=1)
+
+
+def _gates_softmax(s, idx):
+    sel = np.exp(np.take_along_axis(np.asarray(s, F64), idx, axis=1))
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+def _route_biased_gates(x, w_router, bias, k):
+    u, s = O.router_affinity(x, w_router)
+    z = O.biased_scores(s, bias)
+    idx = O.select_topk(z, k)
+    return {"u": u, "s": s, "z": z, "idx": idx,
+            "gates": O.gate_weights(z, idx), "gap": O.topk_gap(z, k)}
+
+
+def _silu_wrong(z):
+    z = np.asarray(z, F64)
+    return z * O.sigmoid(-z)
+
+
+def _swiglu_silu_on_up(x, w_gate, w_up, w_down):
+    x = np.asarray(x, F64)
+    return ((x @ np.asarray(w_gate, F64).T) * O.silu(x @ np.asarray(w_up, F64).T)) @ np.asarray(w_down, F64).T
+
+
+def _swiglu_down_untransposed(x, w_gate, w_up, w_down):
+    x = np.asarray(x, F64)
+    hmid = O.silu(x @ np.asarray(w_gate, F64).T) * (x @ np.asarray(w_up, F64).T)
+    return hmid @ np.asarray(w_down, F64)  # W_down used untransposed
+
+
+def _swiglu_no_up(x, w_gate, w_up, w_down):
+    x = np.asarray(x, F64)
+    return O.silu(x @ np.asarray(w_gate, F64).T) @ np.asarray(w_down, F64).T
+
+
+def _dense_no_shared(x, w_router, bias, experts, shared, k, idx_override=None):
+    z = (np.zeros_like(shared[0]), shared[1], shared[2])
+    return _ORIG["moe_forward_dense"](x, w_router, bias, experts, z, k, idx_override)
+
+
+def _dense_mask_with_s(x, w_router, bias, experts, shared, k, idx_override=None):
+    r = O.route(x, w_router, bias, k)
+    idx = r["idx"]
+    T, E = r["s"].shape
+    mask = np.zeros((T, E))
+    np.put_along_axis(mask, idx, np.take_along_axis(r["s"], idx, axis=1), axis=1)
+    wg, wu, wd = experts
+    y = O.swiglu_expert(x, *shared)
+    for e in range(E):
+        y = y + mask[:, e:e + 1] * O.swiglu_expert(x, wg[e], wu[e], wd[e])
+    out = dict(r)
+    out.update({"idx": idx, "gates": O.gate_weights(r["s"], idx), "y": y})
+    return out
+
+
+def _sparse_first_slot_only(x, w_router, bias, experts, shared, k, idx_override=None):
+    r = O.route(x, w_router, bias, k)
+    idx, gates = r["idx"], r["gates"]
+    wg, wu, wd = experts
+    y = O.swiglu_expert(x, *shared)
+    for t in range(idx.shape[0]):
+        e = int(idx[t, 0])
+        y[t] += gates[t, 0] * O.swiglu_expert(x[t:t + 1], wg[e], wu[e], wd[e])[0]
+    out = dict(r)
+    out.update({"y": y})
+    return out
+
+
+def _rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared):
+    return _ORIG["expert_output_rows"](x_rows, idx_rows, np.ones_like(gate_rows), get_expert, shared)
+
+
+def _load_no_minlength(idx, n_experts):
+    return np.bincount(np.asarray(idx).ravel()).astype(np.int64)
+
+
+def _load_per_token(idx, n_experts):
+    return np.bincount(np.asarray(idx)[:, 0], minlength=n_experts).astype(np.int64)
+
+
+def _bias_sign_flipped(bias, load, gamma, tk):
+    b = np.asarray(bias, np.float32).astype(F64)
+    load = np.asarray(load, np.int64)
+    sgn = np.sign(load.shape[0] * load - int(tk))
+    return (b + F64(np.float32(gamma)) * sgn).astype(np.float32)
+
+
+def _bias_floor_mean(bias, load, gamma, tk):
+    b = np.asarray(bias, np.float32).astype(F64)
+    load = np.asarray(load, np.int64)
+    sgn = np.sign(load - int(tk) // load.shape[0])
+    return (b - F64(np.float32(gamma)) * sgn).astype(np.float32)
+
+
+def _bias_no_round(bias, load, gamma, tk):
+    b = np.asarray(bias, np.float32).astype(F64)
+    load = np.asarray(load, np.int64)
+    sgn = np.sign(load.shape[0] * load - int(tk))
+    return b - gamma * sgn
+
+
+def _gap_off_by_one(z, k):
+    z = np.asarray(z, F64)
+    srt = -np.sort(-z, axis=1)
+    return srt[:, k - 2] - srt[:, k - 1] if k >= 2 else srt[:, 0] - srt[:, 1]
+
+
+def _router_no_sigmoid(x, w_router):
+    u = np.asarray(x, F64) @ np.asarray(w_router, F64).T
+    return u, u
+
+
+_ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
+
+MUTATIONS = [
+    ("sigmoid", _sigmoid_flipped),
+    ("biased_scores", _biased_minus),
+    ("biased_scores", _biased_none),
+    ("select_topk", _topk_high_index_ties),
+    ("select_topk", _topk_smallest),
+    ("select_topk", _topk_nan_first),
+    ("select_topk", _topk_unordered),
+    ("gate_weights", _gates_unnormalised),
+    ("gate_weights", _gates_softmax),
+    ("route", _route_biased_gates),
+    ("silu", _silu_wrong),
+    ("swiglu_expert", _swiglu_silu_on_up),
+    ("swiglu_expert", _swiglu_down_untransposed),
+    ("swiglu_expert", _swiglu_no_up),
+    ("moe_forward_dense", _dense_no_shared),
+    ("moe_forward_dense", _dense_mask_with_s),
+    ("moe_forward_sparse", _sparse_first_slot_only),
+    ("expert_output_rows", _rows_ungated),
+    ("load_counts", _load_no_minlength),
+    ("load_counts", _load_per_token),
+    ("bias_update", _bias_sign_flipped),
+    ("bias_update", _bias_floor_mean),
+    ("bias_update", _bias_no_round),
+    ("topk_gap", _gap_off_by_one),
+    ("router_affinity", _router_no_sigmoid),
+]
+
+
+@pytest.mark.parametrize("target,mutant", MUTATIONS,
+                         ids=[f"{t}:{m.__name__}" for t, m in MUTATIONS])
+def test_mutation_is_caught(monkeypatch, target, mutant):
+    monkeypatch.setattr(O, target, mutant)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(O)
+        except Exception as exc:  # noqa: BLE001 - any failure counts as caught
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"no pin caught the planted mistake in {target}"
