@@ -1,0 +1,374 @@
+"""MoE-layer forward throughput on B300 (tokens/s) and roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one forward pass of the whole layer (router, top-k, load counts,
+dispatch, both expert GEMMs with the shared expert, combine) over one batch
+of the workload, through the C ABI of libmoe.so.  Inputs are synthetic and
+seeded (sparse_moe_layer_fwd_b300.inputs) and resident in device memory when
+the timed region starts.  The default workload is the DeepSeek-V3-shaped
+prefill layer (T = 8192, d = 7168, h = 2048, 256 routed experts, top-8, one
+shared expert): 22.5 GB of expert weights, far larger than the 126 MB L2, so
+no L2 flush is needed between steps.
+
+Per-phase device times come from CUDA events that the library records on the
+launching stream between phases (moe_forward_profiled).  `roofline` is for
+the dominant kernel (expert GEMM 1: gate/up + SwiGLU, shared expert
+included): algorithmic FLOPs (prefill) or bytes (decode) per launch divided
+by its mean event-timed duration, against MEASURED_PEAKS.json.
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+replica on its own batch (the layer forward has no cross-replica exchange):
+weak scaling, value = all ranks' tokens / the slowest rank's time.
+
+--impl reference times the float64 CPU oracle on the host cores on bounded
+samples of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (fwd, bf16) at 1 B300; % of tensor-core or HBM roofline"
+KERNELS_PER_STEP = 8  # router logits, top-k, block ranks, scan, permute, GEMM 1, GEMM 2, combine
+
+# DRAM traffic of expert GEMM 1 per launch from ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by workload, with the SHA-256 of the kernel
+# source at capture time; reported as null once the kernel source changes.
+NCU_TRAFFIC = {}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def _kernel_sha():
+    p = os.path.join(ROOT, "sparse_moe_layer_fwd_b300", "csrc", "experts_tc.cuh")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a window."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                except ValueError:
+                    continue
+                rows.append((ts, parts))
+        os.unlink(self.file.name)
+        inside = [p for ts, p in rows if t0 - 0.05 <= ts <= t1 + 0.05] or [p for _, p in rows[-5:]]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        mx = None
+        for p in inside:
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                pass
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _algorithmic(wl, load):
+    """FLOPs and bytes of the two expert GEMMs for one launch each."""
+    TK, T, d, h = wl.T * wl.k, wl.T, wl.d, wl.h
+    rows = TK + T
+    fl1 = 4.0 * rows * d * h
+    fl2 = 2.0 * rows * d * h
+    touched = int((load > 0).sum()) + 1  # + shared expert
+    by1 = touched * 2 * h * d * 2 + rows * d * 2 + rows * h * 2
+    by2 = touched * d * h * 2 + rows * h * 2 + TK * d * 2 + T * d * 4
+    return fl1, fl2, by1, by2, touched - 1
+
+
+def cpu_oracle_sample(wl, inp, n_tokens, seed=0):
+    """Run the float64 oracle on n_tokens tokens of the workload: routing,
+    shared expert and each token's k routed experts, streaming expert
+    weights from device memory one at a time.  Returns seconds."""
+    from oracle import moe_oracle as O
+    rows = np.sort(np.random.default_rng(seed).choice(wl.T, n_tokens, replace=False))
+    f64 = lambda t: t.detach().to("cpu").to(torch.float64).numpy()  # noqa: E731
+    x = f64(inp["x"][torch.from_numpy(rows).to(inp["x"].device)])
+    wr, b = f64(inp["w_router"]), f64(inp["bias"])
+    t0 = time.perf_counter()
+    r = O.route(x, wr, b, wl.k)
+    sh = (f64(inp["sh_gate"]), f64(inp["sh_up"]), f64(inp["sh_down"]))
+    O.expert_output_rows(x, r["idx"], r["gates"],
+                         lambda e: (f64(inp["w_gate"][e]), f64(inp["w_up"][e]), f64(inp["w_down"][e])),
+                         sh)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, wl):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    from sparse_moe_layer_fwd_b300 import inputs as I
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = I.make_inputs(wl, device=dev)
+    n = args.ref_tokens
+    cores = len(os.sched_getaffinity(0))
+    torch.set_num_threads(cores)
+    for i in range(args.warmup):
+        cpu_oracle_sample(wl, inp, n, seed=1000 + i)
+    times = [cpu_oracle_sample(wl, inp, n, seed=i) for i in range(args.steps)]
+    total = sum(times)
+    value = n * args.steps / total
+    sample = (f"{n} tokens per step of {wl.name}: float64 routing of those tokens, shared "
+              f"expert and their {wl.k} routed experts, expert weights streamed from device memory")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    from sparse_moe_layer_fwd_b300 import inputs as I
+    from sparse_moe_layer_fwd_b300 import moe as M
+    from sparse_moe_layer_fwd_b300.layer import MoeLayer
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    wl_rank = wl.with_(seed=wl.seed + 1000 * rank) if ws > 1 else wl
+    inp = I.make_inputs(wl_rank, device="cuda")
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype)
+    stream = torch.cuda.current_stream()
+    x = inp["x"]
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        layer.forward(x, stream)
+    torch.cuda.synchronize()
+    if M.moe_last_error() != M.MOE_OK:
+        raise RuntimeError("device error word set during warm-up")
+    load = layer.load_counts.cpu().numpy()
+
+    # timed region: per-step phase events on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(M.N_PHASE_EVENTS)]
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        M.moe_forward_profiled(layer.desc, x, layer.w_router, layer.bias, layer.experts,
+                               layer.shared, layer.y, layer.topk_idx, layer.gates,
+                               layer.load_counts, layer.workspace, layer.ws_bytes, stream, ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier()
+    clocks = sampler.stop(t_host0, t_host1) if sampler else None
+    if M.moe_last_error() != M.MOE_OK:
+        raise RuntimeError("device error word set during the timed region")
+    elapsed_ms = start.elapsed_time(end)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    phase_ms = np.zeros(len(M.PHASES))
+    for i in range(args.steps):
+        for p in range(len(M.PHASES)):
+            phase_ms[p] += ev[i][p].elapsed_time(ev[i][p + 1])
+    phase_ms /= args.steps
+
+    # end to end through the host-buffer entry point (pinned x in, y out)
+    e2e = None
+    if not args.no_e2e:
+        hl = MoeLayer.from_inputs(inp, wl.k, wl.dtype, host_io=True)
+        x_host = x.cpu().pin_memory()
+        y_host = torch.empty_like(x_host).pin_memory()
+        for _ in range(2):
+            hl.forward_host_io(x_host, y_host, stream)
+        torch.cuda.synchronize()
+        barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            hl.forward_host_io(x_host, y_host, stream)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s2.elapsed_time(e2)
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        nb = x_host.numel() * x_host.element_size()
+        e2e = {"value": ws * wl.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb,
+               "ms_per_step": e2e_ms / args.steps}
+        del hl
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    fl1, fl2, by1, by2, touched = _algorithmic(wl, load)
+    g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
+    prefill_like = wl.T * wl.k / wl.E >= 96
+    sha = _kernel_sha()
+    cap = NCU_TRAFFIC.get(wl.name)
+    traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
+    if prefill_like:
+        ach = fl1 / g1_s / 1e12
+        roof = {"bound": "tensor", "kernel": "k_expert_tc (GEMM 1: gate/up + SwiGLU)",
+                "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_kind": f"{peaks['source']} bf16 burst",
+                "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
+        both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
+        layer_roof = {"expert_gemms_tflops": both,
+                      "frac_of_burst": both / peaks["bf16_tflops"],
+                      "frac_of_sustained": (both / peaks["bf16_tflops_sustained"]
+                                            if peaks.get("bf16_tflops_sustained") else None)}
+    else:
+        ach = by1 / g1_s / 1e9
+        roof = {"bound": "hbm", "kernel": "k_expert_tc (GEMM 1: gate/up + SwiGLU)",
+                "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_kind": f"{peaks['source']} copy bandwidth",
+                "bytes_per_launch": by1, "ms_per_launch": phase_ms[2]}
+        both = (by1 + by2) / (g1_s + g2_s) / 1e9
+        layer_roof = {"expert_gemms_gbs": both, "frac": both / peaks["hbm_gbs"]}
+    layer_roof["touched_experts"] = touched
+
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cores = len(os.sched_getaffinity(0))
+        torch.set_num_threads(cores)
+        n = args.ref_tokens
+        secs = cpu_oracle_sample(wl, inp, n)
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} tokens of {wl.name}: float64 routing, shared expert and "
+                         f"{wl.k} routed experts per token, weights streamed from device memory"}
+
+    value = ws * wl.T * args.steps / (elapsed_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
+                   "shared_experts": 1, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (22.5 GB of expert weights per step)"},
+        "roofline": roof, "roofline_layer": layer_roof,
+        "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks, "kernel_sha": sha,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="v3_prefill")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, _, _ = _dist()
+    if args.gpus != ws:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}: launch N > 1 with torchrun")
+    from sparse_moe_layer_fwd_b300 import inputs as I
+    wl = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the DeepSeekMoE layer forward for one B300
+ * (sm_103a).
+ *
+ * The layer, as the deepseek-v3-jax pages describe it:
+ *   "190行JAX复刻DeepSeek V3" (openai-hub.com), section "190行代码到底装进了什么":
+ *     routed experts of which each token selects the top k, plus one shared
+ *     expert that every token always passes through;
+ *   same page, section "最有价值的实验:无辅助损失均衡真的有效":
+ *     auxiliary-loss-free balancing -- after each step an over-loaded
+ *     expert's bias is lowered and an idle expert's bias raised, speed
+ *     gamma = 1e-3; the bias decides which experts are selected and never
+ *     changes the gate value of a selected expert;
+ *   "DeepSeek V3 viết lại bằng 190 dòng JAX thuần" (lehuy.net), section
+ *     "Những gì đã được đơn giản hóa": the pages' code runs every expert on
+ *     every token and zeroes the unselected ones, with no sparse dispatch.
+ *     This library is truly sparse: each token reaches only its k experts.
+ *
+ * Per token t (x[t] a row of d numbers), with E routed experts:
+ *   u[t,e]  = x[t] . W_r[e]                (fp32 accumulation)
+ *   s[t,e]  = 1 / (1 + exp(-u[t,e]))       (sigmoid affinity)
+ *   idx[t]  = the k experts with the largest s[t,e] + b[e], ordered by that
+ *             biased score, descending; equal scores go to the lower index;
+ *             a NaN score ranks below every number
+ *   g[t,j]  = s[t,idx[t,j]] / sum_j' s[t,idx[t,j']]   (unbiased affinities)
+ *   y[t]    = S(x[t]) + sum_j g[t,j] * R_{idx[t,j]}(x[t])
+ *   where every expert is SwiGLU: F(x) = W_down (silu(W_gate x) * (W_up x)),
+ *   silu(z) = z / (1 + exp(-z)).
+ *   load[e] = #{(t,j) : idx[t,j] = e}
+ * and, called separately after a step,
+ *   b[e]   -= gamma * sgn(load[e] - T*k/E)     (sgn(0) = 0, fp32 result)
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *     and contiguous, 16-byte aligned.  The library allocates no device
+ *     memory: all scratch comes from the caller's workspace.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; nothing synchronises the host.
+ *   - Return value: MOE_OK (0) once the work is enqueued, or a negative
+ *     MOE_ERR_* code.  Argument errors are found on the host before anything
+ *     is launched (nothing is written).  Errors that only the device can see
+ *     (a pipeline wait that ran out of time) set a device error word which
+ *     moe_last_error() returns after the caller has synchronised.
+ *   - Thread safety: calls on different streams may run concurrently if they
+ *     use different workspaces and outputs.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Only the functions declared here are exported from libmoe.so. */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, y and the expert weights.  The router weights, the
+ * bias, the gates and the load counts are always fp32 / int32. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = -1,           /* a required pointer is NULL */
+  MOE_ERR_SHAPE = -2,          /* sizes out of range (see moe_desc) */
+  MOE_ERR_ALIGN = -3,          /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = -4,      /* ws_bytes < moe_workspace_size(desc) */
+  MOE_ERR_DTYPE = -5,          /* unknown dtype, or flags that the dtype does not support */
+  MOE_ERR_LAUNCH = -6,         /* a kernel launch failed (cudaGetLastError) */
+  MOE_ERR_DEVICE_TIMEOUT = -7, /* device-side wait ran out of time (moe_last_error) */
+  MOE_ERR_DEVICE = -8,         /* no usable sm_103 device, or a CUDA runtime call failed */
+};
+
+/* Flags. */
+#define MOE_ROUTE_ONLY   1u  /* router + load counts only: no dispatch, experts or
+                                combine; y and the expert weights may be NULL */
+#define MOE_SIMT_EXPERTS 2u  /* bf16 only: run the expert GEMMs on the CUDA-core
+                                kernels instead of the tensor cores (a cross-check
+                                of the tensor-core path; slow) */
+
+/* Problem description.
+ *   T  tokens (>= 0)            d  model width          h  expert hidden width
+ *   E  routed experts (1..1024) k  experts per token (1..min(E, 32))
+ * Both dtypes need d and h to be multiples of 64; the bf16 tensor-core path
+ * needs multiples of 128.  T*k*max(d,h) and (T*k+T)*max(d,h) must stay below
+ * 2^31. */
+typedef struct {
+  int T, d, h, E, k;
+  int dtype;        /* moe_dtype */
+  unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS */
+} moe_desc;
+
+/* Expert weights, element type desc->dtype.
+ * Routed experts: w_gate [E, h, d], w_up [E, h, d], w_down [E, d, h].
+ * Shared expert : w_gate [h, d],    w_up [h, d],    w_down [d, h].
+ * (Each matrix is stored output-major: row i holds the weights of output i.) */
+typedef struct {
+  const void *w_gate, *w_up, *w_down;
+} moe_expert_w;
+
+/* Bytes of device workspace that moe_forward needs for `desc` (flags
+ * included).  Returns 0 for an invalid desc.  The value depends only on the
+ * desc, so one buffer can be reused for every call with the same desc. */
+MOE_API size_t moe_workspace_size(const moe_desc* desc);
+
+/* One forward pass of the MoE layer.
+ *   x          [T, d]   dtype         tokens (already normalised; the layer
+ *                                     output excludes any residual)
+ *   w_router   [E, d]   fp32          router weights W_r
+ *   bias       [E]      fp32          selection bias b (read only here)
+ *   experts, shared                   see moe_expert_w (may be NULL with
+ *                                     MOE_ROUTE_ONLY)
+ *   y          [T, d]   dtype   out   layer output (NULL allowed with
+ *                                     MOE_ROUTE_ONLY)
+ *   topk_idx   [T, k]   int32   out   selected experts, slot order as above
+ *   gates      [T, k]   fp32    out   gate values g
+ *   load_counts[E]      int32   out   tokens routed to each expert
+ *   workspace  device buffer of ws_bytes >= moe_workspace_size(desc)
+ * The bias is not updated here: call moe_bias_update after the step. */
+MOE_API int moe_forward(const moe_desc* desc, const void* x, const float* w_router,
+                const float* bias, const moe_expert_w* experts,
+                const moe_expert_w* shared, void* y, int32_t* topk_idx,
+                float* gates, int32_t* load_counts, void* workspace,
+                size_t ws_bytes, void* stream);
+
+/* Same pass with x and y in HOST memory (pinned memory lets the copies run
+ * asynchronously).  x is copied to the device, the layer runs, y is copied
+ * back, all enqueued on `stream`; the host buffers must stay valid until the
+ * stream reaches that point.  Weights, router, bias and the small outputs are
+ * device pointers as in moe_forward.  The workspace must hold
+ * moe_workspace_size(desc) + moe_host_io_extra_bytes(desc) bytes. */
+MOE_API size_t moe_host_io_extra_bytes(const moe_desc* desc);
+MOE_API int moe_forward_host_io(const moe_desc* desc, const void* x_host,
+                        const float* w_router, const float* bias,
+                        const moe_expert_w* experts, const moe_expert_w* shared,
+                        void* y_host, int32_t* topk_idx, float* gates,
+                        int32_t* load_counts, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/* moe_forward with caller-owned CUDA events recorded on `stream` between the
+ * phases of the pass, for timing each phase on the device:
+ *   events[0] before the router (logits + top-k)
+ *   events[1] before dispatch (ranks, scan, permute/gather)
+ *   events[2] before expert GEMM 1 (gate/up + SwiGLU, shared expert included)
+ *   events[3] before expert GEMM 2 (down + gate scale)
+ *   events[4] before the combine
+ *   events[5] after the combine
+ * `events` points to MOE_N_PHASE_EVENTS cudaEvent_t handles (created by the
+ * caller, not destroyed here).  Phases that do not run (route-only, T = 0)
+ * still get their events recorded, back to back. */
+#define MOE_N_PHASE_EVENTS 6
+MOE_API int moe_forward_profiled(const moe_desc* desc, const void* x,
+                                 const float* w_router, const float* bias,
+                                 const moe_expert_w* experts,
+                                 const moe_expert_w* shared, void* y,
+                                 int32_t* topk_idx, float* gates,
+                                 int32_t* load_counts, void* workspace,
+                                 size_t ws_bytes, void* stream,
+                                 void* const* events);
+
+/* Auxiliary-loss-free bias update ("190行JAX复刻DeepSeek V3", section
+ * "最有价值的实验:无辅助损失均衡真的有效"):
+ *   bias[e] = fp32(bias[e] - fp32(gamma) * sgn(E*load_counts[e] - TK))
+ * i.e. an expert above the mean load T*k/E loses gamma, one below gains it,
+ * one exactly at the mean is unchanged.  load_counts [E] int32 and bias [E]
+ * fp32 are device pointers; bias is updated in place.  TK = T*k of the step
+ * the counts came from. */
+MOE_API int moe_bias_update(const int32_t* load_counts, float* bias, float gamma,
+                    int E, int TK, void* stream);
+
+/* Device error word of the calls made so far (MOE_OK or
+ * MOE_ERR_DEVICE_TIMEOUT), and reset it to MOE_OK.  It does not synchronise
+ * the caller's stream: synchronise first.  Returns MOE_ERR_DEVICE if the
+ * word cannot be read. */
+MOE_API int moe_last_error(void);
+
+/* Static string for a MOE_* code. */
+MOE_API const char* moe_error_string(int code);
+
+/* Byte offsets of the named scratch regions inside the workspace for
+ * `desc`, for tests that inspect intermediate results.  `names` receives up
+ * to `cap` entries of (name, offset, bytes); returns the number of regions
+ * (or a negative MOE_ERR_*).  Region names: "router_part" (fp32 partial
+ * logits), "blk_hist", "pair_rank", "groups" (int32 group table),
+ * "perm" (permuted row -> token*k+slot), "inv" (token*k+slot -> permuted row),
+ * "x_perm", "h", "y_perm", "y_shared". */
+typedef struct {
+  char name[16];
+  size_t offset, bytes;
+} moe_region;
+MOE_API int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,490 @@
+// moe.cu -- libmoe.so: the C ABI declared in include/moe.h.
+//
+// Host side of the DeepSeekMoE layer forward on one sm_103a GPU: argument
+// validation, the workspace layout, TMA tensor maps, and the launch sequence
+//   router logits -> router top-k -> block ranks -> scan + tile table ->
+//   permute/gather -> expert GEMM 1 (gate/up + SwiGLU) -> expert GEMM 2
+//   (down + gate scale) -> combine
+// all enqueued on the caller's stream with no host synchronisation (tile
+// counts live in device memory; GEMM grids are sized by an upper bound and
+// surplus CTAs return at once).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "combine.cuh"
+#include "dispatch.cuh"
+#include "experts_simt.cuh"
+#include "experts_tc.cuh"
+#include "ptx.cuh"
+#include "router.cuh"
+
+namespace {
+
+constexpr int kRouterCtaTarget = 296;  // CTAs wanted for the router GEMM (fixed, so
+                                       // results do not depend on the device)
+constexpr int kRouterBK = 16;
+
+// Tensor-core GEMM variants: (BN tokens per tile, pipeline stages).
+constexpr int kBigBN = 256, kBigStages = 3;
+constexpr int kSmallBN = 64, kSmallStages = 5;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Plan {
+  int T, d, h, E, k, TK;
+  bool f32, route_only, simt, big_router, big_tiles;
+  int el;  // bytes per activation / weight element
+  // router
+  int r_bm, r_bn, n_split, kchunk;
+  // dispatch
+  int n_pair_blocks;
+  // expert tiling
+  int bn, ft_a, ft_b, max_tiles_a, max_tiles_b;
+  // workspace regions (byte offsets)
+  size_t o_part, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh, total;
+  size_t b_part, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh;
+};
+
+int validate_desc(const moe_desc* d) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
+  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS)) return MOE_ERR_DTYPE;
+  if ((d->flags & MOE_SIMT_EXPERTS) && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
+  if (d->T < 0 || d->d <= 0 || d->h <= 0 || d->E < 1 || d->E > MOE_MAX_E || d->k < 1 ||
+      d->k > d->E || d->k > 32)
+    return MOE_ERR_SHAPE;
+  if (d->d % 64 || d->h % 64) return MOE_ERR_SHAPE;
+  const bool tc = d->dtype == MOE_BF16 && !(d->flags & MOE_SIMT_EXPERTS);
+  if (tc && (d->d % 128 || d->h % 128)) return MOE_ERR_SHAPE;
+  const long long TK = (long long)d->T * d->k;
+  const long long wmax = d->d > d->h ? d->d : d->h;
+  if ((TK + d->T) * wmax >= (1LL << 31)) return MOE_ERR_SHAPE;
+  if ((long long)d->E * wmax >= (1LL << 31)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+Plan make_plan(const moe_desc* d) {
+  Plan p;
+  memset(&p, 0, sizeof(p));
+  p.T = d->T; p.d = d->d; p.h = d->h; p.E = d->E; p.k = d->k; p.TK = d->T * d->k;
+  p.f32 = d->dtype == MOE_F32;
+  p.route_only = d->flags & MOE_ROUTE_ONLY;
+  p.simt = p.f32 || (d->flags & MOE_SIMT_EXPERTS);
+  p.el = p.f32 ? 4 : 2;
+
+  // router GEMM tiling and split of the model dimension
+  p.big_router = p.E >= 96;
+  p.r_bm = p.big_router ? 128 : 64;
+  p.r_bn = p.big_router ? 128 : 32;
+  const long long tiles = (long long)((p.T + p.r_bm - 1) / p.r_bm) * ((p.E + p.r_bn - 1) / p.r_bn);
+  const int kblocks = p.d / kRouterBK;
+  int ns = tiles > 0 ? (int)((kRouterCtaTarget + tiles - 1) / tiles) : 1;
+  ns = ns < 1 ? 1 : (ns > 64 ? 64 : ns);
+  ns = ns > kblocks ? kblocks : ns;
+  p.kchunk = ((kblocks + ns - 1) / ns) * kRouterBK;
+  p.n_split = (p.d + p.kchunk - 1) / p.kchunk;
+
+  p.n_pair_blocks = (p.TK + MOE_PAIRS_PER_BLOCK - 1) / MOE_PAIRS_PER_BLOCK;
+
+  // expert tiling
+  if (!p.route_only) {
+    if (p.simt) {
+      p.bn = SIMT_TM;
+      p.ft_a = p.h / SIMT_TN;
+      p.ft_b = p.d / SIMT_TN;
+    } else {
+      const double per_expert = p.E > 0 ? (double)p.TK / p.E : 0.0;
+      p.big_tiles = per_expert >= 96.0;
+      p.bn = p.big_tiles ? kBigBN : kSmallBN;
+      p.ft_a = p.h / TC_BM;
+      p.ft_b = (p.d / TC_BM + 1) / 2;
+    }
+    const long long tok_tiles = (long long)p.TK / p.bn + (p.TK < p.E ? p.TK : p.E) +
+                                (p.T + p.bn - 1) / p.bn + 1;
+    p.max_tiles_a = (int)(tok_tiles * p.ft_a);
+    p.max_tiles_b = (int)(tok_tiles * p.ft_b);
+  }
+
+  // workspace
+  size_t off = 0;
+  auto region = [&](size_t bytes, size_t& o, size_t& b) {
+    o = off;
+    b = bytes;
+    off = align_up(off + bytes, 256);
+  };
+  region((size_t)p.n_split * p.T * p.E * 4, p.o_part, p.b_part);
+  region((size_t)p.n_pair_blocks * p.E * 4, p.o_hist, p.b_hist);
+  region((size_t)p.TK * 4, p.o_rank, p.b_rank);
+  region((size_t)(5 * p.E + 8) * 4, p.o_groups, p.b_groups);
+  if (!p.route_only) {
+    region((size_t)p.TK * 4, p.o_perm, p.b_perm);
+    region((size_t)p.TK * 4, p.o_inv, p.b_inv);
+    region((size_t)p.TK * p.d * p.el, p.o_xperm, p.b_xperm);
+    region((size_t)(p.TK + p.T) * p.h * p.el, p.o_h, p.b_h);
+    region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
+    region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
+  }
+  p.total = off > 0 ? off : 256;
+  return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- TMA tensor maps ------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 matrix [rows, cols] (row-major) read in boxes of 64 columns x box_rows
+// rows with the 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+template <typename TX>
+void launch_router(const Plan& p, const TX* x, const float* w_router, float* part,
+                   cudaStream_t s) {
+  if (p.big_router) {
+    dim3 grid((p.E + 127) / 128, (p.T + 127) / 128, p.n_split);
+    k_router_logits<TX, 128, 128, kRouterBK, 8, 8>
+        <<<grid, 256, 0, s>>>(x, w_router, part, p.T, p.E, p.d, p.kchunk);
+  } else {
+    dim3 grid((p.E + 31) / 32, (p.T + 63) / 64, p.n_split);
+    k_router_logits<TX, 64, 32, kRouterBK, 4, 2>
+        <<<grid, 256, 0, s>>>(x, w_router, part, p.T, p.E, p.d, p.kchunk);
+  }
+}
+
+void launch_topk(const Plan& p, const float* part, const float* bias, int32_t* idx, float* gates,
+                 cudaStream_t s) {
+  const int grid = (p.T + 7) / 8;
+  const int epl = (p.E + 31) / 32;
+#define MOE_TOPK(N) \
+  k_router_topk<N><<<grid, 256, 0, s>>>(part, p.n_split, bias, p.T, p.E, p.k, idx, gates)
+  if (epl <= 1) MOE_TOPK(1);
+  else if (epl <= 2) MOE_TOPK(2);
+  else if (epl <= 4) MOE_TOPK(4);
+  else if (epl <= 8) MOE_TOPK(8);
+  else if (epl <= 16) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
+}
+
+struct TcMaps {
+  CUtensorMap g, u, sg, su, xp, x, d, sd, h;
+};
+
+// All tensor maps of the two tensor-core GEMMs, built before anything is
+// launched so that a failure here leaves the stream untouched.
+bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
+                  uint8_t* ws, TcMaps* m) {
+  bool ok = true;
+  ok &= make_map(&m->g, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
+  ok &= make_map(&m->u, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
+  ok &= make_map(&m->sg, sh->w_gate, p.h, p.d, TC_BM);
+  ok &= make_map(&m->su, sh->w_up, p.h, p.d, TC_BM);
+  ok &= make_map(&m->xp, ws + p.o_xperm, p.TK, p.d, 16);
+  ok &= make_map(&m->x, x, p.T, p.d, 16);
+  ok &= make_map(&m->d, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
+  ok &= make_map(&m->sd, sh->w_down, p.d, p.h, TC_BM);
+  ok &= make_map(&m->h, ws + p.o_h, (long long)p.TK + p.T, p.h, 16);
+  return ok;
+}
+
+template <int BN, int STAGES>
+bool set_tc_smem() {
+  using C = TcCfg<BN, STAGES>;
+  return cudaFuncSetAttribute(k_expert_tc<BN, STAGES, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              C::SMEM_BYTES) == cudaSuccess &&
+         cudaFuncSetAttribute(k_expert_tc<BN, STAGES, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              C::SMEM_BYTES) == cudaSuccess;
+}
+
+template <int BN, int STAGES>
+void launch_tc(const Plan& p, const TcMaps& m, uint8_t* ws, int32_t* groups, const float* gates,
+               cudaStream_t s, cudaEvent_t between) {
+  using C = TcCfg<BN, STAGES>;
+  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
+  __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
+  __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
+  float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
+  k_expert_tc<BN, STAGES, false><<<p.max_tiles_a, TC_THREADS, C::SMEM_BYTES, s>>>(
+      m.g, m.u, m.sg, m.su, m.xp, m.x, groups, p.E, p.d, p.h, hbuf, nullptr, perm, gates);
+  if (between) cudaEventRecord(between, s);
+  k_expert_tc<BN, STAGES, true><<<p.max_tiles_b, TC_THREADS, C::SMEM_BYTES, s>>>(
+      m.d, m.d, m.sd, m.sd, m.h, m.h, groups, p.E, p.h, p.d, yperm, ysh, perm, gates);
+}
+
+template <typename T>
+void launch_simt(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
+                 uint8_t* ws, int32_t* groups, const float* gates, cudaStream_t s,
+                 cudaEvent_t between) {
+  const T* xp = reinterpret_cast<const T*>(ws + p.o_xperm);
+  T* hbuf = reinterpret_cast<T*>(ws + p.o_h);
+  T* yperm = reinterpret_cast<T*>(ws + p.o_yperm);
+  float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
+  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
+  k_expert_simt<T, false><<<p.max_tiles_a, 256, 0, s>>>(
+      (const T*)ex->w_gate, (const T*)ex->w_up, (const T*)sh->w_gate, (const T*)sh->w_up, xp,
+      (const T*)x, groups, p.E, p.d, p.h, hbuf, nullptr, perm, gates);
+  if (between) cudaEventRecord(between, s);
+  k_expert_simt<T, true><<<p.max_tiles_b, 256, 0, s>>>(
+      (const T*)ex->w_down, nullptr, (const T*)sh->w_down, nullptr, hbuf, hbuf, groups, p.E, p.h,
+      p.d, yperm, ysh, perm, gates);
+}
+
+int forward_impl(const moe_desc* desc, const void* x, const float* w_router, const float* bias,
+                 const moe_expert_w* experts, const moe_expert_w* shared, void* y,
+                 int32_t* topk_idx, float* gates, int32_t* load_counts, void* workspace,
+                 size_t ws_bytes, cudaStream_t s, void* const* events = nullptr) {
+  auto mark = [&](int i) {
+    if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+  };
+  int rc = validate_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const Plan p = make_plan(desc);
+  const bool need_out = !p.route_only && p.T > 0;
+  if (!w_router || !bias || !load_counts || !workspace) return MOE_ERR_NULL;
+  if (p.T > 0 && (!x || !topk_idx || !gates)) return MOE_ERR_NULL;
+  if (need_out) {
+    if (!y || !experts || !shared) return MOE_ERR_NULL;
+    if (!experts->w_gate || !experts->w_up || !experts->w_down || !shared->w_gate ||
+        !shared->w_up || !shared->w_down)
+      return MOE_ERR_NULL;
+    if (!aligned16(y) || !aligned16(experts->w_gate) || !aligned16(experts->w_up) ||
+        !aligned16(experts->w_down) || !aligned16(shared->w_gate) || !aligned16(shared->w_up) ||
+        !aligned16(shared->w_down))
+      return MOE_ERR_ALIGN;
+  }
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOE_ERR_ALIGN;
+  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  rc = device_ok();
+  if (rc != MOE_OK) return rc;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool use_tc = need_out && !p.simt;
+  TcMaps maps;
+  if (use_tc) {
+    if (!make_tc_maps(p, x, experts, shared, ws, &maps)) return MOE_ERR_DEVICE;
+    const bool ok = p.big_tiles ? set_tc_smem<kBigBN, kBigStages>()
+                                : set_tc_smem<kSmallBN, kSmallStages>();
+    if (!ok) return MOE_ERR_LAUNCH;
+  }
+  float* part = reinterpret_cast<float*>(ws + p.o_part);
+  int32_t* hist = reinterpret_cast<int32_t*>(ws + p.o_hist);
+  int32_t* rank = reinterpret_cast<int32_t*>(ws + p.o_rank);
+  int32_t* groups = reinterpret_cast<int32_t*>(ws + p.o_groups);
+
+  cudaGetLastError();  // clear a stale error so the check below is ours
+  mark(0);
+  if (p.T > 0) {
+    if (p.f32)
+      launch_router<float>(p, static_cast<const float*>(x), w_router, part, s);
+    else
+      launch_router<__nv_bfloat16>(p, static_cast<const __nv_bfloat16*>(x), w_router, part, s);
+    launch_topk(p, part, bias, topk_idx, gates, s);
+  }
+  mark(1);
+  if (p.T > 0) {
+    k_block_rank<<<p.n_pair_blocks, 32, 0, s>>>(topk_idx, p.TK, p.E, rank, hist);
+  }
+  k_scan_groups<<<1, 1024, 0, s>>>(hist, p.n_pair_blocks, p.E, p.T, p.TK, load_counts, groups,
+                                   need_out ? p.bn : 0, p.ft_a, p.ft_b);
+  if (need_out) {
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + p.o_perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(ws + p.o_inv);
+    k_permute_gather<<<(p.TK + 7) / 8, 256, 0, s>>>(
+        topk_idx, rank, hist, p.TK, p.E, p.k, static_cast<const uint8_t*>(x), ws + p.o_xperm,
+        (size_t)p.d * p.el, perm, inv);
+    mark(2);
+    cudaEvent_t between = events ? static_cast<cudaEvent_t>(events[3]) : nullptr;
+    if (p.f32) {
+      launch_simt<float>(p, x, experts, shared, ws, groups, gates, s, between);
+    } else if (p.simt) {
+      launch_simt<__nv_bfloat16>(p, x, experts, shared, ws, groups, gates, s, between);
+    } else {
+      if (p.big_tiles)
+        launch_tc<kBigBN, kBigStages>(p, maps, ws, groups, gates, s, between);
+      else
+        launch_tc<kSmallBN, kSmallStages>(p, maps, ws, groups, gates, s, between);
+    }
+    mark(4);
+    const float* ysh = reinterpret_cast<const float*>(ws + p.o_ysh);
+    if (p.f32)
+      k_combine<float><<<p.T, 128, 0, s>>>(ysh, reinterpret_cast<const float*>(ws + p.o_yperm),
+                                           inv, p.T, p.d, p.k, static_cast<float*>(y));
+    else
+      k_combine<__nv_bfloat16><<<p.T, 128, 0, s>>>(
+          ysh, reinterpret_cast<const __nv_bfloat16*>(ws + p.o_yperm), inv, p.T, p.d, p.k,
+          static_cast<__nv_bfloat16*>(y));
+  } else {
+    mark(2);
+    mark(3);
+    mark(4);
+  }
+  mark(5);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_desc* desc) {
+  if (validate_desc(desc) != MOE_OK) return 0;
+  return make_plan(desc).total;
+}
+
+int moe_forward(const moe_desc* desc, const void* x, const float* w_router, const float* bias,
+                const moe_expert_w* experts, const moe_expert_w* shared, void* y,
+                int32_t* topk_idx, float* gates, int32_t* load_counts, void* workspace,
+                size_t ws_bytes, void* stream) {
+  return forward_impl(desc, x, w_router, bias, experts, shared, y, topk_idx, gates, load_counts,
+                      workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_profiled(const moe_desc* desc, const void* x, const float* w_router,
+                         const float* bias, const moe_expert_w* experts,
+                         const moe_expert_w* shared, void* y, int32_t* topk_idx, float* gates,
+                         int32_t* load_counts, void* workspace, size_t ws_bytes, void* stream,
+                         void* const* events) {
+  if (!events) return MOE_ERR_NULL;
+  for (int i = 0; i < MOE_N_PHASE_EVENTS; ++i)
+    if (!events[i]) return MOE_ERR_NULL;
+  return forward_impl(desc, x, w_router, bias, experts, shared, y, topk_idx, gates, load_counts,
+                      workspace, ws_bytes, static_cast<cudaStream_t>(stream), events);
+}
+
+size_t moe_host_io_extra_bytes(const moe_desc* desc) {
+  if (validate_desc(desc) != MOE_OK) return 0;
+  const size_t el = desc->dtype == MOE_F32 ? 4 : 2;
+  return 2 * align_up((size_t)desc->T * desc->d * el, 256);
+}
+
+int moe_forward_host_io(const moe_desc* desc, const void* x_host, const float* w_router,
+                        const float* bias, const moe_expert_w* experts,
+                        const moe_expert_w* shared, void* y_host, int32_t* topk_idx,
+                        float* gates, int32_t* load_counts, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  int rc = validate_desc(desc);
+  if (rc != MOE_OK) return rc;
+  if (!workspace) return MOE_ERR_NULL;
+  const size_t base = make_plan(desc).total;
+  const size_t el = desc->dtype == MOE_F32 ? 4 : 2;
+  const size_t xbytes = (size_t)desc->T * desc->d * el;
+  if (ws_bytes < base + moe_host_io_extra_bytes(desc)) return MOE_ERR_WORKSPACE;
+  if (desc->T > 0 && !x_host) return MOE_ERR_NULL;
+  const bool need_y = !(desc->flags & MOE_ROUTE_ONLY) && desc->T > 0;
+  if (need_y && !y_host) return MOE_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* xdev = static_cast<uint8_t*>(workspace) + base;
+  uint8_t* ydev = xdev + align_up(xbytes, 256);
+  if (xbytes && cudaMemcpyAsync(xdev, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  rc = forward_impl(desc, xdev, w_router, bias, experts, shared, need_y ? ydev : nullptr,
+                    topk_idx, gates, load_counts, workspace, base, s);
+  if (rc != MOE_OK) return rc;
+  if (need_y && cudaMemcpyAsync(y_host, ydev, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+int moe_bias_update(const int32_t* load_counts, float* bias, float gamma, int E, int TK,
+                    void* stream) {
+  if (!load_counts || !bias) return MOE_ERR_NULL;
+  if (E < 1 || E > MOE_MAX_E || TK < 0) return MOE_ERR_SHAPE;
+  int rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  cudaGetLastError();
+  k_bias_update<<<(E + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(load_counts, bias,
+                                                                                 gamma, E, TK);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+int moe_last_error(void) {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_moe_dev_error, sizeof(v)) != cudaSuccess) return MOE_ERR_DEVICE;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_moe_dev_error, &zero, sizeof(zero)) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return v ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+const char* moe_error_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "sizes out of range";
+    case MOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_DTYPE: return "unsupported dtype or flags";
+    case MOE_ERR_LAUNCH: return "kernel launch failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
+    case MOE_ERR_DEVICE: return "no usable sm_103 device or CUDA call failed";
+    default: return "unknown error";
+  }
+}
+
+int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
+  const int rc = validate_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const Plan p = make_plan(desc);
+  const struct { const char* n; size_t o, b; } all[] = {
+      {"router_part", p.o_part, p.b_part}, {"blk_hist", p.o_hist, p.b_hist},
+      {"pair_rank", p.o_rank, p.b_rank},   {"groups", p.o_groups, p.b_groups},
+      {"perm", p.o_perm, p.b_perm},        {"inv", p.o_inv, p.b_inv},
+      {"x_perm", p.o_xperm, p.b_xperm},    {"h", p.o_h, p.b_h},
+      {"y_perm", p.o_yperm, p.b_yperm},    {"y_shared", p.o_ysh, p.b_ysh},
+  };
+  const int n = p.route_only ? 4 : 10;
+  for (int i = 0; i < n && i < cap && regions; ++i) {
+    memset(regions[i].name, 0, sizeof(regions[i].name));
+    strncpy(regions[i].name, all[i].n, sizeof(regions[i].name) - 1);
+    regions[i].offset = all[i].o;
+    regions[i].bytes = all[i].b;
+  }
+  return n;
+}
+
+}  // extern "C"

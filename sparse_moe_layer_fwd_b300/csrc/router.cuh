@@ -1,0 +1,169 @@
+// router.cuh -- router affinity and biased top-k ("190行JAX复刻DeepSeek V3",
+// sections "190行代码到底装进了什么" and "最有价值的实验:无辅助损失均衡真的有效").
+//
+// k_router_logits: partial logits part[s][t][e] = sum over the s-th slice of
+//   the model dimension of x[t][i] * W_r[e][i], fp32 FFMA on CUDA cores.
+//   Each output accumulates its slice in one fixed sequential order that does
+//   not depend on e, so two experts with identical router rows get
+//   bit-identical logits (exact ties stay exact).
+// k_router_topk: one warp per token.  u = sum_s part[s] in slice order,
+//   s = 1/(1+exp(-u)), z = s + b.  The k largest z are picked one at a time
+//   by a warp arg-max (larger z wins, equal z -> lower index, NaN ranks
+//   below every number), slots in pick order; gates are the picked unbiased
+//   s divided by their sum (summed in slot order).
+#pragma once
+
+#include "ptx.cuh"
+
+template <typename TX>
+MOE_DEV void load4_as_float(const TX* p, float* out);
+
+template <>
+MOE_DEV void load4_as_float<float>(const float* p, float* out) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+}
+
+template <>
+MOE_DEV void load4_as_float<__nv_bfloat16>(const __nv_bfloat16* p, float* out) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  out[0] = fa.x; out[1] = fa.y; out[2] = fb.x; out[3] = fb.y;
+}
+
+// Block tile BM tokens x BN experts, K step BK; each thread owns TM x TN
+// outputs.  grid = (ceil(E/BN), ceil(T/BM), n_split).
+template <typename TX, int BM, int BN, int BK, int TM, int TN>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+k_router_logits(const TX* __restrict__ x, const float* __restrict__ w, float* __restrict__ part,
+                int T, int E, int d, int kchunk) {
+  constexpr int NT = (BM / TM) * (BN / TN);
+  constexpr int TXN = BN / TN;  // threads along experts
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
+
+  const int tid = threadIdx.x;
+  const int tx = tid % TXN, ty = tid / TXN;
+  const int e0 = blockIdx.x * BN, t0 = blockIdx.y * BM;
+  const int kbeg = blockIdx.z * kchunk;
+  const int kend = min(d, kbeg + kchunk);
+
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+  auto load_tiles = [&](int buf, int k0) {
+    for (int i = tid; i < BM * BK / 4; i += NT) {
+      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t0 + row < T) load4_as_float<TX>(x + (size_t)(t0 + row) * d + k0 + c4, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) As[buf][c4 + q][row] = v[q];
+    }
+    for (int i = tid; i < BN * BK / 4; i += NT) {
+      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (e0 + row < E) load4_as_float<float>(w + (size_t)(e0 + row) * d + k0 + c4, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) Bs[buf][c4 + q][row] = v[q];
+    }
+  };
+
+  int buf = 0;
+  if (kbeg < kend) load_tiles(0, kbeg);
+  __syncthreads();
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    if (k0 + BK < kend) load_tiles(buf ^ 1, k0 + BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; ++i) a[i] = As[buf][kk][ty + i * (BM / TM)];
+#pragma unroll
+      for (int j = 0; j < TN; ++j) b[j] = Bs[buf][kk][tx + j * TXN];
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+  float* out = part + (size_t)blockIdx.z * T * E;
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int t = t0 + ty + i * (BM / TM);
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int e = e0 + tx + j * TXN;
+      if (e < E) out[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+// One warp per token; EPL = experts held per lane (E <= 32 * EPL).
+template <int EPL>
+__global__ void __launch_bounds__(256)
+k_router_topk(const float* __restrict__ part, int n_split, const float* __restrict__ bias,
+              int T, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ gates) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+
+  float key[EPL], sval[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = -INFINITY;
+    sval[i] = 0.f;
+    if (e < E) {
+      float u = 0.f;
+      for (int s = 0; s < n_split; ++s) u += part[((size_t)s * T + t) * E + e];
+      const float sg = 1.0f / (1.0f + expf(-u));
+      const float z = sg + bias[e];
+      sval[i] = sg;
+      key[i] = isnan(z) ? -INFINITY : z;
+    }
+  }
+  uint32_t taken = 0;
+  int my_idx = 0;
+  float my_s = 0.f;
+  float ssum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    // best candidate of this lane
+    float bk = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken >> i & 1u)) {
+        if (key[i] > bk || (key[i] == bk && e < bi)) { bk = key[i]; bi = e; }
+      }
+    }
+    // warp arg-max: larger key, then lower index
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ok > bk || (ok == bk && oi < bi)) { bk = ok; bi = oi; }
+    }
+    const int owner = bi & 31, slot = bi >> 5;
+    float s_win = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (i == slot) s_win = sval[i];
+    s_win = __shfl_sync(0xffffffffu, s_win, owner);
+    if (lane == owner) taken |= 1u << slot;
+    if (lane == j) { my_idx = bi; my_s = s_win; }
+    ssum += s_win;
+  }
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_idx;
+    gates[(size_t)t * k + lane] = my_s / ssum;
+  }
+}

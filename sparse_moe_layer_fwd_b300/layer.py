@@ -1,0 +1,77 @@
+"""Device buffers for one MoE layer and calls through the C ABI.
+
+PyTorch provides the device memory and the stream; every step of the layer
+runs in libmoe.so.  ``MoeLayer`` owns the outputs and the workspace for one
+problem size and re-uses them on every call.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import moe as M
+
+
+class MoeLayer:
+    def __init__(self, w_router, bias, w_gate, w_up, w_down, sh_gate, sh_up, sh_down, *,
+                 T: int, k: int, dtype: str, flags: int = 0, host_io: bool = False):
+        self.E, self.d = w_router.shape
+        self.h = w_gate.shape[1]
+        self.T, self.k, self.dtype, self.flags = T, k, dtype, flags
+        dev = w_router.device
+        self.desc = M.make_desc(T, self.d, self.h, self.E, k, dtype, flags)
+        self.w_router, self.bias = w_router, bias
+        self._keep = (w_gate, w_up, w_down, sh_gate, sh_up, sh_down)
+        self.experts = M.make_experts(w_gate, w_up, w_down)
+        self.shared = M.make_experts(sh_gate, sh_up, sh_down)
+        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.ws_bytes = M.moe_workspace_size(self.desc)
+        if self.ws_bytes == 0:
+            raise M.MoeError(M.ERR_CODE["MOE_ERR_SHAPE"], "moe_workspace_size")
+        if host_io:
+            self.ws_bytes += M.moe_host_io_extra_bytes(self.desc)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        route_only = bool(flags & M.MOE_ROUTE_ONLY)
+        self.y = None if (route_only or host_io) else torch.empty((T, self.d), dtype=tdt, device=dev)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.load_counts = torch.empty((self.E,), dtype=torch.int32, device=dev)
+        self.regions = M.moe_workspace_regions(self.desc)
+
+    @classmethod
+    def from_inputs(cls, inp: dict, k: int, dtype: str, flags: int = 0, T: int | None = None,
+                    host_io: bool = False) -> "MoeLayer":
+        T = inp["x"].shape[0] if T is None else T
+        return cls(inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                   inp["sh_gate"], inp["sh_up"], inp["sh_down"], T=T, k=k, dtype=dtype,
+                   flags=flags, host_io=host_io)
+
+    def forward(self, x, stream=None):
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        M.moe_forward(self.desc, x, self.w_router, self.bias, self.experts, self.shared, self.y,
+                      self.topk_idx, self.gates, self.load_counts, self.workspace, self.ws_bytes,
+                      stream)
+        return self.y
+
+    def forward_host_io(self, x_host, y_host, stream=None):
+        if stream is None:
+            stream = torch.cuda.current_stream(self.workspace.device)
+        M.moe_forward_host_io(self.desc, x_host, self.w_router, self.bias, self.experts,
+                              self.shared, y_host, self.topk_idx, self.gates, self.load_counts,
+                              self.workspace, self.ws_bytes, stream)
+        return y_host
+
+    def bias_update(self, gamma: float = 1e-3, stream=None):
+        if stream is None:
+            stream = torch.cuda.current_stream(self.workspace.device)
+        M.moe_bias_update(self.load_counts, self.bias, gamma, self.E, self.T * self.k, stream)
+
+    def region(self, name: str, dtype: torch.dtype, shape) -> torch.Tensor:
+        """A view of a named workspace region (for inspecting intermediates)."""
+        off, nbytes = self.regions[name]
+        el = torch.empty((), dtype=dtype).element_size()
+        n = 1
+        for s in shape:
+            n *= s
+        assert n * el <= nbytes, (name, shape, nbytes)
+        return self.workspace[off:off + n * el].view(dtype).view(*shape)

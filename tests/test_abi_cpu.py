@@ -1,0 +1,129 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, sizes workspaces, and rejects bad arguments on the host
+before anything is launched (the fake pointers below are never touched)."""
+import ctypes
+import subprocess
+
+import pytest
+import torch
+
+from sparse_moe_layer_fwd_b300 import moe as M
+
+FAKE = 1 << 40  # 16-byte aligned, never dereferenced
+
+
+def test_library_exports_every_header_function():
+    names = M.header_functions()
+    assert set(names) == {
+        "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
+        "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
+        "moe_forward_profiled"}
+    lib = ctypes.CDLL(M.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", M.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(names), exported ^ set(names)
+
+
+def test_error_strings():
+    for code in [0, *M.ERRORS]:
+        assert M.moe_error_string(code) and M.moe_error_string(code) != "unknown error"
+    assert M.moe_error_string(12345) == "unknown error"
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=-1), dict(d=0), dict(h=0), dict(E=0), dict(E=1025), dict(k=0), dict(k=33, E=64),
+    dict(k=9, E=8), dict(d=96), dict(h=100), dict(dtype=7), dict(flags=8),
+])
+def test_invalid_desc_has_no_workspace(bad):
+    kw = dict(T=64, d=256, h=128, E=16, k=4, dtype="f32", flags=0)
+    dtype = kw.pop("dtype")
+    if "dtype" in bad:
+        d = M.MoeDesc(kw["T"], kw["d"], kw["h"], kw["E"], kw["k"], bad["dtype"], 0)
+    else:
+        kw.update({k: v for k, v in bad.items()})
+        d = M.make_desc(kw["T"], kw["d"], kw["h"], kw["E"], kw["k"], dtype, kw["flags"])
+    assert M.moe_workspace_size(d) == 0
+    assert M.moe_host_io_extra_bytes(d) == 0
+    rc = M.moe_forward(d, FAKE, FAKE, FAKE, M.make_experts(FAKE, FAKE, FAKE),
+                       M.make_experts(FAKE, FAKE, FAKE), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40,
+                       check=False)
+    assert rc in (M.ERR_CODE["MOE_ERR_SHAPE"], M.ERR_CODE["MOE_ERR_DTYPE"])
+
+
+def test_tensor_core_path_needs_multiples_of_128():
+    assert M.moe_workspace_size(M.make_desc(64, 192, 128, 8, 2, "bf16")) == 0
+    assert M.moe_workspace_size(M.make_desc(64, 192, 128, 8, 2, "bf16",
+                                            M.MOE_SIMT_EXPERTS)) > 0
+    assert M.moe_workspace_size(M.make_desc(64, 192, 128, 8, 2, "f32")) > 0
+    # the CUDA-core cross-check flag is for bf16 only
+    assert M.moe_workspace_size(M.make_desc(64, 256, 128, 8, 2, "f32", M.MOE_SIMT_EXPERTS)) == 0
+
+
+def _args(desc, **over):
+    a = dict(x=FAKE, w_router=FAKE, bias=FAKE, experts=M.make_experts(FAKE, FAKE, FAKE),
+             shared=M.make_experts(FAKE, FAKE, FAKE), y=FAKE, topk_idx=FAKE, gates=FAKE,
+             load_counts=FAKE, workspace=FAKE, ws_bytes=M.moe_workspace_size(desc))
+    a.update(over)
+    return a
+
+
+def _call(desc, **over):
+    a = _args(desc, **over)
+    return M.moe_forward(desc, a["x"], a["w_router"], a["bias"], a["experts"], a["shared"],
+                         a["y"], a["topk_idx"], a["gates"], a["load_counts"], a["workspace"],
+                         a["ws_bytes"], check=False)
+
+
+def test_argument_errors_are_found_on_the_host():
+    d = M.make_desc(64, 256, 128, 16, 4, "bf16")
+    E = M.ERR_CODE
+    assert _call(d, x=None) == E["MOE_ERR_NULL"]
+    assert _call(d, y=None) == E["MOE_ERR_NULL"]
+    assert _call(d, workspace=None) == E["MOE_ERR_NULL"]
+    assert _call(d, experts=M.make_experts(FAKE, None, FAKE)) == E["MOE_ERR_NULL"]
+    assert _call(d, experts=None) == E["MOE_ERR_NULL"]
+    assert _call(d, x=FAKE + 8) == E["MOE_ERR_ALIGN"]
+    assert _call(d, shared=M.make_experts(FAKE, FAKE, FAKE + 2)) == E["MOE_ERR_ALIGN"]
+    assert _call(d, ws_bytes=M.moe_workspace_size(d) - 1) == E["MOE_ERR_WORKSPACE"]
+    # route-only needs neither y nor expert weights
+    r = M.make_desc(64, 256, 128, 16, 4, "bf16", M.MOE_ROUTE_ONLY)
+    rc = _call(r, y=None, experts=None, shared=None)
+    assert rc != E["MOE_ERR_NULL"]
+    # bias update arguments
+    assert M.moe_bias_update(None, FAKE, 1e-3, 16, 64, check=False) == E["MOE_ERR_NULL"]
+    assert M.moe_bias_update(FAKE, FAKE, 1e-3, 0, 64, check=False) == E["MOE_ERR_SHAPE"]
+    assert M.moe_bias_update(FAKE, FAKE, 1e-3, 16, -1, check=False) == E["MOE_ERR_SHAPE"]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_valid_call_without_gpu_reports_device_error():
+    d = M.make_desc(64, 256, 128, 16, 4, "f32")
+    assert _call(d) == M.ERR_CODE["MOE_ERR_DEVICE"]
+    assert M.moe_bias_update(FAKE, FAKE, 1e-3, 16, 64, check=False) == M.ERR_CODE["MOE_ERR_DEVICE"]
+
+
+@pytest.mark.parametrize("shape", [
+    (256, 256, 128, 16, 4, "f32"), (8192, 384, 384, 16, 4, "bf16"),
+    (8192, 7168, 2048, 256, 8, "bf16"), (128, 7168, 2048, 256, 8, "bf16"), (0, 256, 128, 16, 4, "bf16"),
+    (1, 128, 128, 1, 1, "bf16"),
+])
+def test_workspace_regions_are_disjoint_and_aligned(shape):
+    T, d, h, E, k, dt = shape
+    desc = M.make_desc(T, d, h, E, k, dt)
+    total = M.moe_workspace_size(desc)
+    regs = M.moe_workspace_regions(desc)
+    assert total > 0 and len(regs) == 10
+    spans = sorted(regs.values())
+    for (o1, b1), (o2, _) in zip(spans, spans[1:]):
+        assert o1 % 256 == 0 and o1 + b1 <= o2
+    assert spans[-1][0] + spans[-1][1] <= total
+    el = 4 if dt == "f32" else 2
+    assert regs["x_perm"][1] == T * k * d * el
+    assert regs["h"][1] == (T * k + T) * h * el
+    assert regs["y_shared"][1] == T * d * 4
+    ro = M.make_desc(T, d, h, E, k, dt, M.MOE_ROUTE_ONLY)
+    assert M.moe_workspace_size(ro) <= total and len(M.moe_workspace_regions(ro)) == 4
+    assert M.moe_host_io_extra_bytes(desc) >= 2 * T * d * el

@@ -1,0 +1,77 @@
+"""DeepSeek-V3-sized MoE layer vs the float64 oracle, at full size and in the
+launch configuration bench.py times.
+
+Prefill (T = 8192, d = 7168, h = 2048, E = 256, k = 8): routing, load counts
+and the updated bias are checked on every token; outputs on 512 seeded rows,
+which the oracle computes by streaming one expert at a time from device
+memory.  Decode (T = 128), balanced and Zipf(1.2)-skewed: everything on all
+rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from sparse_moe_layer_fwd_b300 import inputs as I
+from sparse_moe_layer_fwd_b300 import moe as M
+from sparse_moe_layer_fwd_b300.layer import MoeLayer
+from tests.parity import check_load, check_output, check_routing, np64, npi
+
+pytestmark = pytest.mark.gpu
+GAMMA = 1e-3
+
+
+def _expert_fetcher(inp):
+    def get(e):
+        return (np64(inp["w_gate"][e]), np64(inp["w_up"][e]), np64(inp["w_down"][e]))
+    return get
+
+
+def _check_v3(name, n_rows):
+    wl = I.WORKLOADS[name]
+    inp = I.make_inputs(wl, device="cuda")
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype)
+    y = layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert M.moe_last_error() == M.MOE_OK
+    x64, wr64, b64 = np64(inp["x"]), np64(inp["w_router"]), np64(inp["bias"])
+    ref = O.route(x64, wr64, b64, wl.k)
+    gidx = npi(layer.topk_idx)
+    flips = check_routing(gidx, layer.gates.cpu().numpy().astype(np.float64), ref, 1e-5)
+    gload = npi(layer.load_counts)
+    check_load(gload, gidx, ref["idx"], wl.E, flips)
+    if n_rows < wl.T:
+        rows = np.sort(np.random.default_rng(wl.seed).choice(wl.T, n_rows, replace=False))
+    else:
+        rows = np.arange(wl.T)
+    sh = (np64(inp["sh_gate"]), np64(inp["sh_up"]), np64(inp["sh_down"]))
+    g_rows = O.gate_weights(ref["s"][rows], gidx[rows])
+    y_ref = O.expert_output_rows(x64[rows], gidx[rows], g_rows, _expert_fetcher(inp), sh)
+    stats = check_output(np64(y[torch.from_numpy(rows).cuda()]), y_ref, wl.dtype)
+    b_before = inp["bias"].cpu().numpy().copy()
+    layer.bias_update(GAMMA)
+    torch.cuda.synchronize()
+    assert np.array_equal(inp["bias"].cpu().numpy(),
+                          O.bias_update(b_before, gload, GAMMA, wl.T * wl.k))
+    touched = int((gload > 0).sum())
+    del layer, inp, y
+    torch.cuda.empty_cache()
+    return stats, flips, touched
+
+
+def test_v3_prefill_full_size():
+    stats, flips, touched = _check_v3("v3_prefill", 512)
+    print(f"v3_prefill: {stats} flips={flips} touched={touched}")
+    assert touched == 256
+
+
+def test_v3_decode_balanced():
+    stats, flips, touched = _check_v3("v3_decode", 128)
+    print(f"v3_decode: {stats} flips={flips} touched={touched}")
+
+
+def test_v3_decode_zipf_skew():
+    stats, flips, touched = _check_v3("v3_decode_zipf", 128)
+    print(f"v3_decode_zipf: {stats} flips={flips} touched={touched}")
+    # the skew concentrates routing on fewer experts than the balanced run
+    assert touched < 200
