@@ -132,6 +132,17 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate(elapsed_ms: float, tokens_per_rank: int, world_size: int, device="cpu"):
+    """Whole-job throughput of independent replicas: the slowest rank's time
+    (max over ranks) and all ranks' tokens.  Returns (max_ms, tokens/s)."""
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    return max_ms, world_size * tokens_per_rank / (max_ms / 1e3)
+
+
 def _algorithmic(wl, load):
     """FLOPs and bytes of the two expert GEMMs for one launch each."""
     TK, T, d, h = wl.T * wl.k, wl.T, wl.d, wl.h
@@ -223,6 +234,10 @@ def run_ours(args, wl):
     # timed region: per-step phase events on the launching stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(M.N_PHASE_EVENTS)]
           for _ in range(args.steps)]
+    for row in ev:  # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -240,12 +255,7 @@ def run_ours(args, wl):
     clocks = sampler.stop(t_host0, t_host1) if sampler else None
     if M.moe_last_error() != M.MOE_OK:
         raise RuntimeError("device error word set during the timed region")
-    elapsed_ms = start.elapsed_time(end)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, value = aggregate(start.elapsed_time(end), wl.T * args.steps, ws, "cuda")
     phase_ms = np.zeros(len(M.PHASES))
     for i in range(args.steps):
         for p in range(len(M.PHASES)):
@@ -268,14 +278,9 @@ def run_ours(args, wl):
             hl.forward_host_io(x_host, y_host, stream)
         e2.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = s2.elapsed_time(e2)
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms, e2e_value = aggregate(s2.elapsed_time(e2), wl.T * args.steps, ws, "cuda")
         nb = x_host.numel() * x_host.element_size()
-        e2e = {"value": ws * wl.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": e2e_value, "unit": "tokens/s",
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb,
                "ms_per_step": e2e_ms / args.steps}
         del hl
@@ -326,7 +331,6 @@ def run_ours(args, wl):
                "sample": f"{n} tokens of {wl.name}: float64 routing, shared expert and "
                          f"{wl.k} routed experts per token, weights streamed from device memory"}
 
-    value = ws * wl.T * args.steps / (elapsed_ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
