@@ -196,6 +196,38 @@ typedef struct {
 } moe_region;
 MOE_API int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap);
 
+/* Routing without any device allocation.  The pages have no counterpart to
+ * this entry point: it exists for callers that must not allocate device
+ * memory and cannot hand the library a workspace -- for example a plugin
+ * whose host framework owns every byte of device memory, or a runtime with
+ * a fixed memory budget that forbids allocation once it has started.
+ *
+ * It computes what moe_forward computes with MOE_ROUTE_ONLY (router
+ * affinities, biased top-k, gates, load counts; desc->flags is ignored and
+ * the route-only pass is run), with the same kernels, so its outputs are
+ * identical to that call's.  Its scratch is a static device array of
+ * MOE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits; the caller passes only inputs and outputs (all device
+ * pointers, as in moe_forward).
+ *
+ *   - A desc whose route-only scratch (moe_workspace_size of the desc with
+ *     MOE_ROUTE_ONLY) exceeds MOE_STATIC_SCRATCH_BYTES is rejected with
+ *     MOE_ERR_WORKSPACE before anything is launched.  32 MiB covers, e.g.,
+ *     T = 8192 tokens with E = 256 experts and d = 7168.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array, which keeps the previous call's
+ *     contents.  Nothing in it needs to start at zero: each call writes
+ *     every scratch byte it reads before reading it.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on the
+ *     array: order them on one stream or synchronise between them. */
+#define MOE_STATIC_SCRATCH_BYTES (32u << 20)
+MOE_API int moe_route_noalloc(const moe_desc* desc, const void* x,
+                              const float* w_router, const float* bias,
+                              int32_t* topk_idx, float* gates,
+                              int32_t* load_counts, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -487,4 +487,51 @@ int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
   return n;
 }
 
+// ---- routing with static scratch (no allocation, no caller workspace) ----
+// File-scope device array: the scratch of moe_route_noalloc.  Host code must
+// not pass its name to a kernel (on the host it is only a stand-in for the
+// symbol); the device address is looked up once per device below.
+static __device__ __align__(256) unsigned char g_route_scratch[MOE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_route_scratch on the current device (looked up on the
+// first call per device, with that device current).
+void* route_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = ptr;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+int moe_route_noalloc(const moe_desc* desc, const void* x, const float* w_router,
+                      const float* bias, int32_t* topk_idx, float* gates, int32_t* load_counts,
+                      void* stream) {
+  if (!desc) return MOE_ERR_NULL;
+  moe_desc d = *desc;
+  d.flags = MOE_ROUTE_ONLY;
+  const int rc = validate_desc(&d);
+  if (rc != MOE_OK) return rc;
+  const size_t need = make_plan(&d).total;
+  if (need > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  const int dev_rc = device_ok();
+  if (dev_rc != MOE_OK) return dev_rc;
+  void* scratch = route_scratch_address();
+  if (!scratch) return MOE_ERR_DEVICE;
+  return forward_impl(&d, x, w_router, bias, nullptr, nullptr, nullptr, topk_idx, gates,
+                      load_counts, scratch, MOE_STATIC_SCRATCH_BYTES,
+                      static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -21,6 +21,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS = 1, 2
 MOE_OK = 0
+MOE_STATIC_SCRATCH_BYTES = 32 << 20
 ERRORS = {
     -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGN", -4: "MOE_ERR_WORKSPACE",
     -5: "MOE_ERR_DTYPE", -6: "MOE_ERR_LAUNCH", -7: "MOE_ERR_DEVICE_TIMEOUT", -8: "MOE_ERR_DEVICE",
@@ -70,6 +71,8 @@ def _load():
     lib.moe_error_string.argtypes, lib.moe_error_string.restype = [I], ctypes.c_char_p
     lib.moe_workspace_regions.argtypes = [dp, ctypes.POINTER(MoeRegion), I]
     lib.moe_workspace_regions.restype = I
+    lib.moe_route_noalloc.argtypes = [dp, P, P, P, P, P, P, P]
+    lib.moe_route_noalloc.restype = I
     del U
     return lib
 
@@ -184,3 +187,16 @@ def moe_workspace_regions(desc: MoeDesc) -> dict:
     if n < 0:
         raise MoeError(n, "moe_workspace_regions")
     return {regs[i].name.decode(): (int(regs[i].offset), int(regs[i].bytes)) for i in range(n)}
+
+
+def moe_route_noalloc(desc, x, w_router, bias, topk_idx, gates, load_counts, stream=None,
+                      check=True) -> int:
+    """Route-only pass (router, top-k, gates, load counts) whose scratch is
+    the library's static device array, for callers that must not allocate
+    device memory or hand over a workspace.  Same outputs as moe_forward with
+    MOE_ROUTE_ONLY; descs needing more than MOE_STATIC_SCRATCH_BYTES of
+    scratch are rejected (MOE_ERR_WORKSPACE).  Calls share the array: do not
+    let two of them overlap on the GPU."""
+    rc = _lib.moe_route_noalloc(ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(bias),
+                                _ptr(topk_idx), _ptr(gates), _ptr(load_counts), _stream(stream))
+    return _check(rc, "moe_route_noalloc") if check else rc

@@ -17,7 +17,7 @@ def test_library_exports_every_header_function():
     assert set(names) == {
         "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
-        "moe_forward_profiled"}
+        "moe_forward_profiled", "moe_route_noalloc"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
