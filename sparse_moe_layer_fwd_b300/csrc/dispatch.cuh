@@ -96,8 +96,9 @@ __device__ int cta_exclusive_scan(int* data, int n, int* warp_tot) {
 //   tsz[E+1]     rows per token tile (multiple of 16, <= bn)
 //   toff_a[E+2]  prefix sum of ntt[g] * ft_a (tiles of the first GEMM)
 //   toff_b[E+2]  prefix sum of ntt[g] * ft_b (tiles of the second GEMM)
+//   next[2]      tile counters of the two GEMMs' schedulers, zeroed here
 struct GroupTable {
-  int32_t *off, *ntt, *tsz, *toff_a, *toff_b;
+  int32_t *off, *ntt, *tsz, *toff_a, *toff_b, *next;
 };
 
 MOE_DEV GroupTable group_table(int32_t* base, int E) {
@@ -107,6 +108,7 @@ MOE_DEV GroupTable group_table(int32_t* base, int E) {
   g.tsz = g.ntt + (E + 1);
   g.toff_a = g.tsz + (E + 1);
   g.toff_b = g.toff_a + (E + 2);
+  g.next = g.toff_b + (E + 2);
   return g;
 }
 
@@ -164,7 +166,11 @@ k_scan_groups(int32_t* __restrict__ blk_hist, int n_blocks, int E, int T, int TK
   __syncthreads();
   tot = cta_exclusive_scan(buf, E + 1, warp_tot);
   for (int g = tid; g <= E; g += blockDim.x) G.toff_b[g] = buf[g];
-  if (tid == 0) G.toff_b[E + 1] = tot;
+  if (tid == 0) {
+    G.toff_b[E + 1] = tot;
+    G.next[0] = 0;
+    G.next[1] = 0;
+  }
 }
 
 // One warp per pair; row_bytes a multiple of 16.

@@ -13,69 +13,220 @@
 // where 128-token M tiles would waste ~25%; in decode (about 4 tokens per
 // expert) the same kernel streams each weight tile once with N = 16.
 //
-// Each CTA owns one tile and two fp32 TMEM accumulators of BN columns each:
+// Each tile has two fp32 TMEM accumulators of BN columns:
 //   first GEMM (DOWN = false): acc0 = W_gate rows f0..f0+127, acc1 = W_up rows
 //       f0..f0+127 (same B tile) -> H[row, f] = bf16(silu(acc0) * acc1)
 //   second GEMM (DOWN = true): acc0 / acc1 = W_down rows f0..+127 / f0+128..+255
 //       -> routed: Y_perm[row, f] = bf16(g(row) * acc); shared: Y_sh[t, f] = acc
-// Both GEMMs therefore read 2 A sub-tiles (2 x 16 KB) per B tile (N x 128 B)
-// per 64-deep K step.
 //
-// Warp roles (192 threads): warp 0 = TMA producer (one lane), warp 1 = TMEM
-// allocator + MMA issuer (one lane), warps 2-5 = epilogue (TMEM -> registers
-// -> global; warp w reads TMEM lanes 32*(w%4)..+31).  A STAGES-deep ring of
-// shared-memory stages, each with a "full" mbarrier (TMA transaction bytes)
-// and an "empty" mbarrier (tcgen05.commit from the MMA lane).  Operands are
-// K-major with the 128-byte swizzle.  Weights are loaded with an L2
-// evict-first hint (each weight tile is read by one CTA, or by the CTAs of
-// one expert's token tiles that run side by side), token rows with
-// evict-last (re-read by every output tile of the group).
+// Pipeline: K steps of 64 elements (128-byte rows, 128-byte swizzle).  The
+// weights (A: 2 x 16 KB per step, streamed from DRAM, long latency) and the
+// token rows (B: N x 128 B per step, re-read by every output tile of the
+// group, mostly L2 hits) have separate shared-memory rings fed by separate
+// producer warps, so the weight ring can run deeper than the token ring in
+// the same shared memory.  Each ring slot has a "full" mbarrier (TMA
+// transaction bytes) and an "empty" mbarrier (tcgen05.commit of the MMAs
+// that read it).
 //
-// Every wait is bounded (ptx.cuh); on a timeout the CTA drains its copies in
-// flight with bounded waits, frees its TMEM and returns, leaving the device
-// error word set.  Later CTAs see the word and return at once.
+// Persistent, in order: one CTA per SM; warp 0's lane takes tiles from a
+// global counter (zeroed by the scan kernel) in table order, so the tiles in
+// flight across the GPU are always a contiguous window of the table -- the
+// token tiles of one expert run side by side and share each weight tile
+// through L2.  The tile index goes to the other roles through a small ring
+// of (tile id, full, empty) slots in shared memory.
+//
+// Warp roles (352 threads): warp 0 = tile scheduler + weight producer,
+// warp 1 = TMEM allocator + MMA issuer, warps 2-9 = epilogue (TMEM ->
+// registers -> global; warp w reads TMEM lanes 32*(w%4)..+31, half of the
+// token columns each), warp 10 = token-row producer.  The epilogue writes
+// whole 16-byte row segments: an 8 x 8 shuffle transpose per group of 8
+// lanes turns the accumulator's one-output-row-per-lane layout into 8
+// consecutive outputs of one token per lane.  The MMA lane starts a tile once the epilogue has
+// drained the previous tile's accumulators ("acc_empty", one arrive per
+// epilogue warp) and hands the tile over with "acc_full"; the producers keep
+// filling their rings meanwhile.
+//
+// Every wait is bounded (ptx.cuh).  On a timeout the role stops, the CTA
+// drains its copies and MMAs in flight with bounded waits, frees its TMEM
+// and returns, leaving the device error word set.
 #pragma once
 
 #include "experts_simt.cuh"
 
 #define TC_BM 128
 #define TC_BK 64
-#define TC_THREADS 192
+#define TC_EPI_WARPS 8                         // two per TMEM lane quarter
+#define TC_THREADS (32 * (3 + TC_EPI_WARPS))  // scheduler/weights, MMA, epilogue, tokens
+#define TC_TOKEN_WARP (2 + TC_EPI_WARPS)
+#define TC_TILE_RING 8
 
-template <int BN, int STAGES>
+// silu(z) = z * sigmoid(z) with the fast exponential and division: their
+// relative error (~1e-6) is far below the bf16 rounding of the stored H.
+MOE_DEV float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// 8 x 8 transpose of 16-bit values inside each group of 8 consecutive lanes:
+// lane i of a group holds row i (positions p = 0..7, w[m] = p 2m | p 2m+1 <<
+// 16) and ends up holding column i, packed the same way.  Three butterfly
+// stages exchange, with lane i ^ k, the values whose position bit k differs
+// from lane bit k (k = 4, 2, 1); six shuffles in all.
+MOE_DEV void transpose8x8_b16(uint32_t (&w)[4], int lane) {
+  const uint32_t F = 0xffffffffu;
+  {
+    const bool hi = lane & 4;
+    const uint32_t r0 = __shfl_xor_sync(F, hi ? w[0] : w[2], 4);
+    const uint32_t r1 = __shfl_xor_sync(F, hi ? w[1] : w[3], 4);
+    if (hi) { w[0] = r0; w[1] = r1; } else { w[2] = r0; w[3] = r1; }
+  }
+  {
+    const bool hi = lane & 2;
+    const uint32_t r0 = __shfl_xor_sync(F, hi ? w[0] : w[1], 2);
+    const uint32_t r1 = __shfl_xor_sync(F, hi ? w[2] : w[3], 2);
+    if (hi) { w[0] = r0; w[2] = r1; } else { w[1] = r0; w[3] = r1; }
+  }
+  {
+    const bool hi = lane & 1;
+    const uint32_t s0 = hi ? __byte_perm(w[0], w[1], 0x5410) : __byte_perm(w[0], w[1], 0x7632);
+    const uint32_t s1 = hi ? __byte_perm(w[2], w[3], 0x5410) : __byte_perm(w[2], w[3], 0x7632);
+    const uint32_t r0 = __shfl_xor_sync(F, s0, 1), r1 = __shfl_xor_sync(F, s1, 1);
+    if (hi) {
+      w[0] = __byte_perm(r0, w[0], 0x7610);
+      w[1] = __byte_perm(r0, w[1], 0x7632);
+      w[2] = __byte_perm(r1, w[2], 0x7610);
+      w[3] = __byte_perm(r1, w[3], 0x7632);
+    } else {
+      w[0] = __byte_perm(w[0], r0, 0x5410);
+      w[1] = __byte_perm(w[1], r0, 0x7610);
+      w[2] = __byte_perm(w[2], r1, 0x5410);
+      w[3] = __byte_perm(w[3], r1, 0x7610);
+    }
+  }
+}
+
+// 4 x 4 transpose of 32-bit values inside each group of 4 consecutive lanes
+// (lane i: row i in f[0..3] -> column i), two butterfly stages.
+MOE_DEV void transpose4x4_f32(float (&f)[4], int lane) {
+  const uint32_t F = 0xffffffffu;
+  {
+    const bool hi = lane & 2;
+    const float r0 = __shfl_xor_sync(F, hi ? f[0] : f[2], 2);
+    const float r1 = __shfl_xor_sync(F, hi ? f[1] : f[3], 2);
+    if (hi) { f[0] = r0; f[1] = r1; } else { f[2] = r0; f[3] = r1; }
+  }
+  {
+    const bool hi = lane & 1;
+    const float r0 = __shfl_xor_sync(F, hi ? f[0] : f[1], 1);
+    const float r1 = __shfl_xor_sync(F, hi ? f[2] : f[3], 1);
+    if (hi) { f[0] = r0; f[2] = r1; } else { f[1] = r0; f[3] = r1; }
+  }
+}
+
+MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Store 32 values of this lane's output row (one per token c0 + j) for the
+// warp's 32 consecutive output rows as 16-byte vectors: 8 outputs of one
+// token per lane after an 8 x 8 transpose per group of 8 lanes.
+// dst = &out[token c0][first output of the warp]; tokens >= ntok are skipped.
+MOE_DEV void store_rows_bf16(__nv_bfloat16* dst, size_t ld, const float (&v)[32], int c0,
+                             int ntok, int lane) {
+  const int grp = lane >> 3, u = lane & 7;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    uint32_t w[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) w[m] = pack_bf16x2(v[8 * r + 2 * m], v[8 * r + 2 * m + 1]);
+    transpose8x8_b16(w, lane);
+    const int tok = 8 * r + u;
+    if (c0 + tok < ntok)
+      *reinterpret_cast<uint4*>(dst + (size_t)tok * ld + 8 * grp) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// The same for fp32 outputs: 4 outputs of one token per lane (4 x 4 transpose).
+MOE_DEV void store_rows_f32(float* dst, size_t ld, const float (&v)[32], int c0, int ntok,
+                            int lane) {
+  const int grp = lane >> 2, u = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    float f[4] = {v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]};
+    transpose4x4_f32(f, lane);
+    const int tok = 4 * r + u;
+    if (c0 + tok < ntok)
+      *reinterpret_cast<float4*>(dst + (size_t)tok * ld + 4 * grp) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+}
+
+template <int BN, int SA, int SB>
 struct TcCfg {
-  static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
-  static constexpr int B_BYTES = BN * TC_BK * 2;     // BN * 128 B
-  static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 1) + 16;
-  static constexpr int GATE_OFF = BAR_OFF + ((BAR_BYTES + 127) / 128) * 128;
-  static constexpr int SMEM_BYTES = GATE_OFF + BN * 4 + 1024;  // + 1024 for base alignment
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile
+  static constexpr int A_STAGE = 2 * A_BYTES;        // both sub-tiles
+  static constexpr int B_STAGE = BN * TC_BK * 2;     // BN rows of 128 B
+  static constexpr int B_OFF = SA * A_STAGE;
+  static constexpr int BAR_OFF = B_OFF + SB * B_STAGE;
+  // a_full[SA], a_empty[SA], b_full[SB], b_empty[SB], acc_full, acc_empty,
+  // drain, tile_full[RING], tile_empty[RING]
+  static constexpr int N_BARS = 2 * SA + 2 * SB + 3 + 2 * TC_TILE_RING;
+  // then: tile ids [RING], tmem slot, abort flag, 3 progress counters
+  static constexpr int MISC_BYTES = 4 * TC_TILE_RING + 4 * 5;
+  static constexpr int SMEM_BYTES = BAR_OFF + 8 * N_BARS + MISC_BYTES + 1024;  // + base alignment
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(SMEM_BYTES + 64 <= 232448, "shared memory");
   static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the TMEM allocation assumes it");
 };
 
-template <int BN, int STAGES, bool DOWN>
+// Geometry of one tile, computed identically by every role.
+struct TcTile {
+  bool shared, has_a1;
+  int ntok, npad, tok0, f0, row_a0, row_a1, row_b, out_row0;
+};
+
+template <bool DOWN>
+MOE_DEV TcTile tc_tile(const GroupTable& G, const int32_t* toff, int E, int b, int n_out) {
+  TcTile t;
+  const int g = find_group(toff, E, b);
+  t.shared = g == E;
+  const int nt = G.ntt[g];
+  const int local = b - toff[g];
+  const int ft = local / nt, tt = local % nt;
+  const int n_g = G.off[g + 1] - G.off[g];
+  const int tsz = G.tsz[g];
+  t.tok0 = tt * tsz;
+  t.ntok = min(tsz, n_g - t.tok0);
+  t.npad = (t.ntok + 15) & ~15;
+  t.f0 = ft * (DOWN ? 2 * TC_BM : TC_BM);
+  t.has_a1 = DOWN ? (t.f0 + TC_BM < n_out) : true;
+  t.row_a0 = (t.shared ? 0 : g * n_out) + t.f0;
+  t.row_a1 = DOWN ? t.row_a0 + TC_BM : t.row_a0;
+  t.row_b = (!DOWN && t.shared) ? t.tok0 : G.off[g] + t.tok0;
+  t.out_row0 = G.off[g] + t.tok0;  // H row (first GEMM) / Y_perm row (routed, second)
+  return t;
+}
+
+struct TcMapsDev {
+  CUtensorMap a0, a1, sa0, sa1;   // weights, 128-row boxes (routed, shared)
+  CUtensorMap b128, b64, b16;     // token rows of the routed groups
+  CUtensorMap bs128, bs64, bs16;  // token rows of the shared group
+};
+
+template <int BN, int SA, int SB, bool DOWN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-k_expert_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-            const __grid_constant__ CUtensorMap tm_sa0, const __grid_constant__ CUtensorMap tm_sa1,
-            const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_bs,
-            const int32_t* __restrict__ groups, int E, int K, int n_out,
-            __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
+k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
+            int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
             const int32_t* __restrict__ perm, const float* __restrict__ gates) {
-  using C = TcCfg<BN, STAGES>;
+  using C = TcCfg<BN, SA, SB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- tile of this CTA (uniform across the CTA) ----
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
   const int32_t* toff = DOWN ? G.toff_b : G.toff_a;
-  const int b = blockIdx.x;
-  if (b >= toff[E + 1]) return;
+  int* counter = G.next + (DOWN ? 1 : 0);
+  const int total = toff[E + 1];
+  if ((int)blockIdx.x >= total) return;
   {
     // a CTA-uniform decision: one thread reads the error word
     __shared__ int s_skip;
@@ -83,49 +234,43 @@ k_expert_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ C
     __syncthreads();
     if (s_skip) return;
   }
-  const int g = find_group(toff, E, b);
-  const bool shared = g == E;
-  const int nt = G.ntt[g];
-  const int local = b - toff[g];
-  const int ft = local / nt, tt = local % nt;
-  const int n_g = G.off[g + 1] - G.off[g];
-  const int tsz = G.tsz[g];
-  const int tok0 = tt * tsz;
-  const int ntok = min(tsz, n_g - tok0);
-  const int npad = (ntok + 15) & ~15;
-  const int f0 = ft * (DOWN ? 2 * TC_BM : TC_BM);
-  const bool has_a1 = DOWN ? (f0 + TC_BM < n_out) : true;
-  const int row_a0 = (shared ? 0 : g * n_out) + f0;
-  const int row_a1 = DOWN ? row_a0 + TC_BM : row_a0;
-  const int row_b = (!DOWN && shared) ? tok0 : G.off[g] + tok0;
-  const CUtensorMap* mA0 = shared ? &tm_sa0 : &tm_a0;
-  const CUtensorMap* mA1 = DOWN ? mA0 : (shared ? &tm_sa1 : &tm_a1);
-  const CUtensorMap* mB = (!DOWN && shared) ? &tm_bs : &tm_b;
 
   uint8_t* bar_base = smem + C::BAR_OFF;
-  auto full_bar = [&](int s) { return smem_u32(bar_base + 8 * s); };
-  auto empty_bar = [&](int s) { return smem_u32(bar_base + 8 * (STAGES + s)); };
-  const uint32_t acc_bar = smem_u32(bar_base + 8 * (2 * STAGES));
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_base + 8 * (2 * STAGES + 1));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + 8 * (2 * STAGES + 1) + 4);
-  volatile int* progress = reinterpret_cast<volatile int*>(bar_base + 8 * (2 * STAGES + 1) + 8);
-  float* gate_s = reinterpret_cast<float*>(smem + C::GATE_OFF);
+  auto bar = [&](int i) { return smem_u32(bar_base + 8 * i); };
+  auto a_full = [&](int s) { return bar(s); };
+  auto a_empty = [&](int s) { return bar(SA + s); };
+  auto b_full = [&](int s) { return bar(2 * SA + s); };
+  auto b_empty = [&](int s) { return bar(2 * SA + SB + s); };
+  const uint32_t acc_full = bar(2 * SA + 2 * SB), acc_empty = bar(2 * SA + 2 * SB + 1);
+  const uint32_t drain_bar = bar(2 * SA + 2 * SB + 2);
+  auto tile_full = [&](int s) { return bar(2 * SA + 2 * SB + 3 + s); };
+  auto tile_empty = [&](int s) { return bar(2 * SA + 2 * SB + 3 + TC_TILE_RING + s); };
+  uint8_t* misc = bar_base + 8 * C::N_BARS;
+  volatile int* tile_id = reinterpret_cast<volatile int*>(misc);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc + 4 * TC_TILE_RING);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4 * TC_TILE_RING + 4);
+  // k-steps issued by the weight producer, by the token producer, consumed by the MMA
+  volatile int* progress = reinterpret_cast<volatile int*>(misc + 4 * TC_TILE_RING + 8);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(a_empty(s), 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(b_full(s), 1);
+      mbar_init(b_empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, TC_EPI_WARPS);  // one arrive per epilogue warp
+    mbar_init(drain_bar, 1);
+    for (int s = 0; s < TC_TILE_RING; ++s) {
+      mbar_init(tile_full(s), 1);
+      mbar_init(tile_empty(s), TC_EPI_WARPS + 2);  // MMA lane, epilogue warps, token producer
+    }
     *abort_flag = 0;
-    progress[0] = 0;  // k-blocks issued by the producer
-    progress[1] = 0;  // k-blocks consumed by the MMA lane
+    progress[0] = progress[1] = progress[2] = 0;
     fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(mA0);
-    prefetch_tensormap(mA1);
-    prefetch_tensormap(mB);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
@@ -136,95 +281,190 @@ k_expert_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nkb = K / TC_BK;
-  bool mma_committed = false;
+  bool mma_issued = false;
+
+  // Tile i of this CTA for a consumer role (-1: no more tiles).  Waits for
+  // the scheduler to publish slot i and reads it; `arrive` releases the slot.
+  auto next_tile = [&](int i, bool arrive) -> int {
+    const int s = i % TC_TILE_RING;
+    if (!mbar_wait(tile_full(s), (i / TC_TILE_RING) & 1)) {
+      *abort_flag = 1;
+      return -1;
+    }
+    const int b = tile_id[s];
+    if (arrive) mbar_arrive(tile_empty(s));
+    return b;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
+      // ------------- tile scheduler + weight (A) producer -------------
       const uint64_t pol_w = l2_policy_evict_first();
+      int it = 0;
+      for (int i = 0;; ++i) {
+        const int s = i % TC_TILE_RING;
+        if (i >= TC_TILE_RING && !mbar_wait(tile_empty(s), ((i / TC_TILE_RING) & 1) ^ 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        int b = *abort_flag ? total : atomicAdd(counter, 1);
+        if (b >= total) b = -1;
+        tile_id[s] = b;
+        mbar_arrive(tile_full(s));
+        if (b < 0) break;
+        const TcTile t = tc_tile<DOWN>(G, toff, E, b, n_out);
+        const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
+        const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
+        const uint32_t bytes = (t.has_a1 ? 2u : 1u) * C::A_BYTES;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sa = it % SA, r = it / SA;
+          if (it >= SA && !mbar_wait(a_empty(sa), (r & 1) ^ 1)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st = smem + sa * C::A_STAGE;
+          const uint32_t fb = a_full(sa);
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_2d(smem_u32(st), mA0, fb, kb * TC_BK, t.row_a0, pol_w);
+          if (t.has_a1) tma_load_2d(smem_u32(st + C::A_BYTES), mA1, fb, kb * TC_BK, t.row_a1, pol_w);
+          progress[0] = it + 1;
+        }
+        // after an abort the next published tile is "none" (b = -1 above)
+      }
+    }
+  } else if (warp == TC_TOKEN_WARP) {
+    if (lane == 0) {
+      // ------------- token-row (B) producer -------------
       const uint64_t pol_x = l2_policy_evict_last();
-      const uint32_t bytes = (has_a1 ? 2u : 1u) * C::A_BYTES + (uint32_t)npad * (TC_BK * 2);
-      int kb = 0;
-      for (; kb < nkb; ++kb) {
-        const int s = kb % STAGES, r = kb / STAGES;
-        if (kb >= STAGES && !mbar_wait(empty_bar(s), (r & 1) ^ 1)) { *abort_flag = 1; break; }
-        uint8_t* st = smem + s * C::STAGE_BYTES;
-        const uint32_t fb = full_bar(s);
-        mbar_arrive_expect_tx(fb, bytes);
-        tma_load_2d(smem_u32(st), mA0, fb, kb * TC_BK, row_a0, pol_w);
-        if (has_a1) tma_load_2d(smem_u32(st + C::A_BYTES), mA1, fb, kb * TC_BK, row_a1, pol_w);
-        uint8_t* sb = st + 2 * C::A_BYTES;
-        for (int i = 0; i < npad; i += 16)
-          tma_load_2d(smem_u32(sb + i * (TC_BK * 2)), mB, fb, kb * TC_BK, row_b + i, pol_x);
-        progress[0] = kb + 1;
-        if (*abort_flag) { ++kb; break; }
+      int it = 0;
+      for (int i = 0;; ++i) {
+        const int b = next_tile(i, true);
+        if (b < 0) break;
+        const TcTile t = tc_tile<DOWN>(G, toff, E, b, n_out);
+        const bool bs = !DOWN && t.shared;
+        const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
+        const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
+        const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
+        const uint32_t bytes = (uint32_t)t.npad * (TC_BK * 2);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sb = it % SB, r = it / SB;
+          if (*abort_flag || (it >= SB && !mbar_wait(b_empty(sb), (r & 1) ^ 1))) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st = smem + C::B_OFF + sb * C::B_STAGE;
+          const uint32_t fb = b_full(sb);
+          const int kx = kb * TC_BK;
+          mbar_arrive_expect_tx(fb, bytes);
+          int j = 0;
+          for (; j + 128 <= t.npad; j += 128)
+            tma_load_2d(smem_u32(st + j * (TC_BK * 2)), m128, fb, kx, t.row_b + j, pol_x);
+          for (; j + 64 <= t.npad; j += 64)
+            tma_load_2d(smem_u32(st + j * (TC_BK * 2)), m64, fb, kx, t.row_b + j, pol_x);
+          for (; j < t.npad; j += 16)
+            tma_load_2d(smem_u32(st + j * (TC_BK * 2)), m16, fb, kx, t.row_b + j, pol_x);
+          progress[1] = it + 1;
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(TC_BM, npad);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % STAGES, r = kb / STAGES;
-        if (!mbar_wait(full_bar(s), r & 1)) { *abort_flag = 1; break; }
-        tc_fence_after();
-        uint8_t* st = smem + s * C::STAGE_BYTES;
-        const uint32_t a0 = smem_u32(st), a1 = smem_u32(st + C::A_BYTES);
-        const uint32_t bb = smem_u32(st + 2 * C::A_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk) {
-          const uint64_t bdesc = umma_desc_sw128(bb + kk * 32);
-          const uint32_t acc = (kb | kk) != 0;
-          umma_bf16(tmem, umma_desc_sw128(a0 + kk * 32), bdesc, idesc, acc);
-          if (has_a1) umma_bf16(tmem + BN, umma_desc_sw128(a1 + kk * 32), bdesc, idesc, acc);
+      // ------------- MMA issuer -------------
+      int it = 0, tl = 0;
+      for (int i = 0;; ++i) {
+        const int b = next_tile(i, true);
+        if (b < 0) break;
+        const TcTile t = tc_tile<DOWN>(G, toff, E, b, n_out);
+        const uint32_t idesc = umma_idesc_bf16(TC_BM, t.npad);
+        if (*abort_flag || (tl > 0 && !mbar_wait(acc_empty, (tl - 1) & 1))) {
+          *abort_flag = 1;
+          continue;  // keep reading the tile ring until the scheduler says "none"
         }
-        umma_commit(empty_bar(s));
-        progress[1] = kb + 1;
-        if (*abort_flag) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sa = it % SA, sb = it % SB;
+          if (!mbar_wait(a_full(sa), (it / SA) & 1) || !mbar_wait(b_full(sb), (it / SB) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + sa * C::A_STAGE), a1 = a0 + C::A_BYTES;
+          const uint32_t bb = smem_u32(smem + C::B_OFF + sb * C::B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const uint64_t bdesc = umma_desc_sw128(bb + kk * 32);
+            const uint32_t acc = (kb | kk) != 0;
+            umma_bf16(tmem, umma_desc_sw128(a0 + kk * 32), bdesc, idesc, acc);
+            if (t.has_a1) umma_bf16(tmem + BN, umma_desc_sw128(a1 + kk * 32), bdesc, idesc, acc);
+          }
+          mma_issued = true;
+          umma_commit(a_empty(sa));
+          umma_commit(b_empty(sb));
+          progress[2] = it + 1;
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          continue;
+        }
+        umma_commit(acc_full);
+        ++tl;
       }
-      umma_commit(acc_bar);
-      mma_committed = true;
     }
     __syncwarp();
   } else {
-    // ---- epilogue warps 2..5 ----
-    const int et = threadIdx.x - 64;  // 0..127
-    if (DOWN && !shared) {
-      for (int i = et; i < ntok; i += 128) gate_s[i] = gates[perm[G.off[g] + tok0 + i]];
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const bool ok = mbar_wait(acc_bar, 0);
-    if (!ok) *abort_flag = 1;
-    tc_fence_after();
-    const int q = warp & 3;
-    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    const int f = f0 + q * 32 + lane;
-    const bool write = ok && (*abort_flag == 0);
-    for (int c = 0; c < npad; c += 32) {
-      float va[32], vb[32];
-      tmem_load_2x32(tl + c, tl + BN + c, va, vb);
-      if (!write) continue;
-      if (!DOWN) {
-        __nv_bfloat16* o = out + (size_t)(G.off[g] + tok0 + c) * n_out + f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c + j < ntok) o[(size_t)j * n_out] = __float2bfloat16_rn(silu_f(va[j]) * vb[j]);
-      } else if (shared) {
-        float* o = y_sh + (size_t)(tok0 + c) * n_out + f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c + j < ntok) {
-            o[(size_t)j * n_out] = va[j];
-            if (has_a1) o[(size_t)j * n_out + TC_BM] = vb[j];
-          }
-      } else {
-        __nv_bfloat16* o = out + (size_t)(G.off[g] + tok0 + c) * n_out + f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c + j < ntok) {
-            const float gv = gate_s[c + j];
-            o[(size_t)j * n_out] = __float2bfloat16_rn(gv * va[j]);
-            if (has_a1) o[(size_t)j * n_out + TC_BM] = __float2bfloat16_rn(gv * vb[j]);
-          }
+    // ------------- epilogue warps 2 .. 2+TC_EPI_WARPS-1 -------------
+    // Warp w reads TMEM lane quarter w % 4 (its 32 output rows) for every
+    // other 32-token chunk (w - 2) / 4 = 0 or 1.  No epilogue warp waits on
+    // another: each decides on its own when to stop, so a timeout cannot
+    // leave one waiting at a barrier for ever.
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const uint32_t tl_addr = tmem + ((uint32_t)(q * 32) << 16);
+    int tl = 0;
+    for (int i = 0;; ++i) {
+      const int b = next_tile(i, false);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tile_empty(i % TC_TILE_RING));
+      if (b < 0) break;
+      const TcTile t = tc_tile<DOWN>(G, toff, E, b, n_out);
+      if (*abort_flag || !mbar_wait(acc_full, tl & 1)) {
+        *abort_flag = 1;
+        continue;  // keep reading the tile ring until the scheduler says "none"
       }
+      tc_fence_after();
+      const int fw = t.f0 + q * 32;  // first output row of this warp
+      for (int c = 32 * half; c < t.npad; c += 64) {
+        float va[32], vb[32];
+        tmem_load_2x32(tl_addr + c, tl_addr + BN + c, va, vb);
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) continue;  // warp-uniform (shuffles below)
+        if (!DOWN) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
+          store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + fw, n_out, va, c, t.ntok, lane);
+        } else if (t.shared) {
+          store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + fw, n_out, va, c, t.ntok, lane);
+          if (t.has_a1)
+            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + fw + TC_BM, n_out, vb, c, t.ntok,
+                           lane);
+        } else {
+          // gate of token c + j, one per lane, broadcast by shuffles
+          const float gl = c + lane < t.ntok ? gates[perm[t.out_row0 + c + lane]] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float gv = __shfl_sync(0xffffffffu, gl, j);
+            va[j] *= gv;
+            vb[j] *= gv;
+          }
+          __nv_bfloat16* o = out + (size_t)(t.out_row0 + c) * n_out + fw;
+          store_rows_bf16(o, n_out, va, c, t.ntok, lane);
+          if (t.has_a1) store_rows_bf16(o + TC_BM, n_out, vb, c, t.ntok, lane);
+        }
+      }
+      // the accumulators may be overwritten once every epilogue warp has read them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      ++tl;
     }
   }
 
@@ -234,10 +474,17 @@ k_expert_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ C
     // Unwind: let every copy this CTA issued land and every MMA it issued
     // finish (each wait bounded) before the shared memory and TMEM go away.
     if (warp == 0 && lane == 0) {
-      for (int kb = progress[1]; kb < progress[0]; ++kb)
-        mbar_wait(full_bar(kb % STAGES), (kb / STAGES) & 1);
+      for (int it = progress[2]; it < progress[0]; ++it)
+        mbar_wait(a_full(it % SA), (it / SA) & 1);
     }
-    if (warp == 1 && lane == 0 && mma_committed) mbar_wait(acc_bar, 0);
+    if (warp == TC_TOKEN_WARP && lane == 0) {
+      for (int it = progress[2]; it < progress[1]; ++it)
+        mbar_wait(b_full(it % SB), (it / SB) & 1);
+    }
+    if (warp == 1 && lane == 0 && mma_issued) {
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0);
+    }
     __syncthreads();
   }
   tc_fence_after();

@@ -13,6 +13,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <math.h>
+
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -25,13 +27,16 @@
 
 namespace {
 
-constexpr int kRouterCtaTarget = 296;  // CTAs wanted for the router GEMM (fixed, so
-                                       // results do not depend on the device)
+constexpr double kRouterCtaSlots = 296;  // router GEMM CTAs resident at once: 2 per SM
+                                         // on 148 SMs (fixed, so the split and hence
+                                         // the results do not depend on the device)
 constexpr int kRouterBK = 16;
 
 // Tensor-core GEMM variants: (BN tokens per tile, pipeline stages).
-constexpr int kBigBN = 256, kBigStages = 3;
-constexpr int kSmallBN = 64, kSmallStages = 5;
+// Tensor-core GEMM variants: BN tokens per tile, weight-ring and token-ring
+// depths (each fills ~224 KB of shared memory).
+constexpr int kBigBN = 256, kBigSA = 4, kBigSB = 3;
+constexpr int kSmallBN = 64, kSmallSA = 6, kSmallSB = 4;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -80,12 +85,26 @@ Plan make_plan(const moe_desc* d) {
   // router GEMM tiling and split of the model dimension
   p.big_router = p.E >= 96;
   p.r_bm = p.big_router ? 128 : 64;
-  p.r_bn = p.big_router ? 128 : 32;
+  p.r_bn = p.big_router ? 128 : 64;
+  // Split of the model dimension: the count whose CTAs fill whole waves best
+  // (2 CTAs per SM on 148 SMs), with the partial logits kept under 24 MiB.
   const long long tiles = (long long)((p.T + p.r_bm - 1) / p.r_bm) * ((p.E + p.r_bn - 1) / p.r_bn);
   const int kblocks = p.d / kRouterBK;
-  int ns = tiles > 0 ? (int)((kRouterCtaTarget + tiles - 1) / tiles) : 1;
-  ns = ns < 1 ? 1 : (ns > 64 ? 64 : ns);
-  ns = ns > kblocks ? kblocks : ns;
+  const long long te_bytes = (long long)p.T * p.E * 4;
+  long long ns_max = te_bytes > 0 ? (24LL << 20) / te_bytes : 64;
+  ns_max = ns_max < 1 ? 1 : (ns_max > 64 ? 64 : ns_max);
+  ns_max = ns_max > kblocks ? kblocks : ns_max;
+  int ns = 1;
+  double best = -1.0;
+  for (int c = 1; c <= ns_max && tiles > 0; ++c) {
+    const double ctas = (double)tiles * c;
+    const double waves = ceil(ctas / kRouterCtaSlots);
+    const double eff = ctas / (waves * kRouterCtaSlots);
+    if (eff > best + 1e-9) {
+      best = eff;
+      ns = c;
+    }
+  }
   p.kchunk = ((kblocks + ns - 1) / ns) * kRouterBK;
   p.n_split = (p.d + p.kchunk - 1) / p.kchunk;
 
@@ -120,7 +139,7 @@ Plan make_plan(const moe_desc* d) {
   region((size_t)p.n_split * p.T * p.E * 4, p.o_part, p.b_part);
   region((size_t)p.n_pair_blocks * p.E * 4, p.o_hist, p.b_hist);
   region((size_t)p.TK * 4, p.o_rank, p.b_rank);
-  region((size_t)(5 * p.E + 8) * 4, p.o_groups, p.b_groups);
+  region((size_t)(5 * p.E + 10) * 4, p.o_groups, p.b_groups);
   if (!p.route_only) {
     region((size_t)p.TK * 4, p.o_perm, p.b_perm);
     region((size_t)p.TK * 4, p.o_inv, p.b_inv);
@@ -155,8 +174,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] (row-major) read in boxes of 64 columns x box_rows
-// rows with the 128-byte swizzle; rows past the end read as zero.
+// bf16 matrix [rows, cols] (row-major) read in boxes of 64 columns (128
+// bytes) x box_rows rows with the 128-byte swizzle; rows past the end read
+// as zero.
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows <= 0) return false;
@@ -167,6 +187,14 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
 }
 
 int device_ok() {
@@ -188,8 +216,8 @@ void launch_router(const Plan& p, const TX* x, const float* w_router, float* par
     k_router_logits<TX, 128, 128, kRouterBK, 8, 8>
         <<<grid, 256, 0, s>>>(x, w_router, part, p.T, p.E, p.d, p.kchunk);
   } else {
-    dim3 grid((p.E + 31) / 32, (p.T + 63) / 64, p.n_split);
-    k_router_logits<TX, 64, 32, kRouterBK, 4, 2>
+    dim3 grid((p.E + 63) / 64, (p.T + 63) / 64, p.n_split);
+    k_router_logits<TX, 64, 64, kRouterBK, 4, 4>
         <<<grid, 256, 0, s>>>(x, w_router, part, p.T, p.E, p.d, p.kchunk);
   }
 }
@@ -210,50 +238,68 @@ void launch_topk(const Plan& p, const float* part, const float* bias, int32_t* i
 }
 
 struct TcMaps {
-  CUtensorMap g, u, sg, su, xp, x, d, sd, h;
+  TcMapsDev up;    // first GEMM: W_gate, W_up; token rows of X_perm and x
+  TcMapsDev down;  // second GEMM: W_down; rows of H
 };
+
+bool make_rows_maps(CUtensorMap* m128, CUtensorMap* m64, CUtensorMap* m16, const void* base,
+                    long long rows, long long cols) {
+  return make_map(m128, base, rows, cols, 128) && make_map(m64, base, rows, cols, 64) &&
+         make_map(m16, base, rows, cols, 16);
+}
 
 // All tensor maps of the two tensor-core GEMMs, built before anything is
 // launched so that a failure here leaves the stream untouched.
 bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
                   uint8_t* ws, TcMaps* m) {
   bool ok = true;
-  ok &= make_map(&m->g, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
-  ok &= make_map(&m->u, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
-  ok &= make_map(&m->sg, sh->w_gate, p.h, p.d, TC_BM);
-  ok &= make_map(&m->su, sh->w_up, p.h, p.d, TC_BM);
-  ok &= make_map(&m->xp, ws + p.o_xperm, p.TK, p.d, 16);
-  ok &= make_map(&m->x, x, p.T, p.d, 16);
-  ok &= make_map(&m->d, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
-  ok &= make_map(&m->sd, sh->w_down, p.d, p.h, TC_BM);
-  ok &= make_map(&m->h, ws + p.o_h, (long long)p.TK + p.T, p.h, 16);
+  ok &= make_map(&m->up.a0, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
+  ok &= make_map(&m->up.a1, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
+  ok &= make_map(&m->up.sa0, sh->w_gate, p.h, p.d, TC_BM);
+  ok &= make_map(&m->up.sa1, sh->w_up, p.h, p.d, TC_BM);
+  ok &= make_rows_maps(&m->up.b128, &m->up.b64, &m->up.b16, ws + p.o_xperm, p.TK, p.d);
+  ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, x, p.T, p.d);
+  ok &= make_map(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
+  m->down.a1 = m->down.a0;
+  ok &= make_map(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
+  m->down.sa1 = m->down.sa0;
+  ok &= make_rows_maps(&m->down.b128, &m->down.b64, &m->down.b16, ws + p.o_h,
+                       (long long)p.TK + p.T, p.h);
+  m->down.bs128 = m->down.b128;
+  m->down.bs64 = m->down.b64;
+  m->down.bs16 = m->down.b16;
   return ok;
 }
 
-template <int BN, int STAGES>
+template <int BN, int SA, int SB>
 bool set_tc_smem() {
-  using C = TcCfg<BN, STAGES>;
-  return cudaFuncSetAttribute(k_expert_tc<BN, STAGES, false>,
+  using C = TcCfg<BN, SA, SB>;
+  return cudaFuncSetAttribute(k_expert_tc<BN, SA, SB, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               C::SMEM_BYTES) == cudaSuccess &&
-         cudaFuncSetAttribute(k_expert_tc<BN, STAGES, true>,
+         cudaFuncSetAttribute(k_expert_tc<BN, SA, SB, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               C::SMEM_BYTES) == cudaSuccess;
 }
 
-template <int BN, int STAGES>
+// Persistent launches: one CTA per SM (at most one per tile); tiles are
+// handed out in table order by the kernels' own scheduler.
+template <int BN, int SA, int SB>
 void launch_tc(const Plan& p, const TcMaps& m, uint8_t* ws, int32_t* groups, const float* gates,
                cudaStream_t s, cudaEvent_t between) {
-  using C = TcCfg<BN, STAGES>;
+  using C = TcCfg<BN, SA, SB>;
+  const int sms = sm_count();
+  const int grid_a = p.max_tiles_a < sms ? p.max_tiles_a : sms;
+  const int grid_b = p.max_tiles_b < sms ? p.max_tiles_b : sms;
   const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
   __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
   __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
   float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
-  k_expert_tc<BN, STAGES, false><<<p.max_tiles_a, TC_THREADS, C::SMEM_BYTES, s>>>(
-      m.g, m.u, m.sg, m.su, m.xp, m.x, groups, p.E, p.d, p.h, hbuf, nullptr, perm, gates);
+  k_expert_tc<BN, SA, SB, false><<<grid_a, TC_THREADS, C::SMEM_BYTES, s>>>(
+      m.up, groups, p.E, p.d, p.h, hbuf, nullptr, perm, gates);
   if (between) cudaEventRecord(between, s);
-  k_expert_tc<BN, STAGES, true><<<p.max_tiles_b, TC_THREADS, C::SMEM_BYTES, s>>>(
-      m.d, m.d, m.sd, m.sd, m.h, m.h, groups, p.E, p.h, p.d, yperm, ysh, perm, gates);
+  k_expert_tc<BN, SA, SB, true><<<grid_b, TC_THREADS, C::SMEM_BYTES, s>>>(
+      m.down, groups, p.E, p.h, p.d, yperm, ysh, perm, gates);
 }
 
 template <typename T>
@@ -307,8 +353,8 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
   TcMaps maps;
   if (use_tc) {
     if (!make_tc_maps(p, x, experts, shared, ws, &maps)) return MOE_ERR_DEVICE;
-    const bool ok = p.big_tiles ? set_tc_smem<kBigBN, kBigStages>()
-                                : set_tc_smem<kSmallBN, kSmallStages>();
+    const bool ok = p.big_tiles ? set_tc_smem<kBigBN, kBigSA, kBigSB>()
+                                : set_tc_smem<kSmallBN, kSmallSA, kSmallSB>();
     if (!ok) return MOE_ERR_LAUNCH;
   }
   float* part = reinterpret_cast<float*>(ws + p.o_part);
@@ -345,9 +391,9 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
       launch_simt<__nv_bfloat16>(p, x, experts, shared, ws, groups, gates, s, between);
     } else {
       if (p.big_tiles)
-        launch_tc<kBigBN, kBigStages>(p, maps, ws, groups, gates, s, between);
+        launch_tc<kBigBN, kBigSA, kBigSB>(p, maps, ws, groups, gates, s, between);
       else
-        launch_tc<kSmallBN, kSmallStages>(p, maps, ws, groups, gates, s, between);
+        launch_tc<kSmallBN, kSmallSA, kSmallSB>(p, maps, ws, groups, gates, s, between);
     }
     mark(4);
     const float* ysh = reinterpret_cast<const float*>(ws + p.o_ysh);

@@ -91,6 +91,12 @@ MOE_DEV uint64_t l2_policy_evict_first() {
   return p;
 }
 
+MOE_DEV uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 MOE_DEV uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -120,17 +126,21 @@ MOE_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor for a K-major bf16 operand tile stored as
+// Shared-memory matrix descriptor of a K-major bf16 operand tile stored as
 // rows of 128 bytes (64 elements) with the 128-byte swizzle that TMA's
-// CU_TENSOR_MAP_SWIZZLE_128B writes: 8-row atoms of 1024 bytes, atoms
-// stacked densely (stride byte offset 1024).  Fields: start address >> 4
-// (bits 0-13), leading byte offset >> 4 (16-29, unused for swizzled K-major,
-// set to 1), stride byte offset >> 4 (32-45), descriptor version 1 (46-47),
-// base offset 0 (49-51; tiles are 1024-byte aligned), layout 2 = SWIZZLE_128B
-// (61-63).
+// CU_TENSOR_MAP_SWIZZLE_128B writes: 8-row atoms of 1024 bytes stacked
+// densely (stride byte offset 1024).  Fields: start address >> 4 (bits
+// 0-13), leading byte offset >> 4 (16-29; unused for swizzled K-major, set to
+// 1), stride byte offset >> 4 (32-45), descriptor version 1 (46-47), base
+// offset 0 (49-51; tiles are 1024-byte aligned), layout 2 = SWIZZLE_128B
+// (61-63).  The k-th 16-element K slice of a row starts 32*k bytes further on.
 MOE_DEV uint64_t umma_desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+MOE_DEV void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B, fp32

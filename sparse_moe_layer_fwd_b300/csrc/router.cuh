@@ -33,16 +33,26 @@ MOE_DEV void load4_as_float<__nv_bfloat16>(const __nv_bfloat16* p, float* out) {
   out[0] = fa.x; out[1] = fa.y; out[2] = fb.x; out[3] = fb.y;
 }
 
-// Block tile BM tokens x BN experts, K step BK; each thread owns TM x TN
-// outputs.  grid = (ceil(E/BN), ceil(T/BM), n_split).
+// Block tile BM tokens x BN experts, K step BK; 256 threads, each owning a
+// TM x TN block of outputs made of 4 x 4 sub-blocks spaced BM/(TM/4) rows and
+// BN/(TN/4) columns apart, so that every shared-memory read is a 16-byte
+// vector.  The next K step's tiles are loaded into registers while the
+// current one is multiplied (double buffering).  grid = (ceil(E/BN),
+// ceil(T/BM), n_split); split z covers columns [z*kchunk, (z+1)*kchunk).
 template <typename TX, int BM, int BN, int BK, int TM, int TN>
-__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+__global__ void __launch_bounds__(256)
 k_router_logits(const TX* __restrict__ x, const float* __restrict__ w, float* __restrict__ part,
                 int T, int E, int d, int kchunk) {
-  constexpr int NT = (BM / TM) * (BN / TN);
+  constexpr int NT = 256;
   constexpr int TXN = BN / TN;  // threads along experts
-  __shared__ __align__(16) float As[2][BK][BM + 4];
-  __shared__ __align__(16) float Bs[2][BK][BN + 4];
+  static_assert((BM / TM) * (BN / TN) == NT, "thread count");
+  static_assert(TM % 4 == 0 && TN % 4 == 0, "4x4 sub-blocks");
+  constexpr int MI = TM / 4, NJ = TN / 4;        // sub-blocks per thread
+  constexpr int XV = BM * BK / 4 / NT;           // 4-element x loads per thread
+  constexpr int WV = BN * BK / 4 / NT;           // 4-element w loads per thread
+  static_assert(XV >= 1 && WV >= 1, "load split");
+  __shared__ __align__(16) float As[2][BK][BM];
+  __shared__ __align__(16) float Bs[2][BK][BN];
 
   const int tid = threadIdx.x;
   const int tx = tid % TXN, ty = tid / TXN;
@@ -56,51 +66,79 @@ k_router_logits(const TX* __restrict__ x, const float* __restrict__ w, float* __
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-  auto load_tiles = [&](int buf, int k0) {
-    for (int i = tid; i < BM * BK / 4; i += NT) {
-      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t0 + row < T) load4_as_float<TX>(x + (size_t)(t0 + row) * d + k0 + c4, v);
+  float xr[XV][4], wr[WV][4];
+  auto gload = [&](int k0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) As[buf][c4 + q][row] = v[q];
+    for (int v = 0; v < XV; ++v) {
+      const int i = tid + v * NT;
+      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
+      xr[v][0] = xr[v][1] = xr[v][2] = xr[v][3] = 0.f;
+      if (t0 + row < T) load4_as_float<TX>(x + (size_t)(t0 + row) * d + k0 + c4, xr[v]);
     }
-    for (int i = tid; i < BN * BK / 4; i += NT) {
-      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (e0 + row < E) load4_as_float<float>(w + (size_t)(e0 + row) * d + k0 + c4, v);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) Bs[buf][c4 + q][row] = v[q];
+    for (int v = 0; v < WV; ++v) {
+      const int i = tid + v * NT;
+      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
+      wr[v][0] = wr[v][1] = wr[v][2] = wr[v][3] = 0.f;
+      if (e0 + row < E) load4_as_float<float>(w + (size_t)(e0 + row) * d + k0 + c4, wr[v]);
+    }
+  };
+  auto sstore = [&](int buf) {
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int i = tid + v * NT;
+      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) As[buf][c4 + q][row] = xr[v][q];
+    }
+#pragma unroll
+    for (int v = 0; v < WV; ++v) {
+      const int i = tid + v * NT;
+      const int row = i / (BK / 4), c4 = (i % (BK / 4)) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) Bs[buf][c4 + q][row] = wr[v][q];
     }
   };
 
   int buf = 0;
-  if (kbeg < kend) load_tiles(0, kbeg);
+  if (kbeg < kend) {
+    gload(kbeg);
+    sstore(0);
+  }
   __syncthreads();
   for (int k0 = kbeg; k0 < kend; k0 += BK) {
-    if (k0 + BK < kend) load_tiles(buf ^ 1, k0 + BK);
+    const bool more = k0 + BK < kend;
+    if (more) gload(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[TM], b[TN];
 #pragma unroll
-      for (int i = 0; i < TM; ++i) a[i] = As[buf][kk][ty + i * (BM / TM)];
+      for (int mi = 0; mi < MI; ++mi) {
+        const float4 v = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4 + mi * (BM / MI)]);
+        a[mi * 4 + 0] = v.x; a[mi * 4 + 1] = v.y; a[mi * 4 + 2] = v.z; a[mi * 4 + 3] = v.w;
+      }
 #pragma unroll
-      for (int j = 0; j < TN; ++j) b[j] = Bs[buf][kk][tx + j * TXN];
+      for (int nj = 0; nj < NJ; ++nj) {
+        const float4 v = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4 + nj * (BN / NJ)]);
+        b[nj * 4 + 0] = v.x; b[nj * 4 + 1] = v.y; b[nj * 4 + 2] = v.z; b[nj * 4 + 3] = v.w;
+      }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
+    if (more) sstore(buf ^ 1);
     __syncthreads();
     buf ^= 1;
   }
   float* out = part + (size_t)blockIdx.z * T * E;
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
-    const int t = t0 + ty + i * (BM / TM);
+    const int t = t0 + ty * 4 + (i / 4) * (BM / MI) + (i % 4);
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
-      const int e = e0 + tx + j * TXN;
+      const int e = e0 + tx * 4 + (j / 4) * (BN / NJ) + (j % 4);
       if (e < E) out[(size_t)t * E + e] = acc[i][j];
     }
   }

@@ -75,7 +75,7 @@ def test_dispatch_is_a_stable_counting_sort():
     assert np.array_equal(inv[perm], np.arange(TK))
     xp = layer.region("x_perm", torch.float32, (TK, wl.d)).cpu()
     assert torch.equal(xp, inp["x"].cpu()[torch.from_numpy(perm // wl.k)])
-    groups = npi(layer.region("groups", torch.int32, (5 * wl.E + 8,)))
+    groups = npi(layer.region("groups", torch.int32, (5 * wl.E + 10,)))
     load = np.bincount(idx, minlength=wl.E)
     off = groups[:wl.E + 2]
     assert np.array_equal(off[:wl.E], np.concatenate([[0], np.cumsum(load)[:-1]]))
