@@ -59,9 +59,10 @@ def _peaks():
         with open(p) as f:
             d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "sm_max_mhz": d.get("sm_max_mhz", 2032.0), "source": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
-            "source": "fallback"}
+            "sm_max_mhz": 2032.0, "source": "fallback"}
 
 
 def _kernel_sha():
@@ -213,8 +214,9 @@ def run_ours(args, wl):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     wl_rank = wl.with_(seed=wl.seed + 1000 * rank) if ws > 1 else wl
-    inp = I.make_inputs(wl_rank, device="cuda")
-    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype)
+    route_only = args.route_only or wl.route_only
+    inp = I.make_inputs(wl_rank, device="cuda", experts=not route_only)
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else 0)
     stream = torch.cuda.current_stream()
     x = inp["x"]
 
@@ -265,7 +267,8 @@ def run_ours(args, wl):
     # end to end through the host-buffer entry point (pinned x in, y out)
     e2e = None
     if not args.no_e2e:
-        hl = MoeLayer.from_inputs(inp, wl.k, wl.dtype, host_io=True)
+        hl = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else 0,
+                                  host_io=True)
         x_host = x.cpu().pin_memory()
         y_host = torch.empty_like(x_host).pin_memory()
         for _ in range(2):
@@ -281,7 +284,7 @@ def run_ours(args, wl):
         e2e_ms, e2e_value = aggregate(s2.elapsed_time(e2), wl.T * args.steps, ws, "cuda")
         nb = x_host.numel() * x_host.element_size()
         e2e = {"value": e2e_value, "unit": "tokens/s",
-               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb,
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": 0 if route_only else nb,
                "ms_per_step": e2e_ms / args.steps}
         del hl
 
@@ -292,6 +295,33 @@ def run_ours(args, wl):
         return
 
     peaks = _peaks()
+    if route_only:
+        # fp32 router GEMM on CUDA cores: 148 SMs x 128 FP32 lanes x 2 FLOP
+        # per clock at the maximum SM clock
+        fma_peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        rflops = 2.0 * wl.T * wl.E * wl.d
+        ach = rflops / (phase_ms[0] / 1e3) / 1e12
+        line = {
+            "metric": METRIC + " [routing only]", "value": wl.T * args.steps / (elapsed_ms / 1e3),
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 router, bf16 x" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,1/d) router)",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
+                       "route_only": True},
+            "roofline": {"bound": "alu", "kernel": "k_router_logits (fp32 FFMA)",
+                         "achieved": ach, "peak": fma_peak, "unit": "TFLOP/s",
+                         "frac": ach / fma_peak, "traffic": None,
+                         "peak_kind": "148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock",
+                         "flops_per_launch": rflops, "ms_per_launch": phase_ms[0]},
+            "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
+            "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     fl1, fl2, by1, by2, touched = _algorithmic(wl, load)
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
@@ -360,6 +390,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time the routing pass only (router, top-k, load counts)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

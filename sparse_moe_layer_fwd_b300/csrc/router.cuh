@@ -50,7 +50,8 @@ k_router_logits(const TX* __restrict__ x, const float* __restrict__ w, float* __
   constexpr int MI = TM / 4, NJ = TN / 4;        // sub-blocks per thread
   constexpr int XV = BM * BK / 4 / NT;           // 4-element x loads per thread
   constexpr int WV = BN * BK / 4 / NT;           // 4-element w loads per thread
-  static_assert(XV >= 1 && WV >= 1, "load split");
+  static_assert(XV >= 1 && WV >= 1 && (BM * BK / 4) % NT == 0 && (BN * BK / 4) % NT == 0,
+                "load split");
   __shared__ __align__(16) float As[2][BK][BM];
   __shared__ __align__(16) float Bs[2][BK][BN];
 
@@ -66,6 +67,8 @@ k_router_logits(const TX* __restrict__ x, const float* __restrict__ w, float* __
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
+  // Load slot i covers row i / (BK/4), columns 4 * (i % (BK/4)) .. +3, so
+  // each row's BK columns are read by neighbouring lanes (coalesced).
   float xr[XV][4], wr[WV][4];
   auto gload = [&](int k0) {
 #pragma unroll

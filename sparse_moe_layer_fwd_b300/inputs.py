@@ -118,13 +118,16 @@ def _skew_offsets(wl: Workload, gen: torch.Generator, device: str) -> torch.Tens
     raise ValueError(wl.skew)
 
 
-def make_inputs(wl: Workload, device: str = "cpu", gen_device: str | None = None) -> dict:
+def make_inputs(wl: Workload, device: str = "cpu", gen_device: str | None = None,
+                experts: bool = True) -> dict:
     """All inputs of one workload as torch tensors on ``device``.
 
     Keys: x [T,d], w_router [E,d] f32, bias [E] f32, w_gate [E,h,d],
     w_up [E,h,d], w_down [E,d,h], sh_gate [h,d], sh_up [h,d], sh_down [d,h],
     and "gen" (the generator, positioned after the draws, which
-    ``next_x`` continues for multi-step workloads).
+    ``next_x`` continues for multi-step workloads).  With experts=False only
+    the routing inputs are drawn (the expert weights come last in the draw
+    order, so x, W_r and b are the same either way).
     """
     if gen_device is None:
         gen_device = "cpu" if wl.weight_bytes < (1 << 28) else device
@@ -144,7 +147,11 @@ def make_inputs(wl: Workload, device: str = "cpu", gen_device: str | None = None
         "x": x.to(device),
         "w_router": w_router.to(device),
         "bias": bias.to(device),
+        "gen": gen,
+        "gen_device": gen_device,
     }
+    if not experts:
+        return out
     w_gate = torch.empty((wl.E, wl.h, wl.d), dtype=dt, device=device)
     w_up = torch.empty((wl.E, wl.h, wl.d), dtype=dt, device=device)
     w_down = torch.empty((wl.E, wl.d, wl.h), dtype=dt, device=device)
@@ -157,8 +164,6 @@ def make_inputs(wl: Workload, device: str = "cpu", gen_device: str | None = None
     out["sh_gate"] = _normal((wl.h, wl.d), sg, gen, gen_device, dt).to(device)
     out["sh_up"] = _normal((wl.h, wl.d), sg, gen, gen_device, dt).to(device)
     out["sh_down"] = _normal((wl.d, wl.h), sd, gen, gen_device, dt).to(device)
-    out["gen"] = gen
-    out["gen_device"] = gen_device
     return out
 
 

@@ -15,14 +15,15 @@ class MoeLayer:
     def __init__(self, w_router, bias, w_gate, w_up, w_down, sh_gate, sh_up, sh_down, *,
                  T: int, k: int, dtype: str, flags: int = 0, host_io: bool = False):
         self.E, self.d = w_router.shape
-        self.h = w_gate.shape[1]
+        self.h = w_gate.shape[1] if w_gate is not None else 128
         self.T, self.k, self.dtype, self.flags = T, k, dtype, flags
         dev = w_router.device
         self.desc = M.make_desc(T, self.d, self.h, self.E, k, dtype, flags)
         self.w_router, self.bias = w_router, bias
         self._keep = (w_gate, w_up, w_down, sh_gate, sh_up, sh_down)
-        self.experts = M.make_experts(w_gate, w_up, w_down)
-        self.shared = M.make_experts(sh_gate, sh_up, sh_down)
+        have_w = w_gate is not None
+        self.experts = M.make_experts(w_gate, w_up, w_down) if have_w else None
+        self.shared = M.make_experts(sh_gate, sh_up, sh_down) if have_w else None
         tdt = torch.float32 if dtype == "f32" else torch.bfloat16
         self.ws_bytes = M.moe_workspace_size(self.desc)
         if self.ws_bytes == 0:
@@ -41,9 +42,9 @@ class MoeLayer:
     def from_inputs(cls, inp: dict, k: int, dtype: str, flags: int = 0, T: int | None = None,
                     host_io: bool = False) -> "MoeLayer":
         T = inp["x"].shape[0] if T is None else T
-        return cls(inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"], inp["w_down"],
-                   inp["sh_gate"], inp["sh_up"], inp["sh_down"], T=T, k=k, dtype=dtype,
-                   flags=flags, host_io=host_io)
+        return cls(inp["w_router"], inp["bias"], inp.get("w_gate"), inp.get("w_up"),
+                   inp.get("w_down"), inp.get("sh_gate"), inp.get("sh_up"), inp.get("sh_down"),
+                   T=T, k=k, dtype=dtype, flags=flags, host_io=host_io)
 
     def forward(self, x, stream=None):
         if stream is None:
