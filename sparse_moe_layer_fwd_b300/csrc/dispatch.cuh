@@ -93,7 +93,7 @@ __device__ int cta_exclusive_scan(int* data, int n, int* warp_tot) {
 //   off[E+2]     first row of group g in the permuted row space; off[E] = TK
 //                is the shared expert's first row (in H), off[E+1] = TK + T
 //   ntt[E+1]     token tiles of group g (0 if the group is empty)
-//   tsz[E+1]     rows per token tile (multiple of 16, <= bn)
+//   tsz[E+1]     rows per token tile (multiple of tile_round, <= bn)
 //   toff_a[E+2]  prefix sum of ntt[g] * ft_a (tiles of the first GEMM)
 //   toff_b[E+2]  prefix sum of ntt[g] * ft_b (tiles of the second GEMM)
 //   next[2]      tile counters of the two GEMMs' schedulers, zeroed here
@@ -115,7 +115,7 @@ MOE_DEV GroupTable group_table(int32_t* base, int E) {
 __global__ void __launch_bounds__(1024)
 k_scan_groups(int32_t* __restrict__ blk_hist, int n_blocks, int E, int T, int TK,
               int32_t* __restrict__ load_counts, int32_t* __restrict__ groups, int bn, int ft_a,
-              int ft_b) {
+              int ft_b, int tile_round) {
   __shared__ int buf[MOE_MAX_E + 2];
   __shared__ int load_s[MOE_MAX_E + 1];
   __shared__ int warp_tot[32];
@@ -154,7 +154,7 @@ k_scan_groups(int32_t* __restrict__ blk_hist, int n_blocks, int E, int T, int TK
     const int nt = n > 0 ? (n + bn - 1) / bn : 0;
     const int per = nt > 0 ? (n + nt - 1) / nt : 0;
     G.ntt[g] = nt;
-    G.tsz[g] = (per + 15) & ~15;
+    G.tsz[g] = (per + tile_round - 1) / tile_round * tile_round;
     buf[g] = nt * ft_a;
   }
   __syncthreads();

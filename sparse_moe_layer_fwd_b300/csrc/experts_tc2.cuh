@@ -1,0 +1,398 @@
+// experts_tc2.cuh -- the grouped expert GEMMs on CTA pairs (2-SM tensor-core
+// MMA, cta_group::2), for token tiles of up to 256 tokens.
+//
+// Same computation and tile table as experts_tc.cuh (swap-AB: weights are the
+// MMA's M side, tokens its N side), with one tile spread over a cluster of
+// two CTAs on two SMs:
+//   first GEMM : a pair tile covers 256 rows of W_gate and the same 256 rows
+//                of W_up; CTA r holds rows f0 + 128 r .. +127 of both, so its
+//                two TMEM accumulators hold gate and up for its own 128
+//                hidden units and the SwiGLU epilogue stays local.
+//   second GEMM: a pair tile covers 256 rows of W_down; CTA r holds rows
+//                f0 + 128 r .. +127 in one accumulator, and TMEM holds two such
+//                accumulators so that the epilogue of one tile overlaps the
+//                MMAs of the next (its K is short: 2048).
+//   Token rows: CTA r holds rows r * N/2 .. of the N-token tile (N a
+//   multiple of 32), so each CTA streams half of the token tile.
+// Per 64-deep K step a CTA loads 32 KB of weights + N/2 x 128 B of tokens
+// (48 KB at N = 256) instead of 64 KB, so the same shared memory holds a
+// deeper weight ring (5 stages) and each SM moves a quarter fewer bytes.
+//
+// Roles per CTA as in the 1-SM kernel (warp 0: weights [+ tile scheduler in
+// the leader], warp 1: MMA in the leader, warps 2-9: epilogue, warp 10:
+// token rows).  Only the leader (cluster rank 0) issues MMAs; both CTAs'
+// TMA loads complete on the leader's "full" barriers (.cta_group::2 TMA), the
+// leader's commits arrive on both CTAs' "empty" and "acc_full" barriers
+// (multicast), and the peer's roles arrive remotely on the leader's
+// tile_empty and acc_empty barriers.  The leader's scheduler takes pair
+// tiles in table order from the global counter and writes each tile id into
+// both CTAs' tile rings.
+//
+// Every wait is bounded; every decision to leave is the same in both CTAs of
+// a pair, so both reach the final cluster barrier.
+#pragma once
+
+#include "experts_tc.cuh"
+
+#define TC2_THREADS TC_THREADS
+#define TC2_CONSUMERS (TC_EPI_WARPS + 2)  // per CTA: epilogue warps, token producer, MMA or weight producer
+
+// NACC accumulators of 256 columns per tile (2: gate and up; 1: one block of
+// down-projection rows) and NBUF TMEM buffers of them (NACC * NBUF <= 2): with
+// two buffers the epilogue of one tile overlaps the MMAs of the next.
+template <int SA, int SB, int NACC, int NBUF>
+struct Tc2Cfg {
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile
+  static constexpr int A_STAGE = NACC * A_BYTES;
+  static constexpr int B_STAGE = 128 * TC_BK * 2;    // half of a 256-token tile
+  static constexpr int B_OFF = SA * A_STAGE;
+  static constexpr int BAR_OFF = B_OFF + SB * B_STAGE;
+  // a_full, a_empty [SA]; b_full, b_empty [SB]; acc_full, acc_empty [2];
+  // drain; tile_full, tile_empty [RING]
+  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING;
+  static constexpr int MISC_BYTES = 4 * TC_TILE_RING + 4 * 5;
+  static constexpr int SMEM_BYTES = BAR_OFF + 8 * N_BARS + MISC_BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(NACC * NBUF <= 2 && NACC >= 1 && NBUF >= 1, "TMEM holds two 256-column blocks");
+  static_assert(SMEM_BYTES + 64 <= 232448, "shared memory");
+  static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the TMEM allocation assumes it");
+};
+
+// Geometry of one pair tile as seen by CTA `rank`.
+struct Tc2Tile {
+  bool shared, v0, v1;  // this CTA's weight sub-tiles exist (rows < n_out)
+  bool mma1;            // the second accumulator is computed
+  int ntok, npad, half, tok0, row_a0, row_a1, row_b, out_row0, out_f0, out_f1;
+  uint32_t bytes_a;     // weight bytes of one K step, both CTAs together
+};
+
+template <bool DOWN, int NACC>
+MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b, int n_out,
+                         uint32_t rank) {
+  Tc2Tile t;
+  const int g = find_group(toff, E, b);
+  t.shared = g == E;
+  const int nt = G.ntt[g];
+  const int local = b - toff[g];
+  const int ft = local / nt, tt = local % nt;
+  const int n_g = G.off[g + 1] - G.off[g];
+  const int tsz = G.tsz[g];
+  t.tok0 = tt * tsz;
+  t.ntok = min(tsz, n_g - t.tok0);
+  t.npad = (t.ntok + 31) & ~31;
+  t.half = t.npad / 2;
+  // rows of the tile: first GEMM 256 (gate and up alike); second GEMM 256 per
+  // accumulator
+  const int f0 = ft * (DOWN ? 2 * TC_BM * NACC : 2 * TC_BM);
+  const int base = t.shared ? 0 : g * n_out;
+  int nsub = 0;  // valid weight sub-tiles of both CTAs
+  for (int r = 0; r < 2; ++r) {
+    const int a = f0 + TC_BM * r, c = DOWN ? f0 + 2 * TC_BM + TC_BM * r : a;
+    nsub += (a < n_out) + (NACC == 2 && c < n_out);
+  }
+  t.out_f0 = f0 + TC_BM * (int)rank;
+  t.out_f1 = DOWN ? f0 + 2 * TC_BM + TC_BM * (int)rank : t.out_f0;
+  t.v0 = t.out_f0 < n_out;
+  t.v1 = NACC == 2 && t.out_f1 < n_out;
+  t.mma1 = NACC == 2 && (DOWN ? f0 + 2 * TC_BM < n_out : true);
+  t.row_a0 = base + t.out_f0;
+  t.row_a1 = base + t.out_f1;
+  t.bytes_a = (uint32_t)nsub * (TC_BM * TC_BK * 2);
+  t.row_b = ((!DOWN && t.shared) ? t.tok0 : G.off[g] + t.tok0) + (int)rank * t.half;
+  t.out_row0 = G.off[g] + t.tok0;
+  return t;
+}
+
+template <int SA, int SB, int NACC, int NBUF, bool DOWN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC2_THREADS, 1)
+k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
+             int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
+             const int32_t* __restrict__ perm, const float* __restrict__ gates) {
+  using C = Tc2Cfg<SA, SB, NACC, NBUF>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  GroupTable G = group_table(const_cast<int32_t*>(groups), E);
+  const int32_t* toff = DOWN ? G.toff_b : G.toff_a;
+  int* counter = G.next + (DOWN ? 1 : 0);
+  const int total = toff[E + 1];
+  // the same decision in both CTAs of the pair (same cluster index)
+  if ((int)(blockIdx.x >> 1) >= total) return;
+
+  uint8_t* bar_base = smem + C::BAR_OFF;
+  auto bar = [&](int i) { return smem_u32(bar_base + 8 * i); };
+  auto a_full = [&](int s) { return bar(s); };
+  auto a_empty = [&](int s) { return bar(SA + s); };
+  auto b_full = [&](int s) { return bar(2 * SA + s); };
+  auto b_empty = [&](int s) { return bar(2 * SA + SB + s); };
+  auto acc_full = [&](int u) { return bar(2 * SA + 2 * SB + u); };
+  auto acc_empty = [&](int u) { return bar(2 * SA + 2 * SB + 2 + u); };
+  const uint32_t drain_bar = bar(2 * SA + 2 * SB + 4);
+  auto tile_full = [&](int s) { return bar(2 * SA + 2 * SB + 5 + s); };
+  auto tile_empty = [&](int s) { return bar(2 * SA + 2 * SB + 5 + TC_TILE_RING + s); };
+  uint8_t* misc = bar_base + 8 * C::N_BARS;
+  volatile int* tile_id = reinterpret_cast<volatile int*>(misc);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc + 4 * TC_TILE_RING);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4 * TC_TILE_RING + 4);
+  volatile int* progress = reinterpret_cast<volatile int*>(misc + 4 * TC_TILE_RING + 8);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(a_full(s), 1);   // the leader's arrive + both CTAs' bytes
+      mbar_init(a_empty(s), 1);  // the leader's multicast commit
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(b_full(s), 1);
+      mbar_init(b_empty(s), 1);
+    }
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(acc_full(u), 1);
+      mbar_init(acc_empty(u), 2 * TC_EPI_WARPS);  // epilogue warps of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    for (int s = 0; s < TC_TILE_RING; ++s) {
+      mbar_init(tile_full(s), 1);
+      mbar_init(tile_empty(s), 2 * TC2_CONSUMERS);  // consumers of both CTAs
+    }
+    *abort_flag = 0;
+    progress[0] = progress[1] = progress[2] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nkb = K / TC_BK;
+  bool mma_issued = false;
+
+  // leader's barriers as seen from this CTA
+  auto lead = [&](uint32_t a) { return leader ? a : cluster_map(a, 0); };
+  auto release_tile = [&](int s) {
+    if (leader) mbar_arrive(tile_empty(s)); else mbar_arrive_cluster(cluster_map(tile_empty(s), 0));
+  };
+  auto next_tile = [&](int i, bool arrive) -> int {
+    const int s = i % TC_TILE_RING;
+    if (!mbar_wait_cluster(tile_full(s), (i / TC_TILE_RING) & 1)) {
+      *abort_flag = 1;
+      return -1;
+    }
+    const int b = tile_id[s];
+    if (arrive) release_tile(s);
+    return b;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------- weight (A) producer; in the leader also the scheduler ----------
+      const uint64_t pol_w = l2_policy_evict_first();
+      int it = 0;
+      for (int i = 0;; ++i) {
+        int b;
+        if (leader) {
+          const int s = i % TC_TILE_RING;
+          if (i >= TC_TILE_RING &&
+              !mbar_wait_cluster(tile_empty(s), ((i / TC_TILE_RING) & 1) ^ 1)) {
+            *abort_flag = 1;
+            break;
+          }
+          b = *abort_flag ? total : atomicAdd(counter, 1);
+          if (b >= total) b = -1;
+          tile_id[s] = b;
+          st_cluster_u32(cluster_map(smem_u32(const_cast<int*>(&tile_id[s])), 1), (uint32_t)b);
+          mbar_arrive(tile_full(s));
+          mbar_arrive_cluster(cluster_map(tile_full(s), 1));
+        } else {
+          b = next_tile(i, true);
+        }
+        if (b < 0) break;
+        const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
+        const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
+        const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sa = it % SA, r = it / SA;
+          if (*abort_flag || (it >= SA && !mbar_wait(a_empty(sa), (r & 1) ^ 1))) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st = smem + sa * C::A_STAGE;
+          const uint32_t fb = lead(a_full(sa));
+          if (leader) mbar_arrive_expect_tx(a_full(sa), t.bytes_a);
+          if (t.v0) tma_load_2d_pair(smem_u32(st), mA0, fb, kb * TC_BK, t.row_a0, pol_w);
+          if (t.v1) tma_load_2d_pair(smem_u32(st + C::A_BYTES), mA1, fb, kb * TC_BK, t.row_a1, pol_w);
+          progress[0] = it + 1;
+        }
+      }
+    }
+  } else if (warp == TC_TOKEN_WARP) {
+    if (lane == 0) {
+      // ---------- token-row (B) producer: this CTA's half of the tile ----------
+      const uint64_t pol_x = l2_policy_evict_last();
+      int it = 0;
+      for (int i = 0;; ++i) {
+        const int b = next_tile(i, true);
+        if (b < 0) break;
+        const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
+        const bool bs = !DOWN && t.shared;
+        const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
+        const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
+        const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sb = it % SB, r = it / SB;
+          if (*abort_flag || (it >= SB && !mbar_wait(b_empty(sb), (r & 1) ^ 1))) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st = smem + C::B_OFF + sb * C::B_STAGE;
+          const uint32_t fb = lead(b_full(sb));
+          const int kx = kb * TC_BK;
+          if (leader) mbar_arrive_expect_tx(b_full(sb), (uint32_t)t.npad * (TC_BK * 2));
+          int j = 0;
+          for (; j + 128 <= t.half; j += 128)
+            tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m128, fb, kx, t.row_b + j, pol_x);
+          for (; j + 64 <= t.half; j += 64)
+            tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m64, fb, kx, t.row_b + j, pol_x);
+          for (; j < t.half; j += 16)
+            tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m16, fb, kx, t.row_b + j, pol_x);
+          progress[1] = it + 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // ---------- MMA issuer (leader only) ----------
+        int it = 0, tl = 0;
+        for (int i = 0;; ++i) {
+          const int b = next_tile(i, true);
+          if (b < 0) break;
+          const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, 0);
+          const uint32_t idesc = umma_idesc_bf16(2 * TC_BM, t.npad);
+          const int u = tl % NBUF;  // TMEM buffer of this tile
+          const uint32_t dacc = tmem + (uint32_t)(u * 256);
+          if (*abort_flag ||
+              (tl >= NBUF && !mbar_wait_cluster(acc_empty(u), ((tl / NBUF) - 1) & 1))) {
+            *abort_flag = 1;
+            continue;  // keep reading the tile ring until the scheduler says "none"
+          }
+          tc_fence_after();
+          bool ok = true;
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const int sa = it % SA, sb = it % SB;
+            if (!mbar_wait(a_full(sa), (it / SA) & 1) || !mbar_wait(b_full(sb), (it / SB) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + sa * C::A_STAGE), a1 = a0 + C::A_BYTES;
+            const uint32_t bb = smem_u32(smem + C::B_OFF + sb * C::B_STAGE);
+#pragma unroll
+            for (int kk = 0; kk < TC_BK / 16; ++kk) {
+              const uint64_t bdesc = umma_desc_sw128(bb + kk * 32);
+              const uint32_t acc = (kb | kk) != 0;
+              umma_bf16_pair(dacc, umma_desc_sw128(a0 + kk * 32), bdesc, idesc, acc);
+              if (t.mma1) umma_bf16_pair(tmem + 256, umma_desc_sw128(a1 + kk * 32), bdesc, idesc, acc);
+            }
+            mma_issued = true;
+            umma_commit_pair(a_empty(sa));
+            umma_commit_pair(b_empty(sb));
+            progress[2] = it + 1;
+          }
+          if (!ok) {
+            *abort_flag = 1;
+            continue;
+          }
+          umma_commit_pair(acc_full(u));
+          ++tl;
+        }
+      }  // the peer has no MMA role
+    }
+    __syncwarp();
+  } else {
+    // ---------- epilogue warps 2 .. 2+TC_EPI_WARPS-1 (both CTAs) ----------
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    int tl = 0;
+    for (int i = 0;; ++i) {
+      const int b = next_tile(i, false);
+      __syncwarp();
+      if (lane == 0) release_tile(i % TC_TILE_RING);
+      if (b < 0) break;
+      const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
+      const int u = tl % NBUF;
+      if (*abort_flag || !mbar_wait(acc_full(u), (tl / NBUF) & 1)) {
+        *abort_flag = 1;
+        continue;
+      }
+      tc_fence_after();
+      // acc0 of buffer u at columns 256 u; acc1 (two accumulators) at 256
+      const uint32_t tl_addr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(u * 256);
+      for (int c = 32 * half; c < t.npad; c += 64) {
+        float va[32], vb[32];
+        tmem_load_2x32(tl_addr + c, tl_addr + (NACC == 2 ? 256 : 0) + c, va, vb);
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) continue;  // warp-uniform (shuffles below)
+        if (!DOWN) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
+          if (t.v0)
+            store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + t.out_f0 + 32 * q, n_out, va, c,
+                            t.ntok, lane);
+        } else if (t.shared) {
+          if (t.v0)
+            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + t.out_f0 + 32 * q, n_out, va, c,
+                           t.ntok, lane);
+          if (t.v1)
+            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + t.out_f1 + 32 * q, n_out, vb, c,
+                           t.ntok, lane);
+        } else {
+          const float gl = c + lane < t.ntok ? gates[perm[t.out_row0 + c + lane]] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float gv = __shfl_sync(0xffffffffu, gl, j);
+            va[j] *= gv;
+            vb[j] *= gv;
+          }
+          __nv_bfloat16* o = out + (size_t)(t.out_row0 + c) * n_out;
+          if (t.v0) store_rows_bf16(o + t.out_f0 + 32 * q, n_out, va, c, t.ntok, lane);
+          if (t.v1) store_rows_bf16(o + t.out_f1 + 32 * q, n_out, vb, c, t.ntok, lane);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(acc_empty(u)); else mbar_arrive_cluster(cluster_map(acc_empty(u), 0));
+      }
+      ++tl;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && leader) {
+    // Unwind (leader): the full barriers count both CTAs' copies; wait for
+    // what was issued, then for the MMAs (each wait bounded).
+    if (warp == 0 && lane == 0) {
+      for (int it = progress[2]; it < progress[0]; ++it)
+        mbar_wait(a_full(it % SA), (it / SA) & 1);
+    }
+    if (warp == TC_TOKEN_WARP && lane == 0) {
+      for (int it = progress[2]; it < progress[1]; ++it)
+        mbar_wait(b_full(it % SB), (it / SB) & 1);
+    }
+    if (warp == 1 && lane == 0 && mma_issued) {
+      umma_commit_pair_local(drain_bar);
+      mbar_wait(drain_bar, 0);
+    }
+    __syncthreads();
+  }
+  cluster_sync_all();  // neither CTA leaves while the other may still use its memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+}

@@ -22,6 +22,7 @@
 #include "dispatch.cuh"
 #include "experts_simt.cuh"
 #include "experts_tc.cuh"
+#include "experts_tc2.cuh"
 #include "ptx.cuh"
 #include "router.cuh"
 
@@ -35,8 +36,21 @@ constexpr int kRouterBK = 16;
 // Tensor-core GEMM variants: (BN tokens per tile, pipeline stages).
 // Tensor-core GEMM variants: BN tokens per tile, weight-ring and token-ring
 // depths (each fills ~224 KB of shared memory).
-constexpr int kBigBN = 256, kBigSA = 4, kBigSB = 3;
-constexpr int kSmallBN = 64, kSmallSA = 6, kSmallSB = 4;
+constexpr int kSmallBN = 64, kSmallSA = 6, kSmallSB = 4;  // 1-SM kernel, small token tiles
+constexpr int kBigBN = 256, kBigSA = 4, kBigSB = 3;        // 1-SM kernel, up to 256 tokens
+// CTA-pair kernels, up to 256 tokens, two 256-column accumulators per tile
+// (gate and up rows; two blocks of down-projection rows).  (One accumulator
+// with two TMEM buffers, which overlaps the epilogue with the next tile's MMAs,
+// measured slower for the second GEMM: it re-reads the token rows for every
+// 256 output rows instead of every 512.)
+constexpr int kPairBN = 256, kPairSA = 5, kPairSB = 4;
+// Kernel of each GEMM for the large token tiles: 1 = CTA pairs, 0 = one SM.
+#ifndef MOE_PAIR_GEMM1
+#define MOE_PAIR_GEMM1 1
+#endif
+#ifndef MOE_PAIR_GEMM2
+#define MOE_PAIR_GEMM2 1
+#endif
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -49,7 +63,7 @@ struct Plan {
   // dispatch
   int n_pair_blocks;
   // expert tiling
-  int bn, ft_a, ft_b, max_tiles_a, max_tiles_b;
+  int bn, ft_a, ft_b, tile_round, max_tiles_a, max_tiles_b;
   // workspace regions (byte offsets)
   size_t o_part, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh, total;
   size_t b_part, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh;
@@ -112,16 +126,27 @@ Plan make_plan(const moe_desc* d) {
 
   // expert tiling
   if (!p.route_only) {
+    p.tile_round = 16;
     if (p.simt) {
       p.bn = SIMT_TM;
       p.ft_a = p.h / SIMT_TN;
       p.ft_b = p.d / SIMT_TN;
     } else {
+      // about a hundred tokens per expert or more: CTA-pair tiles of up to
+      // 256 tokens (N a multiple of 32) over 256 (first GEMM) or 512 (second)
+      // weight rows; fewer: 1-SM tiles of up to 64 tokens over 128 / 256 rows
       const double per_expert = p.E > 0 ? (double)p.TK / p.E : 0.0;
       p.big_tiles = per_expert >= 96.0;
-      p.bn = p.big_tiles ? kBigBN : kSmallBN;
-      p.ft_a = p.h / TC_BM;
-      p.ft_b = (p.d / TC_BM + 1) / 2;
+      if (p.big_tiles) {
+        p.bn = kPairBN;
+        p.tile_round = 32;
+        p.ft_a = MOE_PAIR_GEMM1 ? (p.h + 2 * TC_BM - 1) / (2 * TC_BM) : p.h / TC_BM;
+        p.ft_b = MOE_PAIR_GEMM2 ? (p.d + 4 * TC_BM - 1) / (4 * TC_BM) : (p.d / TC_BM + 1) / 2;
+      } else {
+        p.bn = kSmallBN;
+        p.ft_a = p.h / TC_BM;
+        p.ft_b = (p.d / TC_BM + 1) / 2;
+      }
     }
     const long long tok_tiles = (long long)p.TK / p.bn + (p.TK < p.E ? p.TK : p.E) +
                                 (p.T + p.bn - 1) / p.bn + 1;
@@ -271,35 +296,56 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   return ok;
 }
 
-template <int BN, int SA, int SB>
-bool set_tc_smem() {
-  using C = TcCfg<BN, SA, SB>;
-  return cudaFuncSetAttribute(k_expert_tc<BN, SA, SB, false>,
+// The CTA-pair kernel of each GEMM.
+template <bool DOWN> struct PairCfg;
+template <> struct PairCfg<false> {
+  static constexpr int SA = kPairSA, SB = kPairSB, NACC = 2, NBUF = 1;
+};
+template <> struct PairCfg<true> {
+  static constexpr int SA = kPairSA, SB = kPairSB, NACC = 2, NBUF = 1;
+};
+
+template <bool DOWN>
+bool set_tc2_smem() {
+  using P = PairCfg<DOWN>;
+  return cudaFuncSetAttribute(k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, DOWN>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              C::SMEM_BYTES) == cudaSuccess &&
-         cudaFuncSetAttribute(k_expert_tc<BN, SA, SB, true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              C::SMEM_BYTES) == cudaSuccess;
+                              Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF>::SMEM_BYTES) == cudaSuccess;
 }
 
-// Persistent launches: one CTA per SM (at most one per tile); tiles are
-// handed out in table order by the kernels' own scheduler.
-template <int BN, int SA, int SB>
-void launch_tc(const Plan& p, const TcMaps& m, uint8_t* ws, int32_t* groups, const float* gates,
-               cudaStream_t s, cudaEvent_t between) {
-  using C = TcCfg<BN, SA, SB>;
+template <int BN, int SA, int SB, bool DOWN>
+bool set_tc1_smem() {
+  return cudaFuncSetAttribute(k_expert_tc<BN, SA, SB, DOWN>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TcCfg<BN, SA, SB>::SMEM_BYTES) == cudaSuccess;
+}
+
+// One expert GEMM on CTA pairs (one pair per two SMs) or on single SMs (one
+// CTA per SM), at most one CTA (pair) per tile.
+template <bool DOWN>
+void launch_gemm(const Plan& p, const TcMapsDev& m, bool pair, int BN, int max_tiles,
+                 int32_t* groups, const float* gates, const int32_t* perm, __nv_bfloat16* out,
+                 float* ysh, cudaStream_t s) {
   const int sms = sm_count();
-  const int grid_a = p.max_tiles_a < sms ? p.max_tiles_a : sms;
-  const int grid_b = p.max_tiles_b < sms ? p.max_tiles_b : sms;
-  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
-  __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
-  __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
-  float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
-  k_expert_tc<BN, SA, SB, false><<<grid_a, TC_THREADS, C::SMEM_BYTES, s>>>(
-      m.up, groups, p.E, p.d, p.h, hbuf, nullptr, perm, gates);
-  if (between) cudaEventRecord(between, s);
-  k_expert_tc<BN, SA, SB, true><<<grid_b, TC_THREADS, C::SMEM_BYTES, s>>>(
-      m.down, groups, p.E, p.h, p.d, yperm, ysh, perm, gates);
+  const int K = DOWN ? p.h : p.d, n_out = DOWN ? p.d : p.h;
+  if (pair) {
+    const int pairs = sms / 2;
+    const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
+    using P = PairCfg<DOWN>;
+    k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, DOWN>
+        <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF>::SMEM_BYTES, s>>>(
+            m, groups, p.E, K, n_out, out, ysh, perm, gates);
+  } else if (BN == kBigBN) {
+    const int grid = max_tiles < sms ? max_tiles : sms;
+    k_expert_tc<kBigBN, kBigSA, kBigSB, DOWN><<<grid, TC_THREADS,
+                                                  TcCfg<kBigBN, kBigSA, kBigSB>::SMEM_BYTES, s>>>(
+        m, groups, p.E, K, n_out, out, ysh, perm, gates);
+  } else {
+    const int grid = max_tiles < sms ? max_tiles : sms;
+    k_expert_tc<kSmallBN, kSmallSA, kSmallSB, DOWN>
+        <<<grid, TC_THREADS, TcCfg<kSmallBN, kSmallSA, kSmallSB>::SMEM_BYTES, s>>>(
+            m, groups, p.E, K, n_out, out, ysh, perm, gates);
+  }
 }
 
 template <typename T>
@@ -353,8 +399,12 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
   TcMaps maps;
   if (use_tc) {
     if (!make_tc_maps(p, x, experts, shared, ws, &maps)) return MOE_ERR_DEVICE;
-    const bool ok = p.big_tiles ? set_tc_smem<kBigBN, kBigSA, kBigSB>()
-                                : set_tc_smem<kSmallBN, kSmallSA, kSmallSB>();
+    const bool ok =
+        p.big_tiles
+            ? ((MOE_PAIR_GEMM1 ? set_tc2_smem<false>() : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
+               (MOE_PAIR_GEMM2 ? set_tc2_smem<true>() : set_tc1_smem<kBigBN, kBigSA, kBigSB, true>()))
+            : (set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, false>() &&
+               set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, true>());
     if (!ok) return MOE_ERR_LAUNCH;
   }
   float* part = reinterpret_cast<float*>(ws + p.o_part);
@@ -376,7 +426,7 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     k_block_rank<<<p.n_pair_blocks, 32, 0, s>>>(topk_idx, p.TK, p.E, rank, hist);
   }
   k_scan_groups<<<1, 1024, 0, s>>>(hist, p.n_pair_blocks, p.E, p.T, p.TK, load_counts, groups,
-                                   need_out ? p.bn : 0, p.ft_a, p.ft_b);
+                                   need_out ? p.bn : 0, p.ft_a, p.ft_b, p.tile_round);
   if (need_out) {
     int32_t* perm = reinterpret_cast<int32_t*>(ws + p.o_perm);
     int32_t* inv = reinterpret_cast<int32_t*>(ws + p.o_inv);
@@ -390,10 +440,15 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     } else if (p.simt) {
       launch_simt<__nv_bfloat16>(p, x, experts, shared, ws, groups, gates, s, between);
     } else {
-      if (p.big_tiles)
-        launch_tc<kBigBN, kBigSA, kBigSB>(p, maps, ws, groups, gates, s, between);
-      else
-        launch_tc<kSmallBN, kSmallSA, kSmallSB>(p, maps, ws, groups, gates, s, between);
+      const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
+      __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
+      __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
+      float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
+      launch_gemm<false>(p, maps.up, p.big_tiles && MOE_PAIR_GEMM1, p.bn, p.max_tiles_a, groups,
+                         gates, perm, hbuf, nullptr, s);
+      if (between) cudaEventRecord(between, s);
+      launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b, groups,
+                        gates, perm, yperm, ysh, s);
     }
     mark(4);
     const float* ysh = reinterpret_cast<const float*>(ws + p.o_ysh);
