@@ -148,8 +148,8 @@ MOE_API int moe_forward_host_io(const moe_desc* desc, const void* x_host,
  *   events[0] before the router (logits + top-k)
  *   events[1] before dispatch (ranks, scan, permute/gather)
  *   events[2] before expert GEMM 1 (gate/up + SwiGLU, shared expert included)
- *   events[3] before expert GEMM 2 (down + gate scale)
- *   events[4] before the combine
+ *   events[3] before expert GEMM 2 (down projection)
+ *   events[4] before the combine (gates, slot sums)
  *   events[5] after the combine
  * `events` points to MOE_N_PHASE_EVENTS cudaEvent_t handles (created by the
  * caller, not destroyed here).  Phases that do not run (route-only, T = 0)

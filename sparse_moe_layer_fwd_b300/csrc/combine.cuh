@@ -1,10 +1,13 @@
 // combine.cuh -- gated combine and the bias update.
 //
-// k_combine: y[t] = Y_sh[t] + sum_{j=0..k-1} Y_perm[inv[t*k+j]], summed in
-//   fp32 in that fixed slot order and rounded once to the output type (the
-//   gate g[t,j] was already applied when Y_perm was written).  One CTA per
-//   token, 8 elements (16 bytes of bf16) per thread per step, so every load
-//   and store is a coalesced 16-byte vector.  Deterministic: no atomics.
+// k_combine: y[t] = Y_sh[t] + sum_{j=0..k-1} g[t,j] * Y_perm[inv[t*k+j]],
+//   one fp32 fused multiply-add per slot in that fixed slot order, rounded
+//   once to the output type.  (The gate multiplies the expert's output row
+//   here rather than in the down-projection epilogue: the same product, and
+//   the tensor-core epilogue, which stalls the MMAs while it drains the
+//   accumulators, loses its per-token broadcasts.)  One CTA per token, 8
+//   elements (16 bytes of bf16) per thread per step, so every load and store
+//   is a coalesced 16-byte vector.  Deterministic: no atomics.
 // k_bias_update: b[e] = fp32(b[e] - fp32(gamma) * sgn(E*load[e] - TK))
 //   ("190行JAX复刻DeepSeek V3", section "最有价值的实验:无辅助损失均衡真的有效":
 //   an expert above the mean load T*k/E is lowered, one below it raised).
@@ -48,10 +51,15 @@ MOE_DEV void store8(__nv_bfloat16* p, const float* v) {
 template <typename TA>
 __global__ void __launch_bounds__(128)
 k_combine(const float* __restrict__ y_sh, const TA* __restrict__ y_perm,
-          const int32_t* __restrict__ inv, int T, int d, int k, TA* __restrict__ y) {
+          const int32_t* __restrict__ inv, const float* __restrict__ gates, int T, int d, int k,
+          TA* __restrict__ y) {
   __shared__ int rows[32];
+  __shared__ float gs[32];
   const int t = blockIdx.x;
-  if (threadIdx.x < k) rows[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
+    gs[threadIdx.x] = gates[(size_t)t * k + threadIdx.x];
+  }
   __syncthreads();
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float acc[8];
@@ -59,8 +67,9 @@ k_combine(const float* __restrict__ y_sh, const TA* __restrict__ y_perm,
     for (int j = 0; j < k; ++j) {
       float v[8];
       load8(y_perm + (size_t)rows[j] * d + c, v);
+      const float g = gs[j];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += v[q];
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, v[q], acc[q]);
     }
     store8(y + (size_t)t * d + c, acc);
   }

@@ -9,7 +9,8 @@
 // shared expert over all T tokens.  Tile = SIMT_TM tokens x SIMT_TN outputs;
 // the group table (dispatch.cuh) lists each group's token tiles.
 //   first GEMM  (DOWN = false): H[row] = silu(X W_gate^T) * (X W_up^T)
-//   second GEMM (DOWN = true) : routed  Y_perm[row] = g(row) * (H[row] W_down^T)
+//   second GEMM (DOWN = true) : routed  Y_perm[row] = H[row] W_down^T (the
+//                               gate is applied in the combine)
 //                               shared  Y_sh[t]     = H[TK + t] W_down^T (fp32)
 #pragma once
 
@@ -42,8 +43,7 @@ __global__ void __launch_bounds__(256)
 k_expert_simt(const T* __restrict__ wa0, const T* __restrict__ wa1, const T* __restrict__ sa0,
               const T* __restrict__ sa1, const T* __restrict__ b_routed,
               const T* __restrict__ b_shared, const int32_t* __restrict__ groups, int E, int K,
-              int n_out, T* __restrict__ out, float* __restrict__ y_sh,
-              const int32_t* __restrict__ perm, const float* __restrict__ gates) {
+              int n_out, T* __restrict__ out, float* __restrict__ y_sh) {
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
   const int32_t* toff = DOWN ? G.toff_b : G.toff_a;
   const int b = blockIdx.x;
@@ -118,7 +118,7 @@ k_expert_simt(const T* __restrict__ wa0, const T* __restrict__ wa1, const T* __r
       } else if (shared) {
         y_sh[(size_t)(tok0 + r) * n_out + f] = acc0[i][q];
       } else {
-        out[(size_t)row * n_out + f] = from_f<T>(gates[perm[row]] * acc0[i][q]);
+        out[(size_t)row * n_out + f] = from_f<T>(acc0[i][q]);
       }
     }
   }

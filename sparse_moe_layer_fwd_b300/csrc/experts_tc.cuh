@@ -180,6 +180,7 @@ struct TcCfg {
 // Geometry of one tile, computed identically by every role.
 struct TcTile {
   bool shared, has_a1;
+  bool reread;  // another token tile of this group reads the same weight rows
   int ntok, npad, tok0, f0, row_a0, row_a1, row_b, out_row0;
 };
 
@@ -189,6 +190,7 @@ MOE_DEV TcTile tc_tile(const GroupTable& G, const int32_t* toff, int E, int b, i
   const int g = find_group(toff, E, b);
   t.shared = g == E;
   const int nt = G.ntt[g];
+  t.reread = nt > 1;
   const int local = b - toff[g];
   const int ft = local / nt, tt = local % nt;
   const int n_g = G.off[g + 1] - G.off[g];
@@ -214,8 +216,7 @@ struct TcMapsDev {
 template <int BN, int SA, int SB, bool DOWN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
-            int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
-            const int32_t* __restrict__ perm, const float* __restrict__ gates) {
+            int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh) {
   using C = TcCfg<BN, SA, SB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -299,7 +300,10 @@ k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ 
   if (warp == 0) {
     if (lane == 0) {
       // ------------- tile scheduler + weight (A) producer -------------
-      const uint64_t pol_w = l2_policy_evict_first();
+      // weight rows read by one token tile: evict first; rows that the
+      // group's other token tiles (running at about the same time on other
+      // SMs) read again: normal priority, so that they meet in L2
+      const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
       int it = 0;
       for (int i = 0;; ++i) {
         const int s = i % TC_TILE_RING;
@@ -316,6 +320,7 @@ k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ 
         const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
         const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
         const uint32_t bytes = (t.has_a1 ? 2u : 1u) * C::A_BYTES;
+        const uint64_t pol_w = t.reread ? pol_again : pol_once;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int sa = it % SA, r = it / SA;
           if (it >= SA && !mbar_wait(a_empty(sa), (r & 1) ^ 1)) {
@@ -447,14 +452,6 @@ k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ 
             store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + fw + TC_BM, n_out, vb, c, t.ntok,
                            lane);
         } else {
-          // gate of token c + j, one per lane, broadcast by shuffles
-          const float gl = c + lane < t.ntok ? gates[perm[t.out_row0 + c + lane]] : 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float gv = __shfl_sync(0xffffffffu, gl, j);
-            va[j] *= gv;
-            vb[j] *= gv;
-          }
           __nv_bfloat16* o = out + (size_t)(t.out_row0 + c) * n_out + fw;
           store_rows_bf16(o, n_out, va, c, t.ntok, lane);
           if (t.has_a1) store_rows_bf16(o + TC_BM, n_out, vb, c, t.ntok, lane);

@@ -8,10 +8,12 @@
 //                of W_up; CTA r holds rows f0 + 128 r .. +127 of both, so its
 //                two TMEM accumulators hold gate and up for its own 128
 //                hidden units and the SwiGLU epilogue stays local.
-//   second GEMM: a pair tile covers 256 rows of W_down; CTA r holds rows
-//                f0 + 128 r .. +127 in one accumulator, and TMEM holds two such
-//                accumulators so that the epilogue of one tile overlaps the
-//                MMAs of the next (its K is short: 2048).
+//   second GEMM: a pair tile covers 512 rows of W_down, two blocks of 256;
+//                CTA r holds rows f0 + 128 r .. +127 and f0 + 256 + 128 r ..
+//                +127 in its two accumulators.  (One block per tile with two
+//                TMEM buffers, so that the epilogue overlaps the next tile's
+//                MMAs, streams the token tile twice as often and measured
+//                slower.)
 //   Token rows: CTA r holds rows r * N/2 .. of the N-token tile (N a
 //   multiple of 32), so each CTA streams half of the token tile.
 // Per 64-deep K step a CTA loads 32 KB of weights + N/2 x 128 B of tokens
@@ -37,9 +39,10 @@
 #define TC2_THREADS TC_THREADS
 #define TC2_CONSUMERS (TC_EPI_WARPS + 2)  // per CTA: epilogue warps, token producer, MMA or weight producer
 
-// NACC accumulators of 256 columns per tile (2: gate and up; 1: one block of
-// down-projection rows) and NBUF TMEM buffers of them (NACC * NBUF <= 2): with
-// two buffers the epilogue of one tile overlaps the MMAs of the next.
+// NACC accumulators of 256 columns per tile (2: gate and up, or two blocks
+// of down-projection rows; 1: one block) and NBUF TMEM buffers of them
+// (NACC * NBUF <= 2): with two buffers the epilogue of one tile overlaps the
+// MMAs of the next.
 template <int SA, int SB, int NACC, int NBUF>
 struct Tc2Cfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile
@@ -62,6 +65,7 @@ struct Tc2Cfg {
 struct Tc2Tile {
   bool shared, v0, v1;  // this CTA's weight sub-tiles exist (rows < n_out)
   bool mma1;            // the second accumulator is computed
+  bool reread;          // another token tile of this group reads the same weight rows
   int ntok, npad, half, tok0, row_a0, row_a1, row_b, out_row0, out_f0, out_f1;
   uint32_t bytes_a;     // weight bytes of one K step, both CTAs together
 };
@@ -73,6 +77,7 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   const int g = find_group(toff, E, b);
   t.shared = g == E;
   const int nt = G.ntt[g];
+  t.reread = nt > 1;
   const int local = b - toff[g];
   const int ft = local / nt, tt = local % nt;
   const int n_g = G.off[g + 1] - G.off[g];
@@ -106,8 +111,7 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
 template <int SA, int SB, int NACC, int NBUF, bool DOWN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC2_THREADS, 1)
 k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
-             int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
-             const int32_t* __restrict__ perm, const float* __restrict__ gates) {
+             int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh) {
   using C = Tc2Cfg<SA, SB, NACC, NBUF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -193,7 +197,10 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   if (warp == 0) {
     if (lane == 0) {
       // ---------- weight (A) producer; in the leader also the scheduler ----------
-      const uint64_t pol_w = l2_policy_evict_first();
+      // weight rows read by one token tile: evict first; rows that the
+      // group's other token tiles (taken at about the same time by other
+      // pairs) read again: normal priority, so that they meet in L2
+      const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
       int it = 0;
       for (int i = 0;; ++i) {
         int b;
@@ -217,6 +224,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
         const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
         const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
+        const uint64_t pol_w = t.reread ? pol_again : pol_once;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int sa = it % SA, r = it / SA;
           if (*abort_flag || (it >= SA && !mbar_wait(a_empty(sa), (r & 1) ^ 1))) {
@@ -352,13 +360,6 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + t.out_f1 + 32 * q, n_out, vb, c,
                            t.ntok, lane);
         } else {
-          const float gl = c + lane < t.ntok ? gates[perm[t.out_row0 + c + lane]] : 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float gv = __shfl_sync(0xffffffffu, gl, j);
-            va[j] *= gv;
-            vb[j] *= gv;
-          }
           __nv_bfloat16* o = out + (size_t)(t.out_row0 + c) * n_out;
           if (t.v0) store_rows_bf16(o + t.out_f0 + 32 * q, n_out, va, c, t.ntok, lane);
           if (t.v1) store_rows_bf16(o + t.out_f1 + 32 * q, n_out, vb, c, t.ntok, lane);

@@ -4,7 +4,7 @@
 // validation, the workspace layout, TMA tensor maps, and the launch sequence
 //   router logits -> router top-k -> block ranks -> scan + tile table ->
 //   permute/gather -> expert GEMM 1 (gate/up + SwiGLU) -> expert GEMM 2
-//   (down + gate scale) -> combine
+//   (down projection) -> combine (gates applied)
 // all enqueued on the caller's stream with no host synchronisation (tile
 // counts live in device memory; GEMM grids are sized by an upper bound and
 // surplus CTAs return at once).
@@ -324,8 +324,7 @@ bool set_tc1_smem() {
 // CTA per SM), at most one CTA (pair) per tile.
 template <bool DOWN>
 void launch_gemm(const Plan& p, const TcMapsDev& m, bool pair, int BN, int max_tiles,
-                 int32_t* groups, const float* gates, const int32_t* perm, __nv_bfloat16* out,
-                 float* ysh, cudaStream_t s) {
+                 int32_t* groups, __nv_bfloat16* out, float* ysh, cudaStream_t s) {
   const int sms = sm_count();
   const int K = DOWN ? p.h : p.d, n_out = DOWN ? p.d : p.h;
   if (pair) {
@@ -334,36 +333,34 @@ void launch_gemm(const Plan& p, const TcMapsDev& m, bool pair, int BN, int max_t
     using P = PairCfg<DOWN>;
     k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, DOWN>
         <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF>::SMEM_BYTES, s>>>(
-            m, groups, p.E, K, n_out, out, ysh, perm, gates);
+            m, groups, p.E, K, n_out, out, ysh);
   } else if (BN == kBigBN) {
     const int grid = max_tiles < sms ? max_tiles : sms;
     k_expert_tc<kBigBN, kBigSA, kBigSB, DOWN><<<grid, TC_THREADS,
                                                   TcCfg<kBigBN, kBigSA, kBigSB>::SMEM_BYTES, s>>>(
-        m, groups, p.E, K, n_out, out, ysh, perm, gates);
+        m, groups, p.E, K, n_out, out, ysh);
   } else {
     const int grid = max_tiles < sms ? max_tiles : sms;
     k_expert_tc<kSmallBN, kSmallSA, kSmallSB, DOWN>
         <<<grid, TC_THREADS, TcCfg<kSmallBN, kSmallSA, kSmallSB>::SMEM_BYTES, s>>>(
-            m, groups, p.E, K, n_out, out, ysh, perm, gates);
+            m, groups, p.E, K, n_out, out, ysh);
   }
 }
 
 template <typename T>
 void launch_simt(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
-                 uint8_t* ws, int32_t* groups, const float* gates, cudaStream_t s,
-                 cudaEvent_t between) {
+                 uint8_t* ws, int32_t* groups, cudaStream_t s, cudaEvent_t between) {
   const T* xp = reinterpret_cast<const T*>(ws + p.o_xperm);
   T* hbuf = reinterpret_cast<T*>(ws + p.o_h);
   T* yperm = reinterpret_cast<T*>(ws + p.o_yperm);
   float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
-  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
   k_expert_simt<T, false><<<p.max_tiles_a, 256, 0, s>>>(
       (const T*)ex->w_gate, (const T*)ex->w_up, (const T*)sh->w_gate, (const T*)sh->w_up, xp,
-      (const T*)x, groups, p.E, p.d, p.h, hbuf, nullptr, perm, gates);
+      (const T*)x, groups, p.E, p.d, p.h, hbuf, nullptr);
   if (between) cudaEventRecord(between, s);
   k_expert_simt<T, true><<<p.max_tiles_b, 256, 0, s>>>(
       (const T*)ex->w_down, nullptr, (const T*)sh->w_down, nullptr, hbuf, hbuf, groups, p.E, p.h,
-      p.d, yperm, ysh, perm, gates);
+      p.d, yperm, ysh);
 }
 
 int forward_impl(const moe_desc* desc, const void* x, const float* w_router, const float* bias,
@@ -436,29 +433,28 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     mark(2);
     cudaEvent_t between = events ? static_cast<cudaEvent_t>(events[3]) : nullptr;
     if (p.f32) {
-      launch_simt<float>(p, x, experts, shared, ws, groups, gates, s, between);
+      launch_simt<float>(p, x, experts, shared, ws, groups, s, between);
     } else if (p.simt) {
-      launch_simt<__nv_bfloat16>(p, x, experts, shared, ws, groups, gates, s, between);
+      launch_simt<__nv_bfloat16>(p, x, experts, shared, ws, groups, s, between);
     } else {
-      const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
       __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
       __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
       float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
       launch_gemm<false>(p, maps.up, p.big_tiles && MOE_PAIR_GEMM1, p.bn, p.max_tiles_a, groups,
-                         gates, perm, hbuf, nullptr, s);
+                         hbuf, nullptr, s);
       if (between) cudaEventRecord(between, s);
       launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b, groups,
-                        gates, perm, yperm, ysh, s);
+                        yperm, ysh, s);
     }
     mark(4);
     const float* ysh = reinterpret_cast<const float*>(ws + p.o_ysh);
     if (p.f32)
       k_combine<float><<<p.T, 128, 0, s>>>(ysh, reinterpret_cast<const float*>(ws + p.o_yperm),
-                                           inv, p.T, p.d, p.k, static_cast<float*>(y));
+                                           inv, gates, p.T, p.d, p.k, static_cast<float*>(y));
     else
       k_combine<__nv_bfloat16><<<p.T, 128, 0, s>>>(
-          ysh, reinterpret_cast<const __nv_bfloat16*>(ws + p.o_yperm), inv, p.T, p.d, p.k,
-          static_cast<__nv_bfloat16*>(y));
+          ysh, reinterpret_cast<const __nv_bfloat16*>(ws + p.o_yperm), inv, gates, p.T, p.d,
+          p.k, static_cast<__nv_bfloat16*>(y));
   } else {
     mark(2);
     mark(3);
