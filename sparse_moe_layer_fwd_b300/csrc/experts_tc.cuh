@@ -158,6 +158,51 @@ MOE_DEV void store_rows_f32(float* dst, size_t ld, const float (&v)[32], int c0,
   }
 }
 
+// Staged output box: 32 tokens x 32 outputs of bf16 in shared memory, one
+// 64-byte row per token, its four 16-byte chunks swizzled as the TMA 64-byte
+// swizzle expects (chunk ^ ((row >> 1) & 3)), so that the eight rows written
+// by each stmatrix fall into eight different bank groups.
+#define TC_BOX_BYTES 2048
+
+// One warp stages TMEM columns c .. c+31 of its 32 lanes (ta, tb: the
+// addresses of column c in the warp's lane quarter) into `box`: box row j =
+// column c + j (a token), 32 outputs (the lanes) per row.  Values are
+// silu(acc a) * acc b when SWIGLU, else acc a, rounded to bf16.  The 16x256b
+// loads give each thread pairs of adjacent columns of one lane -- the
+// fragment layout of an 8 x 8 matrix -- and stmatrix .trans writes the
+// transpose, 8 outputs of one token per 16-byte row piece.
+template <bool SWIGLU>
+MOE_DEV void stage_box_bf16(uint32_t ta, uint32_t tb, uint32_t box, int lane) {
+  const int mm = lane >> 3, ii = lane & 7;
+#pragma unroll
+  for (int L = 0; L < 32; L += 16) {
+    uint32_t ra[16], rb[16];
+    if (SWIGLU)
+      tmem_load_16x256b_2(ta + ((uint32_t)L << 16), tb + ((uint32_t)L << 16), ra, rb);
+    else
+      tmem_load_16x256b(ta + ((uint32_t)L << 16), ra);
+    // matrix m = 2 i + hf: lanes L + 8 hf .. +7, columns 8 i .. 8 i + 7
+    uint32_t w[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      float lo = __uint_as_float(ra[2 * m]), hi = __uint_as_float(ra[2 * m + 1]);
+      if (SWIGLU) {
+        lo = silu_fast(lo) * __uint_as_float(rb[2 * m]);
+        hi = silu_fast(hi) * __uint_as_float(rb[2 * m + 1]);
+      }
+      w[m] = pack_bf16x2(lo, hi);
+    }
+    // stmatrix ip covers matrices 4 ip .. 4 ip + 3; thread 8 mm + ii gives
+    // the row of token 8 i + ii, outputs L + 8 hf .. +7, of matrix 4 ip + mm
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip) {
+      const int tok = 8 * (2 * ip + (mm >> 1)) + ii, chunk = (L >> 3) + (mm & 1);
+      stmatrix_x4_trans(box + (uint32_t)(tok * 64 + 16 * (chunk ^ ((tok >> 1) & 3))), w[4 * ip],
+                        w[4 * ip + 1], w[4 * ip + 2], w[4 * ip + 3]);
+    }
+  }
+}
+
 template <int BN, int SA, int SB>
 struct TcCfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile
@@ -211,6 +256,7 @@ struct TcMapsDev {
   CUtensorMap a0, a1, sa0, sa1;   // weights, 128-row boxes (routed, shared)
   CUtensorMap b128, b64, b16;     // token rows of the routed groups
   CUtensorMap bs128, bs64, bs16;  // token rows of the shared group
+  CUtensorMap out;                // bf16 output rows (H or Y_perm), 32 x 32 boxes, 64-byte swizzle
 };
 
 template <int BN, int SA, int SB, bool DOWN>

@@ -43,13 +43,16 @@
 // of down-projection rows; 1: one block) and NBUF TMEM buffers of them
 // (NACC * NBUF <= 2): with two buffers the epilogue of one tile overlaps the
 // MMAs of the next.
-template <int SA, int SB, int NACC, int NBUF>
+// OUTB: output boxes staged per epilogue warp (0: the epilogue stores from
+// registers; 1 or 2: bf16 outputs go out by TMA store from shared memory).
+template <int SA, int SB, int NACC, int NBUF, int OUTB>
 struct Tc2Cfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile
   static constexpr int A_STAGE = NACC * A_BYTES;
   static constexpr int B_STAGE = 128 * TC_BK * 2;    // half of a 256-token tile
   static constexpr int B_OFF = SA * A_STAGE;
-  static constexpr int BAR_OFF = B_OFF + SB * B_STAGE;
+  static constexpr int STG_OFF = B_OFF + SB * B_STAGE;
+  static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * OUTB * TC_BOX_BYTES;
   // a_full, a_empty [SA]; b_full, b_empty [SB]; acc_full, acc_empty [2];
   // drain; tile_full, tile_empty [RING]
   static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING;
@@ -108,11 +111,15 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   return t;
 }
 
-template <int SA, int SB, int NACC, int NBUF, bool DOWN>
+template <int SA, int SB, int NACC, int NBUF, int OUTB, bool DOWN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC2_THREADS, 1)
 k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
              int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh) {
-  using C = Tc2Cfg<SA, SB, NACC, NBUF>;
+  using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB>;
+  static_assert(OUTB >= 0 && OUTB <= 2, "staged boxes per epilogue warp");
+  // second GEMM with both 256-row blocks in one TMEM buffer: staggered blocks
+  constexpr bool STAG = DOWN && NACC == 2 && NBUF == 1;
+  static_assert(!DOWN || STAG || NACC == 1, "second GEMM: two staggered blocks or one block");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -282,43 +289,85 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         for (int i = 0;; ++i) {
           const int b = next_tile(i, true);
           if (b < 0) break;
+          if (*abort_flag) continue;  // keep reading the tile ring until the scheduler says "none"
           const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, 0);
           const uint32_t idesc = umma_idesc_bf16(2 * TC_BM, t.npad);
           const int u = tl % NBUF;  // TMEM buffer of this tile
-          const uint32_t dacc = tmem + (uint32_t)(u * 256);
-          if (*abort_flag ||
-              (tl >= NBUF && !mbar_wait_cluster(acc_empty(u), ((tl / NBUF) - 1) & 1))) {
-            *abort_flag = 1;
-            continue;  // keep reading the tile ring until the scheduler says "none"
-          }
-          tc_fence_after();
-          bool ok = true;
-          for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int sa = it % SA, sb = it % SB;
-            if (!mbar_wait(a_full(sa), (it / SA) & 1) || !mbar_wait(b_full(sb), (it / SB) & 1)) {
-              ok = false;
-              break;
-            }
+          // k step kb of this tile uses ring stage it + kb
+          auto stage_ready = [&](int kb) -> bool {
+            const int st = it + kb;
+            if (!mbar_wait(a_full(st % SA), (st / SA) & 1) || !mbar_wait(b_full(st % SB), (st / SB) & 1))
+              return false;
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + sa * C::A_STAGE), a1 = a0 + C::A_BYTES;
-            const uint32_t bb = smem_u32(smem + C::B_OFF + sb * C::B_STAGE);
+            return true;
+          };
+          // the four K=16 MMAs of k step kb into accumulator w (0: columns
+          // 256 u, 1: columns 256)
+          auto issue = [&](int kb, int w) {
+            const int st = it + kb;
+            const uint32_t a = smem_u32(smem + (st % SA) * C::A_STAGE) + (uint32_t)(w * C::A_BYTES);
+            const uint32_t bb = smem_u32(smem + C::B_OFF + (st % SB) * C::B_STAGE);
+            const uint32_t d = tmem + (w ? 256u : (uint32_t)(u * 256));
 #pragma unroll
-            for (int kk = 0; kk < TC_BK / 16; ++kk) {
-              const uint64_t bdesc = umma_desc_sw128(bb + kk * 32);
-              const uint32_t acc = (kb | kk) != 0;
-              umma_bf16_pair(dacc, umma_desc_sw128(a0 + kk * 32), bdesc, idesc, acc);
-              if (t.mma1) umma_bf16_pair(tmem + 256, umma_desc_sw128(a1 + kk * 32), bdesc, idesc, acc);
-            }
+            for (int kk = 0; kk < TC_BK / 16; ++kk)
+              umma_bf16_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32), idesc,
+                             (kb | kk) != 0);
             mma_issued = true;
-            umma_commit_pair(a_empty(sa));
-            umma_commit_pair(b_empty(sb));
-            progress[2] = it + 1;
+          };
+          auto release = [&](int kb) {  // the stage is free once its MMAs complete
+            const int st = it + kb;
+            umma_commit_pair(a_empty(st % SA));
+            umma_commit_pair(b_empty(st % SB));
+            progress[2] = st + 1;
+          };
+          bool ok;
+          if (STAG) {
+            // Second GEMM: block 0 runs S k steps ahead of block 1 at the
+            // start of the tile and finishes S k steps before it, so the
+            // drain of each block overlaps MMAs of the other.
+            const int S = min(min(SA, SB), nkb / 2);
+            ok = tl == 0 || mbar_wait_cluster(acc_empty(0), (tl - 1) & 1);
+            tc_fence_after();
+            for (int kb = 0; ok && kb < S; ++kb)
+              if ((ok = stage_ready(kb))) issue(kb, 0);
+            ok = ok && (tl == 0 || mbar_wait_cluster(acc_empty(1), (tl - 1) & 1));
+            tc_fence_after();
+            for (int kb = 0; ok && kb < S; ++kb) {
+              if (t.mma1) issue(kb, 1);
+              release(kb);
+            }
+            for (int kb = S; ok && kb < nkb - S; ++kb) {
+              if ((ok = stage_ready(kb))) {
+                issue(kb, 0);
+                if (t.mma1) issue(kb, 1);
+                release(kb);
+              }
+            }
+            for (int kb = nkb - S; ok && kb < nkb; ++kb)
+              if ((ok = stage_ready(kb))) issue(kb, 0);
+            if (ok) umma_commit_pair(acc_full(0));
+            for (int kb = nkb - S; ok && kb < nkb; ++kb) {
+              if (t.mma1) issue(kb, 1);
+              release(kb);
+            }
+            if (ok) umma_commit_pair(acc_full(1));
+          } else {
+            ok = tl < NBUF || mbar_wait_cluster(acc_empty(u), ((tl / NBUF) - 1) & 1);
+            tc_fence_after();
+            for (int kb = 0; ok && kb < nkb; ++kb) {
+              if ((ok = stage_ready(kb))) {
+                issue(kb, 0);
+                if (t.mma1) issue(kb, 1);
+                release(kb);
+              }
+            }
+            if (ok) umma_commit_pair(acc_full(u));
           }
           if (!ok) {
             *abort_flag = 1;
             continue;
           }
-          umma_commit_pair(acc_full(u));
+          it += nkb;
           ++tl;
         }
       }  // the peer has no MMA role
@@ -326,8 +375,13 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     __syncwarp();
   } else {
     // ---------- epilogue warps 2 .. 2+TC_EPI_WARPS-1 (both CTAs) ----------
+    // Warp (q, half) drains TMEM lanes 32 q .. +31 (its 32 output rows),
+    // token columns 32 half + 64 j.  The first GEMM drains both accumulators
+    // at once (SwiGLU); the second drains block 0, frees it, then block 1.
     const int q = warp & 3, half = (warp - 2) >> 2;
-    int tl = 0;
+    const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
+    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+    int tl = 0, nbox = 0;
     for (int i = 0;; ++i) {
       const int b = next_tile(i, false);
       __syncwarp();
@@ -335,43 +389,61 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       if (b < 0) break;
       const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
       const int u = tl % NBUF;
-      if (*abort_flag || !mbar_wait(acc_full(u), (tl / NBUF) & 1)) {
-        *abort_flag = 1;
-        continue;
-      }
-      tc_fence_after();
-      // acc0 of buffer u at columns 256 u; acc1 (two accumulators) at 256
-      const uint32_t tl_addr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(u * 256);
-      for (int c = 32 * half; c < t.npad; c += 64) {
-        float va[32], vb[32];
-        tmem_load_2x32(tl_addr + c, tl_addr + (NACC == 2 ? 256 : 0) + c, va, vb);
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) continue;  // warp-uniform (shuffles below)
-        if (!DOWN) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
-          if (t.v0)
-            store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + t.out_f0 + 32 * q, n_out, va, c,
-                            t.ntok, lane);
-        } else if (t.shared) {
-          if (t.v0)
-            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + t.out_f0 + 32 * q, n_out, va, c,
-                           t.ntok, lane);
-          if (t.v1)
-            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + t.out_f1 + 32 * q, n_out, vb, c,
-                           t.ntok, lane);
-        } else {
-          __nv_bfloat16* o = out + (size_t)(t.out_row0 + c) * n_out;
-          if (t.v0) store_rows_bf16(o + t.out_f0 + 32 * q, n_out, va, c, t.ntok, lane);
-          if (t.v1) store_rows_bf16(o + t.out_f1 + 32 * q, n_out, vb, c, t.ntok, lane);
+      for (int ph = 0; ph < (STAG ? 2 : 1); ++ph) {
+        const int bi = STAG ? ph : u;  // barrier pair of this phase
+        if (*abort_flag || !mbar_wait(acc_full(bi), STAG ? (tl & 1) : ((tl / NBUF) & 1))) {
+          *abort_flag = 1;
+          break;
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(acc_empty(u)); else mbar_arrive_cluster(cluster_map(acc_empty(u), 0));
+        tc_fence_after();
+        const uint32_t ta = lanes + (uint32_t)((STAG ? ph : u) * 256);  // this phase's accumulator
+        const uint32_t tb = lanes + 256;                                // GEMM 1: up projection
+        const bool valid = ph ? t.v1 : t.v0;
+        const int of = (ph ? t.out_f1 : t.out_f0) + 32 * q;  // first output column of the warp
+        for (int c = 32 * half; c < t.npad; c += 64) {
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+          if (OUTB > 0 && c + 32 <= t.ntok && !(DOWN && t.shared)) {
+            // 32 whole tokens of bf16 output: stage the box in shared
+            // memory and store it with TMA (boxes used round robin)
+            const uint32_t box = stg + (uint32_t)((nbox % (OUTB > 0 ? OUTB : 1)) * TC_BOX_BYTES);
+            if (lane == 0) bulk_wait_read<(OUTB > 0 ? OUTB - 1 : 0)>();  // the box's last store read it
+            __syncwarp();
+            stage_box_bf16<!DOWN>(ta + c, tb + c, box, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (valid) tma_store_2d(&maps.out, box, of, t.out_row0 + c);
+              bulk_commit();
+            }
+            ++nbox;
+            continue;
+          }
+          // from registers: a ragged last chunk, or fp32 shared-expert rows
+          float va[32], vb[32];
+          if (!DOWN)
+            tmem_load_2x32(ta + c, tb + c, va, vb);
+          else
+            tmem_load_32(ta + c, va);
+          if (!valid) continue;
+          if (!DOWN) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
+            store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
+          } else if (t.shared) {
+            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
+          } else {
+            store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(acc_empty(bi)); else mbar_arrive_cluster(cluster_map(acc_empty(bi), 0));
+        }
       }
       ++tl;
     }
+    if (OUTB > 0 && lane == 0) bulk_wait_all();  // this warp's stores are complete
   }
 
   tc_fence_before();

@@ -33,7 +33,6 @@ constexpr double kRouterCtaSlots = 296;  // router GEMM CTAs resident at once: 2
                                          // the results do not depend on the device)
 constexpr int kRouterBK = 16;
 
-// Tensor-core GEMM variants: (BN tokens per tile, pipeline stages).
 // Tensor-core GEMM variants: BN tokens per tile, weight-ring and token-ring
 // depths (each fills ~224 KB of shared memory).
 constexpr int kSmallBN = 64, kSmallSA = 6, kSmallSB = 4;  // 1-SM kernel, small token tiles
@@ -43,7 +42,28 @@ constexpr int kBigBN = 256, kBigSA = 4, kBigSB = 3;        // 1-SM kernel, up to
 // with two TMEM buffers, which overlaps the epilogue with the next tile's MMAs,
 // measured slower for the second GEMM: it re-reads the token rows for every
 // 256 output rows instead of every 512.)
-constexpr int kPairBN = 256, kPairSA = 5, kPairSB = 4;
+// Ring depths and staged output boxes per epilogue warp (used round robin)
+// of each pair GEMM: the bf16 outputs go out through shared memory by TMA
+// store, and the staging boxes take the place of ring stages.
+constexpr int kPairBN = 256;
+#ifndef MOE_PAIR1_SA
+#define MOE_PAIR1_SA 4
+#endif
+#ifndef MOE_PAIR1_SB
+#define MOE_PAIR1_SB 4
+#endif
+#ifndef MOE_PAIR1_OUTB
+#define MOE_PAIR1_OUTB 2
+#endif
+#ifndef MOE_PAIR2_SA
+#define MOE_PAIR2_SA 4
+#endif
+#ifndef MOE_PAIR2_SB
+#define MOE_PAIR2_SB 4
+#endif
+#ifndef MOE_PAIR2_OUTB
+#define MOE_PAIR2_OUTB 2
+#endif
 // Kernel of each GEMM for the large token tiles: 1 = CTA pairs, 0 = one SM.
 #ifndef MOE_PAIR_GEMM1
 #define MOE_PAIR_GEMM1 1
@@ -202,6 +222,20 @@ EncodeTiledFn encode_fn() {
 // bf16 matrix [rows, cols] (row-major) read in boxes of 64 columns (128
 // bytes) x box_rows rows with the 128-byte swizzle; rows past the end read
 // as zero.
+// bf16 output rows [rows, cols] for TMA stores of 32 x 32 boxes with the
+// 64-byte swizzle (the epilogue's staging layout).
+bool make_out_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows <= 0) return false;
@@ -293,24 +327,29 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   m->down.bs128 = m->down.b128;
   m->down.bs64 = m->down.b64;
   m->down.bs16 = m->down.b16;
+  ok &= make_out_map(&m->up.out, ws + p.o_h, (long long)p.TK + p.T, p.h);
+  ok &= make_out_map(&m->down.out, ws + p.o_yperm, p.TK, p.d);
   return ok;
 }
 
 // The CTA-pair kernel of each GEMM.
 template <bool DOWN> struct PairCfg;
 template <> struct PairCfg<false> {
-  static constexpr int SA = kPairSA, SB = kPairSB, NACC = 2, NBUF = 1;
+  static constexpr int SA = MOE_PAIR1_SA, SB = MOE_PAIR1_SB, NACC = 2, NBUF = 1,
+                       OUTB = MOE_PAIR1_OUTB;
 };
 template <> struct PairCfg<true> {
-  static constexpr int SA = kPairSA, SB = kPairSB, NACC = 2, NBUF = 1;
+  static constexpr int SA = MOE_PAIR2_SA, SB = MOE_PAIR2_SB, NACC = 2, NBUF = 1,
+                       OUTB = MOE_PAIR2_OUTB;
 };
 
 template <bool DOWN>
 bool set_tc2_smem() {
   using P = PairCfg<DOWN>;
-  return cudaFuncSetAttribute(k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, DOWN>,
+  return cudaFuncSetAttribute(k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, DOWN>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF>::SMEM_BYTES) == cudaSuccess;
+                              Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES) ==
+         cudaSuccess;
 }
 
 template <int BN, int SA, int SB, bool DOWN>
@@ -331,8 +370,8 @@ void launch_gemm(const Plan& p, const TcMapsDev& m, bool pair, int BN, int max_t
     const int pairs = sms / 2;
     const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
     using P = PairCfg<DOWN>;
-    k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, DOWN>
-        <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF>::SMEM_BYTES, s>>>(
+    k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, DOWN>
+        <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES, s>>>(
             m, groups, p.E, K, n_out, out, ysh);
   } else if (BN == kBigBN) {
     const int grid = max_tiles < sms ? max_tiles : sms;

@@ -174,9 +174,24 @@ MOE_DEV void umma_commit(uint32_t bar) {
 #define MOE_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
                   "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 
-// Two 32-column loads of this warp's 32 TMEM lanes (one fp32 value per lane
-// per column), from column addresses ta and tb, followed by the wait, in one
-// asm statement so no register is read before the wait.
+// One 32-column load of this warp's 32 TMEM lanes (one fp32 value per lane
+// per column) and its wait, in one asm statement so that no register is read
+// before the wait.
+MOE_DEV void tmem_load_32(uint32_t ta, float* a) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : MOE_R8(0), MOE_R8(8), MOE_R8(16), MOE_R8(24)
+      : "r"(ta)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(r[i]);
+}
+
+// Two such loads, from column addresses ta and tb, and one wait.
 MOE_DEV void tmem_load_2x32(uint32_t ta, uint32_t tb, float* a, float* b) {
   uint32_t r[64];
   asm volatile(
@@ -198,6 +213,62 @@ MOE_DEV void tmem_load_2x32(uint32_t ta, uint32_t tb, float* a, float* b) {
   }
 }
 #undef MOE_R8
+
+// TMEM -> registers in the 16x256b shape, four repetitions along columns:
+// for a TMEM address with lane field b (a multiple of 16 inside the warp's
+// 32-lane quarter) and column c, thread t receives in r[4 i + j] lane
+// b + t/4 + 8 (j/2), column c + 8 i + 2 (t%4) + (j%2), i = 0..3 -- the
+// accumulator-fragment layout that stmatrix consumes.  Two loads, one wait.
+#define MOE_R16(r) "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), \
+    "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),    \
+    "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+MOE_DEV void tmem_load_16x256b_2(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : MOE_R16(a), MOE_R16(b)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+MOE_DEV void tmem_load_16x256b(uint32_t ta, uint32_t (&a)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : MOE_R16(a)
+      : "r"(ta)
+      : "memory");
+}
+#undef MOE_R16
+
+// Four 8 x 8 b16 matrices from fragment registers (thread t: row t/4,
+// columns 2 (t%4) and +1 of each) to shared memory, transposed: the row whose
+// address thread 8 m + i gives receives column i of matrix m.
+MOE_DEV void stmatrix_x4_trans(uint32_t addr, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+               :: "r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
+}
+
+// Generic-proxy writes to shared memory become visible to the async proxy
+// (TMA) once the writing threads execute this fence.
+MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// TMA store of one box from shared memory; completion tracked by bulk groups.
+MOE_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               :: "l"(map), "r"(x), "r"(y), "r"(src) : "memory");
+}
+MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed store has finished reading its shared-memory source
+MOE_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the N most recently committed stores have read their sources
+template <int N>
+MOE_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory"); }
+// every committed store has completed
+MOE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------------ CTA pairs
 // Primitives for the 2-SM (cta_group::2) tensor-core MMA: a cluster of two
