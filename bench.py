@@ -47,7 +47,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (fwd, bf16) at 1 B300; % of tensor-core or HBM roofline"
-KERNELS_PER_STEP = 8  # router logits, top-k, block ranks, scan, permute, GEMM 1, GEMM 2, combine
+def tc_router(wl):
+    """The library routes bf16 tokens over 96 experts or more on the tensor
+    cores (router weights split into three bf16 terms), else on CUDA cores."""
+    return wl.dtype == "bf16" and wl.E >= 96 and wl.T > 0
+
+
+def kernels_per_step(wl, route_only):
+    """Kernels one forward launches: router (weight split + MMA, or FFMA
+    logits), top-k, block ranks, scan [, permute, GEMM 1, GEMM 2, combine]."""
+    n = (2 if tc_router(wl) else 1) + 3
+    return n if route_only else n + 4
 
 # DRAM traffic of expert GEMM 1 per launch from ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum, one capture of the full-size workload; both are
@@ -356,11 +366,19 @@ def run_ours(args, wl):
 
     peaks = _peaks()
     if route_only:
-        # fp32 router GEMM on CUDA cores: 148 SMs x 128 FP32 lanes x 2 FLOP
-        # per clock at the maximum SM clock
-        fma_peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
         rflops = 2.0 * wl.T * wl.E * wl.d
         ach = rflops / (phase_ms[0] / 1e3) / 1e12
+        if tc_router(wl):
+            # three bf16 MMAs per fp32-exact product: the peak for the
+            # algorithmic FLOPs is a third of the dense bf16 peak
+            rpeak, rbound = peaks["bf16_tflops"] / 3.0, "tensor"
+            rkind = f"{peaks['source']} bf16 burst / 3 (router weights as three bf16 terms)"
+            rkernel = "k_router_split + k_router_tc + k_router_topk (router phase)"
+        else:
+            # fp32 FFMA on CUDA cores: 148 SMs x 128 lanes x 2 FLOP x max clock
+            rpeak, rbound = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "alu"
+            rkind = "148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock"
+            rkernel = "k_router_logits (fp32 FFMA) + k_router_topk (router phase)"
         line = {
             "metric": METRIC + " [routing only]", "value": wl.T * args.steps / (elapsed_ms / 1e3),
             "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -369,13 +387,13 @@ def run_ours(args, wl):
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/d) router)",
             "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
                        "route_only": True, "l2": l2_note},
-            "roofline": {"bound": "alu", "kernel": "k_router_logits (fp32 FFMA)",
-                         "achieved": ach, "peak": fma_peak, "unit": "TFLOP/s",
-                         "frac": ach / fma_peak, "traffic": None,
-                         "peak_kind": "148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock",
+            "roofline": {"bound": rbound, "kernel": rkernel,
+                         "achieved": ach, "peak": rpeak, "unit": "TFLOP/s",
+                         "frac": ach / rpeak, "traffic": None, "peak_kind": rkind,
                          "flops_per_launch": rflops, "ms_per_launch": phase_ms[0]},
             "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
-            "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clocks,
+            "e2e": e2e, "gpu_launches": kernels_per_step(wl, True) * args.steps,
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
         if ws > 1:
@@ -432,7 +450,7 @@ def run_ours(args, wl):
                    "l2": l2_note},
         "roofline": roof, "roofline_layer": layer_roof,
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": kernels_per_step(wl, False) * args.steps,
         "clocks": clocks, "kernel_sha": sha,
     }
     print(json.dumps(line), flush=True)

@@ -187,7 +187,9 @@ MOE_API const char* moe_error_string(int code);
  * `desc`, for tests that inspect intermediate results.  `names` receives up
  * to `cap` entries of (name, offset, bytes); returns the number of regions
  * (or a negative MOE_ERR_*).  Region names: "router_part" (fp32 partial
- * logits), "blk_hist", "pair_rank", "groups" (int32 group table),
+ * logits), "router_w3" (the router weights as three bf16 terms, for the
+ * tensor-core router; empty otherwise), "blk_hist", "pair_rank", "groups"
+ * (int32 group table),
  * "perm" (permuted row -> token*k+slot), "inv" (token*k+slot -> permuted row),
  * "x_perm", "h", "y_perm", "y_shared". */
 typedef struct {

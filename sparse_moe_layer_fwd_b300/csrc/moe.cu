@@ -25,10 +25,12 @@
 #include "experts_tc2.cuh"
 #include "ptx.cuh"
 #include "router.cuh"
+#include "router_tc.cuh"
 
 namespace {
 
 constexpr double kRouterCtaSlots = 296;  // router GEMM CTAs resident at once: 2 per SM
+constexpr double kRouterPairs = 74;      // tensor-core router: one CTA pair per two SMs
                                          // on 148 SMs (fixed, so the split and hence
                                          // the results do not depend on the device)
 constexpr int kRouterBK = 16;
@@ -76,17 +78,19 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Plan {
   int T, d, h, E, k, TK;
-  bool f32, route_only, simt, big_router, big_tiles;
+  bool f32, route_only, simt, big_router, big_tiles, tc_router;
   int el;  // bytes per activation / weight element
-  // router
-  int r_bm, r_bn, n_split, kchunk;
+  // router: CUDA-core tiles (r_bm x r_bn) or tensor-core pairs over E_pad
+  // experts (rt_eb blocks of 256) x rt_tt token tiles x n_split K slices
+  int r_bm, r_bn, n_split, kchunk, E_pad, rt_eb, rt_tt;
   // dispatch
   int n_pair_blocks;
   // expert tiling
   int bn, ft_a, ft_b, tile_round, max_tiles_a, max_tiles_b;
   // workspace regions (byte offsets)
-  size_t o_part, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh, total;
-  size_t b_part, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh;
+  size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh,
+      total;
+  size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh;
 };
 
 int validate_desc(const moe_desc* d) {
@@ -142,6 +146,34 @@ Plan make_plan(const moe_desc* d) {
   p.kchunk = ((kblocks + ns - 1) / ns) * kRouterBK;
   p.n_split = (p.d + p.kchunk - 1) / p.kchunk;
 
+  // bf16 tokens and a hundred experts or more: tensor-core router on CTA
+  // pairs, split-K count chosen to fill whole waves of 74 pairs (partials
+  // under 24 MiB, at least 4 K steps per slice)
+  p.tc_router = !p.f32 && p.E >= 96 && p.T > 0;
+  if (p.tc_router) {
+    p.E_pad = (p.E + 255) / 256 * 256;
+    p.rt_eb = p.E_pad / 256;
+    p.rt_tt = (p.T + 255) / 256;
+    const long long units1 = (long long)p.rt_eb * p.rt_tt;
+    const int kb64 = p.d / 64;
+    long long smax = te_bytes > 0 ? (24LL << 20) / te_bytes : 1;
+    smax = smax < 1 ? 1 : smax;
+    smax = smax > kb64 / 4 ? kb64 / 4 : smax;
+    smax = smax < 1 ? 1 : smax;
+    int sbest = 1;
+    double eff_best = -1.0;
+    for (int c = 1; c <= smax; ++c) {
+      const double u = (double)units1 * c;
+      const double eff = u / (ceil(u / kRouterPairs) * kRouterPairs);
+      if (eff > eff_best + 1e-9) {
+        eff_best = eff;
+        sbest = c;
+      }
+    }
+    p.kchunk = (kb64 + sbest - 1) / sbest * 64;
+    p.n_split = (p.d + p.kchunk - 1) / p.kchunk;
+  }
+
   p.n_pair_blocks = (p.TK + MOE_PAIRS_PER_BLOCK - 1) / MOE_PAIRS_PER_BLOCK;
 
   // expert tiling
@@ -182,6 +214,7 @@ Plan make_plan(const moe_desc* d) {
     off = align_up(off + bytes, 256);
   };
   region((size_t)p.n_split * p.T * p.E * 4, p.o_part, p.b_part);
+  region(p.tc_router ? (size_t)3 * p.E_pad * p.d * 2 : 0, p.o_w3, p.b_w3);
   region((size_t)p.n_pair_blocks * p.E * 4, p.o_hist, p.b_hist);
   region((size_t)p.TK * 4, p.o_rank, p.b_rank);
   region((size_t)(5 * p.E + 10) * 4, p.o_groups, p.b_groups);
@@ -431,6 +464,15 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
   if (rc != MOE_OK) return rc;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  RouterMapsDev rmaps;
+  if (p.tc_router) {
+    if (!make_map(&rmaps.w, ws + p.o_w3, 3LL * p.E_pad, p.d, 128) ||
+        !make_rows_maps(&rmaps.x128, &rmaps.x64, &rmaps.x16, x, p.T, p.d))
+      return MOE_ERR_DEVICE;
+    if (cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             RT_SMEM_BYTES) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+  }
   const bool use_tc = need_out && !p.simt;
   TcMaps maps;
   if (use_tc) {
@@ -454,7 +496,14 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     if (p.f32)
       launch_router<float>(p, static_cast<const float*>(x), w_router, part, s);
     else
-      launch_router<__nv_bfloat16>(p, static_cast<const __nv_bfloat16*>(x), w_router, part, s);
+      if (p.tc_router) {
+        k_router_split<<<2 * sm_count(), 256, 0, s>>>(
+            w_router, reinterpret_cast<__nv_bfloat16*>(ws + p.o_w3), p.E, p.E_pad, p.d);
+        k_router_tc<<<2 * p.rt_eb * p.rt_tt * p.n_split, RT_THREADS, RT_SMEM_BYTES, s>>>(
+            rmaps, p.T, p.E, p.E_pad, p.d, p.kchunk, p.rt_tt, p.rt_eb, part);
+      } else {
+        launch_router<__nv_bfloat16>(p, static_cast<const __nv_bfloat16*>(x), w_router, part, s);
+      }
     launch_topk(p, part, bias, topk_idx, gates, s);
   }
   mark(1);
@@ -607,13 +656,14 @@ int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
   if (rc != MOE_OK) return rc;
   const Plan p = make_plan(desc);
   const struct { const char* n; size_t o, b; } all[] = {
-      {"router_part", p.o_part, p.b_part}, {"blk_hist", p.o_hist, p.b_hist},
+      {"router_part", p.o_part, p.b_part}, {"router_w3", p.o_w3, p.b_w3},
+      {"blk_hist", p.o_hist, p.b_hist},
       {"pair_rank", p.o_rank, p.b_rank},   {"groups", p.o_groups, p.b_groups},
       {"perm", p.o_perm, p.b_perm},        {"inv", p.o_inv, p.b_inv},
       {"x_perm", p.o_xperm, p.b_xperm},    {"h", p.o_h, p.b_h},
       {"y_perm", p.o_yperm, p.b_yperm},    {"y_shared", p.o_ysh, p.b_ysh},
   };
-  const int n = p.route_only ? 4 : 10;
+  const int n = p.route_only ? 5 : 11;
   for (int i = 0; i < n && i < cap && regions; ++i) {
     memset(regions[i].name, 0, sizeof(regions[i].name));
     strncpy(regions[i].name, all[i].n, sizeof(regions[i].name) - 1);

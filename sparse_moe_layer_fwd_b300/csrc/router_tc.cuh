@@ -1,0 +1,218 @@
+// router_tc.cuh -- router logits on the tensor cores ("190行JAX复刻DeepSeek V3",
+// section "190行代码到底装进了什么": every token scores every routed expert).
+//
+// u[t][e] = sum_i x[t][i] W_r[e][i], x bf16, W_r fp32.  W_r is split into
+// three bf16 terms, W1 = bf16(W_r), W2 = bf16(W_r - W1), W3 = bf16(W_r - W1 -
+// W2), which together carry the 24 significant bits of the fp32 value, so
+// every product x W_j is exact in fp32 and u = x W1^T + x W2^T + x W3^T is
+// accumulated in fp32 by tcgen05 MMAs: the same products and accumulator
+// precision as an fp32 FMA loop, in a different summation order.
+//
+// k_router_split: Wsplit[j][e][i], j = 0..2, e < E_pad (rows e >= E zero).
+// k_router_tc: CTA pairs (cta_group::2) in the swap-AB orientation: M = 256
+//   experts (CTA r holds experts 128 r .. +127 of its block: three 16 KB
+//   split tiles per 64-deep K step), N = up to 256 tokens (half per CTA),
+//   K = one slice of d (split-K; k_router_topk sums the partials in slice
+//   order).  Epilogue: TMEM lane = expert, column = token, so for every token
+//   a warp writes its 32 experts' logits as one 128-byte piece of
+//   part[s][t][e].
+#pragma once
+
+#include "ptx.cuh"
+
+#define RT_THREADS 256  // warp 0: TMA producer, warp 1: TMEM + MMA, warps 4-7: epilogue
+#define RT_STAGES 3
+#define RT_A_BYTES 16384                      // 128 expert rows x 64 K of one split term
+#define RT_A_STAGE (3 * RT_A_BYTES)
+#define RT_STAGE (RT_A_STAGE + 16384)         // + up to 128 token rows x 64 K
+#define RT_BAR_OFF (RT_STAGES * RT_STAGE)
+#define RT_SMEM_BYTES (RT_BAR_OFF + 8 * (2 * RT_STAGES + 2) + 16 + 1024)
+#define RT_TMEM_COLS 256
+
+struct RouterMapsDev {
+  CUtensorMap w;               // Wsplit viewed as [3 E_pad, d], 64 x 128 boxes
+  CUtensorMap x128, x64, x16;  // token rows of x, 64 x {128, 64, 16} boxes
+};
+
+// Four consecutive elements of one row per thread (d is a multiple of 64).
+__global__ void k_router_split(const float* __restrict__ w, __nv_bfloat16* __restrict__ ws, int E,
+                               int E_pad, int d) {
+  const size_t n4 = (size_t)E_pad * d / 4, plane = (size_t)E_pad * d;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t o = 4 * i;
+    const int e = (int)(o / d);
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (e < E) {
+      const float4 f = *reinterpret_cast<const float4*>(w + o);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    }
+    __nv_bfloat16 b[3][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const __nv_bfloat16 b1 = __float2bfloat16_rn(v[c]);
+      const float r1 = v[c] - __bfloat162float(b1);  // exact: b1 is v rounded
+      const __nv_bfloat16 b2 = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(b2);
+      const bool fin = isfinite(v[c]);
+      b[0][c] = b1;
+      b[1][c] = fin ? b2 : __float2bfloat16_rn(0.f);
+      b[2][c] = fin ? __float2bfloat16_rn(r2) : __float2bfloat16_rn(0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      uint2 pk;
+      pk.x = (uint32_t)__bfloat16_as_ushort(b[j][0]) | ((uint32_t)__bfloat16_as_ushort(b[j][1]) << 16);
+      pk.y = (uint32_t)__bfloat16_as_ushort(b[j][2]) | ((uint32_t)__bfloat16_as_ushort(b[j][3]) << 16);
+      *reinterpret_cast<uint2*>(ws + j * plane + o) = pk;
+    }
+  }
+}
+
+// One pair per (expert block, token tile, K slice) unit; grid = 2 x units.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(RT_THREADS, 1)
+k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad, int d,
+            int kchunk, int n_tt, int n_eb, float* __restrict__ part) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  const int pid = blockIdx.x >> 1;  // the same unit in both CTAs of the pair
+  const int eb = pid % n_eb, tt = (pid / n_eb) % n_tt, s = pid / (n_eb * n_tt);
+  const int t0 = tt * 256;
+  const int ntok = min(256, T - t0);
+  const int npad = (ntok + 31) & ~31, half = npad / 2;
+  const int k0 = s * kchunk;
+  const int nkb = (min(d, k0 + kchunk) - k0) / 64;
+
+  uint8_t* bar_base = smem + RT_BAR_OFF;
+  auto full = [&](int i) { return smem_u32(bar_base + 8 * i); };
+  auto empty = [&](int i) { return smem_u32(bar_base + 8 * (RT_STAGES + i)); };
+  const uint32_t acc_full = smem_u32(bar_base + 8 * (2 * RT_STAGES));
+  const uint32_t drain_bar = smem_u32(bar_base + 8 * (2 * RT_STAGES + 1));
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_base + 8 * (2 * RT_STAGES + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + 8 * (2 * RT_STAGES + 2) + 4);
+  volatile int* progress = reinterpret_cast<volatile int*>(bar_base + 8 * (2 * RT_STAGES + 2) + 8);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RT_STAGES; ++i) {
+      mbar_init(full(i), 1);   // the leader's arrive + both CTAs' bytes
+      mbar_init(empty(i), 1);  // the leader's multicast commit
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    progress[0] = progress[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), RT_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool mma_issued = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------- producer: three split tiles of 128 experts + half the tokens ----------
+      const uint64_t pol_w = l2_policy_evict_last();   // read by every pair
+      const uint64_t pol_x = l2_policy_evict_first();  // read by one pair per K slice
+      const uint32_t abytes = 2u * RT_A_STAGE + (uint32_t)npad * 128u;  // both CTAs
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int st = kb % RT_STAGES, r = kb / RT_STAGES;
+        if (*abort_flag || (kb >= RT_STAGES && !mbar_wait(empty(st), (r & 1) ^ 1))) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t fb = leader ? full(st) : cluster_map(full(st), 0);
+        if (leader) mbar_arrive_expect_tx(full(st), abytes);
+        uint8_t* a = smem + st * RT_STAGE;
+        const int x = k0 + kb * 64;
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          tma_load_2d_pair(smem_u32(a + j * RT_A_BYTES), &maps.w, fb, x,
+                           j * E_pad + eb * 256 + (int)rank * 128, pol_w);
+        uint8_t* bsm = a + RT_A_STAGE;
+        const int row = t0 + (int)rank * half;
+        int i = 0;
+        for (; i + 128 <= half; i += 128)
+          tma_load_2d_pair(smem_u32(bsm + i * 128), &maps.x128, fb, x, row + i, pol_x);
+        for (; i + 64 <= half; i += 64)
+          tma_load_2d_pair(smem_u32(bsm + i * 128), &maps.x64, fb, x, row + i, pol_x);
+        for (; i < half; i += 16)
+          tma_load_2d_pair(smem_u32(bsm + i * 128), &maps.x16, fb, x, row + i, pol_x);
+        progress[0] = kb + 1;
+      }
+    }
+  } else if (warp == 1) {
+    if (leader && lane == 0) {
+      // ---------- MMA issuer: 3 split terms x 4 K=16 steps per stage ----------
+      const uint32_t idesc = umma_idesc_bf16(256, npad);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int st = kb % RT_STAGES;
+        if (*abort_flag || !mbar_wait(full(st), (kb / RT_STAGES) & 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + st * RT_STAGE), b = a + RT_A_STAGE;
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_pair(tmem, umma_desc_sw128(a + j * RT_A_BYTES + kk * 32),
+                           umma_desc_sw128(b + kk * 32), idesc, (kb | j | kk) != 0);
+        mma_issued = true;
+        umma_commit_pair(empty(st));
+        progress[1] = kb + 1;
+      }
+      if (!*abort_flag) umma_commit_pair(acc_full);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------- epilogue: TMEM lanes 32 q .. +31 = experts, columns = tokens ----------
+    const int q = warp & 3;
+    if (mbar_wait(acc_full, 0)) {
+      tc_fence_after();
+      const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+      const int e = eb * 256 + (int)rank * 128 + q * 32 + lane;
+      float* out = part + (size_t)s * T * E;
+      for (int c = 0; c < npad; c += 32) {
+        float v[32];
+        tmem_load_32(lanes + c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int t = t0 + c + j;
+          if (t < T && e < E) out[(size_t)t * E + e] = v[j];
+        }
+      }
+    } else {
+      *abort_flag = 1;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (*abort_flag && leader) {
+    // unwind: wait (bounded) for the copies issued, then for the MMAs
+    if (warp == 0 && lane == 0) {
+      for (int kb = progress[1]; kb < progress[0]; ++kb)
+        mbar_wait(full(kb % RT_STAGES), (kb / RT_STAGES) & 1);
+    }
+    if (warp == 1 && lane == 0 && mma_issued) {
+      umma_commit_pair_local(drain_bar);
+      mbar_wait(drain_bar, 0);
+    }
+    __syncthreads();
+  }
+  cluster_sync_all();  // neither CTA leaves while the other may still use its memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, RT_TMEM_COLS);
+}

@@ -115,7 +115,7 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     desc = M.make_desc(T, d, h, E, k, dt)
     total = M.moe_workspace_size(desc)
     regs = M.moe_workspace_regions(desc)
-    assert total > 0 and len(regs) == 10
+    assert total > 0 and len(regs) == 11
     spans = sorted(regs.values())
     for (o1, b1), (o2, _) in zip(spans, spans[1:]):
         assert o1 % 256 == 0 and o1 + b1 <= o2
@@ -124,6 +124,10 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     assert regs["x_perm"][1] == T * k * d * el
     assert regs["h"][1] == (T * k + T) * h * el
     assert regs["y_shared"][1] == T * d * 4
+    # the tensor-core router (bf16 tokens, 96 experts or more) keeps the
+    # router weights as three bf16 terms, expert rows padded to 256
+    tc_router = dt == "bf16" and E >= 96 and T > 0
+    assert regs["router_w3"][1] == (3 * ((E + 255) // 256 * 256) * d * 2 if tc_router else 0)
     ro = M.make_desc(T, d, h, E, k, dt, M.MOE_ROUTE_ONLY)
-    assert M.moe_workspace_size(ro) <= total and len(M.moe_workspace_regions(ro)) == 4
+    assert M.moe_workspace_size(ro) <= total and len(M.moe_workspace_regions(ro)) == 5
     assert M.moe_host_io_extra_bytes(desc) >= 2 * T * d * el
