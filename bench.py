@@ -407,12 +407,16 @@ def run_ours(args, wl):
     cap = NCU_TRAFFIC.get(wl.name)
     traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
     if prefill_like:
+        # GEMM 1 is timed inside the back-to-back step loop, under the power
+        # cap: its denominator is the sustained bf16 figure (burst beside it)
         ach = fl1 / g1_s / 1e12
+        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
         roof = {"bound": "tensor",
                 "kernel": "k_expert_tc2 (GEMM 1: gate/up + SwiGLU, CTA pairs)",
-                "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
-                "peak_kind": f"{peaks['source']} bf16 burst",
+                "achieved": ach, "peak": sus, "unit": "TFLOP/s",
+                "frac": ach / sus, "traffic": traffic,
+                "peak_kind": f"{peaks['source']} bf16 sustained (timed inside the step loop)",
+                "frac_of_burst": ach / peaks["bf16_tflops"],
                 "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
         both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
         layer_roof = {"expert_gemms_tflops": both,

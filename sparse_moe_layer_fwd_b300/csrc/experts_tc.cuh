@@ -254,8 +254,8 @@ MOE_DEV TcTile tc_tile(const GroupTable& G, const int32_t* toff, int E, int b, i
 
 struct TcMapsDev {
   CUtensorMap a0, a1, sa0, sa1;   // weights, 128-row boxes (routed, shared)
-  CUtensorMap b128, b64, b16;     // token rows of the routed groups
-  CUtensorMap bs128, bs64, bs16;  // token rows of the shared group
+  CUtensorMap b128, b64, b16, b8;     // token rows of the routed groups
+  CUtensorMap bs128, bs64, bs16, bs8;  // token rows of the shared group
   CUtensorMap out;                // bf16 output rows (H or Y_perm), 32 x 32 boxes, 64-byte swizzle
 };
 

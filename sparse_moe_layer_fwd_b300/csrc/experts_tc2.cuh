@@ -15,7 +15,7 @@
 //                MMAs, streams the token tile twice as often and measured
 //                slower.)
 //   Token rows: CTA r holds rows r * N/2 .. of the N-token tile (N a
-//   multiple of 32), so each CTA streams half of the token tile.
+//   multiple of 16), so each CTA streams half of the token tile.
 // Per 64-deep K step a CTA loads 32 KB of weights + N/2 x 128 B of tokens
 // (48 KB at N = 256) instead of 64 KB, so the same shared memory holds a
 // deeper weight ring (5 stages) and each SM moves a quarter fewer bytes.
@@ -87,7 +87,7 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   const int tsz = G.tsz[g];
   t.tok0 = tt * tsz;
   t.ntok = min(tsz, n_g - t.tok0);
-  t.npad = (t.ntok + 31) & ~31;
+  t.npad = (t.ntok + 15) & ~15;  // N of the pair MMA: a multiple of 16, half per CTA
   t.half = t.npad / 2;
   // rows of the tile: first GEMM 256 (gate and up alike); second GEMM 256 per
   // accumulator
@@ -260,6 +260,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
         const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
         const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
+        const CUtensorMap* m8 = bs ? &maps.bs8 : &maps.b8;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int sb = it % SB, r = it / SB;
           if (*abort_flag || (it >= SB && !mbar_wait(b_empty(sb), (r & 1) ^ 1))) {
@@ -275,8 +276,10 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m128, fb, kx, t.row_b + j, pol_x);
           for (; j + 64 <= t.half; j += 64)
             tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m64, fb, kx, t.row_b + j, pol_x);
-          for (; j < t.half; j += 16)
+          for (; j + 16 <= t.half; j += 16)
             tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m16, fb, kx, t.row_b + j, pol_x);
+          for (; j < t.half; j += 8)
+            tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m8, fb, kx, t.row_b + j, pol_x);
           progress[1] = it + 1;
         }
       }

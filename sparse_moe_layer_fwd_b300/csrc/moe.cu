@@ -185,13 +185,12 @@ Plan make_plan(const moe_desc* d) {
       p.ft_b = p.d / SIMT_TN;
     } else {
       // about a hundred tokens per expert or more: CTA-pair tiles of up to
-      // 256 tokens (N a multiple of 32) over 256 (first GEMM) or 512 (second)
+      // 256 tokens (N a multiple of 16) over 256 (first GEMM) or 512 (second)
       // weight rows; fewer: 1-SM tiles of up to 64 tokens over 128 / 256 rows
       const double per_expert = p.E > 0 ? (double)p.TK / p.E : 0.0;
       p.big_tiles = per_expert >= 96.0;
       if (p.big_tiles) {
         p.bn = kPairBN;
-        p.tile_round = 32;
         p.ft_a = MOE_PAIR_GEMM1 ? (p.h + 2 * TC_BM - 1) / (2 * TC_BM) : p.h / TC_BM;
         p.ft_b = MOE_PAIR_GEMM2 ? (p.d + 4 * TC_BM - 1) / (4 * TC_BM) : (p.d / TC_BM + 1) / 2;
       } else {
@@ -334,10 +333,12 @@ struct TcMaps {
   TcMapsDev down;  // second GEMM: W_down; rows of H
 };
 
-bool make_rows_maps(CUtensorMap* m128, CUtensorMap* m64, CUtensorMap* m16, const void* base,
-                    long long rows, long long cols) {
+// Token-row maps with 128-, 64-, 16- and (if m8) 8-row boxes: a tile of n
+// rows is loaded as the fewest boxes that cover it exactly.
+bool make_rows_maps(CUtensorMap* m128, CUtensorMap* m64, CUtensorMap* m16, CUtensorMap* m8,
+                    const void* base, long long rows, long long cols) {
   return make_map(m128, base, rows, cols, 128) && make_map(m64, base, rows, cols, 64) &&
-         make_map(m16, base, rows, cols, 16);
+         make_map(m16, base, rows, cols, 16) && (!m8 || make_map(m8, base, rows, cols, 8));
 }
 
 // All tensor maps of the two tensor-core GEMMs, built before anything is
@@ -349,17 +350,19 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   ok &= make_map(&m->up.a1, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
   ok &= make_map(&m->up.sa0, sh->w_gate, p.h, p.d, TC_BM);
   ok &= make_map(&m->up.sa1, sh->w_up, p.h, p.d, TC_BM);
-  ok &= make_rows_maps(&m->up.b128, &m->up.b64, &m->up.b16, ws + p.o_xperm, p.TK, p.d);
-  ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, x, p.T, p.d);
+  ok &= make_rows_maps(&m->up.b128, &m->up.b64, &m->up.b16, &m->up.b8, ws + p.o_xperm, p.TK,
+                       p.d);
+  ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8, x, p.T, p.d);
   ok &= make_map(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
   m->down.a1 = m->down.a0;
   ok &= make_map(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
   m->down.sa1 = m->down.sa0;
-  ok &= make_rows_maps(&m->down.b128, &m->down.b64, &m->down.b16, ws + p.o_h,
+  ok &= make_rows_maps(&m->down.b128, &m->down.b64, &m->down.b16, &m->down.b8, ws + p.o_h,
                        (long long)p.TK + p.T, p.h);
   m->down.bs128 = m->down.b128;
   m->down.bs64 = m->down.b64;
   m->down.bs16 = m->down.b16;
+  m->down.bs8 = m->down.b8;
   ok &= make_out_map(&m->up.out, ws + p.o_h, (long long)p.TK + p.T, p.h);
   ok &= make_out_map(&m->down.out, ws + p.o_yperm, p.TK, p.d);
   return ok;
@@ -467,7 +470,7 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
   RouterMapsDev rmaps;
   if (p.tc_router) {
     if (!make_map(&rmaps.w, ws + p.o_w3, 3LL * p.E_pad, p.d, 128) ||
-        !make_rows_maps(&rmaps.x128, &rmaps.x64, &rmaps.x16, x, p.T, p.d))
+        !make_rows_maps(&rmaps.x128, &rmaps.x64, &rmaps.x16, nullptr, x, p.T, p.d))
       return MOE_ERR_DEVICE;
     if (cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              RT_SMEM_BYTES) != cudaSuccess)
