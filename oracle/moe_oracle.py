@@ -40,6 +40,18 @@ as a source, uses the same):
                mean_load = T*k/E, sgn(0) = 0, so that sgn(E*load_e - T*k) is an
                exact integer comparison.
 
+8. sequence-wise balance loss (the pages keep the original report's small
+               auxiliary loss with alpha = 1e-4 beside the bias; "DeepSeek V3
+               viết lại bằng 190 dòng JAX thuần", section "Những gì có trong 190
+               dòng code"; "190行JAX复刻DeepSeek V3", section "最有价值的实验"),
+               per sequence of S consecutive tokens, as the report states it:
+                 f_i  = E / (k S) * #{t in the sequence : i selected for t}
+                 s'   = s[t,i] / sum_j s[t,j]        (unbiased affinities)
+                 P_i  = (1/S) sum_t s'[t,i]
+                 L    = alpha * sum_i f_i P_i
+               "selected" is the layer's own selection (biased top-k); a last
+               sequence shorter than S uses its own length.
+
 ``moe_forward_dense`` is the pages' own formulation (every expert on every
 token, then masked).  ``moe_forward_sparse`` evaluates only the selected
 experts; tests pin it to the dense formulation on small inputs, and it is the
@@ -255,3 +267,24 @@ def route_and_update(x, w_router, bias, k: int, gamma: float) -> dict:
     r["load"] = load
     r["bias_new"] = bias_update(bias, load, gamma, r["idx"].size)
     return r
+
+
+def sequence_balance_loss(s, idx, seq_len: int, alpha: float = 1e-4) -> np.ndarray:
+    """Sequence-wise balance loss (reading 8 above), one value per sequence
+    of ``seq_len`` consecutive tokens.  ``s`` [T, E] are the unbiased
+    affinities, ``idx`` [T, k] the selected experts."""
+    s = _f64(s)
+    idx = np.asarray(idx)
+    T, E = s.shape
+    k = idx.shape[1]
+    out = []
+    for t0 in range(0, T, seq_len):
+        t1 = min(T, t0 + seq_len)
+        S = t1 - t0
+        count = np.bincount(idx[t0:t1].ravel(), minlength=E).astype(F64)
+        f = E / (k * S) * count
+        s_norm = s[t0:t1] / s[t0:t1].sum(axis=1, keepdims=True)
+        P = s_norm.sum(axis=0) / S
+        out.append(alpha * float((f * P).sum()))
+    return np.array(out, dtype=F64)
+

@@ -77,6 +77,9 @@ WORKLOADS = {
         Workload("mini_bf16", 8192, 384, 384, 16, 4, "bf16", 1, bias="zero"),
         Workload("bias_dynamics", 256, 256, 128, 16, 4, "f32", 2, bias="zero",
                  skew="normal", steps=200, route_only=True),
+        # the "small" configuration of the JAX re-creation: 8 routed experts,
+        # top-2, 128-token context (32 sequences); width as the mini model
+        Workload("small_bf16", 4096, 384, 384, 8, 2, "bf16", 5, bias="uniform"),
         Workload("v3_prefill", 8192, 7168, 2048, 256, 8, "bf16", 3, bias="uniform"),
         Workload("v3_decode", 128, 7168, 2048, 256, 8, "bf16", 4, bias="zero"),
         Workload("v3_decode_zipf", 128, 7168, 2048, 256, 8, "bf16", 4, bias="zero",

@@ -388,6 +388,57 @@ def pin_route_and_update(O):
     assert np.all(r["bias_new"][under] > bb[under])
 
 
+def pin_balance_loss_golden(O):
+    """Hand-derived sequence-wise balance losses (tests/golden)."""
+    alpha = 1e-4
+    for row in _read_golden("balance_loss_closed_form.txt"):
+        parts = row.split()
+        E, k, S = int(parts[1]), int(parts[2]), int(parts[3])
+        toks, want = parts[4:-1], float(parts[-1])
+        s = np.array([[float(v) for v in t.split("|")[0].split(",")] for t in toks])
+        idx = np.array([[int(v) for v in t.split("|")[1].split(",")] for t in toks])
+        assert s.shape == (S, E) and idx.shape == (S, k)
+        got = O.sequence_balance_loss(s, idx, S, alpha)
+        assert got.shape == (1,)
+        assert abs(got[0] - want * alpha) <= 1e-15, (parts[0], got[0], want * alpha)
+
+
+def pin_balance_loss_closed_forms(O):
+    """Uniform affinities and perfectly balanced selection give exactly
+    alpha per sequence; full collapse onto one expert gives alpha * E; a
+    short last sequence uses its own length; the loss ignores per-token
+    scaling of s and relabelling of the experts."""
+    alpha = 1e-4
+    E, k, S = 8, 2, 8
+    T = 2 * S
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    s = np.full((T, E), 0.37)
+    L = O.sequence_balance_loss(s, idx, S, alpha)
+    assert L.shape == (2,) and np.allclose(L, alpha, rtol=0, atol=1e-18)
+    # collapse: every token picks expert 3 and all its affinity is there
+    s1 = np.zeros((5, E))
+    s1[:, 3] = 0.9
+    L1 = O.sequence_balance_loss(s1, np.full((5, 1), 3), 5, alpha)
+    assert abs(L1[0] - alpha * E) <= 1e-18
+    # T = 10 with S = 8: the second sequence has 2 tokens, each balanced
+    idx2 = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(8)] + [[0, 1], [2, 3]])
+    s2 = np.full((10, E), 0.5)
+    L2 = O.sequence_balance_loss(s2, idx2, 8, alpha)
+    # second sequence: counts 1 for experts 0..3 -> f = 8/(2*2) = 2 there,
+    # P = 1/8 everywhere -> L = alpha * 4 * 2 / 8 = alpha
+    assert L2.shape == (2,) and np.allclose(L2, alpha, rtol=0, atol=1e-18)
+    rng = np.random.default_rng(21)
+    s3 = rng.uniform(0.05, 0.95, size=(24, 6))
+    idx3 = np.stack([rng.choice(6, size=2, replace=False) for _ in range(24)])
+    base = O.sequence_balance_loss(s3, idx3, 8, alpha)
+    scaled = O.sequence_balance_loss(s3 * rng.uniform(0.5, 2.0, size=(24, 1)), idx3, 8, alpha)
+    assert np.allclose(base, scaled, rtol=1e-12, atol=0)
+    perm = rng.permutation(6)  # expert e becomes perm[e]
+    s_p = np.empty_like(s3)
+    s_p[:, perm] = s3
+    assert np.allclose(O.sequence_balance_loss(s_p, perm[idx3], 8, alpha), base, rtol=1e-12, atol=0)
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -402,4 +453,6 @@ PINS = [
     pin_equivariance,
     pin_dense_sparse_agree,
     pin_route_and_update,
+    pin_balance_loss_golden,
+    pin_balance_loss_closed_forms,
 ]

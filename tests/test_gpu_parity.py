@@ -219,3 +219,37 @@ def test_host_io_entry_matches_device_entry():
 
 def test_error_word_is_clear():
     assert M.moe_last_error() == M.MOE_OK
+
+
+def test_small_config_layer():
+    """The "small" configuration: 8 routed experts, top-2 (full layer)."""
+    wl = I.WORKLOADS["small_bf16"]
+    inp = _to_cuda(I.make_inputs(wl))
+    _, stats, _ = run_and_check(wl, inp)
+    assert stats["rel_l2"] < 1e-2
+
+
+# routing over a spread of (E, k), both router kernels (CUDA cores below 96
+# experts or for fp32 tokens, tensor cores from 96 experts with bf16 tokens)
+EK = [(8, 1), (8, 2), (8, 8), (32, 3), (64, 6), (96, 8), (128, 1), (160, 5), (512, 8), (1024, 32)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("E,k", EK, ids=[f"E{e}_k{k}" for e, k in EK])
+def test_routing_over_expert_counts(E, k, dtype):
+    wl = I.custom(T=333, d=512, h=128, E=E, k=k, dtype=dtype, seed=E + k)
+    inp = {n: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for n, v in I.make_inputs(wl, experts=False).items()}
+    b_before = inp["bias"].cpu().numpy().copy()
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY)
+    layer.forward(inp["x"])
+    layer.bias_update(GAMMA)
+    torch.cuda.synchronize()
+    assert M.moe_last_error() == M.MOE_OK
+    ref = O.route(np64(inp["x"]), np64(inp["w_router"]), b_before.astype(np.float64), k)
+    gidx = npi(layer.topk_idx)
+    flips = check_routing(gidx, layer.gates.cpu().numpy().astype(np.float64), ref,
+                          {"f32": 1e-6, "bf16": 1e-5}[dtype])
+    gload = npi(layer.load_counts)
+    check_load(gload, gidx, ref["idx"], E, flips)
+    assert np.array_equal(inp["bias"].cpu().numpy(), O.bias_update(b_before, gload, GAMMA, wl.T * k))

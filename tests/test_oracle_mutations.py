@@ -163,6 +163,33 @@ def _router_no_sigmoid(x, w_router):
     return u, u
 
 
+def _balance_unnormalised(s, idx, seq_len, alpha=1e-4):
+    s = np.asarray(s, F64)
+    idx = np.asarray(idx)
+    T, E = s.shape
+    k = idx.shape[1]
+    out = []
+    for t0 in range(0, T, seq_len):
+        S = min(T, t0 + seq_len) - t0
+        f = E / (k * S) * np.bincount(idx[t0:t0 + S].ravel(), minlength=E)
+        out.append(alpha * float((f * s[t0:t0 + S].sum(0) / S).sum()))  # s, not s / sum_j s
+    return np.array(out)
+
+
+def _balance_whole_batch(s, idx, seq_len, alpha=1e-4):
+    return _ORIG["sequence_balance_loss"](s, idx, np.asarray(s).shape[0], alpha)
+
+
+def _balance_first_slot(s, idx, seq_len, alpha=1e-4):
+    idx = np.asarray(idx)
+    # counts only the first slot of every token (k kept in E/(k S))
+    return _ORIG["sequence_balance_loss"](s, idx[:, :1], seq_len, alpha) / idx.shape[1]
+
+
+def _balance_no_e_factor(s, idx, seq_len, alpha=1e-4):
+    return _ORIG["sequence_balance_loss"](s, idx, seq_len, alpha) / np.asarray(s).shape[1]
+
+
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
 
 MUTATIONS = [
@@ -191,6 +218,10 @@ MUTATIONS = [
     ("bias_update", _bias_no_round),
     ("topk_gap", _gap_off_by_one),
     ("router_affinity", _router_no_sigmoid),
+    ("sequence_balance_loss", _balance_unnormalised),
+    ("sequence_balance_loss", _balance_whole_batch),
+    ("sequence_balance_loss", _balance_first_slot),
+    ("sequence_balance_loss", _balance_no_e_factor),
 ]
 
 
