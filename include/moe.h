@@ -174,6 +174,26 @@ MOE_API int moe_forward_profiled(const moe_desc* desc, const void* x,
 MOE_API int moe_bias_update(const int32_t* load_counts, float* bias, float gamma,
                     int E, int TK, void* stream);
 
+/* Sequence-wise balance loss of the routing that the last moe_forward (or
+ * moe_forward_profiled, moe_forward_host_io) on `workspace` with the same
+ * `desc` computed: the small auxiliary loss the pages keep beside the bias,
+ * weight alpha = 1e-4 ("DeepSeek V3 viết lại bằng 190 dòng JAX thuần",
+ * section "Những gì có trong 190 dòng code"), as the original report defines
+ * it, for each sequence of seq_len consecutive tokens (the last one may be
+ * shorter and uses its own length S):
+ *   f_e = E/(k S) * #{t in the sequence : e among its selected experts}
+ *   P_e = (1/S) * sum_t s[t,e] / sum_j s[t,j]   (s = sigmoid affinities)
+ *   loss[q] = alpha * sum_e f_e * P_e
+ * Reads the router's partial logits left in the workspace and topk_idx
+ * [T, k] (device, int32, the selection of that forward); writes
+ * loss[ceil(T / seq_len)] (device fp32).  Enqueue it on the same stream after
+ * that forward and before the workspace is reused.  Deterministic.  Returns
+ * MOE_ERR_SHAPE for seq_len < 1, MOE_ERR_NULL / MOE_ERR_WORKSPACE for missing
+ * pointers or a short workspace; T = 0 enqueues nothing. */
+MOE_API int moe_seq_balance_loss(const moe_desc* desc, int seq_len, float alpha,
+                                 const int32_t* topk_idx, const void* workspace,
+                                 size_t ws_bytes, float* loss, void* stream);
+
 /* Device error word of the calls made so far (MOE_OK or
  * MOE_ERR_DEVICE_TIMEOUT), and reset it to MOE_OK.  It does not synchronise
  * the caller's stream: synchronise first.  Returns MOE_ERR_DEVICE if the

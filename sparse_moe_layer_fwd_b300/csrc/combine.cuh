@@ -83,3 +83,70 @@ __global__ void k_bias_update(const int32_t* __restrict__ load, float* __restric
   const float sgn = diff > 0 ? 1.0f : (diff < 0 ? -1.0f : 0.0f);
   bias[e] = __fsub_rn(bias[e], gamma * sgn);
 }
+
+// k_seq_balance_loss: the sequence-wise balance loss that the pages keep
+// beside the bias (alpha = 1e-4; "DeepSeek V3 viết lại bằng 190 dòng JAX
+// thuần", section "Những gì có trong 190 dòng code"), per sequence of S
+// consecutive tokens as the original report defines it:
+//   f_e = E/(k S) * #{t : e selected},  s'[t,e] = s[t,e] / sum_j s[t,j],
+//   P_e = (1/S) sum_t s'[t,e],          L = alpha * sum_e f_e P_e.
+// One CTA (8 warps) per sequence, reading the router's partial logits from
+// the workspace.  Warp w takes tokens w, w+8, ... of the sequence: u = sum
+// of the partials in slice order, s = 1/(1+exp(-u)), the token's sum of s
+// by a fixed butterfly, and s' accumulated per expert in registers.
+// Selections are counted in shared memory (integers).  P_e sums the warps
+// in warp order; warp 0 sums count_e * P_e over the experts in a fixed order.
+// Every floating-point sum has a fixed order: the result is deterministic.
+template <int EPL>
+__global__ void __launch_bounds__(256)
+k_seq_balance_loss(const float* __restrict__ part, int n_split, const int32_t* __restrict__ topk_idx,
+                   int T, int E, int k, int S, float alpha, float* __restrict__ loss) {
+  extern __shared__ float sm_bal[];
+  float* ppart = sm_bal;                                // [8][E]
+  int* cnt = reinterpret_cast<int*>(sm_bal + 8 * E);  // [E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * S, t1 = min(T, t0 + S);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  float acc[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+  for (int t = t0 + warp; t < t1; t += 8) {
+    float sv[EPL];
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      sv[i] = 0.f;
+      if (e < E) {
+        float u = 0.f;
+        for (int s = 0; s < n_split; ++s) u += part[((size_t)s * T + t) * E + e];
+        sv[i] = 1.0f / (1.0f + expf(-u));
+        sum += sv[i];
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] += sv[i] / sum;
+    if (lane < k) atomicAdd(&cnt[topk_idx[(size_t)t * k + lane]], 1);
+  }
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) ppart[warp * E + e] = acc[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float total = 0.f;
+    for (int e = lane; e < E; e += 32) {
+      float P = 0.f;
+      for (int w = 0; w < 8; ++w) P += ppart[w * E + e];
+      total += (float)cnt[e] * P;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+    const float Sq = (float)(t1 - t0);
+    if (lane == 0) loss[blockIdx.x] = alpha * ((float)E / ((float)k * Sq)) * (total / Sq);
+  }
+}

@@ -630,6 +630,38 @@ int moe_bias_update(const int32_t* load_counts, float* bias, float gamma, int E,
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
+int moe_seq_balance_loss(const moe_desc* desc, int seq_len, float alpha, const int32_t* topk_idx,
+                         const void* workspace, size_t ws_bytes, float* loss, void* stream) {
+  int rc = validate_desc(desc);
+  if (rc != MOE_OK) return rc;
+  if (seq_len < 1) return MOE_ERR_SHAPE;
+  const Plan p = make_plan(desc);
+  if (p.T == 0) return MOE_OK;
+  if (!topk_idx || !workspace || !loss) return MOE_ERR_NULL;
+  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MOE_ERR_ALIGN;
+  rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  const float* part =
+      reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + p.o_part);
+  const int nseq = (p.T + seq_len - 1) / seq_len;
+  const size_t smem = (size_t)9 * p.E * 4;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const int epl = (p.E + 31) / 32;
+#define MOE_BAL(N)                                                                          \
+  k_seq_balance_loss<N><<<nseq, 256, smem, s>>>(part, p.n_split, topk_idx, p.T, p.E, p.k, \
+                                                seq_len, alpha, loss)
+  if (epl <= 1) MOE_BAL(1);
+  else if (epl <= 2) MOE_BAL(2);
+  else if (epl <= 4) MOE_BAL(4);
+  else if (epl <= 8) MOE_BAL(8);
+  else if (epl <= 16) MOE_BAL(16);
+  else MOE_BAL(32);
+#undef MOE_BAL
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
 int moe_last_error(void) {
   unsigned v = 0;
   if (cudaMemcpyFromSymbol(&v, g_moe_dev_error, sizeof(v)) != cudaSuccess) return MOE_ERR_DEVICE;

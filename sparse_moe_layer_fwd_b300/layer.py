@@ -67,6 +67,16 @@ class MoeLayer:
             stream = torch.cuda.current_stream(self.workspace.device)
         M.moe_bias_update(self.load_counts, self.bias, gamma, self.E, self.T * self.k, stream)
 
+    def balance_loss(self, seq_len: int, alpha: float = 1e-4, stream=None) -> torch.Tensor:
+        """Per-sequence balance loss of the routing of the last forward."""
+        if stream is None:
+            stream = torch.cuda.current_stream(self.workspace.device)
+        out = torch.empty(((self.T + seq_len - 1) // seq_len,), dtype=torch.float32,
+                          device=self.workspace.device)
+        M.moe_seq_balance_loss(self.desc, seq_len, alpha, self.topk_idx, self.workspace,
+                               self.ws_bytes, out, stream)
+        return out
+
     def region(self, name: str, dtype: torch.dtype, shape) -> torch.Tensor:
         """A view of a named workspace region (for inspecting intermediates)."""
         off, nbytes = self.regions[name]

@@ -67,6 +67,8 @@ def _load():
     lib.moe_forward_profiled.restype = I
     lib.moe_bias_update.argtypes = [P, P, ctypes.c_float, I, I, P]
     lib.moe_bias_update.restype = I
+    lib.moe_seq_balance_loss.argtypes = [dp, I, ctypes.c_float, P, P, S, P, P]
+    lib.moe_seq_balance_loss.restype = I
     lib.moe_last_error.argtypes, lib.moe_last_error.restype = [], I
     lib.moe_error_string.argtypes, lib.moe_error_string.restype = [I], ctypes.c_char_p
     lib.moe_workspace_regions.argtypes = [dp, ctypes.POINTER(MoeRegion), I]
@@ -171,6 +173,14 @@ def moe_bias_update(load_counts, bias, gamma, E, TK, stream=None, check=True) ->
     rc = _lib.moe_bias_update(_ptr(load_counts), _ptr(bias), ctypes.c_float(gamma), int(E),
                               int(TK), _stream(stream))
     return _check(rc, "moe_bias_update") if check else rc
+
+
+def moe_seq_balance_loss(desc, seq_len, alpha, topk_idx, workspace, ws_bytes, loss, stream=None,
+                         check=True) -> int:
+    rc = _lib.moe_seq_balance_loss(ctypes.byref(desc), int(seq_len), ctypes.c_float(alpha),
+                                   _ptr(topk_idx), _ptr(workspace), int(ws_bytes), _ptr(loss),
+                                   _stream(stream))
+    return _check(rc, "moe_seq_balance_loss") if check else rc
 
 
 def moe_last_error() -> int:

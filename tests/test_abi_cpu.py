@@ -17,7 +17,7 @@ def test_library_exports_every_header_function():
     assert set(names) == {
         "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
-        "moe_forward_profiled", "moe_route_noalloc"}
+        "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -96,6 +96,17 @@ def test_argument_errors_are_found_on_the_host():
     assert M.moe_bias_update(None, FAKE, 1e-3, 16, 64, check=False) == E["MOE_ERR_NULL"]
     assert M.moe_bias_update(FAKE, FAKE, 1e-3, 0, 64, check=False) == E["MOE_ERR_SHAPE"]
     assert M.moe_bias_update(FAKE, FAKE, 1e-3, 16, -1, check=False) == E["MOE_ERR_SHAPE"]
+    # balance-loss arguments
+    ws = M.moe_workspace_size(d)
+    bl = lambda **o: M.moe_seq_balance_loss(  # noqa: E731
+        o.get("desc", d), o.get("seq_len", 16), 1e-4, o.get("idx", FAKE), o.get("ws", FAKE),
+        o.get("ws_bytes", ws), o.get("loss", FAKE), check=False)
+    assert bl(seq_len=0) == E["MOE_ERR_SHAPE"]
+    assert bl(idx=None) == E["MOE_ERR_NULL"]
+    assert bl(loss=None) == E["MOE_ERR_NULL"]
+    assert bl(ws_bytes=ws - 1) == E["MOE_ERR_WORKSPACE"]
+    assert bl(ws=FAKE + 4) == E["MOE_ERR_ALIGN"]
+    assert bl(desc=M.make_desc(0, 256, 128, 16, 4, "bf16"), idx=None) == M.MOE_OK
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
@@ -103,6 +114,8 @@ def test_valid_call_without_gpu_reports_device_error():
     d = M.make_desc(64, 256, 128, 16, 4, "f32")
     assert _call(d) == M.ERR_CODE["MOE_ERR_DEVICE"]
     assert M.moe_bias_update(FAKE, FAKE, 1e-3, 16, 64, check=False) == M.ERR_CODE["MOE_ERR_DEVICE"]
+    assert M.moe_seq_balance_loss(d, 16, 1e-4, FAKE, FAKE, M.moe_workspace_size(d), FAKE,
+                                  check=False) == M.ERR_CODE["MOE_ERR_DEVICE"]
 
 
 @pytest.mark.parametrize("shape", [
