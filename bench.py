@@ -463,12 +463,72 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+# The five configurations of the layer's specification by their short names.
+CONFIGS = {"C0": "tiny_fp32", "C1": "mini_bf16", "C2": "bias_dynamics", "C3": "v3_prefill",
+           "C4": "v3_decode", "C4z": "v3_decode_zipf"}
+
+
+def run_bias_dynamics(args, wl):
+    """Route + bias update per step on a fresh batch each step (the
+    bias-balancing run); reports ms per step and the per-expert load share
+    at the first and last timed step."""
+    from sparse_moe_layer_fwd_b300 import inputs as I
+    from sparse_moe_layer_fwd_b300 import moe as M
+    from sparse_moe_layer_fwd_b300.layer import MoeLayer
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    inp = I.make_inputs(wl.with_(seed=wl.seed + 1000 * rank) if ws > 1 else wl, device="cuda",
+                        experts=False)
+    n = args.warmup + args.steps
+    xs = [inp["x"]] + [I.next_x(wl, inp, "cuda") for _ in range(n - 1)]
+    b0 = inp["bias"].clone()
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    shares = []
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        layer.forward(xs[i], stream)
+        layer.bias_update(1e-3, stream)
+        ev[i][1].record(stream)
+        if i in (args.warmup, n - 1):
+            shares.append((layer.load_counts.float() / (wl.T * wl.k)).cpu())
+    torch.cuda.synchronize()
+    if M.moe_last_error() != M.MOE_OK:
+        raise RuntimeError("device error word set")
+    local_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, n))
+    elapsed_ms, value = aggregate(local_ms, wl.T * args.steps, ws, "cuda")
+    layer.bias.copy_(b0)
+    if rank == 0:
+        line = {
+            "metric": METRIC + " [bias dynamics: route + bias update per step]", "value": value,
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if wl.dtype == "f32" else "f32 router, bf16 x",
+            "data": "synthetic (seeded N(0,1) tokens per step, router offsets N(0,1))",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
+                       "l2": "L2 flushed before each step (252 MB write outside the timed spans)"},
+            "roofline": None,
+            "load_share": {"first_step": [float(shares[0].min()), float(shares[0].max())],
+                           "last_step": [float(shares[-1].min()), float(shares[-1].max())],
+                           "uniform": 1.0 / wl.E},
+            "gpu_launches": kernels_per_step(wl, True) * args.steps + args.steps,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="v3_prefill")
+    ap.add_argument("--config", choices=sorted(CONFIGS),
+                    help="a configuration by its short name (sets --workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
@@ -482,9 +542,11 @@ def main():
     if args.gpus != ws:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}: launch N > 1 with torchrun")
     from sparse_moe_layer_fwd_b300 import inputs as I
-    wl = I.WORKLOADS[args.workload]
+    wl = I.WORKLOADS[CONFIGS[args.config] if args.config else args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif wl.steps > 1:
+        run_bias_dynamics(args, wl)
     else:
         run_ours(args, wl)
 
