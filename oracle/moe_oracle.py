@@ -52,6 +52,14 @@ as a source, uses the same):
                "selected" is the layer's own selection (biased top-k); a last
                sequence shorter than S uses its own length.
 
+9. backward    (the pages train with this layer: "DeepSeek V3 viết lại bằng 190
+               dòng JAX thuần", section "Những gì có trong 190 dòng code")
+               gradients of y for an output gradient dy by the chain rule;
+               the selection is piecewise constant and carries no gradient,
+               the gates g = s_sel / sum s_sel carry it to the selected
+               affinities, through the sigmoid to W_r and x; the bias has no
+               gradient (it moves by the sign rule).
+
 ``moe_forward_dense`` is the pages' own formulation (every expert on every
 token, then masked).  ``moe_forward_sparse`` evaluates only the selected
 experts; tests pin it to the dense formulation on small inputs, and it is the
@@ -287,4 +295,62 @@ def sequence_balance_loss(s, idx, seq_len: int, alpha: float = 1e-4) -> np.ndarr
         P = s_norm.sum(axis=0) / S
         out.append(alpha * float((f * P).sum()))
     return np.array(out, dtype=F64)
+
+
+# --------------------------------------------------------------------------
+# 9. backward of the layer
+# --------------------------------------------------------------------------
+def swiglu_expert_backward(x, w_gate, w_up, w_down, dy):
+    """Gradients of E(x) = W_down (silu(W_gate x) * (W_up x)) for the output
+    gradient dy [n, d]: (dx [n,d], dW_gate [h,d], dW_up [h,d], dW_down [d,h]).
+    silu'(a) = sigmoid(a) (1 + a (1 - sigmoid(a)))."""
+    x, dy = _f64(x), _f64(dy)
+    wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
+    a = x @ wg.T
+    c = x @ wu.T
+    sg = sigmoid(a)
+    hmid = a * sg * c
+    dw_down = dy.T @ hmid
+    dh = dy @ wd
+    da = dh * c * (sg * (1.0 + a * (1.0 - sg)))
+    dc = dh * (a * sg)
+    return da @ wg + dc @ wu, da.T @ x, dc.T @ x, dw_down
+
+
+def moe_backward_dense(x, w_router, bias, experts, shared, k: int, dy,
+                       idx_override=None) -> dict:
+    """Gradients of ``moe_forward_dense``'s y for the output gradient dy
+    [T, d] (reading 9): dx, dW_gate/dW_up [E,h,d], dW_down [E,d,h], the
+    shared expert's three, and dW_router [E,d].  Also returns dG [T,E]
+    (gradient of each gate, the dot of dy with the expert's output) and
+    the forward's idx and gates."""
+    fwd = moe_forward_dense(x, w_router, bias, experts, shared, k, idx_override)
+    x, dy = _f64(x), _f64(dy)
+    s, idx, gates = fwd["s"], fwd["idx"], fwd["gates"]
+    T, E = s.shape
+    wg, wu, wd = experts
+    out = {"idx": idx, "gates": gates}
+    dx, out["dsh_gate"], out["dsh_up"], out["dsh_down"] = swiglu_expert_backward(x, *shared, dy)
+    mask = np.zeros((T, E), dtype=F64)
+    np.put_along_axis(mask, idx, gates, axis=1)
+    dG = np.zeros((T, E), dtype=F64)
+    dwg = np.zeros(np.shape(wg), dtype=F64)
+    dwu = np.zeros(np.shape(wu), dtype=F64)
+    dwd = np.zeros(np.shape(wd), dtype=F64)
+    for e in range(E):
+        dG[:, e] = (dy * swiglu_expert(x, wg[e], wu[e], wd[e])).sum(axis=1)
+        dxe, dwg[e], dwu[e], dwd[e] = swiglu_expert_backward(x, wg[e], wu[e], wd[e],
+                                                             mask[:, e:e + 1] * dy)
+        dx = dx + dxe
+    # g_j = s_j / S over the selected experts: dL/ds_i = (dg_i - sum_j dg_j g_j) / S
+    dg_sel = np.take_along_axis(dG, idx, axis=1)
+    s_sel = np.take_along_axis(s, idx, axis=1)
+    ds_sel = (dg_sel - (dg_sel * gates).sum(axis=1, keepdims=True)) / s_sel.sum(axis=1, keepdims=True)
+    ds = np.zeros((T, E), dtype=F64)
+    np.put_along_axis(ds, idx, ds_sel, axis=1)
+    du = ds * s * (1.0 - s)
+    out["dW_router"] = du.T @ x
+    out["dx"] = dx + du @ _f64(w_router)
+    out.update({"dW_gate": dwg, "dW_up": dwu, "dW_down": dwd, "dG": dG, "du": du})
+    return out
 

@@ -439,6 +439,69 @@ def pin_balance_loss_closed_forms(O):
     assert np.allclose(O.sequence_balance_loss(s_p, perm[idx3], 8, alpha), base, rtol=1e-12, atol=0)
 
 
+def _backward_case(seed, T=6, d=5, h=4, E=5, k=2):
+    """Tiny layer whose top-k gaps are wide enough that the finite
+    differences below never change the selection."""
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(T, d))
+    w_r = rng.normal(size=(E, d))
+    b = np.linspace(0.3, -0.3, E)
+    ex = (rng.normal(size=(E, h, d)), rng.normal(size=(E, h, d)), rng.normal(size=(E, d, h)))
+    sh = (rng.normal(size=(h, d)), rng.normal(size=(h, d)), rng.normal(size=(d, h)))
+    return x, w_r, b, ex, sh, rng.normal(size=(T, d))
+
+
+def pin_backward_finite_differences(O):
+    """Every gradient entry against a central difference of the forward
+    oracle's <dy, y>, in float64 (step 1e-6)."""
+    x, w_r, b, ex, sh, dy = _backward_case(31)
+    k, eps = 2, 1e-6
+    assert O.topk_gap(O.route(x, w_r, b, k)["z"], k).min() > 1e-3
+    g = O.moe_backward_dense(x, w_r, b, ex, sh, k, dy)
+
+    def loss(x_, w_r_, ex_, sh_):
+        return float((dy * O.moe_forward_dense(x_, w_r_, b, ex_, sh_, k)["y"]).sum())
+
+    def check(arr, grad, place):
+        worst = 0.0
+        for i in np.ndindex(arr.shape):
+            hi, lo = arr.copy(), arr.copy()
+            hi[i] += eps
+            lo[i] -= eps
+            fd = (loss(*place(hi)) - loss(*place(lo))) / (2 * eps)
+            worst = max(worst, abs(fd - grad[i]) / (1.0 + abs(grad[i])))
+        assert worst < 1e-6, worst
+
+    check(x, g["dx"], lambda a: (a, w_r, ex, sh))
+    check(w_r, g["dW_router"], lambda a: (x, a, ex, sh))
+    for j, name in enumerate(["dW_gate", "dW_up", "dW_down"]):
+        check(ex[j], g[name], lambda a, j=j: (x, w_r, tuple(a if m == j else ex[m] for m in range(3)), sh))
+    for j, name in enumerate(["dsh_gate", "dsh_up", "dsh_down"]):
+        check(sh[j], g[name], lambda a, j=j: (x, w_r, ex, tuple(a if m == j else sh[m] for m in range(3))))
+
+
+def pin_backward_special_cases(O):
+    """One routed expert (gate identically 1): the router gets no gradient.
+    Gates are invariant to scaling the selected affinities together, so
+    sum_j s_j dL/ds_j = 0 over each token's selection.  Zero routed weights:
+    only the shared expert carries dx, and no gate has a gradient."""
+    x, w_r, b, ex, sh, dy = _backward_case(32, E=1, k=1)
+    g = O.moe_backward_dense(x, w_r, b, ex, sh, 1, dy)
+    assert np.array_equal(g["dW_router"], np.zeros_like(w_r))
+    x, w_r, b, ex, sh, dy = _backward_case(33, E=6, k=3)
+    g = O.moe_backward_dense(x, w_r, b, ex, sh, 3, dy)
+    s = O.route(x, w_r, b, 3)["s"]
+    ds = g["du"] / (s * (1.0 - s))
+    s_sel = np.take_along_axis(s, g["idx"], axis=1)
+    ds_sel = np.take_along_axis(ds, g["idx"], axis=1)
+    assert np.abs((s_sel * ds_sel).sum(axis=1)).max() < 1e-12 * (1 + np.abs(ds_sel).max())
+    zero = tuple(np.zeros_like(w) for w in ex)
+    g0 = O.moe_backward_dense(x, w_r, b, zero, sh, 3, dy)
+    dx_sh = O.swiglu_expert_backward(x, *sh, dy)[0]
+    assert np.allclose(g0["dx"], dx_sh, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(g0["dW_router"], np.zeros_like(w_r))
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -455,4 +518,6 @@ PINS = [
     pin_route_and_update,
     pin_balance_loss_golden,
     pin_balance_loss_closed_forms,
+    pin_backward_finite_differences,
+    pin_backward_special_cases,
 ]

@@ -190,6 +190,54 @@ def _balance_no_e_factor(s, idx, seq_len, alpha=1e-4):
     return _ORIG["sequence_balance_loss"](s, idx, seq_len, alpha) / np.asarray(s).shape[1]
 
 
+def _bwd_expert_silu_prime(x, w_gate, w_up, w_down, dy):
+    x, dy = np.asarray(x, F64), np.asarray(dy, F64)
+    wg, wu, wd = (np.asarray(w, F64) for w in (w_gate, w_up, w_down))
+    a, c = x @ wg.T, x @ wu.T
+    sg = O.sigmoid(a)
+    dh = dy @ wd
+    da = dh * c * sg  # drops the a (1 - sigmoid(a)) term of silu'
+    dc = dh * (a * sg)
+    return da @ wg + dc @ wu, da.T @ x, dc.T @ x, dy.T @ (a * sg * c)
+
+
+def _bwd_expert_down_without_silu(x, w_gate, w_up, w_down, dy):
+    dx, dg, du, _ = _ORIG["swiglu_expert_backward"](x, w_gate, w_up, w_down, dy)
+    x = np.asarray(x, F64)
+    a, c = x @ np.asarray(w_gate, F64).T, x @ np.asarray(w_up, F64).T
+    return dx, dg, du, np.asarray(dy, F64).T @ (a * c)  # a * c instead of silu(a) * c
+
+
+def _bwd_no_shared_dx(x, w_router, bias, experts, shared, k, dy, idx_override=None):
+    out = _ORIG["moe_backward_dense"](x, w_router, bias, experts, shared, k, dy, idx_override)
+    out["dx"] = out["dx"] - _ORIG["swiglu_expert_backward"](x, *shared, dy)[0]
+    return out
+
+
+def _bwd_gate_no_quotient(x, w_router, bias, experts, shared, k, dy, idx_override=None):
+    out = _ORIG["moe_backward_dense"](x, w_router, bias, experts, shared, k, dy, idx_override)
+    r = O.route(x, w_router, bias, k)
+    s, idx = r["s"], out["idx"]
+    x64 = np.asarray(x, F64)
+    ds = np.zeros_like(s)
+    dg_sel = np.take_along_axis(out["dG"], idx, axis=1)
+    np.put_along_axis(ds, idx, dg_sel / np.take_along_axis(s, idx, axis=1).sum(1, keepdims=True), axis=1)
+    du = ds * s * (1 - s)
+    out["dx"] = out["dx"] - out["du"] @ np.asarray(w_router, F64) + du @ np.asarray(w_router, F64)
+    out["dW_router"], out["du"] = du.T @ x64, du
+    return out
+
+
+def _bwd_router_no_sigmoid_grad(x, w_router, bias, experts, shared, k, dy, idx_override=None):
+    out = _ORIG["moe_backward_dense"](x, w_router, bias, experts, shared, k, dy, idx_override)
+    s = O.route(x, w_router, bias, k)["s"]
+    du = out["du"] / (s * (1 - s))  # ds in place of du
+    x64 = np.asarray(x, F64)
+    out["dx"] = out["dx"] - out["du"] @ np.asarray(w_router, F64) + du @ np.asarray(w_router, F64)
+    out["dW_router"], out["du"] = du.T @ x64, du
+    return out
+
+
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
 
 MUTATIONS = [
@@ -222,6 +270,11 @@ MUTATIONS = [
     ("sequence_balance_loss", _balance_whole_batch),
     ("sequence_balance_loss", _balance_first_slot),
     ("sequence_balance_loss", _balance_no_e_factor),
+    ("swiglu_expert_backward", _bwd_expert_silu_prime),
+    ("swiglu_expert_backward", _bwd_expert_down_without_silu),
+    ("moe_backward_dense", _bwd_no_shared_dx),
+    ("moe_backward_dense", _bwd_gate_no_quotient),
+    ("moe_backward_dense", _bwd_router_no_sigmoid_grad),
 ]
 
 
