@@ -83,6 +83,9 @@ enum {
 #define MOE_SIMT_EXPERTS 2u  /* bf16 only: run the expert GEMMs on the CUDA-core
                                 kernels instead of the tensor cores (a cross-check
                                 of the tensor-core path; slow) */
+#define MOE_TRAINING     4u  /* bf16 tensor-core path only: the workspace also holds
+                                the backward's buffers, so that moe_backward can
+                                follow moe_forward on it */
 
 /* Problem description.
  *   T  tokens (>= 0)            d  model width          h  expert hidden width
@@ -93,7 +96,7 @@ enum {
 typedef struct {
   int T, d, h, E, k;
   int dtype;        /* moe_dtype */
-  unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS */
+  unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING */
 } moe_desc;
 
 /* Expert weights, element type desc->dtype.
@@ -193,6 +196,34 @@ MOE_API int moe_bias_update(const int32_t* load_counts, float* bias, float gamma
 MOE_API int moe_seq_balance_loss(const moe_desc* desc, int seq_len, float alpha,
                                  const int32_t* topk_idx, const void* workspace,
                                  size_t ws_bytes, float* loss, void* stream);
+
+/* Gradients of expert weights (device, fp32, written in full -- experts that
+ * no token selected get zeros).  Routed: d_gate [E, h, d], d_up [E, h, d],
+ * d_down [E, d, h]; shared: the same with E = 1. */
+typedef struct {
+  float *d_gate, *d_up, *d_down;
+} moe_expert_grad;
+
+/* Backward of the layer ("DeepSeek V3 viết lại bằng 190 dòng JAX thuần",
+ * section "Những gì có trong 190 dòng code": the re-creation trains with this
+ * layer) for the output gradient dy [T, d] (bf16, device): with the forward's
+ * selection held fixed (it carries no gradient) and gates g = s_sel / sum s_sel
+ * over the selected sigmoid affinities,
+ *   dx [T, d]            (bf16) gradient of the tokens
+ *   d_experts, d_shared  (fp32) gradients of the expert weights
+ *   d_router [E, d]      (fp32) gradient of W_r (through the gates only)
+ * The bias gets no gradient (moe_bias_update moves it).  Call it after
+ * moe_forward on the same workspace, stream, desc (with MOE_TRAINING) and
+ * inputs (x, w_router, experts, shared, and that forward's topk_idx and
+ * gates), before the workspace is reused.  Deterministic (no atomics in any
+ * sum).  bf16 with d, h multiples of 128 only (MOE_ERR_DTYPE / MOE_ERR_SHAPE
+ * otherwise); argument errors as moe_forward. */
+MOE_API int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
+                         const moe_expert_w* experts, const moe_expert_w* shared,
+                         const int32_t* topk_idx, const float* gates, const void* dy,
+                         void* dx, const moe_expert_grad* d_experts,
+                         const moe_expert_grad* d_shared, float* d_router, void* workspace,
+                         size_t ws_bytes, void* stream);
 
 /* Device error word of the calls made so far (MOE_OK or
  * MOE_ERR_DEVICE_TIMEOUT), and reset it to MOE_OK.  It does not synchronise

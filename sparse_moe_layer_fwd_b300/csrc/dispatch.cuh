@@ -96,9 +96,15 @@ __device__ int cta_exclusive_scan(int* data, int n, int* warp_tot) {
 //   tsz[E+1]     rows per token tile (multiple of tile_round, <= bn)
 //   toff_a[E+2]  prefix sum of ntt[g] * ft_a (tiles of the first GEMM)
 //   toff_b[E+2]  prefix sum of ntt[g] * ft_b (tiles of the second GEMM)
-//   next[2]      tile counters of the two GEMMs' schedulers, zeroed here
+//   toff_c[E+2]  prefix sum of ntt[g] * ft_c (backward: tiles of dH = dY W_d)
+//   poff[E+2]    backward: first row of group g with every group padded to a
+//                multiple of 16 rows (poff[E] = the shared group's first row,
+//                poff[E+1] = all rows)
+//   next[8]      tile counters of the GEMMs' schedulers: 0, 1 the forward's
+//                (zeroed here), 2..7 the backward's (zeroed by its tables)
+#define MOE_GROUP_INTS(E) (7 * (E) + 18)
 struct GroupTable {
-  int32_t *off, *ntt, *tsz, *toff_a, *toff_b, *next;
+  int32_t *off, *ntt, *tsz, *toff_a, *toff_b, *toff_c, *poff, *next;
 };
 
 MOE_DEV GroupTable group_table(int32_t* base, int E) {
@@ -108,7 +114,9 @@ MOE_DEV GroupTable group_table(int32_t* base, int E) {
   g.tsz = g.ntt + (E + 1);
   g.toff_a = g.tsz + (E + 1);
   g.toff_b = g.toff_a + (E + 2);
-  g.next = g.toff_b + (E + 2);
+  g.toff_c = g.toff_b + (E + 2);
+  g.poff = g.toff_c + (E + 2);
+  g.next = g.poff + (E + 2);
   return g;
 }
 

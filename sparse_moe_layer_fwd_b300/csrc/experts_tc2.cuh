@@ -36,6 +36,20 @@
 
 #include "experts_tc.cuh"
 
+// Operations of the CTA-pair grouped GEMM.  Rows of a weight matrix are the
+// MMA's M side and token rows its N side in all of them.
+enum : int {
+  TC2_FWD_UP = 0,    // H = silu(X W_gate^T) * (X W_up^T)                      K = d
+  TC2_FWD_DOWN = 1,  // Y = H W_down^T                                          K = h
+  TC2_BWD_DH = 2,    // dH = dY W_down (W_down read transposed)                 K = d
+  TC2_BWD_DAB = 3,   // gate/up recomputed: dA = dH up silu'(gate), dB = dH silu(gate)
+  TC2_BWD_DX = 4,    // dX = dA W_gate + dB W_up (weights read transposed)      K = 2h
+};
+// two blocks of 256 rows of one matrix per tile (else gate and up rows)
+__host__ __device__ constexpr bool tc2_down(int op) { return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX; }
+// the weight operand is MN-major (the weights' transpose is multiplied)
+__host__ __device__ constexpr bool tc2_mn_a(int op) { return op == TC2_BWD_DH || op == TC2_BWD_DX; }
+
 #define TC2_THREADS TC_THREADS
 #define TC2_CONSUMERS (TC_EPI_WARPS + 2)  // per CTA: epilogue warps, token producer, MMA or weight producer
 
@@ -69,15 +83,17 @@ struct Tc2Tile {
   bool shared, v0, v1;  // this CTA's weight sub-tiles exist (rows < n_out)
   bool mma1;            // the second accumulator is computed
   bool reread;          // another token tile of this group reads the same weight rows
-  int ntok, npad, half, tok0, row_a0, row_a1, row_b, out_row0, out_f0, out_f1;
+  int g, ntok, npad, half, tok0, row_a0, row_a1, row_b, out_row0, pout_row0, out_f0, out_f1;
   uint32_t bytes_a;     // weight bytes of one K step, both CTAs together
 };
 
-template <bool DOWN, int NACC>
+template <int OP, int NACC>
 MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b, int n_out,
                          uint32_t rank) {
+  constexpr bool DOWN = tc2_down(OP);
   Tc2Tile t;
   const int g = find_group(toff, E, b);
+  t.g = g;
   t.shared = g == E;
   const int nt = G.ntt[g];
   t.reread = nt > 1;
@@ -106,15 +122,27 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   t.row_a0 = base + t.out_f0;
   t.row_a1 = base + t.out_f1;
   t.bytes_a = (uint32_t)nsub * (TC_BM * TC_BK * 2);
-  t.row_b = ((!DOWN && t.shared) ? t.tok0 : G.off[g] + t.tok0) + (int)rank * t.half;
+  // token rows: x_perm / x (shared) for the gate/up products, H for the
+  // down projection, the padded dY rows / dy (shared) for dH, the padded
+  // dA|dB rows for dX
+  int rb;
+  if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB) rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
+  else if (OP == TC2_FWD_DOWN) rb = G.off[g] + t.tok0;
+  else if (OP == TC2_BWD_DH) rb = t.shared ? t.tok0 : G.poff[g] + t.tok0;
+  else rb = G.poff[g] + t.tok0;
+  t.row_b = rb + (int)rank * t.half;
   t.out_row0 = G.off[g] + t.tok0;
+  t.pout_row0 = G.poff[g] + t.tok0;
   return t;
 }
 
-template <int SA, int SB, int NACC, int NBUF, int OUTB, bool DOWN>
+template <int SA, int SB, int NACC, int NBUF, int OUTB, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC2_THREADS, 1)
 k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
-             int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh) {
+             int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
+             const __nv_bfloat16* __restrict__ aux) {
+  constexpr bool DOWN = tc2_down(OP);
+  constexpr bool MNA = tc2_mn_a(OP);
   using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB>;
   static_assert(OUTB >= 0 && OUTB <= 2, "staged boxes per epilogue warp");
   // second GEMM with both 256-row blocks in one TMEM buffer: staggered blocks
@@ -128,8 +156,9 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const bool leader = rank == 0;
 
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
-  const int32_t* toff = DOWN ? G.toff_b : G.toff_a;
-  int* counter = G.next + (DOWN ? 1 : 0);
+  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB) ? G.toff_a
+                        : (OP == TC2_BWD_DH ? G.toff_c : G.toff_b);
+  int* counter = G.next + OP;
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
@@ -228,7 +257,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           b = next_tile(i, true);
         }
         if (b < 0) break;
-        const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
+        const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
         const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
         const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
         const uint64_t pol_w = t.reread ? pol_again : pol_once;
@@ -241,8 +270,29 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           uint8_t* st = smem + sa * C::A_STAGE;
           const uint32_t fb = lead(a_full(sa));
           if (leader) mbar_arrive_expect_tx(a_full(sa), t.bytes_a);
-          if (t.v0) tma_load_2d_pair(smem_u32(st), mA0, fb, kb * TC_BK, t.row_a0, pol_w);
-          if (t.v1) tma_load_2d_pair(smem_u32(st + C::A_BYTES), mA1, fb, kb * TC_BK, t.row_a1, pol_w);
+          if (MNA) {
+            // rows kb*64 .. +63 of the K dimension of the transposed weights,
+            // M columns out_f .. +127 as two 64-column blocks 8 KB apart
+            const int kr = OP == TC2_BWD_DX ? K / 2 : K;  // K rows per matrix
+            const int kk0 = kb * TC_BK;
+            const bool second = OP == TC2_BWD_DX && kk0 >= kr;
+            const CUtensorMap* mA = t.shared ? (second ? &maps.sa1 : &maps.sa0)
+                                             : (second ? &maps.a1 : &maps.a0);
+            const int y = (t.shared ? 0 : t.g * kr) + (second ? kk0 - kr : kk0);
+            if (t.v0) {
+              tma_load_2d_pair(smem_u32(st), mA, fb, t.out_f0, y, pol_w);
+              tma_load_2d_pair(smem_u32(st + C::A_BYTES / 2), mA, fb, t.out_f0 + 64, y, pol_w);
+            }
+            if (t.v1) {
+              tma_load_2d_pair(smem_u32(st + C::A_BYTES), mA, fb, t.out_f1, y, pol_w);
+              tma_load_2d_pair(smem_u32(st + C::A_BYTES + C::A_BYTES / 2), mA, fb, t.out_f1 + 64,
+                               y, pol_w);
+            }
+          } else {
+            if (t.v0) tma_load_2d_pair(smem_u32(st), mA0, fb, kb * TC_BK, t.row_a0, pol_w);
+            if (t.v1)
+              tma_load_2d_pair(smem_u32(st + C::A_BYTES), mA1, fb, kb * TC_BK, t.row_a1, pol_w);
+          }
           progress[0] = it + 1;
         }
       }
@@ -255,8 +305,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       for (int i = 0;; ++i) {
         const int b = next_tile(i, true);
         if (b < 0) break;
-        const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
-        const bool bs = !DOWN && t.shared;
+        const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
+        const bool bs = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH) && t.shared;
         const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
         const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
         const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
@@ -293,8 +343,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           const int b = next_tile(i, true);
           if (b < 0) break;
           if (*abort_flag) continue;  // keep reading the tile ring until the scheduler says "none"
-          const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, 0);
-          const uint32_t idesc = umma_idesc_bf16(2 * TC_BM, t.npad);
+          const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, 0);
+          const uint32_t idesc = umma_idesc_bf16(2 * TC_BM, t.npad) | (MNA ? (1u << 15) : 0u);
           const int u = tl % NBUF;  // TMEM buffer of this tile
           // k step kb of this tile uses ring stage it + kb
           auto stage_ready = [&](int kb) -> bool {
@@ -313,8 +363,10 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             const uint32_t d = tmem + (w ? 256u : (uint32_t)(u * 256));
 #pragma unroll
             for (int kk = 0; kk < TC_BK / 16; ++kk)
-              umma_bf16_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32), idesc,
-                             (kb | kk) != 0);
+              umma_bf16_pair(d,
+                             MNA ? umma_desc_sw128_mn(a + kk * 2048, C::A_BYTES / 2)
+                                 : umma_desc_sw128(a + kk * 32),
+                             umma_desc_sw128(bb + kk * 32), idesc, (kb | kk) != 0);
             mma_issued = true;
           };
           auto release = [&](int kb) {  // the stage is free once its MMAs complete
@@ -379,8 +431,12 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   } else {
     // ---------- epilogue warps 2 .. 2+TC_EPI_WARPS-1 (both CTAs) ----------
     // Warp (q, half) drains TMEM lanes 32 q .. +31 (its 32 output rows),
-    // token columns 32 half + 64 j.  The first GEMM drains both accumulators
-    // at once (SwiGLU); the second drains block 0, frees it, then block 1.
+    // token columns 32 half + 64 j.  Gate/up tiles drain both accumulators
+    // at once (SwiGLU, or its gradient); two-block tiles drain block 0, free
+    // it, then block 1.  bf16 outputs of 32 whole tokens go out through
+    // shared memory by TMA store; the rest (a ragged last chunk, the shared
+    // expert's fp32 rows, the SwiGLU gradient) from registers.
+    constexpr bool F32SH = OP == TC2_FWD_DOWN || OP == TC2_BWD_DX;  // shared rows in fp32
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
@@ -390,7 +446,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       __syncwarp();
       if (lane == 0) release_tile(i % TC_TILE_RING);
       if (b < 0) break;
-      const Tc2Tile t = tc2_tile<DOWN, NACC>(G, toff, E, b, n_out, rank);
+      const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
       const int u = tl % NBUF;
       for (int ph = 0; ph < (STAG ? 2 : 1); ++ph) {
         const int bi = STAG ? ph : u;  // barrier pair of this phase
@@ -405,13 +461,13 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const int of = (ph ? t.out_f1 : t.out_f0) + 32 * q;  // first output column of the warp
         for (int c = 32 * half; c < t.npad; c += 64) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-          if (OUTB > 0 && c + 32 <= t.ntok && !(DOWN && t.shared)) {
+          if (OUTB > 0 && OP != TC2_BWD_DAB && c + 32 <= t.ntok && !(F32SH && t.shared)) {
             // 32 whole tokens of bf16 output: stage the box in shared
             // memory and store it with TMA (boxes used round robin)
             const uint32_t box = stg + (uint32_t)((nbox % (OUTB > 0 ? OUTB : 1)) * TC_BOX_BYTES);
             if (lane == 0) bulk_wait_read<(OUTB > 0 ? OUTB - 1 : 0)>();  // the box's last store read it
             __syncwarp();
-            stage_box_bf16<!DOWN>(ta + c, tb + c, box, lane);
+            stage_box_bf16<OP == TC2_FWD_UP>(ta + c, tb + c, box, lane);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -428,11 +484,25 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           else
             tmem_load_32(ta + c, va);
           if (!valid) continue;
-          if (!DOWN) {
+          if (OP == TC2_FWD_UP) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
             store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
-          } else if (t.shared) {
+          } else if (OP == TC2_BWD_DAB) {
+            // dH of (token c + j, this lane's hidden unit), rows as H's
+            float da[32], db[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float gh = c + j < t.ntok
+                  ? __bfloat162float(aux[(size_t)(t.out_row0 + c + j) * n_out + of + lane]) : 0.f;
+              const float a = va[j], sg = 1.0f / (1.0f + __expf(-a));
+              da[j] = gh * vb[j] * (sg * (1.0f + a * (1.0f - sg)));
+              db[j] = gh * (a * sg);
+            }
+            __nv_bfloat16* o = out + (size_t)(t.pout_row0 + c) * (2 * n_out) + of;
+            store_rows_bf16(o, 2 * n_out, da, c, t.ntok, lane);
+            store_rows_bf16(o + n_out, 2 * n_out, db, c, t.ntok, lane);
+          } else if (F32SH && t.shared) {
             store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
           } else {
             store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);

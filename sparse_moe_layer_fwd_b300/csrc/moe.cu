@@ -26,6 +26,7 @@
 #include "ptx.cuh"
 #include "router.cuh"
 #include "router_tc.cuh"
+#include "backward.cuh"
 
 namespace {
 
@@ -79,6 +80,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Plan {
   int T, d, h, E, k, TK;
   bool f32, route_only, simt, big_router, big_tiles, tc_router;
+  bool training;  // the backward's buffers follow the forward's
   int el;  // bytes per activation / weight element
   // router: CUDA-core tiles (r_bm x r_bn) or tensor-core pairs over E_pad
   // experts (rt_eb blocks of 256) x rt_tt token tiles x n_split K slices
@@ -86,17 +88,23 @@ struct Plan {
   // dispatch
   int n_pair_blocks;
   // expert tiling
-  int bn, ft_a, ft_b, tile_round, max_tiles_a, max_tiles_b;
+  int bn, ft_a, ft_b, ft_c, tile_round, max_tiles_a, max_tiles_b, max_tiles_c;
   // workspace regions (byte offsets)
   size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh,
       total;
+  // backward: padded dY rows, dG, du, dH, padded dA|dB rows, dX rows, shared dX
+  size_t o_dyp, o_dg, o_du, o_dh, o_dab, o_dxp, o_dxs;
+  long long rows_dyp, rows_dab;  // allocated padded rows
   size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh;
 };
 
 int validate_desc(const moe_desc* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
-  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS)) return MOE_ERR_DTYPE;
+  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING)) return MOE_ERR_DTYPE;
+  if ((d->flags & MOE_TRAINING) &&
+      (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY))))
+    return MOE_ERR_DTYPE;
   if ((d->flags & MOE_SIMT_EXPERTS) && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
   if (d->T < 0 || d->d <= 0 || d->h <= 0 || d->E < 1 || d->E > MOE_MAX_E || d->k < 1 ||
       d->k > d->E || d->k > 32)
@@ -188,7 +196,9 @@ Plan make_plan(const moe_desc* d) {
       // 256 tokens (N a multiple of 16) over 256 (first GEMM) or 512 (second)
       // weight rows; fewer: 1-SM tiles of up to 64 tokens over 128 / 256 rows
       const double per_expert = p.E > 0 ? (double)p.TK / p.E : 0.0;
-      p.big_tiles = per_expert >= 96.0;
+      // (training: always the CTA-pair tiles, whose tile table the
+      // backward's products share)
+      p.big_tiles = per_expert >= 96.0 || (d->flags & MOE_TRAINING);
       if (p.big_tiles) {
         p.bn = kPairBN;
         p.ft_a = MOE_PAIR_GEMM1 ? (p.h + 2 * TC_BM - 1) / (2 * TC_BM) : p.h / TC_BM;
@@ -203,6 +213,8 @@ Plan make_plan(const moe_desc* d) {
                                 (p.T + p.bn - 1) / p.bn + 1;
     p.max_tiles_a = (int)(tok_tiles * p.ft_a);
     p.max_tiles_b = (int)(tok_tiles * p.ft_b);
+    p.ft_c = (p.h + 4 * TC_BM - 1) / (4 * TC_BM);  // backward dH: 512 hidden rows per tile
+    p.max_tiles_c = (int)(tok_tiles * p.ft_c);
   }
 
   // workspace
@@ -216,7 +228,7 @@ Plan make_plan(const moe_desc* d) {
   region(p.tc_router ? (size_t)3 * p.E_pad * p.d * 2 : 0, p.o_w3, p.b_w3);
   region((size_t)p.n_pair_blocks * p.E * 4, p.o_hist, p.b_hist);
   region((size_t)p.TK * 4, p.o_rank, p.b_rank);
-  region((size_t)(5 * p.E + 10) * 4, p.o_groups, p.b_groups);
+  region((size_t)MOE_GROUP_INTS(p.E) * 4, p.o_groups, p.b_groups);
   if (!p.route_only) {
     region((size_t)p.TK * 4, p.o_perm, p.b_perm);
     region((size_t)p.TK * 4, p.o_inv, p.b_inv);
@@ -224,6 +236,20 @@ Plan make_plan(const moe_desc* d) {
     region((size_t)(p.TK + p.T) * p.h * p.el, p.o_h, p.b_h);
     region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
     region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
+  }
+  p.training = d->flags & MOE_TRAINING;
+  if (p.training) {
+    size_t b;
+    // every group padded to 16 rows: at most 15 extra rows per group
+    p.rows_dyp = (long long)p.TK + 15LL * p.E;
+    p.rows_dab = (long long)p.TK + p.T + 15LL * (p.E + 1);
+    region((size_t)p.rows_dyp * p.d * 2, p.o_dyp, b);
+    region((size_t)p.TK * 4, p.o_dg, b);
+    region((size_t)p.TK * 4, p.o_du, b);
+    region((size_t)(p.TK + p.T) * p.h * 2, p.o_dh, b);
+    region((size_t)p.rows_dab * 2 * p.h * 2, p.o_dab, b);
+    region((size_t)p.TK * p.d * 2, p.o_dxp, b);
+    region((size_t)p.T * p.d * 4, p.o_dxs, b);
   }
   p.total = off > 0 ? off : 256;
   return p;
@@ -368,24 +394,39 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   return ok;
 }
 
-// The CTA-pair kernel of each GEMM.
-template <bool DOWN> struct PairCfg;
-template <> struct PairCfg<false> {
-  static constexpr int SA = MOE_PAIR1_SA, SB = MOE_PAIR1_SB, NACC = 2, NBUF = 1,
-                       OUTB = MOE_PAIR1_OUTB;
-};
-template <> struct PairCfg<true> {
-  static constexpr int SA = MOE_PAIR2_SA, SB = MOE_PAIR2_SB, NACC = 2, NBUF = 1,
-                       OUTB = MOE_PAIR2_OUTB;
+// The CTA-pair kernel of each operation: ring depths and staged output
+// boxes.  The backward's two-block products (dH, dX) take the second GEMM's
+// configuration; the SwiGLU gradient stores from registers, so its shared
+// memory goes to the rings.
+template <int OP> struct PairCfg {
+  static constexpr bool UP = OP == TC2_FWD_UP;
+  static constexpr int SA = OP == TC2_BWD_DAB ? 5 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
+  static constexpr int SB = OP == TC2_BWD_DAB ? 4 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
+  static constexpr int OUTB = OP == TC2_BWD_DAB ? 0 : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
+  static constexpr int NACC = 2, NBUF = 1;
 };
 
-template <bool DOWN>
+template <int OP>
 bool set_tc2_smem() {
-  using P = PairCfg<DOWN>;
-  return cudaFuncSetAttribute(k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, DOWN>,
+  using P = PairCfg<OP>;
+  return cudaFuncSetAttribute(k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, OP>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES) ==
          cudaSuccess;
+}
+
+// One grouped product on CTA pairs, persistent: one pair per two SMs, at
+// most one pair per tile.
+template <int OP>
+void launch_pair(const Plan& p, const TcMapsDev& m, int max_tiles, int32_t* groups, int K,
+                 int n_out, __nv_bfloat16* out, float* ysh, const __nv_bfloat16* aux,
+                 cudaStream_t s) {
+  const int pairs = sm_count() / 2;
+  const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
+  using P = PairCfg<OP>;
+  k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, OP>
+      <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES, s>>>(
+          m, groups, p.E, K, n_out, out, ysh, aux);
 }
 
 template <int BN, int SA, int SB, bool DOWN>
@@ -403,12 +444,8 @@ void launch_gemm(const Plan& p, const TcMapsDev& m, bool pair, int BN, int max_t
   const int sms = sm_count();
   const int K = DOWN ? p.h : p.d, n_out = DOWN ? p.d : p.h;
   if (pair) {
-    const int pairs = sms / 2;
-    const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
-    using P = PairCfg<DOWN>;
-    k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, DOWN>
-        <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES, s>>>(
-            m, groups, p.E, K, n_out, out, ysh);
+    launch_pair<DOWN ? TC2_FWD_DOWN : TC2_FWD_UP>(p, m, max_tiles, groups, K, n_out, out, ysh,
+                                                  nullptr, s);
   } else if (BN == kBigBN) {
     const int grid = max_tiles < sms ? max_tiles : sms;
     k_expert_tc<kBigBN, kBigSA, kBigSB, DOWN><<<grid, TC_THREADS,
@@ -482,8 +519,10 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     if (!make_tc_maps(p, x, experts, shared, ws, &maps)) return MOE_ERR_DEVICE;
     const bool ok =
         p.big_tiles
-            ? ((MOE_PAIR_GEMM1 ? set_tc2_smem<false>() : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
-               (MOE_PAIR_GEMM2 ? set_tc2_smem<true>() : set_tc1_smem<kBigBN, kBigSA, kBigSB, true>()))
+            ? ((MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
+                               : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
+               (MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
+                               : set_tc1_smem<kBigBN, kBigSA, kBigSB, true>()))
             : (set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, false>() &&
                set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, true>());
     if (!ok) return MOE_ERR_LAUNCH;
@@ -627,6 +666,139 @@ int moe_bias_update(const int32_t* load_counts, float* bias, float gamma, int E,
   cudaGetLastError();
   k_bias_update<<<(E + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(load_counts, bias,
                                                                                  gamma, E, TK);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+// ---- backward ---------------------------------------------------------------
+// Tensor maps of the backward's products, built before anything is launched.
+struct BwdMaps {
+  TcMaps fwd;        // the forward's (gate/up recomputation reuses fwd.up)
+  TcMapsDev dh, dx;  // dH = dY W_down, dX = dA W_gate + dB W_up (weights transposed)
+  WgMapsDev wd, wgu; // weight gradients: dW_down; dW_gate and dW_up
+};
+
+bool make_bwd_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
+                   const void* dy, uint8_t* ws, BwdMaps* m) {
+  bool ok = make_tc_maps(p, x, ex, sh, ws, &m->fwd);
+  const long long rows_h = (long long)p.TK + p.T;
+  // dH: W_down [E*d rows, h cols] read as d-row x h-column boxes (MN-major)
+  ok &= make_map(&m->dh.a0, ex->w_down, (long long)p.E * p.d, p.h, 64);
+  ok &= make_map(&m->dh.sa0, sh->w_down, p.d, p.h, 64);
+  m->dh.a1 = m->dh.a0;
+  m->dh.sa1 = m->dh.sa0;
+  ok &= make_rows_maps(&m->dh.b128, &m->dh.b64, &m->dh.b16, &m->dh.b8, ws + p.o_dyp, p.rows_dyp,
+                       p.d);
+  ok &= make_rows_maps(&m->dh.bs128, &m->dh.bs64, &m->dh.bs16, &m->dh.bs8, dy, p.T, p.d);
+  ok &= make_out_map(&m->dh.out, ws + p.o_dh, rows_h, p.h);
+  // dX: W_gate, W_up [E*h rows, d cols] (MN-major), dA|dB rows [rows, 2h]
+  ok &= make_map(&m->dx.a0, ex->w_gate, (long long)p.E * p.h, p.d, 64);
+  ok &= make_map(&m->dx.a1, ex->w_up, (long long)p.E * p.h, p.d, 64);
+  ok &= make_map(&m->dx.sa0, sh->w_gate, p.h, p.d, 64);
+  ok &= make_map(&m->dx.sa1, sh->w_up, p.h, p.d, 64);
+  ok &= make_rows_maps(&m->dx.b128, &m->dx.b64, &m->dx.b16, &m->dx.b8, ws + p.o_dab, p.rows_dab,
+                       2LL * p.h);
+  m->dx.bs128 = m->dx.b128;
+  m->dx.bs64 = m->dx.b64;
+  m->dx.bs16 = m->dx.b16;
+  m->dx.bs8 = m->dx.b8;
+  ok &= make_out_map(&m->dx.out, ws + p.o_dxp, p.TK, p.d);
+  // weight gradients: both operands MN-major, 64-column x 64-row boxes
+  ok &= make_map(&m->wd.p, ws + p.o_dyp, p.rows_dyp, p.d, 64);
+  ok &= make_map(&m->wd.ps, dy, p.T, p.d, 64);
+  ok &= make_map(&m->wd.q, ws + p.o_h, rows_h, p.h, 64);
+  m->wd.qs = m->wd.q;
+  ok &= make_map(&m->wgu.p, ws + p.o_dab, p.rows_dab, 2LL * p.h, 64);
+  m->wgu.ps = m->wgu.p;
+  ok &= make_map(&m->wgu.q, ws + p.o_xperm, p.TK, p.d, 64);
+  ok &= make_map(&m->wgu.qs, x, p.T, p.d, 64);
+  return ok;
+}
+
+int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
+                 const moe_expert_w* experts, const moe_expert_w* shared,
+                 const int32_t* topk_idx, const float* gates, const void* dy, void* dx,
+                 const moe_expert_grad* d_experts, const moe_expert_grad* d_shared,
+                 float* d_router, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = validate_desc(desc);
+  if (rc != MOE_OK) return rc;
+  if (!(desc->flags & MOE_TRAINING)) return MOE_ERR_DTYPE;
+  const Plan p = make_plan(desc);
+  if (!w_router || !experts || !shared || !d_experts || !d_shared || !d_router || !workspace)
+    return MOE_ERR_NULL;
+  if (!experts->w_gate || !experts->w_up || !experts->w_down || !shared->w_gate ||
+      !shared->w_up || !shared->w_down || !d_experts->d_gate || !d_experts->d_up ||
+      !d_experts->d_down || !d_shared->d_gate || !d_shared->d_up || !d_shared->d_down)
+    return MOE_ERR_NULL;
+  if (p.T > 0 && (!x || !topk_idx || !gates || !dy || !dx)) return MOE_ERR_NULL;
+  const void* ptrs[] = {x, w_router, experts->w_gate, experts->w_up, experts->w_down,
+                        shared->w_gate, shared->w_up, shared->w_down, dy, dx,
+                        d_experts->d_gate, d_experts->d_up, d_experts->d_down, d_shared->d_gate,
+                        d_shared->d_up, d_shared->d_down, d_router, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_ALIGN;
+  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t e_hd = (size_t)p.E * p.h * p.d * 4, hd = (size_t)p.h * p.d * 4;
+  cudaGetLastError();
+  if (p.T == 0) {  // no tokens: every gradient is zero
+    const bool ok = cudaMemsetAsync(d_experts->d_gate, 0, e_hd, s) == cudaSuccess &&
+                    cudaMemsetAsync(d_experts->d_up, 0, e_hd, s) == cudaSuccess &&
+                    cudaMemsetAsync(d_experts->d_down, 0, e_hd, s) == cudaSuccess &&
+                    cudaMemsetAsync(d_shared->d_gate, 0, hd, s) == cudaSuccess &&
+                    cudaMemsetAsync(d_shared->d_up, 0, hd, s) == cudaSuccess &&
+                    cudaMemsetAsync(d_shared->d_down, 0, hd, s) == cudaSuccess &&
+                    cudaMemsetAsync(d_router, 0, (size_t)p.E * p.d * 4, s) == cudaSuccess;
+    return ok ? MOE_OK : MOE_ERR_LAUNCH;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdMaps maps;
+  if (!make_bwd_maps(p, x, experts, shared, dy, ws, &maps)) return MOE_ERR_DEVICE;
+  if (!set_tc2_smem<TC2_BWD_DH>() || !set_tc2_smem<TC2_BWD_DAB>() ||
+      !set_tc2_smem<TC2_BWD_DX>() ||
+      cudaFuncSetAttribute(k_wgrad_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           WG_SMEM_BYTES) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+
+  int32_t* groups = reinterpret_cast<int32_t*>(ws + p.o_groups);
+  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + p.o_perm);
+  const int32_t* inv = reinterpret_cast<const int32_t*>(ws + p.o_inv);
+  const float* part = reinterpret_cast<const float*>(ws + p.o_part);
+  __nv_bfloat16* dyp = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dyp);
+  float* dg = reinterpret_cast<float*>(ws + p.o_dg);
+  float* du = reinterpret_cast<float*>(ws + p.o_du);
+  __nv_bfloat16* dh = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dh);
+  __nv_bfloat16* dab = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dab);
+  __nv_bfloat16* dxp = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dxp);
+  float* dxs = reinterpret_cast<float*>(ws + p.o_dxs);
+  const __nv_bfloat16* dyb = static_cast<const __nv_bfloat16*>(dy);
+
+  k_bwd_tables<<<1, 1024, 0, s>>>(groups, p.E, p.ft_c);
+  k_bwd_prep<<<(p.TK + 7) / 8, 256, 0, s>>>(
+      groups, p.E, perm, topk_idx, gates, p.TK, p.k, p.d, dyb,
+      reinterpret_cast<const __nv_bfloat16*>(ws + p.o_yperm), dyp, dg);
+  k_bwd_zero_gaps<<<p.E + 1, 256, 0, s>>>(groups, p.E, dyp, p.d, dab, 2 * p.h);
+  k_bwd_router<<<(p.T + 7) / 8, 256, 0, s>>>(part, p.n_split, topk_idx, inv, dg, p.T, p.E, p.k,
+                                               du);
+  launch_pair<TC2_BWD_DH>(p, maps.dh, p.max_tiles_c, groups, p.d, p.h, dh, nullptr, nullptr, s);
+  launch_pair<TC2_BWD_DAB>(p, maps.fwd.up, p.max_tiles_a, groups, p.d, p.h, dab, nullptr, dh, s);
+  launch_pair<TC2_BWD_DX>(p, maps.dx, p.max_tiles_b, groups, 2 * p.h, p.d, dxp, dxs, nullptr, s);
+  const int pairs = sm_count() / 2;
+  auto wgrad = [&](const WgMapsDev& m, int M, int N, int pcol0, int slot, int p_from_ps,
+                   int q_from_qs, float* out, float* out_sh) {
+    const long long tiles = (long long)(p.E + 1) * ((M + 255) / 256) * ((N + 255) / 256);
+    const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
+    k_wgrad_tc2<<<grid, WG_THREADS, WG_SMEM_BYTES, s>>>(m, groups, p.E, M, N, pcol0, 0, slot,
+                                                         p_from_ps, q_from_qs, out, out_sh);
+  };
+  wgrad(maps.wd, p.d, p.h, 0, 5, 1, 0, d_experts->d_down, d_shared->d_down);
+  wgrad(maps.wgu, p.h, p.d, 0, 6, 0, 1, d_experts->d_gate, d_shared->d_gate);
+  wgrad(maps.wgu, p.h, p.d, p.h, 7, 0, 1, d_experts->d_up, d_shared->d_up);
+  k_bwd_router_wgrad<__nv_bfloat16><<<dim3(p.E, (p.d + 255) / 256), 256, 0, s>>>(
+      groups, p.E, perm, du, static_cast<const __nv_bfloat16*>(x), p.d, p.k, d_router);
+  k_bwd_combine<__nv_bfloat16><<<p.T, 128, 0, s>>>(dxs, dxp, inv, topk_idx, du, w_router, p.T,
+                                                    p.d, p.k, static_cast<__nv_bfloat16*>(dx));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 

@@ -139,6 +139,17 @@ MOE_DEV uint64_t umma_desc_sw128(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// The same for an MN-major operand (the matrix stored transposed: K rows of
+// contiguous M (or N) elements), as TMA writes a box of 64 elements x 64 K
+// rows with the 128-byte swizzle: 8-row K groups of 1024 bytes (stride byte
+// offset 1024), blocks of 64 M elements `lbo` bytes apart (leading byte
+// offset).  The k-th 16-row K slice starts 2048*k bytes further on.  The
+// instruction descriptor must mark the operand transposed (bit 15 for A).
+MOE_DEV uint64_t umma_desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 MOE_DEV void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -67,6 +67,26 @@ class MoeLayer:
             stream = torch.cuda.current_stream(self.workspace.device)
         M.moe_bias_update(self.load_counts, self.bias, gamma, self.E, self.T * self.k, stream)
 
+    def backward(self, x, dy, stream=None) -> dict:
+        """Gradients for the output gradient dy, after forward(x) on this layer
+        (built with MOE_TRAINING): dx, the expert and shared-expert weight
+        gradients (fp32) and the router's."""
+        if stream is None:
+            stream = torch.cuda.current_stream(self.workspace.device)
+        wg, wu, wd, sg, su, sd = self._keep
+        f32 = dict(dtype=torch.float32, device=self.workspace.device)
+        g = {"dx": torch.empty_like(dy), "dW_gate": torch.empty(wg.shape, **f32),
+             "dW_up": torch.empty(wu.shape, **f32), "dW_down": torch.empty(wd.shape, **f32),
+             "dsh_gate": torch.empty(sg.shape, **f32), "dsh_up": torch.empty(su.shape, **f32),
+             "dsh_down": torch.empty(sd.shape, **f32),
+             "dW_router": torch.empty(self.w_router.shape, **f32)}
+        M.moe_backward(self.desc, x, self.w_router, self.experts, self.shared, self.topk_idx,
+                       self.gates, dy, g["dx"],
+                       M.make_grads(g["dW_gate"], g["dW_up"], g["dW_down"]),
+                       M.make_grads(g["dsh_gate"], g["dsh_up"], g["dsh_down"]),
+                       g["dW_router"], self.workspace, self.ws_bytes, stream)
+        return g
+
     def balance_loss(self, seq_len: int, alpha: float = 1e-4, stream=None) -> torch.Tensor:
         """Per-sequence balance loss of the routing of the last forward."""
         if stream is None:

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 
 MOE_F32, MOE_BF16 = 0, 1
-MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS = 1, 2
+MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS, MOE_TRAINING = 1, 2, 4
 MOE_OK = 0
 MOE_STATIC_SCRATCH_BYTES = 32 << 20
 ERRORS = {
@@ -46,6 +46,11 @@ class MoeExpertW(ctypes.Structure):
                 ("w_down", ctypes.c_void_p)]
 
 
+class MoeExpertGrad(ctypes.Structure):
+    _fields_ = [("d_gate", ctypes.c_void_p), ("d_up", ctypes.c_void_p),
+                ("d_down", ctypes.c_void_p)]
+
+
 class MoeRegion(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 16), ("offset", ctypes.c_size_t),
                 ("bytes", ctypes.c_size_t)]
@@ -67,6 +72,9 @@ def _load():
     lib.moe_forward_profiled.restype = I
     lib.moe_bias_update.argtypes = [P, P, ctypes.c_float, I, I, P]
     lib.moe_bias_update.restype = I
+    gp = ctypes.POINTER(MoeExpertGrad)
+    lib.moe_backward.argtypes = [dp, P, P, ep, ep, P, P, P, P, gp, gp, P, P, S, P]
+    lib.moe_backward.restype = I
     lib.moe_seq_balance_loss.argtypes = [dp, I, ctypes.c_float, P, P, S, P, P]
     lib.moe_seq_balance_loss.restype = I
     lib.moe_last_error.argtypes, lib.moe_last_error.restype = [], I
@@ -116,6 +124,10 @@ def make_desc(T, d, h, E, k, dtype="bf16", flags=0) -> MoeDesc:
 
 def make_experts(w_gate, w_up, w_down) -> MoeExpertW:
     return MoeExpertW(_ptr(w_gate), _ptr(w_up), _ptr(w_down))
+
+
+def make_grads(d_gate, d_up, d_down) -> MoeExpertGrad:
+    return MoeExpertGrad(_ptr(d_gate), _ptr(d_up), _ptr(d_down))
 
 
 def _check(rc: int, where: str) -> int:
@@ -173,6 +185,18 @@ def moe_bias_update(load_counts, bias, gamma, E, TK, stream=None, check=True) ->
     rc = _lib.moe_bias_update(_ptr(load_counts), _ptr(bias), ctypes.c_float(gamma), int(E),
                               int(TK), _stream(stream))
     return _check(rc, "moe_bias_update") if check else rc
+
+
+def moe_backward(desc, x, w_router, experts, shared, topk_idx, gates, dy, dx, d_experts, d_shared,
+                 d_router, workspace, ws_bytes, stream=None, check=True) -> int:
+    rc = _lib.moe_backward(ctypes.byref(desc), _ptr(x), _ptr(w_router),
+                           ctypes.byref(experts) if experts is not None else None,
+                           ctypes.byref(shared) if shared is not None else None,
+                           _ptr(topk_idx), _ptr(gates), _ptr(dy), _ptr(dx),
+                           ctypes.byref(d_experts) if d_experts is not None else None,
+                           ctypes.byref(d_shared) if d_shared is not None else None,
+                           _ptr(d_router), _ptr(workspace), int(ws_bytes), _stream(stream))
+    return _check(rc, "moe_backward") if check else rc
 
 
 def moe_seq_balance_loss(desc, seq_len, alpha, topk_idx, workspace, ws_bytes, loss, stream=None,

@@ -17,7 +17,7 @@ def test_library_exports_every_header_function():
     assert set(names) == {
         "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
-        "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss"}
+        "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -96,6 +96,21 @@ def test_argument_errors_are_found_on_the_host():
     assert M.moe_bias_update(None, FAKE, 1e-3, 16, 64, check=False) == E["MOE_ERR_NULL"]
     assert M.moe_bias_update(FAKE, FAKE, 1e-3, 0, 64, check=False) == E["MOE_ERR_SHAPE"]
     assert M.moe_bias_update(FAKE, FAKE, 1e-3, 16, -1, check=False) == E["MOE_ERR_SHAPE"]
+    # backward arguments: needs the training flag (bf16 tensor-core path only)
+    fk = M.make_experts(FAKE, FAKE, FAKE)
+    gk = M.make_grads(FAKE, FAKE, FAKE)
+    dt = M.make_desc(64, 256, 128, 16, 4, "bf16", M.MOE_TRAINING)
+    wst = M.moe_workspace_size(dt)
+    bw = lambda desc=dt, **o: M.moe_backward(  # noqa: E731
+        desc, o.get("x", FAKE), FAKE, fk, fk, FAKE, FAKE, o.get("dy", FAKE), FAKE,
+        o.get("dexp", gk), gk, FAKE, FAKE, o.get("ws_bytes", wst), check=False)
+    assert wst > M.moe_workspace_size(d)
+    assert bw(desc=d) == E["MOE_ERR_DTYPE"]
+    assert M.moe_workspace_size(M.make_desc(64, 256, 128, 16, 4, "f32", M.MOE_TRAINING)) == 0
+    assert bw(dy=None) == E["MOE_ERR_NULL"]
+    assert bw(dexp=M.make_grads(FAKE, None, FAKE)) == E["MOE_ERR_NULL"]
+    assert bw(x=FAKE + 4) == E["MOE_ERR_ALIGN"]
+    assert bw(ws_bytes=wst - 1) == E["MOE_ERR_WORKSPACE"]
     # balance-loss arguments
     ws = M.moe_workspace_size(d)
     bl = lambda **o: M.moe_seq_balance_loss(  # noqa: E731
