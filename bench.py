@@ -468,6 +468,75 @@ CONFIGS = {"C0": "tiny_fp32", "C1": "mini_bf16", "C2": "bias_dynamics", "C3": "v
            "C4": "v3_decode", "C4z": "v3_decode_zipf"}
 
 
+def run_train(args, wl):
+    """Training step: forward (with the backward's buffers) and backward for
+    a fixed output gradient, timed together; reports tokens/s of the step,
+    the two phases, and the backward's GEMM FLOPs against the sustained bf16
+    peak (12 d h FLOP per routed pair or shared-expert token: dH, dX and the
+    three weight gradients; the recomputed gate/up products are not counted)."""
+    from sparse_moe_layer_fwd_b300 import inputs as I
+    from sparse_moe_layer_fwd_b300 import moe as M
+    from sparse_moe_layer_fwd_b300.layer import MoeLayer
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    inp = I.make_inputs(wl.with_(seed=wl.seed + 1000 * rank) if ws > 1 else wl, device="cuda")
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_TRAINING)
+    gen = torch.Generator(device="cuda").manual_seed(wl.seed + 7)
+    dy = torch.randn((wl.T, wl.d), generator=gen, device="cuda").to(inp["x"].dtype)
+    x = inp["x"]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward(x, stream)
+        layer.backward(x, dy, stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    t0 = time.time()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        layer.forward(x, stream)
+        ev[i][1].record(stream)
+        layer.backward(x, dy, stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop(t0, time.time()) if sampler else None
+    if M.moe_last_error() != M.MOE_OK:
+        raise RuntimeError("device error word set")
+    fwd = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
+    bwd = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    elapsed_ms, value = aggregate(fwd + bwd, wl.T * args.steps, ws, "cuda")
+    if rank != 0:
+        return
+    peaks = _peaks()
+    rows = wl.T * wl.k + wl.T
+    bflops = 12.0 * rows * wl.d * wl.h
+    bwd_ms = bwd / args.steps
+    sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    ach = bflops / (bwd_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC + " [training step: forward + backward]", "value": value,
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 weight gradients)",
+        "data": "synthetic (seeded N(0,1) tokens and output gradient, N(0,1/fan_in) weights)",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
+                   "l2": "inputs larger than L2"},
+        "phase_ms": {"forward": fwd / args.steps, "backward": bwd_ms},
+        "roofline": {"bound": "tensor", "kernel": "backward (dH, dX, weight-gradient GEMMs)",
+                     "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
+                     "traffic": None,
+                     "peak_kind": f"{peaks['source']} bf16 sustained; 12 d h FLOP per row",
+                     "flops_per_launch": bflops, "ms_per_launch": bwd_ms},
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_bias_dynamics(args, wl):
     """Route + bias update per step on a fresh batch each step (the
     bias-balancing run); reports ms per step and the per-expert load share
@@ -533,6 +602,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step: forward and backward")
     ap.add_argument("--route-only", action="store_true",
                     help="time the routing pass only (router, top-k, load counts)")
     args = ap.parse_args()
@@ -545,6 +616,8 @@ def main():
     wl = I.WORKLOADS[CONFIGS[args.config] if args.config else args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.train:
+        run_train(args, wl)
     elif wl.steps > 1:
         run_bias_dynamics(args, wl)
     else:

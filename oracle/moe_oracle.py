@@ -354,3 +354,31 @@ def moe_backward_dense(x, w_router, bias, experts, shared, k: int, dy,
     out.update({"dW_gate": dwg, "dW_up": dwu, "dW_down": dwd, "dG": dG, "du": du})
     return out
 
+
+def backward_token_rows(x_rows, w_router, bias, get_expert, shared, k: int, dy_rows,
+                        idx_override=None) -> np.ndarray:
+    """dx of a sample of tokens: reading 9 restricted to their rows (a token's
+    dx depends only on its own routing and experts), streaming the experts
+    they selected one at a time (get_expert(e) -> (W_gate, W_up, W_down)),
+    for workloads whose weights do not fit a float64 copy."""
+    x_rows, dy_rows = _f64(x_rows), _f64(dy_rows)
+    r = route(x_rows, w_router, bias, k)
+    idx = r["idx"] if idx_override is None else np.asarray(idx_override)
+    s = r["s"]
+    gates = gate_weights(s, idx)
+    dx = swiglu_expert_backward(x_rows, *shared, dy_rows)[0]
+    dg_sel = np.zeros(idx.shape, dtype=F64)
+    for e in np.unique(idx):
+        w = get_expert(int(e))
+        tt, jj = np.nonzero(idx == e)
+        dg_sel[tt, jj] = (dy_rows[tt] * swiglu_expert(x_rows[tt], *w)).sum(axis=1)
+        dxe = swiglu_expert_backward(x_rows[tt], *w, gates[tt, jj][:, None] * dy_rows[tt])[0]
+        np.add.at(dx, tt, dxe)
+    s_sel = np.take_along_axis(s, idx, axis=1)
+    ds_sel = (dg_sel - (dg_sel * gates).sum(axis=1, keepdims=True)) / s_sel.sum(axis=1, keepdims=True)
+    du_sel = ds_sel * s_sel * (1.0 - s_sel)
+    wr = _f64(w_router)
+    for j in range(idx.shape[1]):
+        dx += du_sel[:, j:j + 1] * wr[idx[:, j]]
+    return dx
+

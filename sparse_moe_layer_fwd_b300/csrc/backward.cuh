@@ -206,16 +206,22 @@ k_bwd_combine(const float* __restrict__ dxs, const __nv_bfloat16* __restrict__ d
 // both operands MN-major (stored K rows of contiguous M / N elements), loaded
 // as 64-element x 64-row boxes.  Two TMEM buffers: the epilogue of one tile
 // overlaps the MMAs of the next.  Tiles: (E + 1) groups x M/256 x N/256,
-// groups without rows write zeros.
+// groups without rows write zeros.  The fp32 output leaves through shared
+// memory: each epilogue warp stages 32 rows x 32 columns (a 128-byte-swizzled
+// 4 KB box, so that the row-per-lane writes spread over all banks) and stores
+// it with one TMA store.
 struct WgMapsDev {
   CUtensorMap p, ps;  // P rows: routed (padded layout), shared
   CUtensorMap q, qs;  // Q rows: routed, shared
+  CUtensorMap o, os;  // fp32 output rows: routed [(E) M, N], shared [M, N]; 32 x 32 boxes
 };
 
-#define WG_STAGES 6
+#define WG_STAGES 4
 #define WG_HALF_BYTES 16384  // 128 elements x 64 K rows (two 64-element blocks)
 #define WG_STAGE_BYTES (2 * WG_HALF_BYTES)
-#define WG_BAR_OFF (WG_STAGES * WG_STAGE_BYTES)
+#define WG_BOX_BYTES 4096                      // 32 x 32 fp32
+#define WG_STG_OFF (WG_STAGES * WG_STAGE_BYTES)   // two boxes per epilogue warp
+#define WG_BAR_OFF (WG_STG_OFF + TC_EPI_WARPS * 2 * WG_BOX_BYTES)
 #define WG_N_BARS (2 * WG_STAGES + 4 + 2 * TC_TILE_RING + 1)
 #define WG_SMEM_BYTES (WG_BAR_OFF + 8 * WG_N_BARS + 4 * TC_TILE_RING + 32 + 1024)
 #define WG_THREADS (32 * (2 + TC_EPI_WARPS))  // producer, MMA, epilogue warps
@@ -250,7 +256,7 @@ MOE_DEV WgTile wg_tile(const GroupTable& G, int E, int b, int MB, int NB, int pc
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WG_THREADS, 1)
 k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ groups, int E,
             int M, int N, int pcol0, int qcol0, int counter_slot, int shared_p_from_ps,
-            int shared_q_from_qs, float* __restrict__ dw, float* __restrict__ dw_shared) {
+            int shared_q_from_qs) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -416,7 +422,8 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
   } else {
     // ---------- epilogue: TMEM lane = output row, column = output column ----------
     const int q = warp & 3, hv = (warp - 2) >> 2;  // lanes 32 q .., columns 128 hv ..
-    int tl = 0;
+    const uint32_t stg = smem_u32(smem + WG_STG_OFF) + (uint32_t)((warp - 2) * 2 * WG_BOX_BYTES);
+    int tl = 0, nbox = 0;
     for (int i = 0;; ++i) {
       const int b = next_tile(i);
       __syncwarp();
@@ -429,9 +436,10 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
         continue;  // keep reading the tile ring until the scheduler says "none"
       }
       tc_fence_after();
-      const int row = t.m0 + 128 * (int)rank + 32 * q + lane;  // M a multiple of 128
-      const bool row_ok = t.m0 + 128 * (int)rank < M;
-      float* o = (t.shared ? dw_shared : dw + (size_t)t.g * M * N) + (size_t)row * N + t.n0;
+      const int row0 = t.m0 + 128 * (int)rank + 32 * q;  // this warp's first output row
+      const bool row_ok = t.m0 + 128 * (int)rank < M;    // M a multiple of 128
+      const CUtensorMap* om = t.shared ? &maps.os : &maps.o;
+      const int orow = (t.shared ? 0 : t.g * M) + row0;
       for (int c = 128 * hv; c < 128 * hv + 128; c += 32) {
         float v[32];
         tmem_load_32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(u * 256) + c, v);
@@ -439,10 +447,25 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
-        if (!row_ok || t.n0 + c >= N) continue;  // N a multiple of 32
-        float4* o4 = reinterpret_cast<float4*>(o + c);
+        if (!row_ok || t.n0 + c >= N) continue;  // N a multiple of 32; warp-uniform
+        const uint32_t box = stg + (uint32_t)((nbox & 1) * WG_BOX_BYTES);
+        if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
+        __syncwarp();
+        // row `lane` of the box, 16-byte chunk j at chunk j ^ (lane & 7)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t a = box + (uint32_t)(lane * 128 + 16 * (j ^ (lane & 7)));
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[4 * j]),
+                       "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(om, box, t.n0 + c, orow);
+          bulk_commit();
+        }
+        ++nbox;
       }
       tc_fence_before();
       __syncwarp();
@@ -451,6 +474,7 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
       }
       ++tl;
     }
+    if (lane == 0) bulk_wait_all();  // this warp's stores are complete
   }
 
   tc_fence_before();

@@ -294,6 +294,20 @@ bool make_out_map(CUtensorMap* m, const void* base, long long rows, long long co
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output rows [rows, cols] for TMA stores of 32 x 32 boxes, 128-byte
+// swizzle (the weight-gradient epilogue's staging layout).
+bool make_out_map_f32(CUtensorMap* m, const void* base, long long rows, long long cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows <= 0) return false;
@@ -674,11 +688,12 @@ int moe_bias_update(const int32_t* load_counts, float* bias, float gamma, int E,
 struct BwdMaps {
   TcMaps fwd;        // the forward's (gate/up recomputation reuses fwd.up)
   TcMapsDev dh, dx;  // dH = dY W_down, dX = dA W_gate + dB W_up (weights transposed)
-  WgMapsDev wd, wgu; // weight gradients: dW_down; dW_gate and dW_up
+  WgMapsDev wd, wg, wu; // weight gradients: dW_down, dW_gate, dW_up
 };
 
 bool make_bwd_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
-                   const void* dy, uint8_t* ws, BwdMaps* m) {
+                   const void* dy, uint8_t* ws, const moe_expert_grad* dex,
+                   const moe_expert_grad* dsh, BwdMaps* m) {
   bool ok = make_tc_maps(p, x, ex, sh, ws, &m->fwd);
   const long long rows_h = (long long)p.TK + p.T;
   // dH: W_down [E*d rows, h cols] read as d-row x h-column boxes (MN-major)
@@ -707,10 +722,17 @@ bool make_bwd_maps(const Plan& p, const void* x, const moe_expert_w* ex, const m
   ok &= make_map(&m->wd.ps, dy, p.T, p.d, 64);
   ok &= make_map(&m->wd.q, ws + p.o_h, rows_h, p.h, 64);
   m->wd.qs = m->wd.q;
-  ok &= make_map(&m->wgu.p, ws + p.o_dab, p.rows_dab, 2LL * p.h, 64);
-  m->wgu.ps = m->wgu.p;
-  ok &= make_map(&m->wgu.q, ws + p.o_xperm, p.TK, p.d, 64);
-  ok &= make_map(&m->wgu.qs, x, p.T, p.d, 64);
+  ok &= make_out_map_f32(&m->wd.o, dex->d_down, (long long)p.E * p.d, p.h);
+  ok &= make_out_map_f32(&m->wd.os, dsh->d_down, p.d, p.h);
+  ok &= make_map(&m->wg.p, ws + p.o_dab, p.rows_dab, 2LL * p.h, 64);
+  m->wg.ps = m->wg.p;
+  ok &= make_map(&m->wg.q, ws + p.o_xperm, p.TK, p.d, 64);
+  ok &= make_map(&m->wg.qs, x, p.T, p.d, 64);
+  m->wu = m->wg;
+  ok &= make_out_map_f32(&m->wg.o, dex->d_gate, (long long)p.E * p.h, p.d);
+  ok &= make_out_map_f32(&m->wg.os, dsh->d_gate, p.h, p.d);
+  ok &= make_out_map_f32(&m->wu.o, dex->d_up, (long long)p.E * p.h, p.d);
+  ok &= make_out_map_f32(&m->wu.os, dsh->d_up, p.h, p.d);
   return ok;
 }
 
@@ -754,7 +776,8 @@ int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdMaps maps;
-  if (!make_bwd_maps(p, x, experts, shared, dy, ws, &maps)) return MOE_ERR_DEVICE;
+  if (!make_bwd_maps(p, x, experts, shared, dy, ws, d_experts, d_shared, &maps))
+    return MOE_ERR_DEVICE;
   if (!set_tc2_smem<TC2_BWD_DH>() || !set_tc2_smem<TC2_BWD_DAB>() ||
       !set_tc2_smem<TC2_BWD_DX>() ||
       cudaFuncSetAttribute(k_wgrad_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -786,15 +809,15 @@ int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
   launch_pair<TC2_BWD_DX>(p, maps.dx, p.max_tiles_b, groups, 2 * p.h, p.d, dxp, dxs, nullptr, s);
   const int pairs = sm_count() / 2;
   auto wgrad = [&](const WgMapsDev& m, int M, int N, int pcol0, int slot, int p_from_ps,
-                   int q_from_qs, float* out, float* out_sh) {
+                   int q_from_qs) {
     const long long tiles = (long long)(p.E + 1) * ((M + 255) / 256) * ((N + 255) / 256);
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
     k_wgrad_tc2<<<grid, WG_THREADS, WG_SMEM_BYTES, s>>>(m, groups, p.E, M, N, pcol0, 0, slot,
-                                                         p_from_ps, q_from_qs, out, out_sh);
+                                                         p_from_ps, q_from_qs);
   };
-  wgrad(maps.wd, p.d, p.h, 0, 5, 1, 0, d_experts->d_down, d_shared->d_down);
-  wgrad(maps.wgu, p.h, p.d, 0, 6, 0, 1, d_experts->d_gate, d_shared->d_gate);
-  wgrad(maps.wgu, p.h, p.d, p.h, 7, 0, 1, d_experts->d_up, d_shared->d_up);
+  wgrad(maps.wd, p.d, p.h, 0, 5, 1, 0);
+  wgrad(maps.wg, p.h, p.d, 0, 6, 0, 1);
+  wgrad(maps.wu, p.h, p.d, p.h, 7, 0, 1);
   k_bwd_router_wgrad<__nv_bfloat16><<<dim3(p.E, (p.d + 255) / 256), 256, 0, s>>>(
       groups, p.E, perm, du, static_cast<const __nv_bfloat16*>(x), p.d, p.k, d_router);
   k_bwd_combine<__nv_bfloat16><<<p.T, 128, 0, s>>>(dxs, dxp, inv, topk_idx, du, w_router, p.T,

@@ -502,6 +502,16 @@ def pin_backward_special_cases(O):
     assert np.array_equal(g0["dW_router"], np.zeros_like(w_r))
 
 
+def pin_backward_rows_agree(O):
+    """The per-token-rows backward gives the dense backward's dx rows."""
+    x, w_r, b, ex, sh, dy = _backward_case(34, T=9, E=6, k=3)
+    full = O.moe_backward_dense(x, w_r, b, ex, sh, 3, dy)
+    rows = np.array([0, 4, 8])
+    got = O.backward_token_rows(x[rows], w_r, b, lambda e: (ex[0][e], ex[1][e], ex[2][e]), sh, 3,
+                                dy[rows])
+    assert np.allclose(got, full["dx"][rows], rtol=1e-12, atol=1e-12)
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -520,4 +530,5 @@ PINS = [
     pin_balance_loss_closed_forms,
     pin_backward_finite_differences,
     pin_backward_special_cases,
+    pin_backward_rows_agree,
 ]

@@ -75,3 +75,40 @@ def test_v3_decode_zipf_skew():
     print(f"v3_decode_zipf: {stats} flips={flips} touched={touched}")
     # the skew concentrates routing on fewer experts than the balanced run
     assert touched < 200
+
+
+def test_v3_prefill_backward_sampled():
+    """Full-size backward: every gradient finite, dx of 8 seeded tokens and
+    the weight gradients of the least-loaded expert against the oracle."""
+    wl = I.WORKLOADS["v3_prefill"]
+    inp = I.make_inputs(wl, device="cuda")
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_TRAINING)
+    layer.forward(inp["x"])
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    dy = torch.randn((wl.T, wl.d), generator=gen, device="cuda").to(torch.bfloat16)
+    g = layer.backward(inp["x"], dy)
+    torch.cuda.synchronize()
+    assert M.moe_last_error() == M.MOE_OK
+    for n, v in g.items():
+        assert torch.isfinite(v).all(), n
+    idx = npi(layer.topk_idx)
+    wr64, b64 = np64(inp["w_router"]), np64(inp["bias"])
+    sh = (np64(inp["sh_gate"]), np64(inp["sh_up"]), np64(inp["sh_down"]))
+    rows = np.sort(np.random.default_rng(0).choice(wl.T, 8, replace=False))
+    rt = torch.from_numpy(rows).cuda()
+    ref = O.backward_token_rows(np64(inp["x"][rt]), wr64, b64, _expert_fetcher(inp), sh, wl.k,
+                                np64(dy[rt]), idx_override=idx[rows])
+    got = np64(g["dx"][rt])
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 1e-2
+    # the least-loaded expert's weight gradients from its own tokens
+    load = np.bincount(idx.ravel(), minlength=wl.E)
+    e = int(np.argmin(np.where(load > 0, load, load.max() + 1)))
+    tt, jj = np.nonzero(idx == e)
+    xt = np64(inp["x"][torch.from_numpy(tt).cuda()])
+    gates = O.route(xt, wr64, b64, wl.k)
+    gt = O.gate_weights(gates["s"], idx[tt])[np.arange(len(tt)), jj]
+    dyt = np64(dy[torch.from_numpy(tt).cuda()])
+    _, dwg, dwu, dwd = O.swiglu_expert_backward(xt, *_expert_fetcher(inp)(e), gt[:, None] * dyt)
+    for name, ref_w in (("dW_gate", dwg), ("dW_up", dwu), ("dW_down", dwd)):
+        got_w = np64(g[name][e])
+        assert np.linalg.norm(got_w - ref_w) / np.linalg.norm(ref_w) < 1e-2, name
