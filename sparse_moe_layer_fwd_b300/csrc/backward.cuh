@@ -216,12 +216,17 @@ struct WgMapsDev {
   CUtensorMap o, os;  // fp32 output rows: routed [(E) M, N], shared [M, N]; 32 x 32 boxes
 };
 
-#define WG_STAGES 4
+#ifndef WG_STAGES
+#define WG_STAGES 5
+#endif
+#ifndef WG_BOXES
+#define WG_BOXES 2  // staged output boxes per epilogue warp, used round robin
+#endif
 #define WG_HALF_BYTES 16384  // 128 elements x 64 K rows (two 64-element blocks)
 #define WG_STAGE_BYTES (2 * WG_HALF_BYTES)
 #define WG_BOX_BYTES 4096                      // 32 x 32 fp32
 #define WG_STG_OFF (WG_STAGES * WG_STAGE_BYTES)   // two boxes per epilogue warp
-#define WG_BAR_OFF (WG_STG_OFF + TC_EPI_WARPS * 2 * WG_BOX_BYTES)
+#define WG_BAR_OFF (WG_STG_OFF + TC_EPI_WARPS * WG_BOXES * WG_BOX_BYTES)
 #define WG_N_BARS (2 * WG_STAGES + 4 + 2 * TC_TILE_RING + 1)
 #define WG_SMEM_BYTES (WG_BAR_OFF + 8 * WG_N_BARS + 4 * TC_TILE_RING + 32 + 1024)
 #define WG_THREADS (32 * (2 + TC_EPI_WARPS))  // producer, MMA, epilogue warps
@@ -422,7 +427,7 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
   } else {
     // ---------- epilogue: TMEM lane = output row, column = output column ----------
     const int q = warp & 3, hv = (warp - 2) >> 2;  // lanes 32 q .., columns 128 hv ..
-    const uint32_t stg = smem_u32(smem + WG_STG_OFF) + (uint32_t)((warp - 2) * 2 * WG_BOX_BYTES);
+    const uint32_t stg = smem_u32(smem + WG_STG_OFF) + (uint32_t)((warp - 2) * WG_BOXES * WG_BOX_BYTES);
     int tl = 0, nbox = 0;
     for (int i = 0;; ++i) {
       const int b = next_tile(i);
@@ -448,8 +453,8 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
         if (!row_ok || t.n0 + c >= N) continue;  // N a multiple of 32; warp-uniform
-        const uint32_t box = stg + (uint32_t)((nbox & 1) * WG_BOX_BYTES);
-        if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
+        const uint32_t box = stg + (uint32_t)((nbox % WG_BOXES) * WG_BOX_BYTES);
+        if (lane == 0) bulk_wait_read<WG_BOXES - 1>();  // the box's previous store has read it
         __syncwarp();
         // row `lane` of the box, 16-byte chunk j at chunk j ^ (lane & 7)
 #pragma unroll
