@@ -69,7 +69,8 @@ struct Tc2Cfg {
   static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * OUTB * TC_BOX_BYTES;
   // a_full, a_empty [SA]; b_full, b_empty [SB]; acc_full, acc_empty [2];
   // drain; tile_full, tile_empty [RING]
-  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING;
+  // (+ one per epilogue warp: its staged input box, the SwiGLU gradient's dH)
+  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + TC_EPI_WARPS;
   static constexpr int MISC_BYTES = 4 * TC_TILE_RING + 4 * 5;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * N_BARS + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -144,7 +145,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   constexpr bool DOWN = tc2_down(OP);
   constexpr bool MNA = tc2_mn_a(OP);
   using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB>;
-  static_assert(OUTB >= 0 && OUTB <= 2, "staged boxes per epilogue warp");
+  static_assert(OUTB >= 0 && OUTB <= 3, "staged boxes per epilogue warp");
+  static_assert(OP != TC2_BWD_DAB || OUTB == 0 || OUTB == 3, "dH in, dA and dB out");
   // second GEMM with both 256-row blocks in one TMEM buffer: staggered blocks
   constexpr bool STAG = DOWN && NACC == 2 && NBUF == 1;
   static_assert(!DOWN || STAG || NACC == 1, "second GEMM: two staggered blocks or one block");
@@ -174,6 +176,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const uint32_t drain_bar = bar(2 * SA + 2 * SB + 4);
   auto tile_full = [&](int s) { return bar(2 * SA + 2 * SB + 5 + s); };
   auto tile_empty = [&](int s) { return bar(2 * SA + 2 * SB + 5 + TC_TILE_RING + s); };
+  auto aux_full = [&](int w) { return bar(2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + w); };
   uint8_t* misc = bar_base + 8 * C::N_BARS;
   volatile int* tile_id = reinterpret_cast<volatile int*>(misc);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc + 4 * TC_TILE_RING);
@@ -198,6 +201,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       mbar_init(tile_full(s), 1);
       mbar_init(tile_empty(s), 2 * TC2_CONSUMERS);  // consumers of both CTAs
     }
+    for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(aux_full(w), 1);
     *abort_flag = 0;
     progress[0] = progress[1] = progress[2] = 0;
     fence_barrier_init();
@@ -440,7 +444,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
-    int tl = 0, nbox = 0;
+    int tl = 0, nbox = 0, naux = 0;
     for (int i = 0;; ++i) {
       const int b = next_tile(i, false);
       __syncwarp();
@@ -461,6 +465,35 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const int of = (ph ? t.out_f1 : t.out_f0) + 32 * q;  // first output column of the warp
         for (int c = 32 * half; c < t.npad; c += 64) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+          if (OP == TC2_BWD_DAB && OUTB == 3 && c + 32 <= t.ntok) {
+            // SwiGLU gradient of 32 whole tokens: dH box in by TMA, dA and dB
+            // boxes out by TMA (one buffer of each)
+            const uint32_t dhb = stg, dab_a = stg + TC_BOX_BYTES, dab_b = stg + 2 * TC_BOX_BYTES;
+            const uint32_t ab = aux_full(warp - 2);
+            if (lane == 0) {
+              bulk_wait_read<0>();       // the last stores have read the dA, dB boxes
+              fence_proxy_async_smem();  // after this warp's reads of the last dH box
+              mbar_arrive_expect_tx(ab, TC_BOX_BYTES);
+              tma_load_2d(dhb, &maps.aux, ab, of, t.out_row0 + c, l2_policy_evict_first());
+            }
+            const bool got = mbar_wait(ab, naux & 1);
+            ++naux;
+            if (!__all_sync(0xffffffffu, got)) {
+              if (lane == 0) *abort_flag = 1;
+              break;
+            }
+            stage_swiglu_grad(ta + c, tb + c, dhb, dab_a, dab_b, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (valid) {
+                tma_store_2d(&maps.out, dab_a, of, t.pout_row0 + c);
+                tma_store_2d(&maps.out, dab_b, n_out + of, t.pout_row0 + c);
+              }
+              bulk_commit();
+            }
+            continue;
+          }
           if (OUTB > 0 && OP != TC2_BWD_DAB && c + 32 <= t.ntok && !(F32SH && t.shared)) {
             // 32 whole tokens of bf16 output: stage the box in shared
             // memory and store it with TMA (boxes used round robin)

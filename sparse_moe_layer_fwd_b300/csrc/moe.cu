@@ -408,15 +408,15 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   return ok;
 }
 
-// The CTA-pair kernel of each operation: ring depths and staged output
-// boxes.  The backward's two-block products (dH, dX) take the second GEMM's
-// configuration; the SwiGLU gradient stores from registers, so its shared
-// memory goes to the rings.
+// The CTA-pair kernel of each operation: ring depths and staged boxes.  The
+// backward's two-block products (dH, dX) take the second GEMM's
+// configuration; the SwiGLU gradient stages three boxes per epilogue warp
+// (dH in, dA and dB out).
 template <int OP> struct PairCfg {
   static constexpr bool UP = OP == TC2_FWD_UP;
-  static constexpr int SA = OP == TC2_BWD_DAB ? 5 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
-  static constexpr int SB = OP == TC2_BWD_DAB ? 4 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
-  static constexpr int OUTB = OP == TC2_BWD_DAB ? 0 : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
+  static constexpr int SA = OP == TC2_BWD_DAB ? 4 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
+  static constexpr int SB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
+  static constexpr int OUTB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
   static constexpr int NACC = 2, NBUF = 1;
 };
 
@@ -718,6 +718,9 @@ bool make_bwd_maps(const Plan& p, const void* x, const moe_expert_w* ex, const m
   m->dx.bs8 = m->dx.b8;
   ok &= make_out_map(&m->dx.out, ws + p.o_dxp, p.TK, p.d);
   // weight gradients: both operands MN-major, 64-column x 64-row boxes
+  // the SwiGLU gradient reads dH boxes and writes dA|dB boxes
+  ok &= make_out_map(&m->fwd.up.out, ws + p.o_dab, p.rows_dab, 2LL * p.h);
+  ok &= make_out_map(&m->fwd.up.aux, ws + p.o_dh, rows_h, p.h);
   ok &= make_map(&m->wd.p, ws + p.o_dyp, p.rows_dyp, p.d, 64);
   ok &= make_map(&m->wd.ps, dy, p.T, p.d, 64);
   ok &= make_map(&m->wd.q, ws + p.o_h, rows_h, p.h, 64);

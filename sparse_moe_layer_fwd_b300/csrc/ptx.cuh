@@ -263,6 +263,17 @@ MOE_DEV void stmatrix_x4_trans(uint32_t addr, uint32_t w0, uint32_t w1, uint32_t
                :: "r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
 }
 
+// The inverse: four 8 x 8 b16 matrices from shared memory into fragment
+// registers, transposed (the row whose address thread 8 m + i gives is read
+// as column i of matrix m).
+MOE_DEV void ldmatrix_x4_trans(uint32_t addr, uint32_t& w0, uint32_t& w1, uint32_t& w2,
+                               uint32_t& w3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+               : "r"(addr)
+               : "memory");
+}
+
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA) once the writing threads execute this fence.
 MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
