@@ -60,6 +60,15 @@ as a source, uses the same):
                affinities, through the sigmoid to W_r and x; the bias has no
                gradient (it moves by the sign rule).
 
+10. fp8 gate/up (the official V3 trains its experts in FP8, which the
+               re-creation leaves out: "190行JAX复刻DeepSeek V3", introduction;
+               a B300-native option here, not on the pages): each row of
+               W_gate, W_up and of the token matrix is quantized to e4m3 with
+               one fp32 scale, scale = amax|row| / 448 (1 for a zero row),
+               code = e4m3(row / scale) rounded to nearest even; the layer is
+               then the same layer on the dequantized values code * scale
+               (routing on the unquantized tokens).
+
 ``moe_forward_dense`` is the pages' own formulation (every expert on every
 token, then masked).  ``moe_forward_sparse`` evaluates only the selected
 experts; tests pin it to the dense formulation on small inputs, and it is the
@@ -381,4 +390,21 @@ def backward_token_rows(x_rows, w_router, bias, get_expert, shared, k: int, dy_r
     for j in range(idx.shape[1]):
         dx += du_sel[:, j:j + 1] * wr[idx[:, j]]
     return dx
+
+
+# --------------------------------------------------------------------------
+# 10. fp8 (e4m3) per-row quantization
+# --------------------------------------------------------------------------
+def quantize_rows_e4m3(a):
+    """Per-row e4m3 quantization (reading 10): returns (codes uint8 [..., n],
+    scales fp32 [...], dequantized float64 [..., n]).  The rounding is
+    PyTorch's float8_e4m3fn conversion (nearest, ties to even); the scale
+    and the division are fp32 operations."""
+    import torch
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32))
+    amax = t.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (t / scale).to(torch.float8_e4m3fn)
+    deq = q.to(torch.float64) * scale.to(torch.float64)
+    return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), deq.numpy()
 

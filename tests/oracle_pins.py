@@ -512,6 +512,46 @@ def pin_backward_rows_agree(O):
     assert np.allclose(got, full["dx"][rows], rtol=1e-12, atol=1e-12)
 
 
+def _e4m3_values():
+    """Every finite e4m3 value, from the format's definition (1 sign, 4
+    exponent bits with bias 7, 3 mantissa bits; exponent field 0 is
+    subnormal; code 0x7f / 0xff is NaN)."""
+    vals = []
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        sgn = -1.0 if c >> 7 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        mag = math.ldexp(1 + m / 8, e - 7) if e else math.ldexp(m / 8, -6)
+        vals.append((c, sgn * mag))
+    return vals
+
+
+def pin_quantize_e4m3(O):
+    """Per-row e4m3 quantization: a row already on the e4m3 grid with
+    maximum 448 is kept exactly with scale 1 and the format's own codes;
+    scaling a row by a power of two scales only its scale; the largest
+    magnitude maps to +-448; a zero row gets scale 1 and zero codes; the
+    error of every normal value is at most 2^-4 of it."""
+    grid = _e4m3_values()
+    codes = np.array([c for c, _ in grid], dtype=np.uint8)
+    vals = np.array([v for _, v in grid])
+    q, sc, deq = O.quantize_rows_e4m3(vals[None, :])
+    assert sc[0] == 1.0 and np.array_equal(q[0], codes) and np.array_equal(deq[0], vals)
+    rng = np.random.default_rng(41)
+    row = rng.normal(size=(3, 200)).astype(np.float32)
+    q1, s1, _ = O.quantize_rows_e4m3(row)
+    q2, s2, _ = O.quantize_rows_e4m3(row * np.float32(2.0 ** 7))
+    assert np.array_equal(q1, q2) and np.array_equal(s2, s1 * np.float32(2.0 ** 7))
+    top = np.abs(row).argmax(axis=1)
+    assert set(q1[np.arange(3), top].tolist()) <= {0x7E, 0xFE}
+    qz, sz, dz = O.quantize_rows_e4m3(np.zeros((1, 64), dtype=np.float32))
+    assert sz[0] == 1.0 and not qz.any() and not dz.any()
+    _, s3, d3 = O.quantize_rows_e4m3(row)
+    normal = np.abs(row) >= (2.0 ** -6) * s3[:, None]
+    assert np.all(np.abs(d3 - row)[normal] <= 2.0 ** -4 * np.abs(row)[normal])
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -531,4 +571,5 @@ PINS = [
     pin_backward_finite_differences,
     pin_backward_special_cases,
     pin_backward_rows_agree,
+    pin_quantize_e4m3,
 ]

@@ -238,6 +238,34 @@ def _bwd_router_no_sigmoid_grad(x, w_router, bias, experts, shared, k, dy, idx_o
     return out
 
 
+def _quant_wrong_max(a):
+    import torch
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32))
+    amax = t.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / 240.0, torch.ones_like(amax))  # 240: not e4m3's max
+    q = (t / scale).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), (q.double() * scale.double()).numpy()
+
+
+def _quant_per_column(a):
+    q, s, d = _ORIG["quantize_rows_e4m3"](np.asarray(a, dtype=np.float32).T)
+    return q.T, s, d.T
+
+
+def _quant_truncate(a):
+    import torch
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32))
+    amax = t.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    r = (t / scale).double()
+    # round toward zero to 3 mantissa bits instead of to nearest
+    e = torch.floor(torch.log2(r.abs().clamp_min(2.0 ** -9))).clamp_min(-6)
+    step = torch.pow(2.0, e - 3)
+    tr = (torch.trunc(r / step) * step).float()
+    q = tr.to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), (q.double() * scale.double()).numpy()
+
+
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
 
 MUTATIONS = [
@@ -275,6 +303,9 @@ MUTATIONS = [
     ("moe_backward_dense", _bwd_no_shared_dx),
     ("moe_backward_dense", _bwd_gate_no_quotient),
     ("moe_backward_dense", _bwd_router_no_sigmoid_grad),
+    ("quantize_rows_e4m3", _quant_wrong_max),
+    ("quantize_rows_e4m3", _quant_per_column),
+    ("quantize_rows_e4m3", _quant_truncate),
 ]
 
 
