@@ -53,11 +53,12 @@ def tc_router(wl):
     return wl.dtype == "bf16" and wl.E >= 96 and wl.T > 0
 
 
-def kernels_per_step(wl, route_only):
+def kernels_per_step(wl, route_only, fp8=False):
     """Kernels one forward launches: router (weight split + MMA, or FFMA
-    logits), top-k, block ranks, scan [, permute, GEMM 1, GEMM 2, combine]."""
+    logits), top-k, block ranks, scan [, token quantization (fp8), permute,
+    GEMM 1, GEMM 2, combine]."""
     n = (2 if tc_router(wl) else 1) + 3
-    return n if route_only else n + 4
+    return n if route_only else n + 4 + int(fp8)
 
 # DRAM traffic of expert GEMM 1 per launch from ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum, one capture of the full-size workload; both are
@@ -189,14 +190,18 @@ def _working_set_bytes(wl, route_only):
     return b
 
 
-def _algorithmic(wl, load):
-    """FLOPs and bytes of the two expert GEMMs for one launch each."""
+def _algorithmic(wl, load, fp8=False):
+    """FLOPs and bytes of the two expert GEMMs for one launch each (fp8: the
+    first GEMM reads one-byte codes of weights and tokens, plus row scales)."""
     TK, T, d, h = wl.T * wl.k, wl.T, wl.d, wl.h
     rows = TK + T
     fl1 = 4.0 * rows * d * h
     fl2 = 2.0 * rows * d * h
     touched = int((load > 0).sum()) + 1  # + shared expert
-    by1 = touched * 2 * h * d * 2 + rows * d * 2 + rows * h * 2
+    if fp8:
+        by1 = touched * 2 * h * (d + 4) + rows * (d + 4) + rows * h * 2
+    else:
+        by1 = touched * 2 * h * d * 2 + rows * d * 2 + rows * h * 2
     by2 = touched * d * h * 2 + rows * h * 2 + TK * d * 2 + T * d * 4
     return fl1, fl2, by1, by2, touched - 1
 
@@ -261,7 +266,9 @@ def run_ours(args, wl):
     wl_rank = wl.with_(seed=wl.seed + 1000 * rank) if ws > 1 else wl
     route_only = args.route_only or wl.route_only
     inp = I.make_inputs(wl_rank, device="cuda", experts=not route_only)
-    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else 0)
+    fp8 = bool(args.fp8) and not route_only
+    base_flags = M.MOE_FP8_GATE_UP if fp8 else 0
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else base_flags)
     stream = torch.cuda.current_stream()
     x = inp["x"]
 
@@ -333,7 +340,7 @@ def run_ours(args, wl):
     e2e = None
     if not args.no_e2e:
         nlay = 1 if flush is not None else 2
-        flags_e = M.MOE_ROUTE_ONLY if route_only else 0
+        flags_e = M.MOE_ROUTE_ONLY if route_only else base_flags
         hls = [MoeLayer.from_inputs(inp, wl.k, wl.dtype, flags_e, host_io=True)
                for _ in range(nlay)]
         streams = [stream] + [torch.cuda.Stream() for _ in range(nlay - 1)]
@@ -418,13 +425,27 @@ def run_ours(args, wl):
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    fl1, fl2, by1, by2, touched = _algorithmic(wl, load)
+    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8)
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
     cap = NCU_TRAFFIC.get(wl.name)
-    traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
-    if prefill_like:
+    traffic = cap["bytes"] if cap and cap.get("sha") == sha and not fp8 else None
+    if prefill_like and fp8:
+        # e4m3 codes on kind::f8f6f4: the fp8 dense peak is twice the bf16
+        # one (2.25 vs 4.5 PFLOP/s nominal), applied to the measured figure
+        ach = fl1 / g1_s / 1e12
+        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        roof = {"bound": "tensor",
+                "kernel": "k_expert_tc2 (GEMM 1 on e4m3 codes: gate/up + SwiGLU, CTA pairs)",
+                "achieved": ach, "peak": 2 * sus, "unit": "TFLOP/s",
+                "frac": ach / (2 * sus), "traffic": traffic,
+                "peak_kind": f"2 x {peaks['source']} bf16 sustained (nominal fp8/bf16 ratio)",
+                "frac_of_burst": ach / (2 * peaks["bf16_tflops"]),
+                "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
+        both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
+        layer_roof = {"expert_gemms_tflops": both}
+    elif prefill_like:
         # GEMM 1 is timed inside the back-to-back step loop, under the power
         # cap: its denominator is the sustained bf16 figure (burst beside it)
         ach = fl1 / g1_s / 1e12
@@ -443,7 +464,9 @@ def run_ours(args, wl):
                                             if peaks.get("bf16_tflops_sustained") else None)}
     else:
         ach = by1 / g1_s / 1e9
-        roof = {"bound": "hbm", "kernel": "k_expert_tc (GEMM 1: gate/up + SwiGLU, one SM)",
+        roof = {"bound": "hbm",
+                "kernel": ("k_expert_tc2 (GEMM 1 on e4m3 codes, CTA pairs)" if fp8 else
+                           "k_expert_tc (GEMM 1: gate/up + SwiGLU, one SM)"),
                 "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_kind": f"{peaks['source']} copy bandwidth",
@@ -465,14 +488,15 @@ def run_ours(args, wl):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 gate/up (per-row scales), bf16 down" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
                    "shared_experts": 1, "parallelism": f"replicas x{ws}",
-                   "l2": l2_note},
+                   "l2": l2_note, **({"fp8_gate_up": True} if fp8 else {})},
         "roofline": roof, "roofline_layer": layer_roof,
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": kernels_per_step(wl, False) * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": kernels_per_step(wl, False, fp8) * args.steps,
         "clocks": clocks, "kernel_sha": sha,
     }
     print(json.dumps(line), flush=True)
@@ -622,6 +646,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time a training step: forward and backward")
+    ap.add_argument("--fp8", action="store_true",
+                    help="gate/up products on per-row e4m3 codes (MOE_FP8_GATE_UP)")
     ap.add_argument("--route-only", action="store_true",
                     help="time the routing pass only (router, top-k, load counts)")
     args = ap.parse_args()

@@ -86,6 +86,12 @@ enum {
 #define MOE_TRAINING     4u  /* bf16 tensor-core path only: the workspace also holds
                                 the backward's buffers, so that moe_backward can
                                 follow moe_forward on it */
+#define MOE_FP8_GATE_UP  8u  /* bf16 tensor-core path only, not with MOE_TRAINING:
+                                the gate/up products run on e4m3 codes with one
+                                fp32 scale per row (moe_quantize_rows_e4m3).
+                                w_gate and w_up of experts and shared then point at
+                                packed quantized matrices; w_down stays bf16; the
+                                tokens are quantized per row inside the call */
 
 /* Problem description.
  *   T  tokens (>= 0)            d  model width          h  expert hidden width
@@ -96,7 +102,8 @@ enum {
 typedef struct {
   int T, d, h, E, k;
   int dtype;        /* moe_dtype */
-  unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING */
+  unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING |
+                       MOE_FP8_GATE_UP */
 } moe_desc;
 
 /* Expert weights, element type desc->dtype.
@@ -106,6 +113,32 @@ typedef struct {
 typedef struct {
   const void *w_gate, *w_up, *w_down;
 } moe_expert_w;
+
+/* FP8 gate/up weights.  The official V3 model computes its expert products
+ * in FP8 ("DeepSeek V3 viết lại bằng 190 dòng JAX thuần", section "Những gì
+ * có trong 190 dòng code"); the re-creation leaves that out, and so does the
+ * default path here.  With MOE_FP8_GATE_UP the first expert GEMM multiplies
+ * e4m3 codes (tcgen05 kind::f8f6f4, fp32 accumulation) and applies the two
+ * rows' scales to each product before SwiGLU.  Scaling unit: one row, with
+ *   scale = amax(|row|) / 448 (1 for an all-zero row or a row with a NaN),
+ *   code  = e4m3(row / scale), nearest-even, saturating at +-448,
+ * both fp32 operations.
+ *
+ * Packed layout of a quantized [rows, cols] matrix, one device buffer of
+ * moe_e4m3_packed_bytes(rows, cols) bytes:
+ *   codes  [rows, cols] uint8 (e4m3 bit patterns) at byte 0,
+ *   scales [rows]       fp32 at byte ceil(rows*cols / 256) * 256.
+ * The routed gate (or up) weights are one matrix of E*h rows; the shared
+ * expert's one of h rows. */
+MOE_API size_t moe_e4m3_packed_bytes(long long rows, int cols);
+
+/* Quantize a bf16 matrix a [rows, cols] (device, row-major, 16-byte aligned)
+ * into `packed` (device, moe_e4m3_packed_bytes(rows, cols) bytes, 16-byte
+ * aligned), enqueued on `stream`.  cols: a positive multiple of 8; rows >= 0.
+ * MOE_ERR_NULL / MOE_ERR_SHAPE / MOE_ERR_ALIGN / MOE_ERR_DEVICE /
+ * MOE_ERR_LAUNCH as for moe_forward.  The buffers must not overlap. */
+MOE_API int moe_quantize_rows_e4m3(const void* a, long long rows, int cols, void* packed,
+                                   void* stream);
 
 /* Bytes of device workspace that moe_forward needs for `desc` (flags
  * included).  Returns 0 for an invalid desc.  The value depends only on the
@@ -242,7 +275,8 @@ MOE_API const char* moe_error_string(int code);
  * tensor-core router; empty otherwise), "blk_hist", "pair_rank", "groups"
  * (int32 group table),
  * "perm" (permuted row -> token*k+slot), "inv" (token*k+slot -> permuted row),
- * "x_perm", "h", "y_perm", "y_shared". */
+ * "x_perm", "h", "y_perm", "y_shared", "x_q" (MOE_FP8_GATE_UP: the tokens
+ * quantized, packed as above; empty otherwise). */
 typedef struct {
   char name[16];
   size_t offset, bytes;

@@ -64,7 +64,8 @@ as a source, uses the same):
                re-creation leaves out: "190行JAX复刻DeepSeek V3", introduction;
                a B300-native option here, not on the pages): each row of
                W_gate, W_up and of the token matrix is quantized to e4m3 with
-               one fp32 scale, scale = amax|row| / 448 (1 for a zero row),
+               one fp32 scale, scale = amax|row| / 448 (1 for a zero row or
+               a row holding a NaN),
                code = e4m3(row / scale) rounded to nearest even; the layer is
                then the same layer on the dequantized values code * scale
                (routing on the unquantized tokens).
@@ -407,4 +408,19 @@ def quantize_rows_e4m3(a):
     q = (t / scale).to(torch.float8_e4m3fn)
     deq = q.to(torch.float64) * scale.to(torch.float64)
     return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), deq.numpy()
+
+
+def fp8_gate_up_rows(x_rows, idx_rows, gate_rows, get_expert, shared):
+    """Layer output for sampled rows with the gate/up products in e4m3
+    (reading 10): the tokens and every row of W_gate and W_up replaced by
+    their per-row dequantized values; W_down, the selection and the gates as
+    in the unquantized layer (routing is done beforehand on the unquantized
+    tokens and passed in).  Same arguments as expert_output_rows."""
+    xq = quantize_rows_e4m3(x_rows)[2]
+
+    def quantized(w):
+        return quantize_rows_e4m3(w[0])[2], quantize_rows_e4m3(w[1])[2], _f64(w[2])
+
+    return expert_output_rows(xq, idx_rows, gate_rows, lambda e: quantized(get_expert(e)),
+                              quantized(shared))
 

@@ -203,6 +203,41 @@ MOE_DEV void stage_box_bf16(uint32_t ta, uint32_t tb, uint32_t box, int lane) {
   }
 }
 
+// stage_box_bf16 for the fp8 gate/up products: the accumulators hold code
+// products, so gate and up are first multiplied by their rows' weight
+// scales and the tokens' scales.  rsg / rsu: scales of the rows
+// (lane >> 2) + 8 r, r = 0..3 of the warp's 32; tsc[2 i + e]: scale of token
+// column 8 i + 2 (lane & 3) + e.
+MOE_DEV void stage_box_swiglu_scaled(uint32_t ta, uint32_t tb, uint32_t box, int lane,
+                                     const float (&rsg)[4], const float (&rsu)[4],
+                                     const float (&tsc)[8]) {
+  const int mm = lane >> 3, ii = lane & 7;
+#pragma unroll
+  for (int L = 0; L < 32; L += 16) {
+    uint32_t ra[16], rb[16];
+    tmem_load_16x256b_2(ta + ((uint32_t)L << 16), tb + ((uint32_t)L << 16), ra, rb);
+    uint32_t w[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {  // m = 2 i + hf: rows L + 8 hf + lane/4, columns 8 i ..
+      const int r = (L >> 3) + (m & 1), i = m >> 1;
+      float o[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float g = __uint_as_float(ra[2 * m + e]) * (rsg[r] * tsc[2 * i + e]);
+        const float u = __uint_as_float(rb[2 * m + e]) * (rsu[r] * tsc[2 * i + e]);
+        o[e] = silu_fast(g) * u;
+      }
+      w[m] = pack_bf16x2(o[0], o[1]);
+    }
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip) {
+      const int tok = 8 * (2 * ip + (mm >> 1)) + ii, chunk = (L >> 3) + (mm & 1);
+      stmatrix_x4_trans(box + (uint32_t)(tok * 64 + 16 * (chunk ^ ((tok >> 1) & 3))), w[4 * ip],
+                        w[4 * ip + 1], w[4 * ip + 2], w[4 * ip + 3]);
+    }
+  }
+}
+
 // SwiGLU gradient of 32 tokens x this warp's 32 hidden units, through shared
 // memory: `dh_box` holds dH (box row = token, as stage_box_bf16 writes
 // them); gate (ta) and up (tb) accumulators are read in the 16x256b shape,
@@ -290,6 +325,14 @@ MOE_DEV TcTile tc_tile(const GroupTable& G, const int32_t* toff, int E, int b, i
   t.out_row0 = G.off[g] + t.tok0;  // H row (first GEMM) / Y_perm row (routed, second)
   return t;
 }
+
+// Scales of the fp8 gate/up products: per weight row (routed [E*h], shared
+// [h]) and per token ([T]; a routed row's token is perm[row] / k).
+struct Fp8Scales {
+  const float *g, *u, *sg, *su, *tok;
+  const int32_t* perm;
+  int k;
+};
 
 struct TcMapsDev {
   CUtensorMap a0, a1, sa0, sa1;   // weights, 128-row boxes (routed, shared)

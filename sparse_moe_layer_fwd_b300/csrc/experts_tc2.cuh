@@ -44,6 +44,8 @@ enum : int {
   TC2_BWD_DH = 2,    // dH = dY W_down (W_down read transposed)                 K = d
   TC2_BWD_DAB = 3,   // gate/up recomputed: dA = dH up silu'(gate), dB = dH silu(gate)
   TC2_BWD_DX = 4,    // dX = dA W_gate + dB W_up (weights read transposed)      K = 2h
+  TC2_FWD_UP_FP8 = 5,  // H as TC2_FWD_UP from e4m3 codes of weights and tokens
+                       // with per-row scales (kind::f8f6f4)          K = d (bytes)
 };
 // two blocks of 256 rows of one matrix per tile (else gate and up rows)
 __host__ __device__ constexpr bool tc2_down(int op) { return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX; }
@@ -127,7 +129,8 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   // down projection, the padded dY rows / dy (shared) for dH, the padded
   // dA|dB rows for dX
   int rb;
-  if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB) rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
+  if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_FWD_UP_FP8)
+    rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
   else if (OP == TC2_FWD_DOWN) rb = G.off[g] + t.tok0;
   else if (OP == TC2_BWD_DH) rb = t.shared ? t.tok0 : G.poff[g] + t.tok0;
   else rb = G.poff[g] + t.tok0;
@@ -141,9 +144,11 @@ template <int SA, int SB, int NACC, int NBUF, int OUTB, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC2_THREADS, 1)
 k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
              int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
-             const __nv_bfloat16* __restrict__ aux) {
+             const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs) {
   constexpr bool DOWN = tc2_down(OP);
   constexpr bool MNA = tc2_mn_a(OP);
+  constexpr bool FP8 = OP == TC2_FWD_UP_FP8;
+  constexpr int KB_ELEMS = FP8 ? 128 : TC_BK;  // elements per 128-byte K step
   using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB>;
   static_assert(OUTB >= 0 && OUTB <= 3, "staged boxes per epilogue warp");
   static_assert(OP != TC2_BWD_DAB || OUTB == 0 || OUTB == 3, "dH in, dA and dB out");
@@ -158,9 +163,9 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const bool leader = rank == 0;
 
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
-  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB) ? G.toff_a
+  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8) ? G.toff_a
                         : (OP == TC2_BWD_DH ? G.toff_c : G.toff_b);
-  int* counter = G.next + OP;
+  int* counter = G.next + (FP8 ? 0 : OP);
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
@@ -293,9 +298,9 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
                                y, pol_w);
             }
           } else {
-            if (t.v0) tma_load_2d_pair(smem_u32(st), mA0, fb, kb * TC_BK, t.row_a0, pol_w);
+            if (t.v0) tma_load_2d_pair(smem_u32(st), mA0, fb, kb * KB_ELEMS, t.row_a0, pol_w);
             if (t.v1)
-              tma_load_2d_pair(smem_u32(st + C::A_BYTES), mA1, fb, kb * TC_BK, t.row_a1, pol_w);
+              tma_load_2d_pair(smem_u32(st + C::A_BYTES), mA1, fb, kb * KB_ELEMS, t.row_a1, pol_w);
           }
           progress[0] = it + 1;
         }
@@ -310,7 +315,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const int b = next_tile(i, true);
         if (b < 0) break;
         const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
-        const bool bs = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH) && t.shared;
+        const bool bs = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH || FP8) && t.shared;
         const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
         const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
         const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
@@ -323,7 +328,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           }
           uint8_t* st = smem + C::B_OFF + sb * C::B_STAGE;
           const uint32_t fb = lead(b_full(sb));
-          const int kx = kb * TC_BK;
+          const int kx = kb * KB_ELEMS;
           if (leader) mbar_arrive_expect_tx(b_full(sb), (uint32_t)t.npad * (TC_BK * 2));
           int j = 0;
           for (; j + 128 <= t.half; j += 128)
@@ -348,7 +353,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           if (b < 0) break;
           if (*abort_flag) continue;  // keep reading the tile ring until the scheduler says "none"
           const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, 0);
-          const uint32_t idesc = umma_idesc_bf16(2 * TC_BM, t.npad) | (MNA ? (1u << 15) : 0u);
+          const uint32_t idesc = FP8 ? umma_idesc_e4m3(2 * TC_BM, t.npad)
+                                     : umma_idesc_bf16(2 * TC_BM, t.npad) | (MNA ? (1u << 15) : 0u);
           const int u = tl % NBUF;  // TMEM buffer of this tile
           // k step kb of this tile uses ring stage it + kb
           auto stage_ready = [&](int kb) -> bool {
@@ -366,11 +372,16 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             const uint32_t bb = smem_u32(smem + C::B_OFF + (st % SB) * C::B_STAGE);
             const uint32_t d = tmem + (w ? 256u : (uint32_t)(u * 256));
 #pragma unroll
-            for (int kk = 0; kk < TC_BK / 16; ++kk)
-              umma_bf16_pair(d,
-                             MNA ? umma_desc_sw128_mn(a + kk * 2048, C::A_BYTES / 2)
-                                 : umma_desc_sw128(a + kk * 32),
-                             umma_desc_sw128(bb + kk * 32), idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {  // four 32-byte K slices
+              if (FP8)
+                umma_f8_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32), idesc,
+                             (kb | kk) != 0);
+              else
+                umma_bf16_pair(d,
+                               MNA ? umma_desc_sw128_mn(a + kk * 2048, C::A_BYTES / 2)
+                                   : umma_desc_sw128(a + kk * 32),
+                               umma_desc_sw128(bb + kk * 32), idesc, (kb | kk) != 0);
+            }
             mma_issued = true;
           };
           auto release = [&](int kb) {  // the stage is free once its MMAs complete
@@ -463,6 +474,20 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const uint32_t tb = lanes + 256;                                // GEMM 1: up projection
         const bool valid = ph ? t.v1 : t.v0;
         const int of = (ph ? t.out_f1 : t.out_f0) + 32 * q;  // first output column of the warp
+        // fp8: scales of this warp's weight rows (row of + lane for the
+        // register path; of + lane/4 + 8 r for the fragment layout)
+        float rsg[4] = {1.f, 1.f, 1.f, 1.f}, rsu[4] = {1.f, 1.f, 1.f, 1.f}, rlg = 1.f, rlu = 1.f;
+        if (FP8 && valid) {
+          const float* sgp = t.shared ? fs.sg : fs.g + (size_t)t.g * n_out;
+          const float* sup = t.shared ? fs.su : fs.u + (size_t)t.g * n_out;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            rsg[r] = sgp[of + (lane >> 2) + 8 * r];
+            rsu[r] = sup[of + (lane >> 2) + 8 * r];
+          }
+          rlg = sgp[of + lane];
+          rlu = sup[of + lane];
+        }
         for (int c = 32 * half; c < t.npad; c += 64) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
           if (OP == TC2_BWD_DAB && OUTB == 3 && c + 32 <= t.ntok) {
@@ -494,13 +519,27 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             }
             continue;
           }
+          // fp8: scale of token column c + lane
+          float tsl = 0.f;
+          if (FP8 && c + lane < t.ntok)
+            tsl = fs.tok[t.shared ? t.tok0 + c + lane : fs.perm[t.out_row0 + c + lane] / fs.k];
           if (OUTB > 0 && OP != TC2_BWD_DAB && c + 32 <= t.ntok && !(F32SH && t.shared)) {
             // 32 whole tokens of bf16 output: stage the box in shared
             // memory and store it with TMA (boxes used round robin)
             const uint32_t box = stg + (uint32_t)((nbox % (OUTB > 0 ? OUTB : 1)) * TC_BOX_BYTES);
             if (lane == 0) bulk_wait_read<(OUTB > 0 ? OUTB - 1 : 0)>();  // the box's last store read it
             __syncwarp();
-            stage_box_bf16<OP == TC2_FWD_UP>(ta + c, tb + c, box, lane);
+            if (FP8) {
+              float tsc[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  tsc[2 * i + e] = __shfl_sync(0xffffffffu, tsl, 8 * i + 2 * (lane & 3) + e);
+              stage_box_swiglu_scaled(ta + c, tb + c, box, lane, rsg, rsu, tsc);
+            } else {
+              stage_box_bf16<OP == TC2_FWD_UP>(ta + c, tb + c, box, lane);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -517,7 +556,14 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           else
             tmem_load_32(ta + c, va);
           if (!valid) continue;
-          if (OP == TC2_FWD_UP) {
+          if (FP8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float ts = __shfl_sync(0xffffffffu, tsl, j);
+              va[j] = silu_fast(va[j] * (rlg * ts)) * (vb[j] * (rlu * ts));
+            }
+            store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
+          } else if (OP == TC2_FWD_UP) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
             store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);

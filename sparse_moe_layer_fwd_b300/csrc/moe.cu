@@ -27,6 +27,7 @@
 #include "router.cuh"
 #include "router_tc.cuh"
 #include "backward.cuh"
+#include "quant.cuh"
 
 namespace {
 
@@ -81,6 +82,7 @@ struct Plan {
   int T, d, h, E, k, TK;
   bool f32, route_only, simt, big_router, big_tiles, tc_router;
   bool training;  // the backward's buffers follow the forward's
+  bool fp8;       // gate/up products on e4m3 codes (packed weights, tokens quantized here)
   int el;  // bytes per activation / weight element
   // router: CUDA-core tiles (r_bm x r_bn) or tensor-core pairs over E_pad
   // experts (rt_eb blocks of 256) x rt_tt token tiles x n_split K slices
@@ -91,17 +93,22 @@ struct Plan {
   int bn, ft_a, ft_b, ft_c, tile_round, max_tiles_a, max_tiles_b, max_tiles_c;
   // workspace regions (byte offsets)
   size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh,
-      total;
+      o_xq, total;
   // backward: padded dY rows, dG, du, dH, padded dA|dB rows, dX rows, shared dX
   size_t o_dyp, o_dg, o_du, o_dh, o_dab, o_dxp, o_dxs;
   long long rows_dyp, rows_dab;  // allocated padded rows
-  size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh;
+  size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh,
+      b_xq;
 };
 
 int validate_desc(const moe_desc* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
-  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING)) return MOE_ERR_DTYPE;
+  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_GATE_UP))
+    return MOE_ERR_DTYPE;
+  if ((d->flags & MOE_FP8_GATE_UP) &&
+      (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY | MOE_TRAINING))))
+    return MOE_ERR_DTYPE;
   if ((d->flags & MOE_TRAINING) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY))))
     return MOE_ERR_DTYPE;
@@ -127,6 +134,7 @@ Plan make_plan(const moe_desc* d) {
   p.route_only = d->flags & MOE_ROUTE_ONLY;
   p.simt = p.f32 || (d->flags & MOE_SIMT_EXPERTS);
   p.el = p.f32 ? 4 : 2;
+  p.fp8 = d->flags & MOE_FP8_GATE_UP;
 
   // router GEMM tiling and split of the model dimension
   p.big_router = p.E >= 96;
@@ -198,7 +206,8 @@ Plan make_plan(const moe_desc* d) {
       const double per_expert = p.E > 0 ? (double)p.TK / p.E : 0.0;
       // (training: always the CTA-pair tiles, whose tile table the
       // backward's products share)
-      p.big_tiles = per_expert >= 96.0 || (d->flags & MOE_TRAINING);
+      // (fp8: the CTA-pair kernel alone has the e4m3 product)
+      p.big_tiles = per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_GATE_UP));
       if (p.big_tiles) {
         p.bn = kPairBN;
         p.ft_a = MOE_PAIR_GEMM1 ? (p.h + 2 * TC_BM - 1) / (2 * TC_BM) : p.h / TC_BM;
@@ -232,10 +241,11 @@ Plan make_plan(const moe_desc* d) {
   if (!p.route_only) {
     region((size_t)p.TK * 4, p.o_perm, p.b_perm);
     region((size_t)p.TK * 4, p.o_inv, p.b_inv);
-    region((size_t)p.TK * p.d * p.el, p.o_xperm, p.b_xperm);
+    region((size_t)p.TK * p.d * (p.fp8 ? 1 : p.el), p.o_xperm, p.b_xperm);
     region((size_t)(p.TK + p.T) * p.h * p.el, p.o_h, p.b_h);
     region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
     region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
+    region(p.fp8 ? e4m3_scale_offset(p.T, p.d) + (size_t)p.T * 4 : 0, p.o_xq, p.b_xq);
   }
   p.training = d->flags & MOE_TRAINING;
   if (p.training) {
@@ -306,6 +316,21 @@ bool make_out_map_f32(CUtensorMap* m, const void* base, long long rows, long lon
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// e4m3 codes [rows, cols] (one byte each) read in boxes of 128 columns (128
+// bytes) x box_rows rows with the 128-byte swizzle; rows past the end read
+// as zero.
+bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
@@ -386,13 +411,29 @@ bool make_rows_maps(CUtensorMap* m128, CUtensorMap* m64, CUtensorMap* m16, CUten
 bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
                   uint8_t* ws, TcMaps* m) {
   bool ok = true;
-  ok &= make_map(&m->up.a0, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
-  ok &= make_map(&m->up.a1, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
-  ok &= make_map(&m->up.sa0, sh->w_gate, p.h, p.d, TC_BM);
-  ok &= make_map(&m->up.sa1, sh->w_up, p.h, p.d, TC_BM);
-  ok &= make_rows_maps(&m->up.b128, &m->up.b64, &m->up.b16, &m->up.b8, ws + p.o_xperm, p.TK,
-                       p.d);
-  ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8, x, p.T, p.d);
+  if (p.fp8) {
+    // e4m3 codes: packed weights (codes first), X_perm codes, x codes
+    const uint8_t* xq = ws + p.o_xq;
+    ok &= make_map_u8(&m->up.a0, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
+    ok &= make_map_u8(&m->up.a1, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
+    ok &= make_map_u8(&m->up.sa0, sh->w_gate, p.h, p.d, TC_BM);
+    ok &= make_map_u8(&m->up.sa1, sh->w_up, p.h, p.d, TC_BM);
+    for (int i = 0; i < 4; ++i) {
+      static const int rows[4] = {128, 64, 16, 8};
+      CUtensorMap* b[4] = {&m->up.b128, &m->up.b64, &m->up.b16, &m->up.b8};
+      CUtensorMap* bs[4] = {&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8};
+      ok &= make_map_u8(b[i], ws + p.o_xperm, p.TK, p.d, rows[i]);
+      ok &= make_map_u8(bs[i], xq, p.T, p.d, rows[i]);
+    }
+  } else {
+    ok &= make_map(&m->up.a0, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
+    ok &= make_map(&m->up.a1, ex->w_up, (long long)p.E * p.h, p.d, TC_BM);
+    ok &= make_map(&m->up.sa0, sh->w_gate, p.h, p.d, TC_BM);
+    ok &= make_map(&m->up.sa1, sh->w_up, p.h, p.d, TC_BM);
+    ok &= make_rows_maps(&m->up.b128, &m->up.b64, &m->up.b16, &m->up.b8, ws + p.o_xperm, p.TK,
+                         p.d);
+    ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8, x, p.T, p.d);
+  }
   ok &= make_map(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
   m->down.a1 = m->down.a0;
   ok &= make_map(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
@@ -413,7 +454,7 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
 // configuration; the SwiGLU gradient stages three boxes per epilogue warp
 // (dH in, dA and dB out).
 template <int OP> struct PairCfg {
-  static constexpr bool UP = OP == TC2_FWD_UP;
+  static constexpr bool UP = OP == TC2_FWD_UP || OP == TC2_FWD_UP_FP8;
   static constexpr int SA = OP == TC2_BWD_DAB ? 4 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
   static constexpr int SB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
   static constexpr int OUTB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
@@ -434,13 +475,13 @@ bool set_tc2_smem() {
 template <int OP>
 void launch_pair(const Plan& p, const TcMapsDev& m, int max_tiles, int32_t* groups, int K,
                  int n_out, __nv_bfloat16* out, float* ysh, const __nv_bfloat16* aux,
-                 cudaStream_t s) {
+                 cudaStream_t s, const Fp8Scales& fs = Fp8Scales{}) {
   const int pairs = sm_count() / 2;
   const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
   using P = PairCfg<OP>;
   k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, OP>
       <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES, s>>>(
-          m, groups, p.E, K, n_out, out, ysh, aux);
+          m, groups, p.E, K, n_out, out, ysh, aux, fs);
 }
 
 template <int BN, int SA, int SB, bool DOWN>
@@ -533,7 +574,8 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     if (!make_tc_maps(p, x, experts, shared, ws, &maps)) return MOE_ERR_DEVICE;
     const bool ok =
         p.big_tiles
-            ? ((MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
+            ? ((p.fp8 ? set_tc2_smem<TC2_FWD_UP_FP8>()
+                      : MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
                (MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, true>()))
@@ -571,9 +613,14 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
   if (need_out) {
     int32_t* perm = reinterpret_cast<int32_t*>(ws + p.o_perm);
     int32_t* inv = reinterpret_cast<int32_t*>(ws + p.o_inv);
+    uint8_t* xq = ws + p.o_xq;
+    float* xs = reinterpret_cast<float*>(xq + e4m3_scale_offset(p.T, p.d));
+    if (p.fp8)  // the tokens' codes and scales; the gather moves codes
+      k_quant_rows<__nv_bfloat16><<<(p.T + 7) / 8, 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(x), p.T, p.d, xq, xs);
     k_permute_gather<<<(p.TK + 7) / 8, 256, 0, s>>>(
-        topk_idx, rank, hist, p.TK, p.E, p.k, static_cast<const uint8_t*>(x), ws + p.o_xperm,
-        (size_t)p.d * p.el, perm, inv);
+        topk_idx, rank, hist, p.TK, p.E, p.k, p.fp8 ? xq : static_cast<const uint8_t*>(x),
+        ws + p.o_xperm, (size_t)p.d * (p.fp8 ? 1 : p.el), perm, inv);
     mark(2);
     cudaEvent_t between = events ? static_cast<cudaEvent_t>(events[3]) : nullptr;
     if (p.f32) {
@@ -584,8 +631,21 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
       __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
       __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
       float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
-      launch_gemm<false>(p, maps.up, p.big_tiles && MOE_PAIR_GEMM1, p.bn, p.max_tiles_a, groups,
-                         hbuf, nullptr, s);
+      if (p.fp8) {
+        const size_t so = e4m3_scale_offset((long long)p.E * p.h, p.d),
+                     ss = e4m3_scale_offset(p.h, p.d);
+        auto scl = [](const void* w, size_t o) {
+          return reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) + o);
+        };
+        const Fp8Scales fs{scl(experts->w_gate, so), scl(experts->w_up, so),
+                           scl(shared->w_gate, ss), scl(shared->w_up, ss), xs, perm, p.k};
+        // K in bf16 units of 128 bytes per step: d codes = d / 2 "elements"
+        launch_pair<TC2_FWD_UP_FP8>(p, maps.up, p.max_tiles_a, groups, p.d / 2, p.h, hbuf,
+                                    nullptr, nullptr, s, fs);
+      } else {
+        launch_gemm<false>(p, maps.up, p.big_tiles && MOE_PAIR_GEMM1, p.bn, p.max_tiles_a,
+                           groups, hbuf, nullptr, s);
+      }
       if (between) cudaEventRecord(between, s);
       launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b, groups,
                         yperm, ysh, s);
@@ -669,6 +729,27 @@ int moe_forward_host_io(const moe_desc* desc, const void* x_host, const float* w
   if (need_y && cudaMemcpyAsync(y_host, ydev, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MOE_ERR_DEVICE;
   return MOE_OK;
+}
+
+size_t moe_e4m3_packed_bytes(long long rows, int cols) {
+  if (rows < 0 || cols <= 0) return 0;
+  return e4m3_scale_offset(rows, cols) + (size_t)rows * 4;
+}
+
+int moe_quantize_rows_e4m3(const void* a, long long rows, int cols, void* packed, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 8 || rows > (1LL << 40) / cols) return MOE_ERR_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!a || !packed) return MOE_ERR_NULL;
+  if (!aligned16(a) || !aligned16(packed)) return MOE_ERR_ALIGN;
+  int rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  cudaGetLastError();
+  uint8_t* q = static_cast<uint8_t*>(packed);
+  k_quant_rows<__nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0,
+                                static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(a), rows, cols, q,
+      reinterpret_cast<float*>(q + e4m3_scale_offset(rows, cols)));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 int moe_bias_update(const int32_t* load_counts, float* bias, float gamma, int E, int TK,
@@ -895,8 +976,9 @@ int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
       {"perm", p.o_perm, p.b_perm},        {"inv", p.o_inv, p.b_inv},
       {"x_perm", p.o_xperm, p.b_xperm},    {"h", p.o_h, p.b_h},
       {"y_perm", p.o_yperm, p.b_yperm},    {"y_shared", p.o_ysh, p.b_ysh},
+      {"x_q", p.o_xq, p.b_xq},
   };
-  const int n = p.route_only ? 5 : 11;
+  const int n = p.route_only ? 5 : 12;
   for (int i = 0; i < n && i < cap && regions; ++i) {
     memset(regions[i].name, 0, sizeof(regions[i].name));
     strncpy(regions[i].name, all[i].n, sizeof(regions[i].name) - 1);

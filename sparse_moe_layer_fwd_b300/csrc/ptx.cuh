@@ -364,6 +364,25 @@ MOE_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uin
       : "memory");
 }
 
+// The same with e4m3 A and B (kind::f8f6f4, K = 32 per instruction, so one
+// 32-byte K slice of a 128-byte row as for bf16).
+MOE_DEV void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format 0), fp32
+// accumulator, both K-major: the bf16 descriptor's fields without the bf16
+// format codes.
+MOE_DEV uint32_t umma_idesc_e4m3(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
 // Arrive once on the mbarrier at the same offset in both CTAs of the pair
 // when every pair MMA issued so far has completed.
 MOE_DEV void umma_commit_pair(uint32_t bar) {

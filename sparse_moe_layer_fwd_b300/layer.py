@@ -22,6 +22,14 @@ class MoeLayer:
         self.w_router, self.bias = w_router, bias
         self._keep = (w_gate, w_up, w_down, sh_gate, sh_up, sh_down)
         have_w = w_gate is not None
+        self.packed = None
+        if have_w and flags & M.MOE_FP8_GATE_UP:
+            # gate and up weights as packed e4m3 matrices (codes + row scales)
+            self.packed = {n: self.quantize(w) for n, w in
+                           (("w_gate", w_gate), ("w_up", w_up), ("sh_gate", sh_gate),
+                            ("sh_up", sh_up))}
+            w_gate, w_up = self.packed["w_gate"], self.packed["w_up"]
+            sh_gate, sh_up = self.packed["sh_gate"], self.packed["sh_up"]
         self.experts = M.make_experts(w_gate, w_up, w_down) if have_w else None
         self.shared = M.make_experts(sh_gate, sh_up, sh_down) if have_w else None
         tdt = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -37,6 +45,26 @@ class MoeLayer:
         self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
         self.load_counts = torch.empty((self.E,), dtype=torch.int32, device=dev)
         self.regions = M.moe_workspace_regions(self.desc)
+
+    @staticmethod
+    def quantize(w: torch.Tensor, stream=None) -> torch.Tensor:
+        """Packed per-row e4m3 copy of a bf16 weight tensor (rows = all but the
+        last dimension): codes, then fp32 scales from a 256-byte boundary."""
+        cols = w.shape[-1]
+        rows = w.numel() // cols
+        out = torch.empty(M.moe_e4m3_packed_bytes(rows, cols), dtype=torch.uint8,
+                          device=w.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(w.device)
+        M.moe_quantize_rows_e4m3(w.contiguous(), rows, cols, out, stream)
+        return out
+
+    @staticmethod
+    def unpack(packed: torch.Tensor, rows: int, cols: int):
+        """(codes uint8 [rows, cols], scales fp32 [rows]) views of a packed matrix."""
+        so = M.e4m3_scale_offset(rows, cols)
+        return (packed[:rows * cols].view(rows, cols),
+                packed[so:so + 4 * rows].view(torch.float32))
 
     @classmethod
     def from_inputs(cls, inp: dict, k: int, dtype: str, flags: int = 0, T: int | None = None,

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 
 MOE_F32, MOE_BF16 = 0, 1
-MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS, MOE_TRAINING = 1, 2, 4
+MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS, MOE_TRAINING, MOE_FP8_GATE_UP = 1, 2, 4, 8
 MOE_OK = 0
 MOE_STATIC_SCRATCH_BYTES = 32 << 20
 ERRORS = {
@@ -83,6 +83,10 @@ def _load():
     lib.moe_workspace_regions.restype = I
     lib.moe_route_noalloc.argtypes = [dp, P, P, P, P, P, P, P]
     lib.moe_route_noalloc.restype = I
+    lib.moe_e4m3_packed_bytes.argtypes = [ctypes.c_longlong, I]
+    lib.moe_e4m3_packed_bytes.restype = S
+    lib.moe_quantize_rows_e4m3.argtypes = [P, ctypes.c_longlong, I, P, P]
+    lib.moe_quantize_rows_e4m3.restype = I
     del U
     return lib
 
@@ -234,3 +238,21 @@ def moe_route_noalloc(desc, x, w_router, bias, topk_idx, gates, load_counts, str
     rc = _lib.moe_route_noalloc(ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(bias),
                                 _ptr(topk_idx), _ptr(gates), _ptr(load_counts), _stream(stream))
     return _check(rc, "moe_route_noalloc") if check else rc
+
+
+def moe_e4m3_packed_bytes(rows: int, cols: int) -> int:
+    """Bytes of a packed e4m3 matrix: codes [rows, cols], then fp32 scales
+    [rows] from the next multiple of 256 bytes."""
+    return int(_lib.moe_e4m3_packed_bytes(int(rows), int(cols)))
+
+
+def e4m3_scale_offset(rows: int, cols: int) -> int:
+    return (rows * cols + 255) // 256 * 256
+
+
+def moe_quantize_rows_e4m3(a, rows, cols, packed, stream=None, check=True) -> int:
+    """Per-row e4m3 quantization of the bf16 matrix a [rows, cols] into the
+    packed buffer (moe_e4m3_packed_bytes(rows, cols) bytes)."""
+    rc = _lib.moe_quantize_rows_e4m3(_ptr(a), int(rows), int(cols), _ptr(packed),
+                                     _stream(stream))
+    return _check(rc, "moe_quantize_rows_e4m3") if check else rc

@@ -552,6 +552,49 @@ def pin_quantize_e4m3(O):
     assert np.all(np.abs(d3 - row)[normal] <= 2.0 ** -4 * np.abs(row)[normal])
 
 
+def _fp8_case(seed, exact):
+    """A small layer whose gate/up weights are on the e4m3 grid times a power
+    of two with each row's maximum at 448 times that power (so per-row
+    quantization keeps them exactly); tokens on that grid too if ``exact``."""
+    rng = np.random.default_rng(seed)
+    grid = np.array([v for _, v in _e4m3_values() if abs(v) <= 448.0])
+
+    def on_grid(shape):
+        a = rng.choice(grid, size=shape)
+        a[..., 0] = 448.0 * rng.choice([-1.0, 1.0], size=shape[:-1])  # row max 448
+        return a * 2.0 ** rng.integers(-12, -6, size=shape[:-1])[..., None]
+
+    T, d, h, E, k = 5, 16, 8, 4, 2
+    x = on_grid((T, d)) if exact else rng.normal(size=(T, d)).astype(np.float32).astype(np.float64)
+    experts = [(on_grid((h, d)), on_grid((h, d)), rng.normal(size=(d, h)) * 0.1) for _ in range(E)]
+    shared = (on_grid((h, d)), on_grid((h, d)), rng.normal(size=(d, h)) * 0.1)
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)])
+    gates = rng.uniform(0.1, 1.0, size=(T, k))
+    return x, idx, gates, experts, shared
+
+
+def pin_fp8_gate_up(O):
+    """The fp8 gate/up layer: with tokens and gate/up weights that per-row
+    e4m3 quantization keeps exactly, it IS the unquantized layer; with
+    weights kept exactly, it is the unquantized layer on the tokens'
+    dequantized values; the down projection is never quantized."""
+    x, idx, gates, ex, sh = _fp8_case(43, exact=True)
+    got = O.fp8_gate_up_rows(x, idx, gates, lambda e: ex[e], sh)
+    ref = O.expert_output_rows(x, idx, gates, lambda e: ex[e], sh)
+    assert np.array_equal(got, ref)
+    x, idx, gates, ex, sh = _fp8_case(44, exact=False)
+    xq = O.quantize_rows_e4m3(x)[2]
+    assert not np.array_equal(xq, x)
+    got = O.fp8_gate_up_rows(x, idx, gates, lambda e: ex[e], sh)
+    ref = O.expert_output_rows(xq, idx, gates, lambda e: ex[e], sh)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+    # a W_down off the e4m3 grid (normal values) enters unrounded
+    sh2 = (sh[0], sh[1], sh[2] * 1.0001)
+    ref2 = O.expert_output_rows(xq, idx, gates, lambda e: ex[e], sh2)
+    got2 = O.fp8_gate_up_rows(x, idx, gates, lambda e: ex[e], sh2)
+    assert np.allclose(got2, ref2, rtol=0, atol=1e-12 * np.abs(ref2).max())
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -572,4 +615,5 @@ PINS = [
     pin_backward_special_cases,
     pin_backward_rows_agree,
     pin_quantize_e4m3,
+    pin_fp8_gate_up,
 ]

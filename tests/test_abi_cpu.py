@@ -17,7 +17,8 @@ def test_library_exports_every_header_function():
     assert set(names) == {
         "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
-        "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward"}
+        "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward",
+        "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -35,7 +36,7 @@ def test_error_strings():
 
 @pytest.mark.parametrize("bad", [
     dict(T=-1), dict(d=0), dict(h=0), dict(E=0), dict(E=1025), dict(k=0), dict(k=33, E=64),
-    dict(k=9, E=8), dict(d=96), dict(h=100), dict(dtype=7), dict(flags=8),
+    dict(k=9, E=8), dict(d=96), dict(h=100), dict(dtype=7), dict(flags=8), dict(flags=16),
 ])
 def test_invalid_desc_has_no_workspace(bad):
     kw = dict(T=64, d=256, h=128, E=16, k=4, dtype="f32", flags=0)
@@ -143,7 +144,7 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     desc = M.make_desc(T, d, h, E, k, dt)
     total = M.moe_workspace_size(desc)
     regs = M.moe_workspace_regions(desc)
-    assert total > 0 and len(regs) == 11
+    assert total > 0 and len(regs) == 12
     spans = sorted(regs.values())
     for (o1, b1), (o2, _) in zip(spans, spans[1:]):
         assert o1 % 256 == 0 and o1 + b1 <= o2
@@ -152,6 +153,7 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     assert regs["x_perm"][1] == T * k * d * el
     assert regs["h"][1] == (T * k + T) * h * el
     assert regs["y_shared"][1] == T * d * 4
+    assert regs["x_q"][1] == 0
     # the tensor-core router (bf16 tokens, 96 experts or more) keeps the
     # router weights as three bf16 terms, expert rows padded to 256
     tc_router = dt == "bf16" and E >= 96 and T > 0
@@ -159,3 +161,34 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     ro = M.make_desc(T, d, h, E, k, dt, M.MOE_ROUTE_ONLY)
     assert M.moe_workspace_size(ro) <= total and len(M.moe_workspace_regions(ro)) == 5
     assert M.moe_host_io_extra_bytes(desc) >= 2 * T * d * el
+
+
+def test_fp8_gate_up_flag():
+    F = M.MOE_FP8_GATE_UP
+    # bf16 tensor-core forward only
+    for bad in (("f32", F), ("bf16", F | M.MOE_SIMT_EXPERTS), ("bf16", F | M.MOE_ROUTE_ONLY),
+                ("bf16", F | M.MOE_TRAINING)):
+        assert M.moe_workspace_size(M.make_desc(64, 256, 128, 16, 4, bad[0], bad[1])) == 0
+    T, d, h, E, k = 300, 7168, 2048, 256, 8
+    desc = M.make_desc(T, d, h, E, k, "bf16", F)
+    regs = M.moe_workspace_regions(desc)
+    assert len(regs) == 12
+    # the gathered token rows hold one-byte codes; x_q: codes, then row scales
+    assert regs["x_perm"][1] == T * k * d
+    assert regs["x_q"][1] == (T * d + 255) // 256 * 256 + 4 * T
+    assert regs["x_q"][0] % 256 == 0
+
+
+def test_e4m3_packed_layout_and_argument_errors():
+    assert M.moe_e4m3_packed_bytes(10, 24) == 256 + 40
+    assert M.moe_e4m3_packed_bytes(256, 7168) == 256 * 7168 + 1024
+    assert M.moe_e4m3_packed_bytes(0, 128) == 0
+    assert M.moe_e4m3_packed_bytes(-1, 128) == 0 and M.moe_e4m3_packed_bytes(4, 0) == 0
+    E = M.ERR_CODE
+    q = lambda a=FAKE, rows=4, cols=128, out=FAKE: M.moe_quantize_rows_e4m3(  # noqa: E731
+        a, rows, cols, out, check=False)
+    assert q(cols=100) == E["MOE_ERR_SHAPE"]
+    assert q(rows=-1) == E["MOE_ERR_SHAPE"]
+    assert q(a=None) == E["MOE_ERR_NULL"] and q(out=None) == E["MOE_ERR_NULL"]
+    assert q(out=FAKE + 8) == E["MOE_ERR_ALIGN"]
+    assert q(rows=0, a=None) == M.MOE_OK

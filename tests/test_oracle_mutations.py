@@ -266,6 +266,35 @@ def _quant_truncate(a):
     return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), (q.double() * scale.double()).numpy()
 
 
+def _fp8_unquantized_tokens(x_rows, idx_rows, gate_rows, get_expert, shared):
+    def q(w):
+        return (_ORIG["quantize_rows_e4m3"](w[0])[2], _ORIG["quantize_rows_e4m3"](w[1])[2],
+                np.asarray(w[2], F64))
+    return _ORIG["expert_output_rows"](x_rows, idx_rows, gate_rows, lambda e: q(get_expert(e)),
+                                       q(shared))
+
+
+def _fp8_down_quantized(x_rows, idx_rows, gate_rows, get_expert, shared):
+    xq = _ORIG["quantize_rows_e4m3"](x_rows)[2]
+
+    def q(w):
+        return tuple(_ORIG["quantize_rows_e4m3"](m)[2] for m in w)
+    return _ORIG["expert_output_rows"](xq, idx_rows, gate_rows, lambda e: q(get_expert(e)),
+                                       q(shared))
+
+
+def _fp8_codes_only(x_rows, idx_rows, gate_rows, get_expert, shared):
+    # drops the scales: codes taken as values
+    def codes(a):
+        return _ORIG["quantize_rows_e4m3"](a)[0].view(np.int8).astype(F64)
+    xq = codes(x_rows)
+
+    def q(w):
+        return codes(w[0]), codes(w[1]), np.asarray(w[2], F64)
+    return _ORIG["expert_output_rows"](xq, idx_rows, gate_rows, lambda e: q(get_expert(e)),
+                                       q(shared))
+
+
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
 
 MUTATIONS = [
@@ -306,6 +335,9 @@ MUTATIONS = [
     ("quantize_rows_e4m3", _quant_wrong_max),
     ("quantize_rows_e4m3", _quant_per_column),
     ("quantize_rows_e4m3", _quant_truncate),
+    ("fp8_gate_up_rows", _fp8_unquantized_tokens),
+    ("fp8_gate_up_rows", _fp8_down_quantized),
+    ("fp8_gate_up_rows", _fp8_codes_only),
 ]
 
 
