@@ -69,6 +69,10 @@ as a source, uses the same):
                code = e4m3(row / scale) rounded to nearest even; the layer is
                then the same layer on the dequantized values code * scale
                (routing on the unquantized tokens).
+               With the down projection in e4m3 as well, each row of W_down
+               and each hidden row H of a (token, expert) pair (and of the
+               shared expert) is quantized the same way before W_down is
+               applied; H itself is computed as above.
 
 ``moe_forward_dense`` is the pages' own formulation (every expert on every
 token, then masked).  ``moe_forward_sparse`` evaluates only the selected
@@ -408,6 +412,32 @@ def quantize_rows_e4m3(a):
     q = (t / scale).to(torch.float8_e4m3fn)
     deq = q.to(torch.float64) * scale.to(torch.float64)
     return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), deq.numpy()
+
+
+def fp8_swiglu_expert(x, w_gate, w_up, w_down, down: bool):
+    """One expert under reading 10: gate/up on the dequantized tokens and
+    weights; if ``down``, H and W_down dequantized row by row as well."""
+    xq = quantize_rows_e4m3(x)[2]
+    g = xq @ quantize_rows_e4m3(w_gate)[2].T
+    u = xq @ quantize_rows_e4m3(w_up)[2].T
+    hid = silu(g) * u
+    if down:
+        return quantize_rows_e4m3(hid)[2] @ quantize_rows_e4m3(w_down)[2].T
+    return hid @ _f64(w_down).T
+
+
+def fp8_expert_rows(x_rows, idx_rows, gate_rows, get_expert, shared, down: bool):
+    """Layer output for sampled rows under reading 10 (``down``: the down
+    projection in e4m3 too); arguments as expert_output_rows, the selection
+    and gates coming from the unquantized routing."""
+    x_rows = _f64(x_rows)
+    y = fp8_swiglu_expert(x_rows, *shared, down)
+    idx_rows = np.asarray(idx_rows)
+    for e in np.unique(idx_rows):
+        tt, jj = np.nonzero(idx_rows == e)
+        ye = fp8_swiglu_expert(x_rows[tt], *get_expert(int(e)), down)
+        y[tt] += gate_rows[tt, jj][:, None] * ye
+    return y
 
 
 def fp8_gate_up_rows(x_rows, idx_rows, gate_rows, get_expert, shared):

@@ -595,6 +595,35 @@ def pin_fp8_gate_up(O):
     assert np.allclose(got2, ref2, rtol=0, atol=1e-12 * np.abs(ref2).max())
 
 
+def pin_fp8_down(O):
+    """The fp8 down projection: without it the expert is the gate/up-only
+    layer; with it, the result factors into the e4m3 codes and the two rows'
+    scales, y = s_H[:, None] * (C_H C_W^T) * s_W[None, :], with H the
+    gate/up-only hidden rows; scaling W_down by a power of two scales y."""
+    x, idx, gates, ex, sh = _fp8_case(45, exact=False)
+    wg, wu, wd = ex[1]
+    xt = x[:3]
+    y0 = O.fp8_swiglu_expert(xt, wg, wu, wd, down=False)
+    assert np.allclose(y0, O.fp8_gate_up_rows(xt, np.full((3, 1), 0), np.ones((3, 1)),
+                                              lambda e: ex[1], (wg, wu, 0 * wd)), rtol=1e-12)
+    xq = O.quantize_rows_e4m3(xt)[2]
+    hid = O.silu(xq @ O.quantize_rows_e4m3(wg)[2].T) * (xq @ O.quantize_rows_e4m3(wu)[2].T)
+    ch, shs, _ = O.quantize_rows_e4m3(hid)
+    cw, sw, _ = O.quantize_rows_e4m3(wd)
+    e4 = dict(_e4m3_values())
+    val = np.vectorize(lambda c: e4[int(c)])
+    y_codes = shs.astype(np.float64)[:, None] * (val(ch) @ val(cw).T) * sw.astype(np.float64)[None, :]
+    y1 = O.fp8_swiglu_expert(xt, wg, wu, wd, down=True)
+    assert np.allclose(y1, y_codes, rtol=1e-12, atol=1e-300)
+    assert not np.allclose(y1, y0, rtol=1e-6)
+    y2 = O.fp8_swiglu_expert(xt, wg, wu, wd * 2.0 ** -9, down=True)
+    assert np.array_equal(y2, y1 * 2.0 ** -9)
+    rows = O.fp8_expert_rows(x, idx, gates, lambda e: ex[e], sh, down=True)
+    one = O.fp8_swiglu_expert(x[2:3], *sh, down=True) + sum(
+        gates[2, j] * O.fp8_swiglu_expert(x[2:3], *ex[idx[2, j]], down=True) for j in range(idx.shape[1]))
+    assert np.allclose(rows[2:3], one, rtol=1e-12)
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -616,4 +645,5 @@ PINS = [
     pin_backward_rows_agree,
     pin_quantize_e4m3,
     pin_fp8_gate_up,
+    pin_fp8_down,
 ]

@@ -295,6 +295,24 @@ def _fp8_codes_only(x_rows, idx_rows, gate_rows, get_expert, shared):
                                        q(shared))
 
 
+def _fp8_expert_down_ignored(x, w_gate, w_up, w_down, down):
+    return _ORIG["fp8_swiglu_expert"](x, w_gate, w_up, w_down, False)
+
+
+def _fp8_expert_h_per_column(x, w_gate, w_up, w_down, down):
+    q = _ORIG["quantize_rows_e4m3"]
+    xq = q(x)[2]
+    hid = _ORIG["silu"](xq @ q(w_gate)[2].T) * (xq @ q(w_up)[2].T)
+    if down:
+        return q(hid.T)[2].T @ q(w_down)[2].T
+    return hid @ np.asarray(w_down, F64).T
+
+
+def _fp8_rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared, down):
+    return _ORIG["fp8_expert_rows"](x_rows, idx_rows, np.ones_like(gate_rows), get_expert,
+                                    shared, down)
+
+
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
 
 MUTATIONS = [
@@ -338,6 +356,9 @@ MUTATIONS = [
     ("fp8_gate_up_rows", _fp8_unquantized_tokens),
     ("fp8_gate_up_rows", _fp8_down_quantized),
     ("fp8_gate_up_rows", _fp8_codes_only),
+    ("fp8_swiglu_expert", _fp8_expert_down_ignored),
+    ("fp8_swiglu_expert", _fp8_expert_h_per_column),
+    ("fp8_expert_rows", _fp8_rows_ungated),
 ]
 
 
