@@ -190,9 +190,9 @@ def _working_set_bytes(wl, route_only):
     return b
 
 
-def _algorithmic(wl, load, fp8=False):
-    """FLOPs and bytes of the two expert GEMMs for one launch each (fp8: the
-    first GEMM reads one-byte codes of weights and tokens, plus row scales)."""
+def _algorithmic(wl, load, fp8=False, fp8_down=False):
+    """FLOPs and bytes of the two expert GEMMs for one launch each (fp8: a
+    GEMM reads one-byte codes of weights and tokens, plus row scales)."""
     TK, T, d, h = wl.T * wl.k, wl.T, wl.d, wl.h
     rows = TK + T
     fl1 = 4.0 * rows * d * h
@@ -202,7 +202,10 @@ def _algorithmic(wl, load, fp8=False):
         by1 = touched * 2 * h * (d + 4) + rows * (d + 4) + rows * h * 2
     else:
         by1 = touched * 2 * h * d * 2 + rows * d * 2 + rows * h * 2
-    by2 = touched * d * h * 2 + rows * h * 2 + TK * d * 2 + T * d * 4
+    if fp8_down:
+        by2 = touched * d * (h + 4) + rows * (h + 4) + TK * d * 2 + T * d * 4
+    else:
+        by2 = touched * d * h * 2 + rows * h * 2 + TK * d * 2 + T * d * 4
     return fl1, fl2, by1, by2, touched - 1
 
 
@@ -267,7 +270,8 @@ def run_ours(args, wl):
     route_only = args.route_only or wl.route_only
     inp = I.make_inputs(wl_rank, device="cuda", experts=not route_only)
     fp8 = bool(args.fp8) and not route_only
-    base_flags = M.MOE_FP8_GATE_UP if fp8 else 0
+    fp8_down = fp8 and args.fp8 == "experts"
+    base_flags = (M.MOE_FP8_EXPERTS if fp8_down else M.MOE_FP8_GATE_UP) if fp8 else 0
     layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else base_flags)
     stream = torch.cuda.current_stream()
     x = inp["x"]
@@ -425,7 +429,7 @@ def run_ours(args, wl):
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8)
+    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8, fp8_down)
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
@@ -489,14 +493,16 @@ def run_ours(args, wl):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 gate/up (per-row scales), bf16 down" if fp8 else "bf16",
+        "dtype": ("e4m3 experts (per-row scales)" if fp8_down else
+                  "e4m3 gate/up (per-row scales), bf16 down" if fp8 else "bf16"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
                    "shared_experts": 1, "parallelism": f"replicas x{ws}",
-                   "l2": l2_note, **({"fp8_gate_up": True} if fp8 else {})},
+                   "l2": l2_note, **({"fp8": args.fp8} if fp8 else {})},
         "roofline": roof, "roofline_layer": layer_roof,
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": kernels_per_step(wl, False, fp8) * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": (kernels_per_step(wl, False, fp8) + int(fp8_down)) * args.steps,
         "clocks": clocks, "kernel_sha": sha,
     }
     print(json.dumps(line), flush=True)
@@ -646,8 +652,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time a training step: forward and backward")
-    ap.add_argument("--fp8", action="store_true",
-                    help="gate/up products on per-row e4m3 codes (MOE_FP8_GATE_UP)")
+    ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "experts"],
+                    help="expert products on per-row e4m3 codes: gate/up only "
+                         "(MOE_FP8_GATE_UP, the default) or gate/up and down "
+                         "(MOE_FP8_EXPERTS)")
     ap.add_argument("--route-only", action="store_true",
                     help="time the routing pass only (router, top-k, load counts)")
     args = ap.parse_args()

@@ -92,6 +92,11 @@ enum {
                                 w_gate and w_up of experts and shared then point at
                                 packed quantized matrices; w_down stays bf16; the
                                 tokens are quantized per row inside the call */
+#define MOE_FP8_DOWN    16u  /* as MOE_FP8_GATE_UP for the down projection: w_down
+                                of experts and shared point at packed quantized
+                                matrices, and the hidden rows H are quantized
+                                per row inside the call */
+#define MOE_FP8_EXPERTS (MOE_FP8_GATE_UP | MOE_FP8_DOWN)
 
 /* Problem description.
  *   T  tokens (>= 0)            d  model width          h  expert hidden width
@@ -103,7 +108,7 @@ typedef struct {
   int T, d, h, E, k;
   int dtype;        /* moe_dtype */
   unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING |
-                       MOE_FP8_GATE_UP */
+                       MOE_FP8_GATE_UP | MOE_FP8_DOWN */
 } moe_desc;
 
 /* Expert weights, element type desc->dtype.
@@ -128,8 +133,11 @@ typedef struct {
  * moe_e4m3_packed_bytes(rows, cols) bytes:
  *   codes  [rows, cols] uint8 (e4m3 bit patterns) at byte 0,
  *   scales [rows]       fp32 at byte ceil(rows*cols / 256) * 256.
- * The routed gate (or up) weights are one matrix of E*h rows; the shared
- * expert's one of h rows. */
+ * The routed gate (or up) weights are one matrix of E*h rows, the routed
+ * down weights one of E*d rows (h columns); the shared expert's h rows (gate,
+ * up) or d rows (down).  With MOE_FP8_DOWN the hidden row of each (token,
+ * expert) pair and of the shared expert is quantized the same way before the
+ * down projection. */
 MOE_API size_t moe_e4m3_packed_bytes(long long rows, int cols);
 
 /* Quantize a bf16 matrix a [rows, cols] (device, row-major, 16-byte aligned)
@@ -276,7 +284,8 @@ MOE_API const char* moe_error_string(int code);
  * (int32 group table),
  * "perm" (permuted row -> token*k+slot), "inv" (token*k+slot -> permuted row),
  * "x_perm", "h", "y_perm", "y_shared", "x_q" (MOE_FP8_GATE_UP: the tokens
- * quantized, packed as above; empty otherwise). */
+ * quantized, packed as above; empty otherwise), "h_q" (MOE_FP8_DOWN: the
+ * rows of "h" quantized, packed; empty otherwise). */
 typedef struct {
   char name[16];
   size_t offset, bytes;

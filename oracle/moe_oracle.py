@@ -72,7 +72,9 @@ as a source, uses the same):
                With the down projection in e4m3 as well, each row of W_down
                and each hidden row H of a (token, expert) pair (and of the
                shared expert) is quantized the same way before W_down is
-               applied; H itself is computed as above.
+               applied; H is computed as above and held in bf16, the
+               layer's activation type (round to nearest even), before it
+               is quantized.
 
 ``moe_forward_dense`` is the pages' own formulation (every expert on every
 token, then masked).  ``moe_forward_sparse`` evaluates only the selected
@@ -414,28 +416,40 @@ def quantize_rows_e4m3(a):
     return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), deq.numpy()
 
 
-def fp8_swiglu_expert(x, w_gate, w_up, w_down, down: bool):
-    """One expert under reading 10: gate/up on the dequantized tokens and
-    weights; if ``down``, H and W_down dequantized row by row as well."""
-    xq = quantize_rows_e4m3(x)[2]
-    g = xq @ quantize_rows_e4m3(w_gate)[2].T
-    u = xq @ quantize_rows_e4m3(w_up)[2].T
+def round_bf16(a):
+    """Nearest bf16 value (ties to even) of each element, as float64: the
+    storage of the hidden rows before they are quantized (reading 10)."""
+    import torch
+    return torch.as_tensor(np.asarray(a, dtype=F64)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def fp8_swiglu_expert(x, w_gate, w_up, w_down, down: bool, gate_up: bool = True):
+    """One expert under reading 10: if ``gate_up``, gate/up on the
+    dequantized tokens and weights; if ``down``, H and W_down dequantized row
+    by row before the down projection."""
+    if gate_up:
+        xq = quantize_rows_e4m3(x)[2]
+        g = xq @ quantize_rows_e4m3(w_gate)[2].T
+        u = xq @ quantize_rows_e4m3(w_up)[2].T
+    else:
+        g, u = _f64(x) @ _f64(w_gate).T, _f64(x) @ _f64(w_up).T
     hid = silu(g) * u
     if down:
-        return quantize_rows_e4m3(hid)[2] @ quantize_rows_e4m3(w_down)[2].T
+        return quantize_rows_e4m3(round_bf16(hid))[2] @ quantize_rows_e4m3(w_down)[2].T
     return hid @ _f64(w_down).T
 
 
-def fp8_expert_rows(x_rows, idx_rows, gate_rows, get_expert, shared, down: bool):
-    """Layer output for sampled rows under reading 10 (``down``: the down
-    projection in e4m3 too); arguments as expert_output_rows, the selection
-    and gates coming from the unquantized routing."""
+def fp8_expert_rows(x_rows, idx_rows, gate_rows, get_expert, shared, down: bool,
+                    gate_up: bool = True):
+    """Layer output for sampled rows under reading 10 (which products are in
+    e4m3: ``gate_up``, ``down``); arguments as expert_output_rows, the
+    selection and gates coming from the unquantized routing."""
     x_rows = _f64(x_rows)
-    y = fp8_swiglu_expert(x_rows, *shared, down)
+    y = fp8_swiglu_expert(x_rows, *shared, down, gate_up)
     idx_rows = np.asarray(idx_rows)
     for e in np.unique(idx_rows):
         tt, jj = np.nonzero(idx_rows == e)
-        ye = fp8_swiglu_expert(x_rows[tt], *get_expert(int(e)), down)
+        ye = fp8_swiglu_expert(x_rows[tt], *get_expert(int(e)), down, gate_up)
         y[tt] += gate_rows[tt, jj][:, None] * ye
     return y
 

@@ -203,19 +203,23 @@ MOE_DEV void stage_box_bf16(uint32_t ta, uint32_t tb, uint32_t box, int lane) {
   }
 }
 
-// stage_box_bf16 for the fp8 gate/up products: the accumulators hold code
-// products, so gate and up are first multiplied by their rows' weight
-// scales and the tokens' scales.  rsg / rsu: scales of the rows
-// (lane >> 2) + 8 r, r = 0..3 of the warp's 32; tsc[2 i + e]: scale of token
-// column 8 i + 2 (lane & 3) + e.
-MOE_DEV void stage_box_swiglu_scaled(uint32_t ta, uint32_t tb, uint32_t box, int lane,
-                                     const float (&rsg)[4], const float (&rsu)[4],
-                                     const float (&tsc)[8]) {
+// stage_box_bf16 for the fp8 products: the accumulators hold sums of code
+// products, so each value is first multiplied by its weight row's scale and
+// its token's scale (SWIGLU: gate and up, each with its own row scales).
+// rsg / rsu: scales of the rows (lane >> 2) + 8 r, r = 0..3 of the warp's 32;
+// tsc[2 i + e]: scale of token column 8 i + 2 (lane & 3) + e.
+template <bool SWIGLU>
+MOE_DEV void stage_box_scaled(uint32_t ta, uint32_t tb, uint32_t box, int lane,
+                              const float (&rsg)[4], const float (&rsu)[4],
+                              const float (&tsc)[8]) {
   const int mm = lane >> 3, ii = lane & 7;
 #pragma unroll
   for (int L = 0; L < 32; L += 16) {
     uint32_t ra[16], rb[16];
-    tmem_load_16x256b_2(ta + ((uint32_t)L << 16), tb + ((uint32_t)L << 16), ra, rb);
+    if (SWIGLU)
+      tmem_load_16x256b_2(ta + ((uint32_t)L << 16), tb + ((uint32_t)L << 16), ra, rb);
+    else
+      tmem_load_16x256b(ta + ((uint32_t)L << 16), ra);
     uint32_t w[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {  // m = 2 i + hf: rows L + 8 hf + lane/4, columns 8 i ..
@@ -224,8 +228,12 @@ MOE_DEV void stage_box_swiglu_scaled(uint32_t ta, uint32_t tb, uint32_t box, int
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float g = __uint_as_float(ra[2 * m + e]) * (rsg[r] * tsc[2 * i + e]);
-        const float u = __uint_as_float(rb[2 * m + e]) * (rsu[r] * tsc[2 * i + e]);
-        o[e] = silu_fast(g) * u;
+        if (SWIGLU) {
+          const float u = __uint_as_float(rb[2 * m + e]) * (rsu[r] * tsc[2 * i + e]);
+          o[e] = silu_fast(g) * u;
+        } else {
+          o[e] = g;
+        }
       }
       w[m] = pack_bf16x2(o[0], o[1]);
     }
@@ -326,8 +334,10 @@ MOE_DEV TcTile tc_tile(const GroupTable& G, const int32_t* toff, int E, int b, i
   return t;
 }
 
-// Scales of the fp8 gate/up products: per weight row (routed [E*h], shared
-// [h]) and per token ([T]; a routed row's token is perm[row] / k).
+// Scales of the fp8 products.  Gate/up: per weight row (g, u routed [E*h];
+// sg, su shared [h]) and per token (tok [T]; a routed row's token is
+// perm[row] / k).  Down: per W_down row (g [E*d], sg [d]) and per row of H
+// (tok [T*k + T], numbered as the output rows); u, su, perm unused.
 struct Fp8Scales {
   const float *g, *u, *sg, *su, *tok;
   const int32_t* perm;

@@ -46,9 +46,12 @@ enum : int {
   TC2_BWD_DX = 4,    // dX = dA W_gate + dB W_up (weights read transposed)      K = 2h
   TC2_FWD_UP_FP8 = 5,  // H as TC2_FWD_UP from e4m3 codes of weights and tokens
                        // with per-row scales (kind::f8f6f4)          K = d (bytes)
+  TC2_FWD_DOWN_FP8 = 6,  // Y as TC2_FWD_DOWN from e4m3 codes of W_down and H  K = h (bytes)
 };
 // two blocks of 256 rows of one matrix per tile (else gate and up rows)
-__host__ __device__ constexpr bool tc2_down(int op) { return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX; }
+__host__ __device__ constexpr bool tc2_down(int op) {
+  return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX || op == TC2_FWD_DOWN_FP8;
+}
 // the weight operand is MN-major (the weights' transpose is multiplied)
 __host__ __device__ constexpr bool tc2_mn_a(int op) { return op == TC2_BWD_DH || op == TC2_BWD_DX; }
 
@@ -131,7 +134,7 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   int rb;
   if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_FWD_UP_FP8)
     rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
-  else if (OP == TC2_FWD_DOWN) rb = G.off[g] + t.tok0;
+  else if (OP == TC2_FWD_DOWN || OP == TC2_FWD_DOWN_FP8) rb = G.off[g] + t.tok0;
   else if (OP == TC2_BWD_DH) rb = t.shared ? t.tok0 : G.poff[g] + t.tok0;
   else rb = G.poff[g] + t.tok0;
   t.row_b = rb + (int)rank * t.half;
@@ -147,7 +150,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
              const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs) {
   constexpr bool DOWN = tc2_down(OP);
   constexpr bool MNA = tc2_mn_a(OP);
-  constexpr bool FP8 = OP == TC2_FWD_UP_FP8;
+  constexpr bool FP8U = OP == TC2_FWD_UP_FP8, FP8D = OP == TC2_FWD_DOWN_FP8;
+  constexpr bool FP8 = FP8U || FP8D;
   constexpr int KB_ELEMS = FP8 ? 128 : TC_BK;  // elements per 128-byte K step
   using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB>;
   static_assert(OUTB >= 0 && OUTB <= 3, "staged boxes per epilogue warp");
@@ -163,9 +167,9 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const bool leader = rank == 0;
 
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
-  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8) ? G.toff_a
+  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8U) ? G.toff_a
                         : (OP == TC2_BWD_DH ? G.toff_c : G.toff_b);
-  int* counter = G.next + (FP8 ? 0 : OP);
+  int* counter = G.next + (FP8U ? TC2_FWD_UP : FP8D ? TC2_FWD_DOWN : OP);
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
@@ -315,7 +319,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const int b = next_tile(i, true);
         if (b < 0) break;
         const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
-        const bool bs = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH || FP8) && t.shared;
+        const bool bs = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH || FP8U) && t.shared;
         const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
         const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
         const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
@@ -451,7 +455,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     // it, then block 1.  bf16 outputs of 32 whole tokens go out through
     // shared memory by TMA store; the rest (a ragged last chunk, the shared
     // expert's fp32 rows, the SwiGLU gradient) from registers.
-    constexpr bool F32SH = OP == TC2_FWD_DOWN || OP == TC2_BWD_DX;  // shared rows in fp32
+    constexpr bool F32SH = OP == TC2_FWD_DOWN || OP == TC2_BWD_DX || FP8D;  // shared rows in fp32
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
@@ -479,14 +483,15 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         float rsg[4] = {1.f, 1.f, 1.f, 1.f}, rsu[4] = {1.f, 1.f, 1.f, 1.f}, rlg = 1.f, rlu = 1.f;
         if (FP8 && valid) {
           const float* sgp = t.shared ? fs.sg : fs.g + (size_t)t.g * n_out;
-          const float* sup = t.shared ? fs.su : fs.u + (size_t)t.g * n_out;
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            rsg[r] = sgp[of + (lane >> 2) + 8 * r];
-            rsu[r] = sup[of + (lane >> 2) + 8 * r];
-          }
+          for (int r = 0; r < 4; ++r) rsg[r] = sgp[of + (lane >> 2) + 8 * r];
           rlg = sgp[of + lane];
-          rlu = sup[of + lane];
+          if (FP8U) {
+            const float* sup = t.shared ? fs.su : fs.u + (size_t)t.g * n_out;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) rsu[r] = sup[of + (lane >> 2) + 8 * r];
+            rlu = sup[of + lane];
+          }
         }
         for (int c = 32 * half; c < t.npad; c += 64) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -519,10 +524,12 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             }
             continue;
           }
-          // fp8: scale of token column c + lane
+          // fp8: scale of token column c + lane (gate/up: the token's row of
+          // x; down: the row of H, numbered as the output rows)
           float tsl = 0.f;
           if (FP8 && c + lane < t.ntok)
-            tsl = fs.tok[t.shared ? t.tok0 + c + lane : fs.perm[t.out_row0 + c + lane] / fs.k];
+            tsl = FP8D ? fs.tok[t.out_row0 + c + lane]
+                       : fs.tok[t.shared ? t.tok0 + c + lane : fs.perm[t.out_row0 + c + lane] / fs.k];
           if (OUTB > 0 && OP != TC2_BWD_DAB && c + 32 <= t.ntok && !(F32SH && t.shared)) {
             // 32 whole tokens of bf16 output: stage the box in shared
             // memory and store it with TMA (boxes used round robin)
@@ -536,7 +543,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
                   tsc[2 * i + e] = __shfl_sync(0xffffffffu, tsl, 8 * i + 2 * (lane & 3) + e);
-              stage_box_swiglu_scaled(ta + c, tb + c, box, lane, rsg, rsu, tsc);
+              stage_box_scaled<FP8U>(ta + c, tb + c, box, lane, rsg, rsu, tsc);
             } else {
               stage_box_bf16<OP == TC2_FWD_UP>(ta + c, tb + c, box, lane);
             }
@@ -556,7 +563,11 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           else
             tmem_load_32(ta + c, va);
           if (!valid) continue;
-          if (FP8) {
+          if (FP8D) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) va[j] *= rlg * __shfl_sync(0xffffffffu, tsl, j);
+          }
+          if (FP8U) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float ts = __shfl_sync(0xffffffffu, tsl, j);

@@ -83,6 +83,7 @@ struct Plan {
   bool f32, route_only, simt, big_router, big_tiles, tc_router;
   bool training;  // the backward's buffers follow the forward's
   bool fp8;       // gate/up products on e4m3 codes (packed weights, tokens quantized here)
+  bool fp8_down;  // down projection on e4m3 codes (packed W_down, H quantized here)
   int el;  // bytes per activation / weight element
   // router: CUDA-core tiles (r_bm x r_bn) or tensor-core pairs over E_pad
   // experts (rt_eb blocks of 256) x rt_tt token tiles x n_split K slices
@@ -93,20 +94,20 @@ struct Plan {
   int bn, ft_a, ft_b, ft_c, tile_round, max_tiles_a, max_tiles_b, max_tiles_c;
   // workspace regions (byte offsets)
   size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh,
-      o_xq, total;
+      o_xq, o_hq, total;
   // backward: padded dY rows, dG, du, dH, padded dA|dB rows, dX rows, shared dX
   size_t o_dyp, o_dg, o_du, o_dh, o_dab, o_dxp, o_dxs;
   long long rows_dyp, rows_dab;  // allocated padded rows
   size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh,
-      b_xq;
+      b_xq, b_hq;
 };
 
 int validate_desc(const moe_desc* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
-  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_GATE_UP))
+  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_EXPERTS))
     return MOE_ERR_DTYPE;
-  if ((d->flags & MOE_FP8_GATE_UP) &&
+  if ((d->flags & MOE_FP8_EXPERTS) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY | MOE_TRAINING))))
     return MOE_ERR_DTYPE;
   if ((d->flags & MOE_TRAINING) &&
@@ -135,6 +136,7 @@ Plan make_plan(const moe_desc* d) {
   p.simt = p.f32 || (d->flags & MOE_SIMT_EXPERTS);
   p.el = p.f32 ? 4 : 2;
   p.fp8 = d->flags & MOE_FP8_GATE_UP;
+  p.fp8_down = d->flags & MOE_FP8_DOWN;
 
   // router GEMM tiling and split of the model dimension
   p.big_router = p.E >= 96;
@@ -207,7 +209,7 @@ Plan make_plan(const moe_desc* d) {
       // (training: always the CTA-pair tiles, whose tile table the
       // backward's products share)
       // (fp8: the CTA-pair kernel alone has the e4m3 product)
-      p.big_tiles = per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_GATE_UP));
+      p.big_tiles = per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_EXPERTS));
       if (p.big_tiles) {
         p.bn = kPairBN;
         p.ft_a = MOE_PAIR_GEMM1 ? (p.h + 2 * TC_BM - 1) / (2 * TC_BM) : p.h / TC_BM;
@@ -246,6 +248,9 @@ Plan make_plan(const moe_desc* d) {
     region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
     region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
     region(p.fp8 ? e4m3_scale_offset(p.T, p.d) + (size_t)p.T * 4 : 0, p.o_xq, p.b_xq);
+    region(p.fp8_down ? e4m3_scale_offset((long long)p.TK + p.T, p.h) + (size_t)(p.TK + p.T) * 4
+                      : 0,
+           p.o_hq, p.b_hq);
   }
   p.training = d->flags & MOE_TRAINING;
   if (p.training) {
@@ -434,12 +439,22 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
                          p.d);
     ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8, x, p.T, p.d);
   }
-  ok &= make_map(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
+  if (p.fp8_down) {
+    // e4m3 codes: packed W_down (codes first), rows of H quantized
+    ok &= make_map_u8(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
+    ok &= make_map_u8(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
+    ok &= make_map_u8(&m->down.b128, ws + p.o_hq, (long long)p.TK + p.T, p.h, 128);
+    ok &= make_map_u8(&m->down.b64, ws + p.o_hq, (long long)p.TK + p.T, p.h, 64);
+    ok &= make_map_u8(&m->down.b16, ws + p.o_hq, (long long)p.TK + p.T, p.h, 16);
+    ok &= make_map_u8(&m->down.b8, ws + p.o_hq, (long long)p.TK + p.T, p.h, 8);
+  } else {
+    ok &= make_map(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
+    ok &= make_map(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
+    ok &= make_rows_maps(&m->down.b128, &m->down.b64, &m->down.b16, &m->down.b8, ws + p.o_h,
+                         (long long)p.TK + p.T, p.h);
+  }
   m->down.a1 = m->down.a0;
-  ok &= make_map(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
   m->down.sa1 = m->down.sa0;
-  ok &= make_rows_maps(&m->down.b128, &m->down.b64, &m->down.b16, &m->down.b8, ws + p.o_h,
-                       (long long)p.TK + p.T, p.h);
   m->down.bs128 = m->down.b128;
   m->down.bs64 = m->down.b64;
   m->down.bs16 = m->down.b16;
@@ -577,7 +592,8 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
             ? ((p.fp8 ? set_tc2_smem<TC2_FWD_UP_FP8>()
                       : MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
-               (MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
+               (p.fp8_down ? set_tc2_smem<TC2_FWD_DOWN_FP8>()
+                : MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, true>()))
             : (set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, false>() &&
                set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, true>());
@@ -647,8 +663,26 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
                            groups, hbuf, nullptr, s);
       }
       if (between) cudaEventRecord(between, s);
-      launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b, groups,
-                        yperm, ysh, s);
+      if (p.fp8_down) {
+        // the rows of H to codes and scales, then the down projection on them
+        const long long rows_h = (long long)p.TK + p.T;
+        uint8_t* hq = ws + p.o_hq;
+        float* hs = reinterpret_cast<float*>(hq + e4m3_scale_offset(rows_h, p.h));
+        k_quant_rows<__nv_bfloat16><<<(unsigned)((rows_h + 7) / 8), 256, 0, s>>>(
+            hbuf, rows_h, p.h, hq, hs);
+        const size_t so = e4m3_scale_offset((long long)p.E * p.d, p.h),
+                     ss = e4m3_scale_offset(p.d, p.h);
+        auto scl = [](const void* w, size_t o) {
+          return reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) + o);
+        };
+        const Fp8Scales fs{scl(experts->w_down, so), nullptr, scl(shared->w_down, ss), nullptr,
+                           hs, nullptr, p.k};
+        launch_pair<TC2_FWD_DOWN_FP8>(p, maps.down, p.max_tiles_b, groups, p.h / 2, p.d, yperm,
+                                      ysh, nullptr, s, fs);
+      } else {
+        launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b,
+                          groups, yperm, ysh, s);
+      }
     }
     mark(4);
     const float* ysh = reinterpret_cast<const float*>(ws + p.o_ysh);
@@ -976,9 +1010,9 @@ int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
       {"perm", p.o_perm, p.b_perm},        {"inv", p.o_inv, p.b_inv},
       {"x_perm", p.o_xperm, p.b_xperm},    {"h", p.o_h, p.b_h},
       {"y_perm", p.o_yperm, p.b_yperm},    {"y_shared", p.o_ysh, p.b_ysh},
-      {"x_q", p.o_xq, p.b_xq},
+      {"x_q", p.o_xq, p.b_xq},             {"h_q", p.o_hq, p.b_hq},
   };
-  const int n = p.route_only ? 5 : 12;
+  const int n = p.route_only ? 5 : 13;
   for (int i = 0; i < n && i < cap && regions; ++i) {
     memset(regions[i].name, 0, sizeof(regions[i].name));
     strncpy(regions[i].name, all[i].n, sizeof(regions[i].name) - 1);

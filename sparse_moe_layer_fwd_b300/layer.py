@@ -22,14 +22,18 @@ class MoeLayer:
         self.w_router, self.bias = w_router, bias
         self._keep = (w_gate, w_up, w_down, sh_gate, sh_up, sh_down)
         have_w = w_gate is not None
-        self.packed = None
+        # fp8 modes: the weights they name as packed e4m3 matrices (codes +
+        # row scales), quantized once here
+        self.packed = {}
         if have_w and flags & M.MOE_FP8_GATE_UP:
-            # gate and up weights as packed e4m3 matrices (codes + row scales)
-            self.packed = {n: self.quantize(w) for n, w in
-                           (("w_gate", w_gate), ("w_up", w_up), ("sh_gate", sh_gate),
-                            ("sh_up", sh_up))}
+            self.packed.update({"w_gate": self.quantize(w_gate), "w_up": self.quantize(w_up),
+                                "sh_gate": self.quantize(sh_gate), "sh_up": self.quantize(sh_up)})
             w_gate, w_up = self.packed["w_gate"], self.packed["w_up"]
             sh_gate, sh_up = self.packed["sh_gate"], self.packed["sh_up"]
+        if have_w and flags & M.MOE_FP8_DOWN:
+            self.packed.update({"w_down": self.quantize(w_down),
+                                "sh_down": self.quantize(sh_down)})
+            w_down, sh_down = self.packed["w_down"], self.packed["sh_down"]
         self.experts = M.make_experts(w_gate, w_up, w_down) if have_w else None
         self.shared = M.make_experts(sh_gate, sh_up, sh_down) if have_w else None
         tdt = torch.float32 if dtype == "f32" else torch.bfloat16

@@ -37,6 +37,7 @@ def test_error_strings():
 @pytest.mark.parametrize("bad", [
     dict(T=-1), dict(d=0), dict(h=0), dict(E=0), dict(E=1025), dict(k=0), dict(k=33, E=64),
     dict(k=9, E=8), dict(d=96), dict(h=100), dict(dtype=7), dict(flags=8), dict(flags=16),
+    dict(flags=32),
 ])
 def test_invalid_desc_has_no_workspace(bad):
     kw = dict(T=64, d=256, h=128, E=16, k=4, dtype="f32", flags=0)
@@ -144,7 +145,7 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     desc = M.make_desc(T, d, h, E, k, dt)
     total = M.moe_workspace_size(desc)
     regs = M.moe_workspace_regions(desc)
-    assert total > 0 and len(regs) == 12
+    assert total > 0 and len(regs) == 13
     spans = sorted(regs.values())
     for (o1, b1), (o2, _) in zip(spans, spans[1:]):
         assert o1 % 256 == 0 and o1 + b1 <= o2
@@ -153,7 +154,7 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     assert regs["x_perm"][1] == T * k * d * el
     assert regs["h"][1] == (T * k + T) * h * el
     assert regs["y_shared"][1] == T * d * 4
-    assert regs["x_q"][1] == 0
+    assert regs["x_q"][1] == 0 and regs["h_q"][1] == 0
     # the tensor-core router (bf16 tokens, 96 experts or more) keeps the
     # router weights as three bf16 terms, expert rows padded to 256
     tc_router = dt == "bf16" and E >= 96 and T > 0
@@ -163,8 +164,8 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     assert M.moe_host_io_extra_bytes(desc) >= 2 * T * d * el
 
 
-def test_fp8_gate_up_flag():
-    F = M.MOE_FP8_GATE_UP
+@pytest.mark.parametrize("F", [M.MOE_FP8_GATE_UP, M.MOE_FP8_DOWN, M.MOE_FP8_EXPERTS])
+def test_fp8_flags(F):
     # bf16 tensor-core forward only
     for bad in (("f32", F), ("bf16", F | M.MOE_SIMT_EXPERTS), ("bf16", F | M.MOE_ROUTE_ONLY),
                 ("bf16", F | M.MOE_TRAINING)):
@@ -172,11 +173,15 @@ def test_fp8_gate_up_flag():
     T, d, h, E, k = 300, 7168, 2048, 256, 8
     desc = M.make_desc(T, d, h, E, k, "bf16", F)
     regs = M.moe_workspace_regions(desc)
-    assert len(regs) == 12
-    # the gathered token rows hold one-byte codes; x_q: codes, then row scales
-    assert regs["x_perm"][1] == T * k * d
-    assert regs["x_q"][1] == (T * d + 255) // 256 * 256 + 4 * T
-    assert regs["x_q"][0] % 256 == 0
+    assert len(regs) == 13
+    gu, dn = bool(F & M.MOE_FP8_GATE_UP), bool(F & M.MOE_FP8_DOWN)
+    # gate/up: the gathered token rows hold one-byte codes; x_q: the tokens'
+    # codes, then their row scales.  down: h_q holds H's codes and scales.
+    assert regs["x_perm"][1] == T * k * d * (1 if gu else 2)
+    assert regs["x_q"][1] == ((T * d + 255) // 256 * 256 + 4 * T if gu else 0)
+    R = T * k + T
+    assert regs["h_q"][1] == ((R * h + 255) // 256 * 256 + 4 * R if dn else 0)
+    assert regs["x_q"][0] % 256 == 0 and regs["h_q"][0] % 256 == 0
 
 
 def test_e4m3_packed_layout_and_argument_errors():

@@ -1,11 +1,12 @@
-"""FP8 (e4m3) gate/up products against the float64 oracle.
+"""FP8 (e4m3) expert products against the float64 oracle.
 
 Per-row quantization (moe_quantize_rows_e4m3, and the tokens inside the
 forward) must give the oracle's codes and scales bit for bit: both sides take
 the same fp32 division and nearest-even rounding.  The layer with
-MOE_FP8_GATE_UP is compared with the oracle's fp8 reading (gate/up on the
-dequantized tokens and weights, W_down and the routing unquantized) under the
-bf16 tolerances; the routing checks are those of the bf16 layer.
+MOE_FP8_GATE_UP, MOE_FP8_DOWN or both is compared with the oracle's fp8
+reading (the named products on per-row dequantized operands, the routing
+unquantized) under the bf16 tolerances; the routing checks are those of the
+bf16 layer.
 """
 import numpy as np
 import pytest
@@ -72,9 +73,14 @@ def _fetch(inp):
     return get
 
 
-def _check_fp8(wl, n_rows=None):
+MODES = {"gate_up": M.MOE_FP8_GATE_UP, "down": M.MOE_FP8_DOWN, "experts": M.MOE_FP8_EXPERTS}
+
+
+def _check_fp8(wl, mode, n_rows=None):
+    flags = MODES[mode]
+    gate_up, down = bool(flags & M.MOE_FP8_GATE_UP), bool(flags & M.MOE_FP8_DOWN)
     inp = I.make_inputs(wl, device="cuda")
-    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_FP8_GATE_UP)
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, flags)
     y = layer.forward(inp["x"])
     torch.cuda.synchronize()
     assert M.moe_last_error() == M.MOE_OK
@@ -83,18 +89,20 @@ def _check_fp8(wl, n_rows=None):
     gidx = npi(layer.topk_idx)
     flips = check_routing(gidx, layer.gates.cpu().numpy().astype(np.float64), ref, 1e-5)
     check_load(npi(layer.load_counts), gidx, ref["idx"], wl.E, flips)
-    # the tokens' codes and scales in the workspace: the oracle's, bit for bit
-    xq = layer.region("x_q", torch.uint8, (layer.regions["x_q"][1],))
-    codes, scales = MoeLayer.unpack(xq, wl.T, wl.d)
-    q, sc, _ = O.quantize_rows_e4m3(inp["x"].float().cpu().numpy())
-    assert np.array_equal(codes.cpu().numpy(), q) and np.array_equal(scales.cpu().numpy(), sc)
+    if gate_up:
+        # the tokens' codes and scales in the workspace: the oracle's, bit for bit
+        xq = layer.region("x_q", torch.uint8, (layer.regions["x_q"][1],))
+        codes, scales = MoeLayer.unpack(xq, wl.T, wl.d)
+        q, sc, _ = O.quantize_rows_e4m3(inp["x"].float().cpu().numpy())
+        assert np.array_equal(codes.cpu().numpy(), q)
+        assert np.array_equal(scales.cpu().numpy(), sc)
     if n_rows is None or n_rows >= wl.T:
         rows = np.arange(wl.T)
     else:
         rows = np.sort(np.random.default_rng(wl.seed).choice(wl.T, n_rows, replace=False))
     sh = (np64(inp["sh_gate"]), np64(inp["sh_up"]), np64(inp["sh_down"]))
     g_rows = O.gate_weights(ref["s"][rows], gidx[rows])
-    y_ref = O.fp8_gate_up_rows(x64[rows], gidx[rows], g_rows, _fetch(inp), sh)
+    y_ref = O.fp8_expert_rows(x64[rows], gidx[rows], g_rows, _fetch(inp), sh, down, gate_up)
     stats = check_output(np64(y[torch.from_numpy(rows).cuda()]), y_ref, "bf16")
     # the quantization is visible: the unquantized layer differs by more
     y_bf = O.expert_output_rows(x64[rows], gidx[rows], g_rows, _fetch(inp), sh)
@@ -104,20 +112,21 @@ def _check_fp8(wl, n_rows=None):
     return stats, flips
 
 
-CASES = [
+CASES = [(m, *c) for m in MODES for c in (
     ("small_bf16", dict(), None),
-    ("mini_bf16", dict(T=2048), None),
     ("v3_decode", dict(), None),
-    ("v3_decode_zipf", dict(), None),
     ("v3_prefill", dict(), 48),
+)] + [
+    ("experts", "mini_bf16", dict(T=2048), None),
+    ("experts", "v3_decode_zipf", dict(), None),
 ]
 
 
-@pytest.mark.parametrize("name,over,n_rows", CASES,
-                         ids=[f"{n}_{o.get('T', 'T')}" for n, o, _ in CASES])
-def test_fp8_layer_matches_oracle(name, over, n_rows):
-    stats, flips = _check_fp8(I.WORKLOADS[name].with_(**over), n_rows)
-    print(f"{name}: {stats} flips={flips}")
+@pytest.mark.parametrize("mode,name,over,n_rows", CASES,
+                         ids=[f"{m}-{n}_{o.get('T', 'T')}" for m, n, o, _ in CASES])
+def test_fp8_layer_matches_oracle(mode, name, over, n_rows):
+    stats, flips = _check_fp8(I.WORKLOADS[name].with_(**over), mode, n_rows)
+    print(f"{mode} {name}: {stats} flips={flips}")
     assert stats["rel_l2_vs_unquantized"] > 2 * stats["rel_l2"]
 
 
@@ -128,7 +137,8 @@ EDGES = [
 ]
 
 
+@pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("shape", EDGES, ids=[f"T{s['T']}_h{s['h']}_E{s['E']}_k{s['k']}" for s in EDGES])
-def test_fp8_edges(shape):
-    stats, _ = _check_fp8(I.custom(dtype="bf16", seed=7 + shape["T"], **shape))
-    print(shape, stats)
+def test_fp8_edges(shape, mode):
+    stats, _ = _check_fp8(I.custom(dtype="bf16", seed=7 + shape["T"], **shape), mode)
+    print(mode, shape, stats)

@@ -295,22 +295,43 @@ def _fp8_codes_only(x_rows, idx_rows, gate_rows, get_expert, shared):
                                        q(shared))
 
 
-def _fp8_expert_down_ignored(x, w_gate, w_up, w_down, down):
-    return _ORIG["fp8_swiglu_expert"](x, w_gate, w_up, w_down, False)
+def _fp8_expert_down_ignored(x, w_gate, w_up, w_down, down, gate_up=True):
+    return _ORIG["fp8_swiglu_expert"](x, w_gate, w_up, w_down, False, gate_up)
 
 
-def _fp8_expert_h_per_column(x, w_gate, w_up, w_down, down):
+def _fp8_expert_always_gate_up(x, w_gate, w_up, w_down, down, gate_up=True):
+    return _ORIG["fp8_swiglu_expert"](x, w_gate, w_up, w_down, down, True)
+
+
+def _fp8_expert_h_per_column(x, w_gate, w_up, w_down, down, gate_up=True):
     q = _ORIG["quantize_rows_e4m3"]
-    xq = q(x)[2]
-    hid = _ORIG["silu"](xq @ q(w_gate)[2].T) * (xq @ q(w_up)[2].T)
+    xq = q(x)[2] if gate_up else np.asarray(x, F64)
+    wq = (lambda w: q(w)[2]) if gate_up else (lambda w: np.asarray(w, F64))
+    hid = _ORIG["silu"](xq @ wq(w_gate).T) * (xq @ wq(w_up).T)
     if down:
-        return q(hid.T)[2].T @ q(w_down)[2].T
+        return q(_ORIG["round_bf16"](hid).T)[2].T @ q(w_down)[2].T
     return hid @ np.asarray(w_down, F64).T
 
 
-def _fp8_rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared, down):
+def _fp8_expert_h_unrounded(x, w_gate, w_up, w_down, down, gate_up=True):
+    q = _ORIG["quantize_rows_e4m3"]
+    xq = q(x)[2] if gate_up else np.asarray(x, F64)
+    wq = (lambda w: q(w)[2]) if gate_up else (lambda w: np.asarray(w, F64))
+    hid = _ORIG["silu"](xq @ wq(w_gate).T) * (xq @ wq(w_up).T)
+    if down:
+        return q(hid)[2] @ q(w_down)[2].T
+    return hid @ np.asarray(w_down, F64).T
+
+
+def _round_bf16_truncates(a):
+    import torch
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32))
+    return (t.view(torch.int32) & ~0xFFFF).view(torch.float32).double().numpy()
+
+
+def _fp8_rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared, down, gate_up=True):
     return _ORIG["fp8_expert_rows"](x_rows, idx_rows, np.ones_like(gate_rows), get_expert,
-                                    shared, down)
+                                    shared, down, gate_up)
 
 
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
@@ -358,6 +379,9 @@ MUTATIONS = [
     ("fp8_gate_up_rows", _fp8_codes_only),
     ("fp8_swiglu_expert", _fp8_expert_down_ignored),
     ("fp8_swiglu_expert", _fp8_expert_h_per_column),
+    ("fp8_swiglu_expert", _fp8_expert_always_gate_up),
+    ("fp8_swiglu_expert", _fp8_expert_h_unrounded),
+    ("round_bf16", _round_bf16_truncates),
     ("fp8_expert_rows", _fp8_rows_ungated),
 ]
 
