@@ -7,7 +7,17 @@ MOE_FP8_GATE_UP, MOE_FP8_DOWN or both is compared with the oracle's fp8
 reading (the named products on per-row dequantized operands, the routing
 unquantized) under the bf16 tolerances; the routing checks are those of the
 bf16 layer.
+
+With the down projection in e4m3 the hidden rows are quantized from their
+bf16 values, and the GPU's bf16 H (fp32 accumulation) and the oracle's
+(float64, then rounded) can round an element to neighbouring bf16 values.
+Where that element is its row's maximum, the row's scale moves by 2^-8 and
+every code of the row can move by one e4m3 step (2^-4 relative), so one
+(token, expert) contribution can be off by that much: the largest error is
+bounded by 2^-3 * rms(y) (two steps of a contribution of rms size) in those
+modes; the relative L2 bound is the bf16 one in every mode.
 """
+DOWN_MAX_ABS_RMS = 2.0 ** -3
 import numpy as np
 import pytest
 import torch
@@ -103,7 +113,8 @@ def _check_fp8(wl, mode, n_rows=None):
     sh = (np64(inp["sh_gate"]), np64(inp["sh_up"]), np64(inp["sh_down"]))
     g_rows = O.gate_weights(ref["s"][rows], gidx[rows])
     y_ref = O.fp8_expert_rows(x64[rows], gidx[rows], g_rows, _fetch(inp), sh, down, gate_up)
-    stats = check_output(np64(y[torch.from_numpy(rows).cuda()]), y_ref, "bf16")
+    stats = check_output(np64(y[torch.from_numpy(rows).cuda()]), y_ref, "bf16",
+                         DOWN_MAX_ABS_RMS if down else None)
     # the quantization is visible: the unquantized layer differs by more
     y_bf = O.expert_output_rows(x64[rows], gidx[rows], g_rows, _fetch(inp), sh)
     stats["rel_l2_vs_unquantized"] = float(np.linalg.norm(y_bf - y_ref) / np.linalg.norm(y_bf))
