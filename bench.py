@@ -65,7 +65,8 @@ def kernels_per_step(wl, route_only, fp8=False):
 # single-pass counters), keyed by workload, with the hash of the GEMM sources
 # at capture time; reported as null once those sources change.
 NCU_TRAFFIC = {
-    "v3_prefill": {"sha": "bddf83a079266003", "bytes": 17.73e9 + 0.29755e9},
+    "v3_prefill": {"sha": "5a126901055d4fb3", "bytes": 17.581e9 + 0.29616e9},
+    "v3_prefill:fp8": {"sha": "5a126901055d4fb3", "bytes": 8.5356e9 + 0.29206e9},
 }
 
 
@@ -433,8 +434,8 @@ def run_ours(args, wl):
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
-    cap = NCU_TRAFFIC.get(wl.name)
-    traffic = cap["bytes"] if cap and cap.get("sha") == sha and not fp8 else None
+    cap = NCU_TRAFFIC.get(wl.name + (":fp8" if fp8 else ""))  # GEMM 1 (gate/up)
+    traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
     if prefill_like and fp8:
         # e4m3 codes on kind::f8f6f4: the fp8 dense peak is twice the bf16
         # one (2.25 vs 4.5 PFLOP/s nominal), applied to the measured figure
