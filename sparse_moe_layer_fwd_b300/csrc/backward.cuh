@@ -142,21 +142,43 @@ k_bwd_router(const float* __restrict__ part, int n_split, const int32_t* __restr
 }
 
 // dW_r[e][c] = sum over the pairs of expert e, in row order, of du * x[token]
-// (fp32).  grid (E, d / 256): thread = one column.
+// (fp32).  grid (E, ceil(d / 1024)), 128 threads: thread = eight columns (one
+// 16-byte load per row), four rows' loads in flight before their FMAs, which
+// still run in row order.
 template <typename TX>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 k_bwd_router_wgrad(const int32_t* __restrict__ groups, int E, const int32_t* __restrict__ perm,
                    const float* __restrict__ du, const TX* __restrict__ x, int d, int k,
                    float* __restrict__ dwr) {
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
-  const int e = blockIdx.x, c = blockIdx.y * blockDim.x + threadIdx.x;
+  const int e = blockIdx.x, c = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (c >= d) return;
-  float acc = 0.f;
-  for (int pos = G.off[e]; pos < G.off[e + 1]; ++pos) {
-    const int p = perm[pos];
-    acc = fmaf(du[p], to_f(x[(size_t)(p / k) * d + c]), acc);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int r1 = G.off[e + 1];
+  int pos = G.off[e];
+  for (; pos + 4 <= r1; pos += 4) {
+    float u[4], v[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = perm[pos + i];
+      u[i] = du[p];
+      load8(x + (size_t)(p / k) * d + c, v[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(u[i], v[i][q], acc[q]);
   }
-  dwr[(size_t)e * d + c] = acc;
+  for (; pos < r1; ++pos) {
+    const int p = perm[pos];
+    float v[8];
+    load8(x + (size_t)(p / k) * d + c, v);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = fmaf(du[p], v[q], acc[q]);
+  }
+  float4* o = reinterpret_cast<float4*>(dwr + (size_t)e * d + c);
+  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // ---------------------------------------------------------------- combine

@@ -936,7 +936,7 @@ int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
   wgrad(maps.wd, p.d, p.h, 0, 5, 1, 0);
   wgrad(maps.wg, p.h, p.d, 0, 6, 0, 1);
   wgrad(maps.wu, p.h, p.d, p.h, 7, 0, 1);
-  k_bwd_router_wgrad<__nv_bfloat16><<<dim3(p.E, (p.d + 255) / 256), 256, 0, s>>>(
+  k_bwd_router_wgrad<__nv_bfloat16><<<dim3(p.E, (p.d + 1023) / 1024), 128, 0, s>>>(
       groups, p.E, perm, du, static_cast<const __nv_bfloat16*>(x), p.d, p.k, d_router);
   k_bwd_combine<__nv_bfloat16><<<p.T, 128, 0, s>>>(dxs, dxp, inv, topk_idx, du, w_router, p.T,
                                                     p.d, p.k, static_cast<__nv_bfloat16*>(dx));
