@@ -272,6 +272,18 @@ MOE_API int moe_backward(const moe_desc* desc, const void* x, const float* w_rou
  * word cannot be read. */
 MOE_API int moe_last_error(void);
 
+/* Self-test of the failure path.  Every wait of the library's kernels on a
+ * pipeline barrier is bounded: when it runs out (4 s), the kernel sets the
+ * device error word and returns, and moe_last_error then reports
+ * MOE_ERR_DEVICE_TIMEOUT; the context stays usable.  This call enqueues one
+ * small kernel on `stream` whose single wait, on a barrier that nothing
+ * arrives on, runs out after limit_ms (1..10000) milliseconds, so a caller or
+ * a test can check that path end to end: synchronise, expect
+ * MOE_ERR_DEVICE_TIMEOUT from moe_last_error, then MOE_OK from the next
+ * call.  No fault or trap is involved.  Returns MOE_ERR_SHAPE for limit_ms
+ * out of range, MOE_ERR_DEVICE / MOE_ERR_LAUNCH as moe_forward. */
+MOE_API int moe_selftest_timeout(unsigned limit_ms, void* stream);
+
 /* Static string for a MOE_* code. */
 MOE_API const char* moe_error_string(int code);
 

@@ -28,6 +28,7 @@
 #include "router_tc.cuh"
 #include "backward.cuh"
 #include "quant.cuh"
+#include "selftest.cuh"
 
 namespace {
 
@@ -763,6 +764,15 @@ int moe_forward_host_io(const moe_desc* desc, const void* x_host, const float* w
   if (need_y && cudaMemcpyAsync(y_host, ydev, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MOE_ERR_DEVICE;
   return MOE_OK;
+}
+
+int moe_selftest_timeout(unsigned limit_ms, void* stream) {
+  if (limit_ms < 1 || limit_ms > 10000) return MOE_ERR_SHAPE;
+  int rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  cudaGetLastError();
+  k_selftest_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_ms * 1000000ull);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 size_t moe_e4m3_packed_bytes(long long rows, int cols) {

@@ -84,6 +84,7 @@ def _load():
     lib.moe_workspace_regions.restype = I
     lib.moe_route_noalloc.argtypes = [dp, P, P, P, P, P, P, P]
     lib.moe_route_noalloc.restype = I
+    lib.moe_selftest_timeout.argtypes, lib.moe_selftest_timeout.restype = [U, P], I
     lib.moe_e4m3_packed_bytes.argtypes = [ctypes.c_longlong, I]
     lib.moe_e4m3_packed_bytes.restype = S
     lib.moe_quantize_rows_e4m3.argtypes = [P, ctypes.c_longlong, I, P, P]
@@ -257,3 +258,10 @@ def moe_quantize_rows_e4m3(a, rows, cols, packed, stream=None, check=True) -> in
     rc = _lib.moe_quantize_rows_e4m3(_ptr(a), int(rows), int(cols), _ptr(packed),
                                      _stream(stream))
     return _check(rc, "moe_quantize_rows_e4m3") if check else rc
+
+
+def moe_selftest_timeout(limit_ms: int, stream=None, check=True) -> int:
+    """Enqueue a kernel whose one bounded wait runs out after limit_ms; after
+    a synchronise, moe_last_error() reports MOE_ERR_DEVICE_TIMEOUT."""
+    rc = _lib.moe_selftest_timeout(int(limit_ms), _stream(stream))
+    return _check(rc, "moe_selftest_timeout") if check else rc

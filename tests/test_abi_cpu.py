@@ -18,7 +18,7 @@ def test_library_exports_every_header_function():
         "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
         "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward",
-        "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3"}
+        "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3", "moe_selftest_timeout"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -197,3 +197,11 @@ def test_e4m3_packed_layout_and_argument_errors():
     assert q(a=None) == E["MOE_ERR_NULL"] and q(out=None) == E["MOE_ERR_NULL"]
     assert q(out=FAKE + 8) == E["MOE_ERR_ALIGN"]
     assert q(rows=0, a=None) == M.MOE_OK
+
+
+def test_selftest_timeout_arguments():
+    E = M.ERR_CODE
+    assert M.moe_selftest_timeout(0, check=False) == E["MOE_ERR_SHAPE"]
+    assert M.moe_selftest_timeout(10001, check=False) == E["MOE_ERR_SHAPE"]
+    if not torch.cuda.is_available():
+        assert M.moe_selftest_timeout(100, check=False) == E["MOE_ERR_DEVICE"]
