@@ -4,30 +4,39 @@
 // u[t][e] = sum_i x[t][i] W_r[e][i], x bf16, W_r fp32.  W_r is split into
 // three bf16 terms, W1 = bf16(W_r), W2 = bf16(W_r - W1), W3 = bf16(W_r - W1 -
 // W2), which together carry the 24 significant bits of the fp32 value, so
-// every product x W_j is exact in fp32 and u = x W1^T + x W2^T + x W3^T is
-// accumulated in fp32 by tcgen05 MMAs: the same products and accumulator
-// precision as an fp32 FMA loop, in a different summation order.
+// every product x W_j is exact in fp32 and u = x W1^T + x W2^T + x W3^T.
+// The MMA's fp32 accumulator loses a little to each addition of a partial
+// dot product, always toward zero, so a chain of the 3 x d/16 MMAs of one
+// slice would shrink u by ~1e-5 relative at d = 7168 (measured; the error
+// grows in proportion to the chain's length).  So each 64-deep K step goes
+// into a fresh TMEM accumulator (two, used in turn) and the epilogue warps
+// add it into fp32 registers with round-to-nearest adds while the MMAs of the
+// next step run: a hardware chain is 12 MMAs long, the W3 and W2 terms first,
+// so that only the four W1 MMAs add to a sum of u's magnitude.
 //
 // k_router_split: Wsplit[j][e][i], j = 0..2, e < E_pad (rows e >= E zero).
 // k_router_tc: CTA pairs (cta_group::2) in the swap-AB orientation: M = 256
 //   experts (CTA r holds experts 128 r .. +127 of its block: three 16 KB
 //   split tiles per 64-deep K step), N = up to 256 tokens (half per CTA),
 //   K = one slice of d (split-K; k_router_topk sums the partials in slice
-//   order).  Epilogue: TMEM lane = expert, column = token, so for every token
-//   a warp writes its 32 experts' logits as one 128-byte piece of
+//   order).  Epilogue: TMEM lane = expert, column = token; eight warps, each
+//   holding 32 experts x 128 tokens in registers; at the end, for every
+//   token a warp writes its 32 experts' logits as one 128-byte piece of
 //   part[s][t][e].
 #pragma once
 
 #include "ptx.cuh"
 
-#define RT_THREADS 256  // warp 0: TMA producer, warp 1: TMEM + MMA, warps 4-7: epilogue
+#define RT_THREADS 320  // warp 0: TMA producer, warp 1: TMEM + MMA, warps 2-9: epilogue
 #define RT_STAGES 3
 #define RT_A_BYTES 16384                      // 128 expert rows x 64 K of one split term
 #define RT_A_STAGE (3 * RT_A_BYTES)
 #define RT_STAGE (RT_A_STAGE + 16384)         // + up to 128 token rows x 64 K
 #define RT_BAR_OFF (RT_STAGES * RT_STAGE)
-#define RT_SMEM_BYTES (RT_BAR_OFF + 8 * (2 * RT_STAGES + 2) + 16 + 1024)
-#define RT_TMEM_COLS 256
+#define RT_N_BARS (2 * RT_STAGES + 5)  // full, empty [STAGES]; acc_full, acc_empty [2]; drain
+#define RT_SMEM_BYTES (RT_BAR_OFF + 8 * RT_N_BARS + 16 + 1024)
+#define RT_TMEM_COLS 512  // two 256-column accumulators
+#define RT_EPI_WARPS 8
 
 struct RouterMapsDev {
   CUtensorMap w;               // Wsplit viewed as [3 E_pad, d], 64 x 128 boxes
@@ -91,18 +100,22 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
   uint8_t* bar_base = smem + RT_BAR_OFF;
   auto full = [&](int i) { return smem_u32(bar_base + 8 * i); };
   auto empty = [&](int i) { return smem_u32(bar_base + 8 * (RT_STAGES + i)); };
-  const uint32_t acc_full = smem_u32(bar_base + 8 * (2 * RT_STAGES));
-  const uint32_t drain_bar = smem_u32(bar_base + 8 * (2 * RT_STAGES + 1));
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_base + 8 * (2 * RT_STAGES + 2));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + 8 * (2 * RT_STAGES + 2) + 4);
-  volatile int* progress = reinterpret_cast<volatile int*>(bar_base + 8 * (2 * RT_STAGES + 2) + 8);
+  auto acc_full = [&](int u) { return smem_u32(bar_base + 8 * (2 * RT_STAGES + u)); };
+  auto acc_empty = [&](int u) { return smem_u32(bar_base + 8 * (2 * RT_STAGES + 2 + u)); };
+  const uint32_t drain_bar = smem_u32(bar_base + 8 * (2 * RT_STAGES + 4));
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_base + 8 * RT_N_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + 8 * RT_N_BARS + 4);
+  volatile int* progress = reinterpret_cast<volatile int*>(bar_base + 8 * RT_N_BARS + 8);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < RT_STAGES; ++i) {
       mbar_init(full(i), 1);   // the leader's arrive + both CTAs' bytes
       mbar_init(empty(i), 1);  // the leader's multicast commit
     }
-    mbar_init(acc_full, 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(acc_full(u), 1);                   // the leader's multicast commit
+      mbar_init(acc_empty(u), 2 * RT_EPI_WARPS);   // epilogue warps of both CTAs
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     progress[0] = progress[1] = 0;
@@ -153,50 +166,76 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
     }
   } else if (warp == 1) {
     if (leader && lane == 0) {
-      // ---------- MMA issuer: 3 split terms x 4 K=16 steps per stage ----------
+      // ---------- MMA issuer: 3 split terms x 4 K=16 steps per stage, ----------
+      // ---------- each stage into a fresh accumulator (kb & 1)       ----------
       const uint32_t idesc = umma_idesc_bf16(256, npad);
       for (int kb = 0; kb < nkb; ++kb) {
-        const int st = kb % RT_STAGES;
-        if (*abort_flag || !mbar_wait(full(st), (kb / RT_STAGES) & 1)) {
+        const int st = kb % RT_STAGES, u = kb & 1;
+        if (*abort_flag || !mbar_wait(full(st), (kb / RT_STAGES) & 1) ||
+            (kb >= 2 && !mbar_wait(acc_empty(u), ((kb >> 1) - 1) & 1))) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
         const uint32_t a = smem_u32(smem + st * RT_STAGE), b = a + RT_A_STAGE;
+        // smallest term first: while W3 and W2 products accumulate, the sum
+        // is 2^8 to 2^16 times smaller than u, so only the four W1 MMAs add
+        // at full magnitude
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
+        for (int jj = 0; jj < 3; ++jj)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_pair(tmem, umma_desc_sw128(a + j * RT_A_BYTES + kk * 32),
-                           umma_desc_sw128(b + kk * 32), idesc, (kb | j | kk) != 0);
+            umma_bf16_pair(tmem + (uint32_t)(u * 256),
+                           umma_desc_sw128(a + (2 - jj) * RT_A_BYTES + kk * 32),
+                           umma_desc_sw128(b + kk * 32), idesc, (jj | kk) != 0);
         mma_issued = true;
         umma_commit_pair(empty(st));
+        umma_commit_pair(acc_full(u));
         progress[1] = kb + 1;
       }
-      if (!*abort_flag) umma_commit_pair(acc_full);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ---------- epilogue: TMEM lanes 32 q .. +31 = experts, columns = tokens ----------
-    const int q = warp & 3;
-    if (mbar_wait(acc_full, 0)) {
+  } else {
+    // ---------- epilogue: TMEM lanes 32 q .. +31 = experts, columns = tokens; ----------
+    // ---------- this warp's 128 token columns summed in registers            ----------
+    const int q = warp & 3, hv = (warp - 2) >> 2;
+    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hv * 128);
+    float acc[128];
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int u = kb & 1;
+      if (*abort_flag || !mbar_wait(acc_full(u), (kb >> 1) & 1)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        float v[32];
+        tmem_load_32(lanes + (uint32_t)(u * 256 + c), v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[c + j] = __fadd_rn(acc[c + j], v[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(acc_empty(u));
+        else mbar_arrive_cluster(cluster_map(acc_empty(u), 0));
+      }
+    }
+    if (ok) {
       const int e = eb * 256 + (int)rank * 128 + q * 32 + lane;
       float* out = part + (size_t)s * T * E;
-      for (int c = 0; c < npad; c += 32) {
-        float v[32];
-        tmem_load_32(lanes + c, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int t = t0 + c + j;
-          if (t < T && e < E) out[(size_t)t * E + e] = v[j];
-        }
+      for (int j = 0; j < 128; ++j) {
+        const int t = t0 + hv * 128 + j;
+        if (hv * 128 + j < npad && t < T && e < E) out[(size_t)t * E + e] = acc[j];
       }
     } else {
       *abort_flag = 1;
     }
-    tc_fence_before();
   }
 
   __syncthreads();

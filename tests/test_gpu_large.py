@@ -77,6 +77,34 @@ def test_v3_decode_zipf_skew():
     assert touched < 200
 
 
+def test_v3_largest_token_count():
+    """The largest T the description accepts at V3 widths: (T*k + T) * d
+    just below 2^31, so every 32-bit row offset in the kernels is at its
+    limit; routing on every token, outputs on 64 seeded rows; one token more
+    is rejected."""
+    T_max = ((1 << 31) - 1) // (9 * 7168)
+    assert M.moe_workspace_size(M.make_desc(T_max + 1, 7168, 2048, 256, 8, "bf16")) == 0
+    wl = I.WORKLOADS["v3_prefill"].with_(T=T_max, seed=13)
+    inp = I.make_inputs(wl, device="cuda")
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype)
+    y = layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert M.moe_last_error() == M.MOE_OK
+    x64, wr64, b64 = np64(inp["x"]), np64(inp["w_router"]), np64(inp["bias"])
+    ref = O.route(x64, wr64, b64, wl.k)
+    gidx = npi(layer.topk_idx)
+    flips = check_routing(gidx, layer.gates.cpu().numpy().astype(np.float64), ref, 1e-5)
+    check_load(npi(layer.load_counts), gidx, ref["idx"], wl.E, flips)
+    rows = np.sort(np.random.default_rng(13).choice(wl.T, 64, replace=False))
+    rows[-1] = wl.T - 1  # the last token: its rows sit at the end of every buffer
+    sh = (np64(inp["sh_gate"]), np64(inp["sh_up"]), np64(inp["sh_down"]))
+    y_ref = O.expert_output_rows(x64[rows], gidx[rows], O.gate_weights(ref["s"][rows], gidx[rows]),
+                                 _expert_fetcher(inp), sh)
+    check_output(np64(y[torch.from_numpy(rows).cuda()]), y_ref, wl.dtype)
+    del layer, inp, y
+    torch.cuda.empty_cache()
+
+
 def test_v3_prefill_backward_sampled():
     """Full-size backward: every gradient finite, dx of 8 seeded tokens and
     the weight gradients of the least-loaded expert against the oracle."""

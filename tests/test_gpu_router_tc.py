@@ -1,12 +1,20 @@
 """The tensor-core router (bf16 tokens, 96 experts or more) against the oracle.
 
 The router weights are split into three bf16 terms that carry their 24
-significant bits, so the logits must agree with the float64 logits to fp32
-accumulation accuracy; the selection, gates and load counts follow the same
-acceptance rules as the rest of the layer.  Cases cover one token, ragged
-token tiles, several 256-expert blocks with padded expert rows, split-K
-slices, exact ties from duplicated router rows, and a NaN token.
+significant bits, so every product is exact and the logits must agree with
+the float64 logits to fp32 accumulation accuracy: each error within one fp32
+epsilon of the logit's sum of |products| (an fp32 loop of d FMAs may in the
+worst case be off by d of them), and on average within a tenth of it.  A
+single tensor-core accumulator carried through a whole 7168-deep slice was 17
+times over that bound (its additions lose toward zero); the kernel folds each
+64-deep K step into fp32 registers instead.  The selection, gates and load
+counts follow the same acceptance rules as the rest of the layer.  Cases
+cover one token, ragged token tiles, several 256-expert blocks with padded
+expert rows, split-K slices, one unsplit 7168-deep slice (25000 tokens: the
+partial logits would pass 24 MiB with two), exact ties from duplicated router
+rows, and a NaN token.
 """
+EPS32 = 2.0 ** -23
 import numpy as np
 import pytest
 import torch
@@ -49,6 +57,7 @@ SHAPES = [
     dict(T=300, d=2048, E=128, k=6),     # two token tiles, 128 padded expert rows
     dict(T=1000, d=7168, E=256, k=8),    # split-K over many slices
     dict(T=513, d=1024, E=384, k=8),     # two expert blocks, ragged third token tile
+    dict(T=25000, d=7168, E=256, k=8),   # one slice over the whole model width
 ]
 
 
@@ -61,8 +70,11 @@ def test_tc_router_matches_oracle(shape):
     # logits: fp32 accumulation of exact products, against float64
     u_ref = x64 @ wr64.T
     u = _logits(layer, wl)
-    scale = np.sqrt((x64 ** 2).sum(1))[:, None] * np.sqrt((wr64 ** 2).sum(1))[None, :]
-    assert np.abs(u - u_ref).max() <= 1e-6 * scale.max() + 1e-7
+    if shape["T"] >= 25000:
+        assert layer.regions["router_part"][1] == wl.T * wl.E * 4  # one K slice
+    mag = np.abs(x64) @ np.abs(wr64).T  # sum of |products| per logit
+    rel = np.abs(u - u_ref) / np.maximum(EPS32 * mag, 1e-300)
+    assert rel.max() <= 1.0 and rel.mean() <= 0.1, (rel.max(), rel.mean())
     ref = O.route(x64, wr64, b64, wl.k)
     gidx = npi(layer.topk_idx)
     flips = check_routing(gidx, layer.gates.cpu().numpy().astype(np.float64), ref, 1e-5)
