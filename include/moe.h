@@ -114,7 +114,10 @@ typedef struct {
 /* Expert weights, element type desc->dtype.
  * Routed experts: w_gate [E, h, d], w_up [E, h, d], w_down [E, d, h].
  * Shared expert : w_gate [h, d],    w_up [h, d],    w_down [d, h].
- * (Each matrix is stored output-major: row i holds the weights of output i.) */
+ * (Each matrix is stored output-major: row i holds the weights of output i.)
+ * With MOE_FP8_GATE_UP (w_gate, w_up) or MOE_FP8_DOWN (w_down) those
+ * pointers instead hold the packed e4m3 form of the same matrices, written
+ * by moe_quantize_rows_e4m3 (layout below). */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
 } moe_expert_w;
