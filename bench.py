@@ -65,8 +65,8 @@ def kernels_per_step(wl, route_only, fp8=False):
 # single-pass counters), keyed by workload, with the hash of the GEMM sources
 # at capture time; reported as null once those sources change.
 NCU_TRAFFIC = {
-    "v3_prefill": {"sha": "5a126901055d4fb3", "bytes": 17.581e9 + 0.29616e9},
-    "v3_prefill:fp8": {"sha": "5a126901055d4fb3", "bytes": 8.5356e9 + 0.29206e9},
+    "v3_prefill": {"sha": "7c7fabfbfd8ab89f", "bytes": 17.7129e9 + 0.29699e9},
+    "v3_prefill:fp8": {"sha": "7c7fabfbfd8ab89f", "bytes": 8.5332e9 + 0.29247e9},
 }
 
 
