@@ -9,10 +9,13 @@
 // dot product, always toward zero, so a chain of the 3 x d/16 MMAs of one
 // slice would shrink u by ~1e-5 relative at d = 7168 (measured; the error
 // grows in proportion to the chain's length).  So each 64-deep K step goes
-// into a fresh TMEM accumulator (two, used in turn) and the epilogue warps
-// add it into fp32 registers with round-to-nearest adds while the MMAs of the
-// next step run: a hardware chain is 12 MMAs long, the W3 and W2 terms first,
-// so that only the four W1 MMAs add to a sum of u's magnitude.
+// into fresh TMEM accumulators and the epilogue warps add them into fp32
+// registers with round-to-nearest adds while the MMAs of the next steps run:
+// a hardware chain is 12 MMAs long, the W3 and W2 terms first, so that only
+// the four W1 MMAs add to a sum of u's magnitude.  The token tile is issued as
+// two MMAs of N = 128 (token rows 0..63 and 64..127 of each CTA's half) into
+// four 128-column accumulators used in turn, so a drain has one and a half K
+// steps of MMAs to hide behind.
 //
 // k_router_split: Wsplit[j][e][i], j = 0..2, e < E_pad (rows e >= E zero).
 // k_router_tc: CTA pairs (cta_group::2) in the swap-AB orientation: M = 256
@@ -20,9 +23,9 @@
 //   split tiles per 64-deep K step), N = up to 256 tokens (half per CTA),
 //   K = one slice of d (split-K; k_router_topk sums the partials in slice
 //   order).  Epilogue: TMEM lane = expert, column = token; eight warps, each
-//   holding 32 experts x 128 tokens in registers; at the end, for every
-//   token a warp writes its 32 experts' logits as one 128-byte piece of
-//   part[s][t][e].
+//   holding 32 experts x one MMA half's 128 tokens in registers; at the end,
+//   for every token a warp writes its 32 experts' logits as one 128-byte
+//   piece of part[s][t][e].
 #pragma once
 
 #include "ptx.cuh"
@@ -33,9 +36,10 @@
 #define RT_A_STAGE (3 * RT_A_BYTES)
 #define RT_STAGE (RT_A_STAGE + 16384)         // + up to 128 token rows x 64 K
 #define RT_BAR_OFF (RT_STAGES * RT_STAGE)
-#define RT_N_BARS (2 * RT_STAGES + 5)  // full, empty [STAGES]; acc_full, acc_empty [2]; drain
+#define RT_N_ACC 4                     // 128-column accumulators
+#define RT_N_BARS (2 * RT_STAGES + 2 * RT_N_ACC + 1)  // full, empty; acc_full, acc_empty; drain
 #define RT_SMEM_BYTES (RT_BAR_OFF + 8 * RT_N_BARS + 16 + 1024)
-#define RT_TMEM_COLS 512  // two 256-column accumulators
+#define RT_TMEM_COLS 512  // four 128-column accumulators
 #define RT_EPI_WARPS 8
 
 struct RouterMapsDev {
@@ -101,8 +105,8 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
   auto full = [&](int i) { return smem_u32(bar_base + 8 * i); };
   auto empty = [&](int i) { return smem_u32(bar_base + 8 * (RT_STAGES + i)); };
   auto acc_full = [&](int u) { return smem_u32(bar_base + 8 * (2 * RT_STAGES + u)); };
-  auto acc_empty = [&](int u) { return smem_u32(bar_base + 8 * (2 * RT_STAGES + 2 + u)); };
-  const uint32_t drain_bar = smem_u32(bar_base + 8 * (2 * RT_STAGES + 4));
+  auto acc_empty = [&](int u) { return smem_u32(bar_base + 8 * (2 * RT_STAGES + RT_N_ACC + u)); };
+  const uint32_t drain_bar = smem_u32(bar_base + 8 * (2 * RT_STAGES + 2 * RT_N_ACC));
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_base + 8 * RT_N_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + 8 * RT_N_BARS + 4);
   volatile int* progress = reinterpret_cast<volatile int*>(bar_base + 8 * RT_N_BARS + 8);
@@ -112,9 +116,9 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
       mbar_init(full(i), 1);   // the leader's arrive + both CTAs' bytes
       mbar_init(empty(i), 1);  // the leader's multicast commit
     }
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < RT_N_ACC; ++u) {
       mbar_init(acc_full(u), 1);                   // the leader's multicast commit
-      mbar_init(acc_empty(u), 2 * RT_EPI_WARPS);   // epilogue warps of both CTAs
+      mbar_init(acc_empty(u), RT_EPI_WARPS);       // the 4 warps of its half, both CTAs
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -166,47 +170,61 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
     }
   } else if (warp == 1) {
     if (leader && lane == 0) {
-      // ---------- MMA issuer: 3 split terms x 4 K=16 steps per stage, ----------
-      // ---------- each stage into a fresh accumulator (kb & 1)       ----------
-      const uint32_t idesc = umma_idesc_bf16(256, npad);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int st = kb % RT_STAGES, u = kb & 1;
-        if (*abort_flag || !mbar_wait(full(st), (kb / RT_STAGES) & 1) ||
-            (kb >= 2 && !mbar_wait(acc_empty(u), ((kb >> 1) - 1) & 1))) {
-          *abort_flag = 1;
+      // ---------- MMA issuer: per stage and token half, 3 split terms x 4 ----------
+      // ---------- K=16 steps into a fresh accumulator (2 kb + h) mod 4   ----------
+      const uint32_t idesc = umma_idesc_bf16(256, 128);
+      bool ok = true;
+      for (int kb = 0; ok && kb < nkb; ++kb) {
+        const int st = kb % RT_STAGES;
+        if (*abort_flag || !mbar_wait(full(st), (kb / RT_STAGES) & 1)) {
+          ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t a = smem_u32(smem + st * RT_STAGE), b = a + RT_A_STAGE;
-        // smallest term first: while W3 and W2 products accumulate, the sum
-        // is 2^8 to 2^16 times smaller than u, so only the four W1 MMAs add
-        // at full magnitude
 #pragma unroll
-        for (int jj = 0; jj < 3; ++jj)
+        for (int h = 0; h < 2; ++h) {
+          const int n = 2 * kb + h, u = n % RT_N_ACC;  // n-th use of the accumulators
+          if (n >= RT_N_ACC && !mbar_wait(acc_empty(u), ((n / RT_N_ACC) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // smallest term first: while W3 and W2 products accumulate, the sum
+          // is 2^8 to 2^16 times smaller than u, so only the four W1 MMAs add
+          // at full magnitude.  B: token rows 64 h .. +63 of each CTA's half.
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_pair(tmem + (uint32_t)(u * 256),
-                           umma_desc_sw128(a + (2 - jj) * RT_A_BYTES + kk * 32),
-                           umma_desc_sw128(b + kk * 32), idesc, (jj | kk) != 0);
-        mma_issued = true;
+          for (int jj = 0; jj < 3; ++jj)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_pair(tmem + (uint32_t)(u * 128),
+                             umma_desc_sw128(a + (2 - jj) * RT_A_BYTES + kk * 32),
+                             umma_desc_sw128(b + (uint32_t)(h * 64 * 128) + kk * 32), idesc,
+                             (jj | kk) != 0);
+          mma_issued = true;
+          umma_commit_pair(acc_full(u));
+        }
+        if (!ok) break;
         umma_commit_pair(empty(st));
-        umma_commit_pair(acc_full(u));
         progress[1] = kb + 1;
       }
+      if (!ok) *abort_flag = 1;
     }
     __syncwarp();
   } else {
     // ---------- epilogue: TMEM lanes 32 q .. +31 = experts, columns = tokens; ----------
-    // ---------- this warp's 128 token columns summed in registers            ----------
+    // ---------- token half hv: its accumulators summed in registers           ----------
+    // Column c of a half-h accumulator: token row 64 h + c % 64 of CTA c / 64's
+    // half of the tile (the MMA's N concatenates the two CTAs' B rows).
     const int q = warp & 3, hv = (warp - 2) >> 2;
-    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hv * 128);
+    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
     float acc[128];
 #pragma unroll
     for (int j = 0; j < 128; ++j) acc[j] = 0.f;
     bool ok = true;
     for (int kb = 0; kb < nkb; ++kb) {
-      const int u = kb & 1;
-      if (*abort_flag || !mbar_wait(acc_full(u), (kb >> 1) & 1)) {
+      const int n = 2 * kb + hv, u = n % RT_N_ACC;
+      if (*abort_flag || !mbar_wait(acc_full(u), (n / RT_N_ACC) & 1)) {
         ok = false;
         break;
       }
@@ -214,7 +232,7 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
 #pragma unroll
       for (int c = 0; c < 128; c += 32) {
         float v[32];
-        tmem_load_32(lanes + (uint32_t)(u * 256 + c), v);
+        tmem_load_32(lanes + (uint32_t)(u * 128 + c), v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[c + j] = __fadd_rn(acc[c + j], v[j]);
       }
@@ -230,8 +248,9 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
       float* out = part + (size_t)s * T * E;
 #pragma unroll
       for (int j = 0; j < 128; ++j) {
-        const int t = t0 + hv * 128 + j;
-        if (hv * 128 + j < npad && t < T && e < E) out[(size_t)t * E + e] = acc[j];
+        const int r = 64 * hv + (j & 63);               // row within its CTA's half
+        const int t = t0 + (j < 64 ? 0 : half) + r;
+        if (r < half && t < T && e < E) out[(size_t)t * E + e] = acc[j];
       }
     } else {
       *abort_flag = 1;
