@@ -210,12 +210,14 @@ k_router_topk(const float* __restrict__ part, int n_split, const float* __restri
         if (key[i] > bk || (key[i] == bk && e < bi)) { bk = key[i]; bi = e; }
       }
     }
-    // warp arg-max: larger key, then lower index
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ok > bk || (ok == bk && oi < bi)) { bk = ok; bi = oi; }
+    // warp arg-max: larger key, then lower index -- two warp reductions: the
+    // largest key as order-preserving bits, then the lowest index among the
+    // lanes holding it (keys are never -0: z = s + b with s > 0)
+    {
+      const uint32_t kb = __float_as_uint(bk);
+      const uint32_t ob = (kb & 0x80000000u) ? ~kb : (kb | 0x80000000u);
+      const uint32_t mx = __reduce_max_sync(0xffffffffu, ob);
+      bi = (int)__reduce_min_sync(0xffffffffu, ob == mx ? (uint32_t)bi : 0xffffffffu);
     }
     const int owner = bi & 31, slot = bi >> 5;
     float s_win = 0.f;
