@@ -576,6 +576,9 @@ def run_train(args, wl):
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
                    "l2": "inputs larger than L2"},
         "phase_ms": {"forward": fwd / args.steps, "backward": bwd_ms},
+        # forward kernels, then the backward's 12 (tables, dY rows, gaps, du,
+        # dH, SwiGLU gradient, dX, three weight gradients, dW_r, dx)
+        "gpu_launches": (kernels_per_step(wl, False) + 12) * args.steps,
         "roofline": {"bound": "tensor", "kernel": "backward (dH, dX, weight-gradient GEMMs)",
                      "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
                      "traffic": None,
