@@ -337,6 +337,30 @@ def run_ours(args, wl):
             phase_ms[p] += ev[i][p].elapsed_time(ev[i][p + 1])
     phase_ms /= args.steps
 
+    # optional: the same steps replayed from one captured CUDA graph (no host
+    # launches; the step is timed around each replay, L2 flushed as above)
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer.forward(x, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        ge = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            ge[i][0].record(stream)
+            g.replay()
+            ge[i][1].record(stream)
+        torch.cuda.synchronize()
+        if M.moe_last_error() != M.MOE_OK:
+            raise RuntimeError("device error word set during the graph replays")
+        g_ms, g_value = aggregate(sum(a.elapsed_time(b) for a, b in ge), wl.T * args.steps, ws,
+                                  "cuda")
+        graph = {"value": g_value, "unit": "tokens/s", "ms_per_step": g_ms / args.steps}
+        del g
+
     # end to end through the host-buffer entry point (pinned x in, y out).
     # Inputs larger than L2: two layers on two streams, as a serving loop
     # would run them, so one step's copies overlap the other's kernels (each
@@ -423,6 +447,7 @@ def run_ours(args, wl):
                          "flops_per_launch": rflops, "ms_per_launch": phase_ms[0]},
             "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
             "e2e": e2e, "gpu_launches": kernels_per_step(wl, True) * args.steps,
+            **({"cuda_graph": graph} if graph else {}),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -502,7 +527,7 @@ def run_ours(args, wl):
                    "l2": l2_note, **({"fp8": args.fp8} if fp8 else {})},
         "roofline": roof, "roofline_layer": layer_roof,
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
-        "cpu_baseline": cpu, "e2e": e2e,
+        "cpu_baseline": cpu, "e2e": e2e, **({"cuda_graph": graph} if graph else {}),
         "gpu_launches": (kernels_per_step(wl, False, fp8) + int(fp8_down)) * args.steps,
         "clocks": clocks, "kernel_sha": sha,
     }
@@ -660,6 +685,8 @@ def main():
                     help="expert products on per-row e4m3 codes: gate/up only "
                          "(MOE_FP8_GATE_UP, the default) or gate/up and down "
                          "(MOE_FP8_EXPERTS)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the forward replayed from a captured CUDA graph")
     ap.add_argument("--route-only", action="store_true",
                     help="time the routing pass only (router, top-k, load counts)")
     args = ap.parse_args()
