@@ -146,6 +146,7 @@ EDGE = [
     dict(T=200, d=256, h=128, E=20, k=3),    # E not a power of two
     dict(T=600, d=128, h=128, E=4, k=2),     # several token tiles per expert
     dict(T=100, d=384, h=640, E=40, k=6),
+    dict(T=64, d=128, h=128, E=1024, k=32),  # the largest E and k the description accepts
 ]
 
 
@@ -253,3 +254,23 @@ def test_routing_over_expert_counts(E, k, dtype):
     gload = npi(layer.load_counts)
     check_load(gload, gidx, ref["idx"], E, flips)
     assert np.array_equal(inp["bias"].cpu().numpy(), O.bias_update(b_before, gload, GAMMA, wl.T * k))
+
+
+def test_many_experts_on_cta_pair_tiles():
+    """384 experts (two 256-expert router blocks, 385 groups in the tile
+    table) with about 96 tokens per expert, so both GEMMs take the CTA-pair
+    tiles; the sparse oracle on every row."""
+    wl = I.custom(T=4608, d=256, h=256, E=384, k=8, dtype="bf16", seed=17)
+    inp = _to_cuda(I.make_inputs(wl))
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype)
+    y = layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert M.moe_last_error() == M.MOE_OK
+    x64, wr64, b64 = np64(inp["x"]), np64(inp["w_router"]), np64(inp["bias"])
+    ref = O.route(x64, wr64, b64, wl.k)
+    gidx = npi(layer.topk_idx)
+    flips = check_routing(gidx, layer.gates.cpu().numpy().astype(np.float64), ref, 1e-5)
+    check_load(npi(layer.load_counts), gidx, ref["idx"], wl.E, flips)
+    ex, sh = _oracle_weights(inp)
+    out = O.moe_forward_sparse(x64, wr64, b64, ex, sh, wl.k, idx_override=gidx)
+    check_output(np64(y), out["y"], "bf16")
