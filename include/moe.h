@@ -325,9 +325,13 @@ MOE_API int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int
  *     MOE_ROUTE_ONLY) exceeds MOE_STATIC_SCRATCH_BYTES is rejected with
  *     MOE_ERR_WORKSPACE before anything is launched.  32 MiB covers, e.g.,
  *     T = 8192 tokens with E = 256 experts and d = 7168.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *     with the caller's device current.  With CUDA's lazy module loading
+ *     (the default) the array is reserved on a device when the library's
+ *     module is first loaded there, which may be during the first call of
+ *     any entry point, this one included.  A caller with a fixed memory
+ *     budget should therefore make one call at start-up, before the budget
+ *     is fixed and before any stream capture; later calls reserve nothing.
  *   - Every call uses the same array, which keeps the previous call's
  *     contents.  Nothing in it needs to start at zero: each call writes
  *     every scratch byte it reads before reading it.  Calls whose work

@@ -1035,27 +1035,20 @@ int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
 // ---- routing with static scratch (no allocation, no caller workspace) ----
 // File-scope device array: the scratch of moe_route_noalloc.  Host code must
 // not pass its name to a kernel (on the host it is only a stand-in for the
-// symbol); the device address is looked up once per device below.
+// symbol); its device address is looked up on every call, with the caller's
+// device current.
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_STATIC_SCRATCH_BYTES];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of g_route_scratch on the current device (looked up on the
-// first call per device, with that device current).
+// Device address of g_route_scratch in the current context.  Not cached: a
+// context that is destroyed and created again (cudaDeviceReset) loads the
+// module anew, possibly at another address, and the lookup costs about a
+// microsecond.
 void* route_scratch_address() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = ptr;
-  }
-  return g_scratch_ptr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess) return nullptr;
+  return ptr;
 }
 
 }  // namespace

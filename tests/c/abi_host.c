@@ -54,6 +54,13 @@ int main(void) {
   CHECK(moe_quantize_rows_e4m3((const void*)0x10000, 4, 100, (void*)0x10000, NULL) ==
         MOE_ERR_SHAPE);
   CHECK(moe_selftest_timeout(0, NULL) == MOE_ERR_SHAPE);
+  /* routing with the static array: a problem whose scratch exceeds it is
+   * refused before any device is touched */
+  moe_desc big = {65536, 128, 128, 256, 1, MOE_BF16, MOE_ROUTE_ONLY};
+  CHECK(moe_workspace_size(&big) > MOE_STATIC_SCRATCH_BYTES);
+  CHECK(moe_route_noalloc(&big, (const void*)0x10000, (const float*)0x10000,
+                          (const float*)0x10000, (int32_t*)0x10000, (float*)0x10000,
+                          (int32_t*)0x10000, NULL) == MOE_ERR_WORKSPACE);
   puts("C ABI host checks passed");
   return 0;
 }

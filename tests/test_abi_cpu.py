@@ -205,3 +205,26 @@ def test_selftest_timeout_arguments():
     assert M.moe_selftest_timeout(10001, check=False) == E["MOE_ERR_SHAPE"]
     if not torch.cuda.is_available():
         assert M.moe_selftest_timeout(100, check=False) == E["MOE_ERR_DEVICE"]
+
+
+def test_static_scratch_size_matches_the_header():
+    """The binding's copy of MOE_STATIC_SCRATCH_BYTES is the header's value."""
+    import re
+    text = open(M.HEADER_PATH).read()
+    m = re.search(r"#define\s+MOE_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "MOE_STATIC_SCRATCH_BYTES not found in moe.h"
+    assert M.MOE_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_noalloc_rejects_problems_larger_than_its_array():
+    """The size check comes before anything touches a device: fake pointers
+    and no GPU are enough."""
+    # 65536 tokens x 256 experts: the fp32 router logits alone take 64 MiB
+    big = M.make_desc(65536, 128, 128, 256, 1, "bf16")
+    need = M.moe_workspace_size(M.make_desc(65536, 128, 128, 256, 1, "bf16", M.MOE_ROUTE_ONLY))
+    assert M.moe_workspace_size(big) > 0  # a valid problem ...
+    assert need > M.MOE_STATIC_SCRATCH_BYTES  # ... whose routing scratch does not fit
+    rc = M.moe_route_noalloc(big, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, check=False)
+    assert rc == M.ERR_CODE["MOE_ERR_WORKSPACE"]
+    assert M.library().moe_route_noalloc(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                         None) == M.ERR_CODE["MOE_ERR_NULL"]

@@ -31,7 +31,8 @@ def _route_reference(desc_ro, x, w_router, bias, T, k, E):
 @pytest.mark.parametrize("shape", [
     dict(T=256, d=256, E=16, k=4, dtype="f32"),
     dict(T=1000, d=7168, E=256, k=8, dtype="bf16"),
-], ids=["tiny_fp32", "v3_router_1000_tokens"])
+    dict(T=8192, d=7168, E=256, k=8, dtype="bf16"),
+], ids=["tiny_fp32", "v3_router_1000_tokens", "v3_router_8192_tokens"])
 def test_noalloc_routing_matches_workspace_routing_twice(shape):
     T, d, E, k, dtype = shape["T"], shape["d"], shape["E"], shape["k"], shape["dtype"]
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -57,12 +58,27 @@ def test_noalloc_routing_matches_workspace_routing_twice(shape):
         assert int(load.sum()) == T * k
 
 
-def test_noalloc_rejects_problems_larger_than_its_array():
-    # 65536 tokens x 256 experts: the fp32 router logits alone take 64 MiB
-    big = M.make_desc(65536, 128, 128, 256, 1, "bf16")
-    need = M.moe_workspace_size(M.make_desc(65536, 128, 128, 256, 1, "bf16", M.MOE_ROUTE_ONLY))
-    assert M.moe_workspace_size(big) > 0  # a valid problem ...
-    assert need > M.MOE_STATIC_SCRATCH_BYTES  # ... whose routing scratch does not fit
-    dummy = torch.empty(16, dtype=torch.int32, device="cuda")
-    rc = M.moe_route_noalloc(big, dummy, dummy, dummy, dummy, dummy, dummy, check=False)
-    assert rc == M.ERR_CODE["MOE_ERR_WORKSPACE"]
+def test_noalloc_calls_reserve_no_device_memory():
+    """After one call (which may load the library's module on this device and
+    with it the static array), further calls leave the device's free memory
+    unchanged: they allocate nothing."""
+    T, d, E, k = 512, 1024, 64, 6
+    g = torch.Generator("cuda").manual_seed(5)
+    x = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
+    w_router = torch.randn((E, d), generator=g, device="cuda") / d ** 0.5
+    bias = torch.zeros((E,), device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    load = torch.empty((E,), dtype=torch.int32, device="cuda")
+    desc = M.make_desc(T, d, 128, E, k, "bf16")
+    M.moe_route_noalloc(desc, x, w_router, bias, idx, gates, load, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        M.moe_route_noalloc(desc, x, w_router, bias, idx, gates, load,
+                            torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert M.moe_last_error() == M.MOE_OK
+    assert free1 == free0
+    assert int(load.sum()) == T * k
