@@ -228,6 +228,40 @@ def cpu_oracle_sample(wl, inp, n_tokens, seed=0):
     return time.perf_counter() - t0
 
 
+def cpu_baseline_layer(wl, inp, n_rows=512, seed=0):
+    """The float64 oracle on the host cores, as the layer's measurement plan
+    asks: routing of all T tokens, then the outputs of n_rows seeded rows
+    (all rows when T <= n_rows), experts streamed from device memory one at
+    a time.  Returns the cpu_baseline object: value = sampled rows per second
+    of the whole layer (their share of the routing time plus their outputs)."""
+    from oracle import moe_oracle as O
+    cores = len(os.sched_getaffinity(0))
+    torch.set_num_threads(cores)
+    f64 = lambda t: t.detach().to("cpu").to(torch.float64).numpy()  # noqa: E731
+    x = f64(inp["x"])
+    wr, b = f64(inp["w_router"]), f64(inp["bias"])
+    t0 = time.perf_counter()
+    r = O.route(x, wr, b, wl.k)
+    t_route = time.perf_counter() - t0
+    n = min(n_rows, wl.T)
+    rows = (np.sort(np.random.default_rng(seed).choice(wl.T, n, replace=False))
+            if n < wl.T else np.arange(wl.T))
+    sh_dev = (inp["sh_gate"], inp["sh_up"], inp["sh_down"])
+    t1 = time.perf_counter()
+    sh = tuple(f64(w) for w in sh_dev)
+    O.expert_output_rows(x[rows], r["idx"][rows], r["gates"][rows],
+                         lambda e: (f64(inp["w_gate"][e]), f64(inp["w_up"][e]), f64(inp["w_down"][e])),
+                         sh)
+    t_out = time.perf_counter() - t1
+    per_row = t_route / wl.T + t_out / n
+    return {"value": 1.0 / per_row, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "routing_tokens_per_s": wl.T / t_route, "output_rows_per_s": n / t_out,
+            "sample": (f"float64 oracle on {wl.name}: routing of all {wl.T} tokens, then the "
+                       f"outputs of {n} seeded rows (shared expert and their {wl.k} routed "
+                       f"experts, weights streamed from device memory one expert at a time); "
+                       f"value = 1 / (routing time per token + output time per row)")}
+
+
 def run_reference(args, wl):
     ws, rank, local = _dist()
     if rank != 0:
@@ -257,6 +291,101 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None):
+    """`steps` forward passes back to back on `stream` with per-phase events
+    (moe_forward_profiled); flush: a buffer written before every step
+    (outside the per-step spans).  Returns (loop ms, per-step ms list, mean
+    phase ms array, clocks or None)."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(M.N_PHASE_EVENTS)]
+          for _ in range(steps)]
+    for row in ev:  # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        M.moe_forward_profiled(layer.desc, x, layer.w_router, layer.bias, layer.experts,
+                               layer.shared, layer.y, layer.topk_idx, layer.gates,
+                               layer.load_counts, layer.workspace, layer.ws_bytes, stream, ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    clocks = sampler.stop(t_host0, t_host1) if sampler else None
+    if M.moe_last_error() != M.MOE_OK:
+        raise RuntimeError("device error word set during the timed region")
+    per_step = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
+    loop_ms = start.elapsed_time(end) if flush is None else sum(per_step)
+    phase_ms = np.zeros(len(M.PHASES))
+    for i in range(steps):
+        for p in range(len(M.PHASES)):
+            phase_ms[p] += ev[i][p].elapsed_time(ev[i][p + 1])
+    return loop_ms, per_step, phase_ms / steps, clocks
+
+
+def _tensor_peak(peaks, clocks, fp8=False):
+    """Denominator of a tensor-core roofline: the measured burst bf16 figure
+    (times the nominal fp8/bf16 ratio 2 for e4m3 products).  The step loop
+    runs for a fraction of a second, so the burst figure applies; where the
+    clock record of the timed window shows the power cap, the fraction at
+    the sampled clock (peak x median SM MHz / max SM MHz) is given beside
+    it, not in its place."""
+    mult = 2.0 if fp8 else 1.0
+    peak = mult * peaks["bf16_tflops"]
+    kind = (f"{'2 x ' if fp8 else ''}{peaks['source']} bf16 burst"
+            + (" (nominal fp8/bf16 ratio)" if fp8 else ""))
+    scale = None
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz") and \
+            "sw_power_cap" in clocks.get("reasons", []):
+        scale = clocks["sm_mhz"] / clocks["sm_max_mhz"]
+    return peak, kind, scale
+
+
+def _decode_line(M, I, MoeLayer, name, args, peaks, local):
+    """One V3 decode workload (T = 128) timed as the main line is, reported
+    against the HBM roofline: the layer's algorithmic bytes (touched routed
+    experts + the shared expert, all three matrices; router weights; tokens
+    in and out) per step over the step time, and expert GEMM 1 alone."""
+    wl = I.WORKLOADS[name]
+    inp = I.make_inputs(wl, device="cuda")
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype)
+    stream = torch.cuda.current_stream()
+    x = inp["x"]
+    for _ in range(args.warmup):
+        layer.forward(x, stream)
+    torch.cuda.synchronize()
+    if M.moe_last_error() != M.MOE_OK:
+        raise RuntimeError("device error word set during warm-up")
+    load = layer.load_counts.cpu().numpy()
+    loop_ms, per_step, phase_ms, clocks = _timed_forward(M, layer, x, stream, args.steps, None,
+                                                         local)
+    touched = int((load > 0).sum())
+    expert_bytes = 3 * wl.d * wl.h * 2
+    layer_bytes = ((touched + 1) * expert_bytes + wl.E * wl.d * 4 + 2 * wl.T * wl.d * 2)
+    ms = loop_ms / args.steps
+    fl1, fl2, by1, by2, _ = _algorithmic(wl, load)
+    g1 = by1 / (phase_ms[2] / 1e3) / 1e9
+    layer_gbs = layer_bytes / (ms / 1e3) / 1e9
+    out = {"workload": name, "T": wl.T, "value": wl.T / (ms / 1e3), "unit": "tokens/s",
+           "ms_per_step": ms, "ms_per_step_median": statistics.median(per_step),
+           "touched_experts": touched,
+           "layer_bytes_per_step": layer_bytes, "layer_gbs": layer_gbs,
+           "frac": layer_gbs / peaks["hbm_gbs"],
+           "gemm1_gbs": g1, "gemm1_frac": g1 / peaks["hbm_gbs"],
+           "peak": peaks["hbm_gbs"], "peak_kind": f"{peaks['source']} HBM copy bandwidth",
+           "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
+           "gpu_launches": kernels_per_step(wl, False) * args.steps,
+           "clocks": clocks}
+    del layer, inp
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl):
     from sparse_moe_layer_fwd_b300 import inputs as I
     from sparse_moe_layer_fwd_b300 import moe as M
@@ -276,6 +405,7 @@ def run_ours(args, wl):
     layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else base_flags)
     stream = torch.cuda.current_stream()
     x = inp["x"]
+    fingerprint = I.fingerprint(inp) if rank == 0 else None
 
     def barrier():
         if ws > 1:
@@ -301,41 +431,12 @@ def run_ours(args, wl):
                f"inputs larger than L2 ({ws_bytes / 1e9:.1f} GB read per step)")
 
     # timed region: per-step phase events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(M.N_PHASE_EVENTS)]
-          for _ in range(args.steps)]
-    for row in ev:  # torch creates the CUDA event on its first record
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local) if rank == 0 else None
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    torch.cuda.synchronize()
-    t_host0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        M.moe_forward_profiled(layer.desc, x, layer.w_router, layer.bias, layer.experts,
-                               layer.shared, layer.y, layer.topk_idx, layer.gates,
-                               layer.load_counts, layer.workspace, layer.ws_bytes, stream, ev[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    t_host1 = time.time()
+    local_ms, per_step, phase_ms, clocks = _timed_forward(
+        M, layer, x, stream, args.steps, flush, local if rank == 0 else None)
     barrier()
-    clocks = sampler.stop(t_host0, t_host1) if sampler else None
-    if M.moe_last_error() != M.MOE_OK:
-        raise RuntimeError("device error word set during the timed region")
-    if flush is None:
-        local_ms = start.elapsed_time(end)
-    else:
-        local_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps))
     elapsed_ms, value = aggregate(local_ms, wl.T * args.steps, ws, "cuda")
-    phase_ms = np.zeros(len(M.PHASES))
-    for i in range(args.steps):
-        for p in range(len(M.PHASES)):
-            phase_ms[p] += ev[i][p].elapsed_time(ev[i][p + 1])
-    phase_ms /= args.steps
+    median_ms = statistics.median(per_step)
 
     # optional: the same steps replayed from one captured CUDA graph (no host
     # launches; the step is timed around each replay, L2 flushed as above)
@@ -392,7 +493,7 @@ def run_ours(args, wl):
             for j in range(nlay):
                 ends[j].record(streams[j])
             torch.cuda.synchronize()
-            local_ms = max(s0.elapsed_time(e) for e in ends)
+            e_local = max(s0.elapsed_time(e) for e in ends)
         else:
             s2 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
             e2 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -402,10 +503,10 @@ def run_ours(args, wl):
                 hls[0].forward_host_io(x_hosts[0], y_hosts[0], stream)
                 e2[i].record(stream)
             torch.cuda.synchronize()
-            local_ms = sum(s2[i].elapsed_time(e2[i]) for i in range(args.steps))
+            e_local = sum(s2[i].elapsed_time(e2[i]) for i in range(args.steps))
         if M.moe_last_error() != M.MOE_OK:
             raise RuntimeError("device error word set during the end-to-end run")
-        e2e_ms, e2e_value = aggregate(local_ms, wl.T * args.steps, ws, "cuda")
+        e2e_ms, e2e_value = aggregate(e_local, wl.T * args.steps, ws, "cuda")
         nb = x_hosts[0].numel() * x_hosts[0].element_size()
         e2e = {"value": e2e_value, "unit": "tokens/s",
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": 0 if route_only else nb,
@@ -419,6 +520,7 @@ def run_ours(args, wl):
         return
 
     peaks = _peaks()
+    meta = {"torch": torch.__version__, "inputs": fingerprint}
     if route_only:
         rflops = 2.0 * wl.T * wl.E * wl.d
         ach = rflops / (phase_ms[0] / 1e3) / 1e12
@@ -436,7 +538,8 @@ def run_ours(args, wl):
         line = {
             "metric": METRIC + " [routing only]", "value": wl.T * args.steps / (elapsed_ms / 1e3),
             "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": elapsed_ms / args.steps, "ms_per_step_median": median_ms,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 router, bf16 x" if wl.dtype == "bf16" else "f32",
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/d) router)",
             "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
@@ -448,7 +551,7 @@ def run_ours(args, wl):
             "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
             "e2e": e2e, "gpu_launches": kernels_per_step(wl, True) * args.steps,
             **({"cuda_graph": graph} if graph else {}),
-            "clocks": clocks,
+            "clocks": clocks, **meta,
         }
         print(json.dumps(line), flush=True)
         if ws > 1:
@@ -461,37 +564,23 @@ def run_ours(args, wl):
     sha = _kernel_sha()
     cap = NCU_TRAFFIC.get(wl.name + (":fp8" if fp8 else ""))  # GEMM 1 (gate/up)
     traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
-    if prefill_like and fp8:
-        # e4m3 codes on kind::f8f6f4: the fp8 dense peak is twice the bf16
-        # one (2.25 vs 4.5 PFLOP/s nominal), applied to the measured figure
+    if prefill_like:
         ach = fl1 / g1_s / 1e12
-        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        peak, kind, scale = _tensor_peak(peaks, clocks, fp8)
         roof = {"bound": "tensor",
-                "kernel": "k_expert_tc2 (GEMM 1 on e4m3 codes: gate/up + SwiGLU, CTA pairs)",
-                "achieved": ach, "peak": 2 * sus, "unit": "TFLOP/s",
-                "frac": ach / (2 * sus), "traffic": traffic,
-                "peak_kind": f"2 x {peaks['source']} bf16 sustained (nominal fp8/bf16 ratio)",
-                "frac_of_burst": ach / (2 * peaks["bf16_tflops"]),
+                "kernel": ("k_expert_tc2 (GEMM 1 on e4m3 codes: gate/up + SwiGLU, CTA pairs)"
+                           if fp8 else "k_expert_tc2 (GEMM 1: gate/up + SwiGLU, CTA pairs)"),
+                "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "traffic": traffic, "peak_kind": kind,
                 "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
+        if scale is not None:
+            roof["frac_at_sampled_clock"] = ach / (peak * scale)
         both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
-        layer_roof = {"expert_gemms_tflops": both}
-    elif prefill_like:
-        # GEMM 1 is timed inside the back-to-back step loop, under the power
-        # cap: its denominator is the sustained bf16 figure (burst beside it)
-        ach = fl1 / g1_s / 1e12
-        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
-        roof = {"bound": "tensor",
-                "kernel": "k_expert_tc2 (GEMM 1: gate/up + SwiGLU, CTA pairs)",
-                "achieved": ach, "peak": sus, "unit": "TFLOP/s",
-                "frac": ach / sus, "traffic": traffic,
-                "peak_kind": f"{peaks['source']} bf16 sustained (timed inside the step loop)",
-                "frac_of_burst": ach / peaks["bf16_tflops"],
-                "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
-        both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
-        layer_roof = {"expert_gemms_tflops": both,
-                      "frac_of_burst": both / peaks["bf16_tflops"],
-                      "frac_of_sustained": (both / peaks["bf16_tflops_sustained"]
-                                            if peaks.get("bf16_tflops_sustained") else None)}
+        layer_roof = {"expert_gemms_tflops": both, "frac": both / peak,
+                      "gemm2_tflops": fl2 / g2_s / 1e12, "gemm2_frac": fl2 / g2_s / 1e12 / peak,
+                      "gemm2_gbs": by2 / g2_s / 1e9}
+        if scale is not None:
+            layer_roof["frac_at_sampled_clock"] = both / (peak * scale)
     else:
         ach = by1 / g1_s / 1e9
         roof = {"bound": "hbm",
@@ -507,17 +596,22 @@ def run_ours(args, wl):
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
-        cores = len(os.sched_getaffinity(0))
-        torch.set_num_threads(cores)
-        n = args.ref_tokens
-        secs = cpu_oracle_sample(wl, inp, n)
-        cpu = {"value": n / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} tokens of {wl.name}: float64 routing, shared expert and "
-                         f"{wl.k} routed experts per token, weights streamed from device memory"}
+        cpu = cpu_baseline_layer(wl, inp, n_rows=args.cpu_rows)
+
+    # the V3 decode layer (balanced and Zipf-skewed routing), measured in the
+    # same process after the main workload, against the HBM roofline
+    decode = None
+    if wl.name == "v3_prefill" and not fp8 and not args.no_decode and ws == 1:
+        del layer
+        inp = None
+        torch.cuda.empty_cache()
+        decode = [_decode_line(M, I, MoeLayer, n, args, peaks, local)
+                  for n in ("v3_decode", "v3_decode_zipf")]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "ms_per_step_median": median_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3 experts (per-row scales)" if fp8_down else
                   "e4m3 gate/up (per-row scales), bf16 down" if fp8 else "bf16"),
@@ -529,7 +623,8 @@ def run_ours(args, wl):
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
         "cpu_baseline": cpu, "e2e": e2e, **({"cuda_graph": graph} if graph else {}),
         "gpu_launches": (kernels_per_step(wl, False, fp8) + int(fp8_down)) * args.steps,
-        "clocks": clocks, "kernel_sha": sha,
+        **({"decode": decode} if decode else {}),
+        "clocks": clocks, "kernel_sha": sha, **meta,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -545,7 +640,7 @@ CONFIGS = {"C0": "tiny_fp32", "C1": "mini_bf16", "C2": "bias_dynamics", "C3": "v
 def run_train(args, wl):
     """Training step: forward (with the backward's buffers) and backward for
     a fixed output gradient, timed together; reports tokens/s of the step,
-    the two phases, and the backward's GEMM FLOPs against the sustained bf16
+    the two phases, and the backward's GEMM FLOPs against the burst bf16
     peak (12 d h FLOP per routed pair or shared-expert token: dH, dX and the
     three weight gradients; the recomputed gate/up products are not counted)."""
     from sparse_moe_layer_fwd_b300 import inputs as I
@@ -590,7 +685,7 @@ def run_train(args, wl):
     rows = wl.T * wl.k + wl.T
     bflops = 12.0 * rows * wl.d * wl.h
     bwd_ms = bwd / args.steps
-    sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    peak, kind, scale = _tensor_peak(peaks, clocks)
     ach = bflops / (bwd_ms / 1e3) / 1e12
     line = {
         "metric": METRIC + " [training step: forward + backward]", "value": value,
@@ -605,10 +700,10 @@ def run_train(args, wl):
         # dH, SwiGLU gradient, dX, three weight gradients, dW_r, dx)
         "gpu_launches": (kernels_per_step(wl, False) + 12) * args.steps,
         "roofline": {"bound": "tensor", "kernel": "backward (dH, dX, weight-gradient GEMMs)",
-                     "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
-                     "traffic": None,
-                     "peak_kind": f"{peaks['source']} bf16 sustained; 12 d h FLOP per row",
-                     "flops_per_launch": bflops, "ms_per_launch": bwd_ms},
+                     "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                     "traffic": None, "peak_kind": f"{kind}; 12 d h FLOP per row",
+                     "flops_per_launch": bflops, "ms_per_launch": bwd_ms,
+                     **({"frac_at_sampled_clock": ach / (peak * scale)} if scale else {})},
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -679,6 +774,10 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="output rows the CPU oracle computes for cpu_baseline")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the V3 decode runs that follow the V3 prefill line")
     ap.add_argument("--train", action="store_true",
                     help="time a training step: forward and backward")
     ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "experts"],

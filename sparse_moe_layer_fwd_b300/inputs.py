@@ -181,3 +181,26 @@ def custom(T, d, h, E, k, dtype="bf16", seed=0, bias="uniform", skew="none",
     """A workload with arbitrary sizes (edge cases, ragged tails)."""
     return Workload(name or f"custom_T{T}_d{d}_h{h}_E{E}_k{k}_{dtype}",
                     T, d, h, E, k, dtype, seed, bias=bias, skew=skew)
+
+
+def fingerprint(inputs: dict, weight_row_stride: int = 64) -> dict:
+    """SHA-256 of a workload's inputs as they sit in memory: every byte of x,
+    W_r and b, and every ``weight_row_stride``-th row of each expert weight
+    matrix (the V3 weights are 22.5 GB; a strided sample keeps this fast).
+    Returns {"sha256": hex digest, "scope": what was hashed}."""
+    import hashlib
+    h = hashlib.sha256()
+
+    def add(t):
+        h.update(t.detach().contiguous().view(torch.uint8).cpu().numpy().tobytes())
+
+    for name in ("x", "w_router", "bias"):
+        add(inputs[name])
+    have_w = "w_gate" in inputs
+    if have_w:
+        for name in ("w_gate", "w_up", "w_down", "sh_gate", "sh_up", "sh_down"):
+            w = inputs[name]
+            add(w.reshape(-1, w.shape[-1])[::weight_row_stride])
+    scope = "x, W_r, b in full" + (
+        f"; every {weight_row_stride}th row of each expert weight matrix" if have_w else "")
+    return {"sha256": h.hexdigest(), "scope": scope}

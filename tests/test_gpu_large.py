@@ -63,16 +63,21 @@ def test_v3_prefill_full_size():
     stats, flips, touched = _check_v3("v3_prefill", 512)
     print(f"v3_prefill: {stats} flips={flips} touched={touched}")
     assert touched == 256
+    # the kernels are deterministic, so this seed's selection is fixed: it
+    # matches the oracle's on every token, with no tolerated near-tie flip
+    assert flips == 0
 
 
 def test_v3_decode_balanced():
     stats, flips, touched = _check_v3("v3_decode", 128)
     print(f"v3_decode: {stats} flips={flips} touched={touched}")
+    assert flips == 0
 
 
 def test_v3_decode_zipf_skew():
     stats, flips, touched = _check_v3("v3_decode_zipf", 128)
     print(f"v3_decode_zipf: {stats} flips={flips} touched={touched}")
+    assert flips == 0
     # the skew concentrates routing on fewer experts than the balanced run
     assert touched < 200
 
@@ -128,6 +133,7 @@ def test_v3_prefill_backward_sampled():
                                 np64(dy[rt]), idx_override=idx[rows])
     got = np64(g["dx"][rt])
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 1e-2
+    assert np.abs(got - ref).max() <= 5e-2 * np.sqrt(np.mean(ref * ref))
     # the least-loaded expert's weight gradients from its own tokens
     load = np.bincount(idx.ravel(), minlength=wl.E)
     e = int(np.argmin(np.where(load > 0, load, load.max() + 1)))
@@ -140,3 +146,4 @@ def test_v3_prefill_backward_sampled():
     for name, ref_w in (("dW_gate", dwg), ("dW_up", dwu), ("dW_down", dwd)):
         got_w = np64(g[name][e])
         assert np.linalg.norm(got_w - ref_w) / np.linalg.norm(ref_w) < 1e-2, name
+        assert np.abs(got_w - ref_w).max() <= 5e-2 * np.sqrt(np.mean(ref_w * ref_w)), name
