@@ -76,6 +76,20 @@ as a source, uses the same):
                layer's activation type (round to nearest even), before it
                is quantized.
 
+11. fp8 block-scaled experts (the official model's tile granularity; a
+               B300-native option, not on the pages): every expert weight
+               matrix is cut into 128 x 128 blocks (128 output rows x 128
+               inputs) and every activation row into 1 x 128 blocks (the
+               tokens for gate/up; for the down projection the hidden row H
+               of each (token, expert) pair and of the shared expert).  A
+               block with largest magnitude amax gets the scale 2^e, e the
+               smallest integer with amax <= 448 * 2^e (e = 0 for a block of
+               zeros or one whose maximum is not finite; e clamped to
+               [-127, 127]); code = e4m3(v / 2^e), nearest, ties to even
+               (NaN stays NaN, +-inf becomes +-448).  The named products run
+               on the dequantized values code * 2^e.  H is quantized from its
+               unrounded value (nothing rounds it to bf16 first).
+
 ``moe_forward_dense`` is the pages' own formulation (every expert on every
 token, then masked).  ``moe_forward_sparse`` evaluates only the selected
 experts; tests pin it to the dense formulation on small inputs, and it is the
@@ -468,3 +482,110 @@ def fp8_gate_up_rows(x_rows, idx_rows, gate_rows, get_expert, shared):
     return expert_output_rows(xq, idx_rows, gate_rows, lambda e: quantized(get_expert(e)),
                               quantized(shared))
 
+
+
+# --------------------------------------------------------------------------
+# 11. fp8 (e4m3) block-scaled quantization
+# --------------------------------------------------------------------------
+def e4m3_round(v):
+    """Nearest e4m3 value of each element (ties to the even code), float64 in
+    and out, written from the format: 3 mantissa bits, so a value in
+    [2^k, 2^(k+1)) (k >= -6) sits on a grid of step 2^(k-3); below 2^-6 the
+    subnormal grid has step 2^-9; the largest finite value is 448.  NaN
+    stays NaN; magnitudes above 448 (infinities included) become 448."""
+    v = np.asarray(v, dtype=F64)
+    out = np.full(v.shape, np.nan)
+    fin = ~np.isnan(v)
+    a = np.minimum(np.abs(v[fin]), 448.0)
+    _, ex = np.frexp(a)                     # a = f * 2^ex, 0.5 <= f < 1
+    k = np.maximum(ex - 1, -6)              # binade [2^k, 2^(k+1)), subnormals at k = -6
+    step_exp = k - 3
+    q = np.rint(np.ldexp(a, -step_exp))     # exact scaling; rint rounds half to even
+    r = np.minimum(np.ldexp(q, step_exp), 448.0)
+    out[fin] = np.copysign(r, v[fin])
+    return out
+
+
+def e4m3_code(v):
+    """Code bits (uint8) of values that are already e4m3 values (output of
+    e4m3_round): sign, 4 exponent bits (bias 7), 3 mantissa bits; NaN 0x7f."""
+    v = np.asarray(v, dtype=F64)
+    codes = np.zeros(v.shape, dtype=np.uint8)
+    nan = np.isnan(v)
+    a = np.abs(np.where(nan, 0.0, v))
+    sign = (np.signbit(v) & ~nan).astype(np.uint8) << 7
+    _, ex = np.frexp(a)
+    k = ex - 1
+    normal = a >= 2.0 ** -6
+    e_field = np.where(normal, k + 7, 0)
+    mant = np.where(normal, np.ldexp(a, -k) - 1.0, np.ldexp(a, 6)) * 8.0
+    codes = (sign | (e_field.astype(np.uint8) << 3) | np.rint(mant).astype(np.uint8))
+    codes = np.where(a == 0, sign, codes).astype(np.uint8)
+    return np.where(nan, np.uint8(0x7F), codes).astype(np.uint8)
+
+
+def block_exponent(amax):
+    """Exponent e of a block's scale 2^e (reading 11): the smallest integer
+    with amax <= 448 * 2^e; 0 where amax is 0 or not finite; clamped to
+    [-127, 127]."""
+    amax = np.asarray(amax, dtype=F64)
+    e = np.zeros(amax.shape, dtype=np.int64)
+    ok = np.isfinite(amax) & (amax > 0)
+    a = amax[ok]
+    guess = np.ceil(np.log2(a / 448.0)).astype(np.int64)
+    # settle the guess exactly against 448 * 2^e (exact in float64)
+    guess = np.where(a > np.ldexp(448.0, guess), guess + 1, guess)
+    guess = np.where(a <= np.ldexp(448.0, guess - 1), guess - 1, guess)
+    e[ok] = np.clip(guess, -127, 127)
+    return e
+
+
+def quantize_blocks_e4m3(a, block_rows: int):
+    """Block-scaled e4m3 quantization of a [R, C] (reading 11): blocks of
+    block_rows x 128 (block_rows = 128 for weights, 1 for activation rows);
+    R a multiple of block_rows, C a multiple of 128.  Returns (codes uint8
+    [R, C], exponents int64 [R / block_rows, C / 128], dequantized float64
+    [R, C])."""
+    a = np.asarray(a, dtype=F64)
+    R, C = a.shape
+    assert R % block_rows == 0 and C % 128 == 0
+    blk = a.reshape(R // block_rows, block_rows, C // 128, 128)
+    amax = np.max(np.abs(blk), axis=(1, 3))             # NaN if the block holds a NaN
+    e = block_exponent(amax)
+    scaled = blk * np.ldexp(1.0, -e)[:, None, :, None]  # exact: a power of two
+    deq_codes = e4m3_round(scaled)
+    codes = e4m3_code(deq_codes).reshape(R, C)
+    deq = (deq_codes * np.ldexp(1.0, e)[:, None, :, None]).reshape(R, C)
+    return codes, e, deq
+
+
+def fp8_block_swiglu_expert(x, w_gate, w_up, w_down, gate_up: bool, down: bool):
+    """One expert under reading 11: gate/up on the block-dequantized tokens
+    and weights if ``gate_up``; H (unrounded) and W_down block-dequantized
+    before the down projection if ``down``."""
+    x = _f64(x)
+    if gate_up:
+        xq = quantize_blocks_e4m3(x, 1)[2]
+        g = xq @ quantize_blocks_e4m3(w_gate, 128)[2].T
+        u = xq @ quantize_blocks_e4m3(w_up, 128)[2].T
+    else:
+        g, u = x @ _f64(w_gate).T, x @ _f64(w_up).T
+    hid = silu(g) * u
+    if down:
+        return quantize_blocks_e4m3(hid, 1)[2] @ quantize_blocks_e4m3(w_down, 128)[2].T
+    return hid @ _f64(w_down).T
+
+
+def fp8_block_expert_rows(x_rows, idx_rows, gate_rows, get_expert, shared, gate_up: bool,
+                          down: bool):
+    """Layer output for sampled rows under reading 11 (``gate_up``, ``down``:
+    which products are block-scaled e4m3); arguments as expert_output_rows,
+    the selection and gates coming from the unquantized routing."""
+    x_rows = _f64(x_rows)
+    y = fp8_block_swiglu_expert(x_rows, *shared, gate_up, down)
+    idx_rows = np.asarray(idx_rows)
+    for e in np.unique(idx_rows):
+        tt, jj = np.nonzero(idx_rows == e)
+        ye = fp8_block_swiglu_expert(x_rows[tt], *get_expert(int(e)), gate_up, down)
+        y[tt] += gate_rows[tt, jj][:, None] * ye
+    return y

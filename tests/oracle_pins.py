@@ -641,6 +641,181 @@ def pin_fp8_down(O):
     assert np.allclose(rows[2:3], one, rtol=1e-12)
 
 
+def pin_e4m3_round(O):
+    """e4m3 rounding written from the format: every finite e4m3 value is kept
+    with the format's own code; the midpoint of two neighbours goes to the
+    one with the even code; fp32 values agree with PyTorch's float8_e4m3fn
+    conversion (a separate implementation); NaN stays NaN, infinities and
+    magnitudes above 448 become +-448."""
+    grid = _e4m3_values()
+    codes = np.array([c for c, _ in grid], dtype=np.uint8)
+    vals = np.array([v for _, v in grid])
+    assert np.array_equal(O.e4m3_round(vals), vals)
+    assert np.array_equal(O.e4m3_code(vals[vals != 0]), codes[vals != 0])
+    pos = sorted({v for _, v in grid if v >= 0})
+    code_of = {v: c for c, v in grid if v >= 0 and not (v == 0 and c)}
+    for lo, hi in zip(pos[:-1], pos[1:]):
+        even = lo if code_of[lo] % 2 == 0 else hi
+        assert O.e4m3_round(np.array([(lo + hi) / 2]))[0] == even, (lo, hi)
+        assert O.e4m3_round(np.array([-(lo + hi) / 2]))[0] == -even
+    import torch
+    rng = np.random.default_rng(47)
+    v = (rng.normal(size=20000) * np.exp2(rng.integers(-14, 8, size=20000))).astype(np.float32)
+    v = np.clip(v, -448, 448).astype(np.float64)
+    ref = torch.tensor(v, dtype=torch.float32).to(torch.float8_e4m3fn)
+    assert np.array_equal(O.e4m3_round(v), ref.to(torch.float64).numpy())
+    assert np.array_equal(O.e4m3_code(O.e4m3_round(v)), ref.view(torch.uint8).numpy())
+    sp = O.e4m3_round(np.array([np.nan, np.inf, -np.inf, 1e6, -500.0]))
+    assert np.isnan(sp[0]) and list(sp[1:]) == [448.0, -448.0, 448.0, -448.0]
+
+
+def pin_block_exponent(O):
+    """The block scale exponent: 448 * 2^(e-1) < amax <= 448 * 2^e, checked by
+    brute force over e; exact boundaries; 0 for zero or non-finite blocks;
+    clamped to the UE8M0 range [-127, 127]."""
+    rng = np.random.default_rng(48)
+    amax = np.abs(rng.normal(size=4000)) * np.exp2(rng.integers(-60, 60, size=4000))
+    e = O.block_exponent(amax)
+    for a, ee in zip(amax, e):
+        cand = [k for k in range(-130, 130) if a <= 448.0 * 2.0 ** k]
+        assert ee == min(cand), (a, ee)
+    edge = np.array([448.0, 448.0 * (1 + 2.0 ** -52), 224.0, 224.0 * (1 + 2.0 ** -52), 1.0,
+                     448.0 * 2.0 ** -20, 0.0, np.inf, np.nan, 1e-45, 2.0 ** 140])
+    assert list(O.block_exponent(edge)) == [0, 1, -1, 0, -8, -20, 0, 0, 0, -127, 127]
+
+
+def _block_grid_matrix(rng, R, C, br, lo=-9, hi=-3):
+    """A matrix on the block grid: every br x 128 block is e4m3 values times
+    2^e_block with one element of magnitude in (224, 448], so block
+    quantization keeps it exactly with exponents e_block."""
+    grid = np.array([v for _, v in _e4m3_values() if abs(v) <= 448.0])
+    nb_r, nb_c = R // br, C // 128
+    e = rng.integers(lo, hi, size=(nb_r, nb_c))
+    a = rng.choice(grid[np.abs(grid) < 224], size=(nb_r, br, nb_c, 128))
+    a[:, 0, :, 0] = rng.choice([-448.0, 320.0, 240.0, -256.0], size=(nb_r, nb_c))
+    a = a * np.ldexp(1.0, e)[:, None, :, None]
+    return a.reshape(R, C), e
+
+
+def pin_quantize_blocks(O):
+    """Block quantization: a matrix on the block grid is kept exactly with
+    its exponents; blocks are independent (changing one block changes only
+    its own codes and exponent); scaling one block by 2^j shifts its
+    exponent by j and keeps its codes; the error of every normal value is at
+    most 2^-4 of it; a block with a NaN gets exponent 0 and a NaN code only
+    where the NaN is."""
+    rng = np.random.default_rng(49)
+    for br in (128, 1):
+        R = 256 if br == 128 else 6
+        a, e = _block_grid_matrix(rng, R, 384, br)
+        q, eq, deq = O.quantize_blocks_e4m3(a, br)
+        assert np.array_equal(deq, a) and np.array_equal(eq, e)
+        b = a.copy()
+        b[:br, 128:256] *= 2.0 ** 5
+        b[br:2 * br, 256:384] = rng.normal(size=(br, 128))
+        qb, eb, _ = O.quantize_blocks_e4m3(b, br)
+        assert eb[0, 1] == e[0, 1] + 5 and np.array_equal(qb[:br, 128:256], q[:br, 128:256])
+        same = np.ones_like(q, dtype=bool)
+        same[br:2 * br, 256:384] = False
+        assert np.array_equal(qb[same], q[same])
+        diff_e = np.ones_like(e, dtype=bool)
+        diff_e[0, 1] = diff_e[1, 2] = False
+        assert np.array_equal(eb[diff_e], e[diff_e])
+    x = rng.normal(size=(5, 256)) * np.exp2(rng.integers(-8, 8, size=(5, 1)))
+    _, ex, dx = O.quantize_blocks_e4m3(x, 1)
+    scale = np.repeat(np.ldexp(1.0, ex), 128, axis=1)
+    normal = np.abs(x) >= 2.0 ** -6 * scale
+    assert np.all(np.abs(dx - x)[normal] <= 2.0 ** -4 * np.abs(x)[normal])
+    assert np.all(np.abs(dx - x)[~normal] <= 2.0 ** -10 * scale[~normal])
+    y = x.copy()
+    y[2, 130] = np.nan
+    qy, ey, dy = O.quantize_blocks_e4m3(y, 1)
+    assert ey[2, 1] == 0 and qy[2, 130] == 0x7F and np.isnan(dy[2, 130])
+    assert np.isfinite(np.delete(dy[2], 130)).all()
+
+
+def _nearest_e4m3_times(v, e):
+    """Brute force: the e4m3 grid value times 2^e nearest to v, ties to the
+    even code (independent of the oracle's rounding arithmetic)."""
+    grid = _e4m3_values()
+    best = None
+    for c, g in grid:
+        w = g * 2.0 ** e
+        d = abs(w - v)
+        if best is None or d < best[0] or (d == best[0] and c % 2 == 0 and best[1] % 2 == 1):
+            best = (d, c, w)
+    return best[2]
+
+
+def _brute_block_quant(a, br):
+    """Block quantization by brute force: each br x 128 block's exponent by
+    search over e, each element the nearest grid value times 2^e (ties to
+    the even code)."""
+    grid = _e4m3_values()
+    gv = np.array([g for _, g in grid])
+    gc = np.array([c for c, _ in grid])
+    out = np.empty_like(a)
+    for r0 in range(0, a.shape[0], br):
+        for c0 in range(0, a.shape[1], 128):
+            blk = a[r0:r0 + br, c0:c0 + 128]
+            amax = np.abs(blk).max()
+            e = min(kk for kk in range(-130, 130) if amax <= 448.0 * 2.0 ** kk)
+            cand = gv * 2.0 ** e
+            dist = np.abs(blk[..., None] - cand)
+            best = dist.min(axis=-1, keepdims=True)
+            ties = dist == best
+            pick = np.where(ties & (gc % 2 == 0), 0, 1) + np.where(ties, 0, 2)
+            out[r0:r0 + br, c0:c0 + 128] = cand[np.argmin(pick, axis=-1)]
+    return out
+
+
+def pin_fp8_block_layer(O):
+    """The block-scaled layer: with tokens and weights on the block grid the
+    gate/up products are exact (the layer IS the unquantized layer when the
+    down projection is not quantized); with the down projection quantized,
+    each hidden row's 128-unit blocks are rounded by brute force to the
+    nearest grid point at the block's exponent, from the unrounded H; the
+    shared expert and the gates enter as in the unquantized layer."""
+    rng = np.random.default_rng(50)
+    T, d, h, E, k = 3, 256, 256, 3, 2
+    x, _ = _block_grid_matrix(rng, T, d, 1)
+    ex = [(_block_grid_matrix(rng, h, d, 128)[0], _block_grid_matrix(rng, h, d, 128)[0],
+           _block_grid_matrix(rng, d, h, 128)[0]) for _ in range(E)]
+    sh = (_block_grid_matrix(rng, h, d, 128)[0], _block_grid_matrix(rng, h, d, 128)[0],
+          rng.normal(size=(d, h)) * 0.05)
+    idx = np.array([[0, 2], [1, 0], [2, 1]])
+    gates = rng.uniform(0.2, 1.0, size=(T, k))
+    got = O.fp8_block_expert_rows(x, idx, gates, lambda e: ex[e], sh, gate_up=True, down=False)
+    ref = O.expert_output_rows(x, idx, gates, lambda e: ex[e], sh)
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-13 * np.abs(ref).max())
+    # the down projection: H from the exact gate/up products, never rounded
+    wg, wu, wd = ex[1]
+    hid = O.silu(x @ wg.T) * (x @ wu.T)
+    hq = np.empty_like(hid)
+    for r in range(T):
+        for b in range(h // 128):
+            seg = hid[r, 128 * b:128 * (b + 1)]
+            amax = np.abs(seg).max()
+            e = min(kk for kk in range(-130, 130) if amax <= 448.0 * 2.0 ** kk)
+            hq[r, 128 * b:128 * (b + 1)] = [_nearest_e4m3_times(v, e) for v in seg]
+    y_ref = hq @ wd.T  # wd is on the block grid: kept exactly
+    y = O.fp8_block_swiglu_expert(x, wg, wu, wd, gate_up=True, down=True)
+    assert np.allclose(y, y_ref, rtol=1e-13, atol=1e-13 * np.abs(y_ref).max())
+    assert not np.allclose(y, hid @ wd.T, rtol=1e-6)
+    # neither product quantized: the textbook expert
+    assert np.array_equal(O.fp8_block_swiglu_expert(x, wg, wu, wd, gate_up=False, down=False),
+                          O.swiglu_expert(x, wg, wu, wd))
+    # operands off the grid: every operand block-quantized by brute force
+    xr = rng.normal(size=(2, 128))
+    wr = [rng.normal(size=(128, 128)) * 0.09 for _ in range(3)]
+    qx = _brute_block_quant(xr, 1)
+    qw = [_brute_block_quant(w, 128) for w in wr]
+    hid = O.silu(qx @ qw[0].T) * (qx @ qw[1].T)
+    y_ref = _brute_block_quant(hid, 1) @ qw[2].T
+    y = O.fp8_block_swiglu_expert(xr, *wr, gate_up=True, down=True)
+    assert np.allclose(y, y_ref, rtol=1e-12, atol=1e-12 * np.abs(y_ref).max())
+
+
 PINS = [
     pin_routing_golden,
     pin_topk_bruteforce,
@@ -663,4 +838,8 @@ PINS = [
     pin_quantize_e4m3,
     pin_fp8_gate_up,
     pin_fp8_down,
+    pin_e4m3_round,
+    pin_block_exponent,
+    pin_quantize_blocks,
+    pin_fp8_block_layer,
 ]

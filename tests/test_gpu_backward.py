@@ -3,9 +3,15 @@
 The oracle (pinned by finite differences of the forward oracle) is evaluated
 on the GPU's own selection, so a tolerated near-tie flip cannot make the two
 differ.  Every gradient -- tokens, routed and shared expert weights, router
-weights -- is compared with relative L2 error below 1e-2 and, element by
-element, max |diff| <= 5e-2 * rms(reference) (the layer's bf16 bar: the
-backward rounds g*dy, dH and dA|dB to bf16 and accumulates in fp32).
+weights -- is compared with relative L2 error below 1e-2 (the layer's bf16
+bar: the backward rounds g*dy, dH and dA|dB to bf16 and accumulates in
+fp32), and locally: every row (one output unit of one expert, one token of
+dx, one expert of dW_r) within 3e-2 of the larger of its reference row's
+norm and the tensor's typical row norm, and dx element by element within
+5e-2 * rms(reference).  (A weight-gradient element of an expert with a
+handful of tokens is a sum of a few products of heavy-tailed factors, so
+its largest elements sit far above the tensor's rms; a per-row bound
+catches a localised error without that bias.)
 Shapes cover ragged token tiles, experts that no token selected (their
 gradients must be exactly zero), partial 256-row blocks of the weight
 gradients, and several token tiles per expert.
@@ -23,6 +29,7 @@ from tests.parity import np64, npi
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
 MAX_ABS_RMS = 5e-2
+ROW_TOL = 3e-2
 
 SHAPES = [
     dict(T=300, d=256, h=256, E=8, k=2),
@@ -45,6 +52,24 @@ def _max_abs_over_rms(a, b):
     return mx / rms if rms > 0 else (0.0 if mx == 0 else np.inf)
 
 
+def _worst_row(a, b):
+    """Largest row error of a gradient (rows along the last axis), each row's
+    error measured against the larger of its own reference norm and the rms
+    of the tensor's non-zero reference row norms: a wrong row shows up at
+    any size, while a row whose reference nearly cancels (a few tokens whose
+    upstream gradient is close to zero) is held to the tensor's scale rather
+    than to its own.  Rows whose reference is zero must be exactly zero."""
+    a2, b2 = a.reshape(-1, a.shape[-1]), b.reshape(-1, b.shape[-1])
+    nb = np.linalg.norm(b2, axis=1)
+    nd = np.linalg.norm(a2 - b2, axis=1)
+    zero = nb == 0
+    assert np.all(nd[zero] == 0), "non-zero gradient where the reference is zero"
+    if not (~zero).any():
+        return 0.0
+    typical = np.sqrt(np.mean(nb[~zero] ** 2))
+    return float((nd[~zero] / np.maximum(nb[~zero], typical)).max())
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"T{s['T']}_d{s['d']}_h{s['h']}_E{s['E']}_k{s['k']}" for s in SHAPES])
 def test_backward_matches_oracle(shape):
     wl = I.custom(dtype="bf16", seed=7 + shape["T"], **shape)
@@ -64,8 +89,9 @@ def test_backward_matches_oracle(shape):
     errs = {n: _rel(np64(g[n]), ref[n]) for n in
             ["dx", "dW_gate", "dW_up", "dW_down", "dsh_gate", "dsh_up", "dsh_down", "dW_router"]}
     assert all(v < TOL for v in errs.values()), errs
-    peaks = {n: _max_abs_over_rms(np64(g[n]), ref[n]) for n in errs}
-    assert all(v <= MAX_ABS_RMS for v in peaks.values()), peaks
+    rows = {n: _worst_row(np64(g[n]), ref[n]) for n in errs}
+    assert all(v <= ROW_TOL for v in rows.values()), rows
+    assert _max_abs_over_rms(np64(g["dx"]), ref["dx"]) <= MAX_ABS_RMS
     empty = np.setdiff1d(np.arange(wl.E), np.unique(idx))
     for n in ["dW_gate", "dW_up", "dW_down"]:
         assert np.all(np64(g[n])[empty] == 0.0)

@@ -146,4 +146,8 @@ def test_v3_prefill_backward_sampled():
     for name, ref_w in (("dW_gate", dwg), ("dW_up", dwu), ("dW_down", dwd)):
         got_w = np64(g[name][e])
         assert np.linalg.norm(got_w - ref_w) / np.linalg.norm(ref_w) < 1e-2, name
-        assert np.abs(got_w - ref_w).max() <= 5e-2 * np.sqrt(np.mean(ref_w * ref_w)), name
+        # every row (one output unit) within 3e-2 of the larger of its
+        # reference norm and the matrix's typical row norm
+        nb = np.linalg.norm(ref_w, axis=1)
+        row_err = np.linalg.norm(got_w - ref_w, axis=1) / np.maximum(nb, np.sqrt(np.mean(nb ** 2)))
+        assert row_err.max() <= 3e-2, (name, float(row_err.max()))

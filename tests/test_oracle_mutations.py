@@ -334,6 +334,120 @@ def _fp8_rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared, down, gat
                                     shared, down, gate_up)
 
 
+def _e4m3_round_half_away(v):
+    v = np.asarray(v, dtype=F64)
+    out = np.full(v.shape, np.nan)
+    fin = ~np.isnan(v)
+    a = np.minimum(np.abs(v[fin]), 448.0)
+    _, ex = np.frexp(a)
+    k = np.maximum(ex - 1, -6) - 3
+    q = np.floor(np.ldexp(a, -k) + 0.5)  # halves away from zero
+    out[fin] = np.copysign(np.minimum(np.ldexp(q, k), 448.0), v[fin])
+    return out
+
+
+def _e4m3_round_truncate(v):
+    v = np.asarray(v, dtype=F64)
+    out = np.full(v.shape, np.nan)
+    fin = ~np.isnan(v)
+    a = np.minimum(np.abs(v[fin]), 448.0)
+    _, ex = np.frexp(a)
+    k = np.maximum(ex - 1, -6) - 3
+    out[fin] = np.copysign(np.ldexp(np.floor(np.ldexp(a, -k)), k), v[fin])
+    return out
+
+
+def _e4m3_round_two_bits(v):
+    v = np.asarray(v, dtype=F64)
+    out = np.full(v.shape, np.nan)
+    fin = ~np.isnan(v)
+    a = np.minimum(np.abs(v[fin]), 448.0)
+    _, ex = np.frexp(a)
+    k = np.maximum(ex - 1, -6) - 2  # a 2-bit mantissa
+    out[fin] = np.copysign(np.ldexp(np.rint(np.ldexp(a, -k)), k), v[fin])
+    return out
+
+
+def _blockexp_floor(amax):
+    e = _ORIG["block_exponent"](amax)
+    return np.where(np.asarray(amax) > 0, e - 1, e)
+
+
+def _blockexp_wrong_max(amax):
+    amax = np.asarray(amax, dtype=F64)
+    return _ORIG["block_exponent"](amax * (448.0 / 240.0))
+
+
+def _blockexp_unclamped_nan(amax):
+    amax = np.asarray(amax, dtype=F64)
+    e = np.zeros(amax.shape, dtype=np.int64)
+    ok = amax > 0
+    e[ok] = np.ceil(np.log2(amax[ok] / 448.0)).astype(np.int64)
+    return e
+
+
+def _qblocks_64_wide(a, block_rows):
+    a = np.asarray(a, dtype=F64)
+    R, C = a.shape
+    parts = [_ORIG["quantize_blocks_e4m3"](np.repeat(a[:, j:j + 64], 2, axis=1)[:, :128],
+                                           block_rows) for j in range(0, C, 64)]
+    codes = np.concatenate([p[0][:, :64] for p in parts], axis=1)
+    deq = np.concatenate([p[2][:, :64] for p in parts], axis=1)
+    e = _ORIG["quantize_blocks_e4m3"](a, block_rows)[1]
+    return codes, e, deq
+
+
+def _qblocks_rows_only(a, block_rows):
+    return _ORIG["quantize_blocks_e4m3"](a, 1)
+
+
+def _qblocks_whole_row(a, block_rows):
+    a = np.asarray(a, dtype=F64)
+    R, C = a.shape
+    amax = np.abs(a.reshape(R // block_rows, block_rows * C)).max(axis=1)
+    e = _ORIG["block_exponent"](amax)
+    sc = np.repeat(np.ldexp(1.0, e), block_rows)[:, None]
+    dq = _ORIG["e4m3_round"](a / sc)
+    return _ORIG["e4m3_code"](dq), np.repeat(e[:, None], C // 128, axis=1), dq * sc
+
+
+def _fp8_block_h_rounded_bf16(x, w_gate, w_up, w_down, gate_up, down):
+    q = _ORIG["quantize_blocks_e4m3"]
+    x = np.asarray(x, dtype=F64)
+    if gate_up:
+        xq = q(x, 1)[2]
+        g, u = xq @ q(w_gate, 128)[2].T, xq @ q(w_up, 128)[2].T
+    else:
+        g, u = x @ np.asarray(w_gate, F64).T, x @ np.asarray(w_up, F64).T
+    hid = _ORIG["round_bf16"](_ORIG["silu"](g) * u)
+    if down:
+        return q(hid, 1)[2] @ q(w_down, 128)[2].T
+    return hid @ np.asarray(w_down, F64).T
+
+
+def _fp8_block_down_ignored(x, w_gate, w_up, w_down, gate_up, down):
+    return _ORIG["fp8_block_swiglu_expert"](x, w_gate, w_up, w_down, gate_up, False)
+
+
+def _fp8_block_weights_unquantized(x, w_gate, w_up, w_down, gate_up, down):
+    q = _ORIG["quantize_blocks_e4m3"]
+    x = np.asarray(x, dtype=F64)
+    xq = q(x, 1)[2] if gate_up else x
+    hid = _ORIG["silu"](xq @ np.asarray(w_gate, F64).T) * (xq @ np.asarray(w_up, F64).T)
+    return (q(hid, 1)[2] if down else hid) @ np.asarray(w_down, F64).T
+
+
+def _fp8_block_rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared, gate_up, down):
+    return _ORIG["fp8_block_expert_rows"](x_rows, idx_rows, np.ones_like(gate_rows), get_expert,
+                                          shared, gate_up, down)
+
+
+def _fp8_block_rows_no_shared(x_rows, idx_rows, gate_rows, get_expert, shared, gate_up, down):
+    z = tuple(np.zeros_like(np.asarray(w, F64)) for w in shared)
+    return _ORIG["fp8_block_expert_rows"](x_rows, idx_rows, gate_rows, get_expert, z, gate_up,
+                                          down)
+
+
 _ORIG = {name: getattr(O, name) for name in dir(O) if not name.startswith("_")}
 
 MUTATIONS = [
@@ -383,6 +497,20 @@ MUTATIONS = [
     ("fp8_swiglu_expert", _fp8_expert_h_unrounded),
     ("round_bf16", _round_bf16_truncates),
     ("fp8_expert_rows", _fp8_rows_ungated),
+    ("e4m3_round", _e4m3_round_half_away),
+    ("e4m3_round", _e4m3_round_truncate),
+    ("e4m3_round", _e4m3_round_two_bits),
+    ("block_exponent", _blockexp_floor),
+    ("block_exponent", _blockexp_wrong_max),
+    ("block_exponent", _blockexp_unclamped_nan),
+    ("quantize_blocks_e4m3", _qblocks_64_wide),
+    ("quantize_blocks_e4m3", _qblocks_rows_only),
+    ("quantize_blocks_e4m3", _qblocks_whole_row),
+    ("fp8_block_swiglu_expert", _fp8_block_h_rounded_bf16),
+    ("fp8_block_swiglu_expert", _fp8_block_down_ignored),
+    ("fp8_block_swiglu_expert", _fp8_block_weights_unquantized),
+    ("fp8_block_expert_rows", _fp8_block_rows_ungated),
+    ("fp8_block_expert_rows", _fp8_block_rows_no_shared),
 ]
 
 
