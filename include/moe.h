@@ -97,6 +97,12 @@ enum {
                                 matrices, and the hidden rows H are quantized
                                 per row inside the call */
 #define MOE_FP8_EXPERTS (MOE_FP8_GATE_UP | MOE_FP8_DOWN)
+#define MOE_FP8_BLOCK   32u  /* bf16 tensor-core path only, not with MOE_TRAINING or
+                                the per-row flags above: both expert products on
+                                block-scaled e4m3 codes (moe_quantize_blocks_e4m3);
+                                w_gate, w_up and w_down of experts and shared point
+                                at packed block-quantized matrices; the tokens and
+                                the hidden rows are quantized inside the call */
 
 /* Problem description.
  *   T  tokens (>= 0)            d  model width          h  expert hidden width
@@ -108,7 +114,7 @@ typedef struct {
   int T, d, h, E, k;
   int dtype;        /* moe_dtype */
   unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING |
-                       MOE_FP8_GATE_UP | MOE_FP8_DOWN */
+                       MOE_FP8_GATE_UP | MOE_FP8_DOWN | MOE_FP8_BLOCK */
 } moe_desc;
 
 /* Expert weights, element type desc->dtype.
@@ -150,6 +156,43 @@ MOE_API size_t moe_e4m3_packed_bytes(long long rows, int cols);
  * MOE_ERR_LAUNCH as for moe_forward.  The buffers must not overlap. */
 MOE_API int moe_quantize_rows_e4m3(const void* a, long long rows, int cols, void* packed,
                                    void* stream);
+
+/* Block-scaled FP8 experts (MOE_FP8_BLOCK): the official model's FP8 tile
+ * granularity ("DeepSeek V3 viết lại bằng 190 dòng JAX thuần", section
+ * "Những gì đã được đơn giản hóa": the re-creation leaves FP8 training out;
+ * the pages give no scheme, so the granularity is a reading of this
+ * library), on the B300's block-scaled MMA (tcgen05 kind::mxf8f6f4, fp32
+ * accumulation).  Each expert weight matrix is cut into 128 x 128 blocks
+ * (128 output rows x 128 inputs), each activation row -- a token for
+ * gate/up, the hidden row of a (token, expert) pair for the down projection
+ * -- into 1 x 128 blocks.  A block with largest magnitude amax gets the scale
+ * 2^e, e the smallest integer with amax <= 448 * 2^e (0 for a block of zeros
+ * or one whose maximum is not finite, clamped to [-127, 127]), and its codes
+ * are e4m3(v / 2^e), nearest-even (NaN stays NaN, +-inf saturates to +-448).
+ * The hidden rows are quantized from their fp32 values inside the first
+ * expert GEMM; nothing rounds them to bf16 first.
+ *
+ * Packed layout of a block-quantized [rows, cols] matrix (rows and cols
+ * multiples of 128), one device buffer of moe_e4m3_block_packed_bytes(rows,
+ * cols) bytes:
+ *   codes [rows, cols] uint8 (e4m3 bit patterns) at byte 0,
+ *   exponent words [rows / 128][ceil(cols / 512)] uint32 at byte
+ *   ceil(rows*cols / 256) * 256; byte j of word w of a block row holds e + 127
+ *   of block 4 w + j along the row.
+ * The routed gate (or up) weights are one matrix of E*h rows, the routed down
+ * weights one of E*d rows; the shared expert's h (gate, up) or d (down) rows.
+ * moe_e4m3_block_packed_bytes returns 0 for sizes that are not multiples of
+ * 128. */
+MOE_API size_t moe_e4m3_block_packed_bytes(long long rows, int cols);
+
+/* Block-quantize a bf16 matrix a [rows, cols] (device, row-major, 16-byte
+ * aligned) into `packed` (device, moe_e4m3_block_packed_bytes(rows, cols)
+ * bytes, 16-byte aligned), enqueued on `stream`.  rows and cols: multiples of
+ * 128 (rows / 128 <= 65535).  MOE_ERR_NULL / MOE_ERR_SHAPE / MOE_ERR_ALIGN /
+ * MOE_ERR_DEVICE / MOE_ERR_LAUNCH as for moe_forward.  The buffers must not
+ * overlap. */
+MOE_API int moe_quantize_blocks_e4m3(const void* a, long long rows, int cols, void* packed,
+                                     void* stream);
 
 /* Bytes of device workspace that moe_forward needs for `desc` (flags
  * included).  Returns 0 for an invalid desc.  The value depends only on the
@@ -299,8 +342,12 @@ MOE_API const char* moe_error_string(int code);
  * (int32 group table),
  * "perm" (permuted row -> token*k+slot), "inv" (token*k+slot -> permuted row),
  * "x_perm", "h", "y_perm", "y_shared", "x_q" (MOE_FP8_GATE_UP: the tokens
- * quantized, packed as above; empty otherwise), "h_q" (MOE_FP8_DOWN: the
- * rows of "h" quantized, packed; empty otherwise). */
+ * quantized, packed as above; MOE_FP8_BLOCK: the tokens' codes [T, d], then
+ * their exponent words [ceil(d / 512)][T] from byte ceil(T*d / 256) * 256;
+ * empty otherwise), "h_q" (MOE_FP8_DOWN: the rows of "h" quantized, packed;
+ * MOE_FP8_BLOCK: the hidden rows' codes [T*k + T, h] and exponent words
+ * [ceil(h / 512)][T*k + T], laid out as x_q; empty otherwise; with
+ * MOE_FP8_BLOCK "h" is empty). */
 typedef struct {
   char name[16];
   size_t offset, bytes;

@@ -494,16 +494,12 @@ def e4m3_round(v):
     subnormal grid has step 2^-9; the largest finite value is 448.  NaN
     stays NaN; magnitudes above 448 (infinities included) become 448."""
     v = np.asarray(v, dtype=F64)
-    out = np.full(v.shape, np.nan)
-    fin = ~np.isnan(v)
-    a = np.minimum(np.abs(v[fin]), 448.0)
+    a = np.minimum(np.abs(v), 448.0)        # NaN stays NaN through every step below
     _, ex = np.frexp(a)                     # a = f * 2^ex, 0.5 <= f < 1
-    k = np.maximum(ex - 1, -6)              # binade [2^k, 2^(k+1)), subnormals at k = -6
-    step_exp = k - 3
+    step_exp = np.maximum(ex - 1, -6) - 3   # binade [2^k, 2^(k+1)) (k >= -6) has step 2^(k-3)
     q = np.rint(np.ldexp(a, -step_exp))     # exact scaling; rint rounds half to even
     r = np.minimum(np.ldexp(q, step_exp), 448.0)
-    out[fin] = np.copysign(r, v[fin])
-    return out
+    return np.copysign(r, v)
 
 
 def e4m3_code(v):
@@ -540,12 +536,12 @@ def block_exponent(amax):
     return e
 
 
-def quantize_blocks_e4m3(a, block_rows: int):
+def quantize_blocks_e4m3(a, block_rows: int, codes: bool = True):
     """Block-scaled e4m3 quantization of a [R, C] (reading 11): blocks of
     block_rows x 128 (block_rows = 128 for weights, 1 for activation rows);
     R a multiple of block_rows, C a multiple of 128.  Returns (codes uint8
-    [R, C], exponents int64 [R / block_rows, C / 128], dequantized float64
-    [R, C])."""
+    [R, C] or None when ``codes`` is false, exponents int64 [R / block_rows,
+    C / 128], dequantized float64 [R, C])."""
     a = np.asarray(a, dtype=F64)
     R, C = a.shape
     assert R % block_rows == 0 and C % 128 == 0
@@ -554,9 +550,9 @@ def quantize_blocks_e4m3(a, block_rows: int):
     e = block_exponent(amax)
     scaled = blk * np.ldexp(1.0, -e)[:, None, :, None]  # exact: a power of two
     deq_codes = e4m3_round(scaled)
-    codes = e4m3_code(deq_codes).reshape(R, C)
+    bits = e4m3_code(deq_codes).reshape(R, C) if codes else None
     deq = (deq_codes * np.ldexp(1.0, e)[:, None, :, None]).reshape(R, C)
-    return codes, e, deq
+    return bits, e, deq
 
 
 def fp8_block_swiglu_expert(x, w_gate, w_up, w_down, gate_up: bool, down: bool):
@@ -565,14 +561,15 @@ def fp8_block_swiglu_expert(x, w_gate, w_up, w_down, gate_up: bool, down: bool):
     before the down projection if ``down``."""
     x = _f64(x)
     if gate_up:
-        xq = quantize_blocks_e4m3(x, 1)[2]
-        g = xq @ quantize_blocks_e4m3(w_gate, 128)[2].T
-        u = xq @ quantize_blocks_e4m3(w_up, 128)[2].T
+        xq = quantize_blocks_e4m3(x, 1, codes=False)[2]
+        g = xq @ quantize_blocks_e4m3(w_gate, 128, codes=False)[2].T
+        u = xq @ quantize_blocks_e4m3(w_up, 128, codes=False)[2].T
     else:
         g, u = x @ _f64(w_gate).T, x @ _f64(w_up).T
     hid = silu(g) * u
     if down:
-        return quantize_blocks_e4m3(hid, 1)[2] @ quantize_blocks_e4m3(w_down, 128)[2].T
+        return (quantize_blocks_e4m3(hid, 1, codes=False)[2]
+                @ quantize_blocks_e4m3(w_down, 128, codes=False)[2].T)
     return hid @ _f64(w_down).T
 
 

@@ -47,10 +47,55 @@ enum : int {
   TC2_FWD_UP_FP8 = 5,  // H as TC2_FWD_UP from e4m3 codes of weights and tokens
                        // with per-row scales (kind::f8f6f4)          K = d (bytes)
   TC2_FWD_DOWN_FP8 = 6,  // Y as TC2_FWD_DOWN from e4m3 codes of W_down and H  K = h (bytes)
+  TC2_FWD_UP_B8 = 7,     // H as TC2_FWD_UP from block-scaled e4m3 codes (kind::mxf8f6f4), H
+                         // written as e4m3 codes with one scale per 1 x 128 block   K = d (bytes)
+  TC2_FWD_DOWN_B8 = 8,   // Y as TC2_FWD_DOWN from block-scaled e4m3 codes of W_down and H
 };
 // two blocks of 256 rows of one matrix per tile (else gate and up rows)
 __host__ __device__ constexpr bool tc2_down(int op) {
-  return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX || op == TC2_FWD_DOWN_FP8;
+  return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX || op == TC2_FWD_DOWN_FP8 ||
+         op == TC2_FWD_DOWN_B8;
+}
+// block-scaled e4m3 products: scales in TMEM, one more warp stages them
+__host__ __device__ constexpr bool tc2_blk(int op) {
+  return op == TC2_FWD_UP_B8 || op == TC2_FWD_DOWN_B8;
+}
+__host__ __device__ constexpr int tc2_threads(int op) {
+  return 32 * (3 + TC_EPI_WARPS + (tc2_blk(op) ? 1 : 0));
+}
+#define TC2_SF_WARP (TC_TOKEN_WARP + 1)
+// Token tiles of the block-scaled products hold at most 240 tokens: TMEM
+// keeps two accumulators of N columns (0.. and 256..) and two scale sets of
+// 16 columns (240.. and 496..).
+#define TC2_BLK_BN 240
+
+// Exponent words of the block-scaled products: one byte per 128-wide block,
+// the scale 2^(byte - 127), four consecutive blocks of a row per word (byte
+// j = block 4 w + j).  Weights: [row blocks][wg] words (wa0 / wa1 routed:
+// gate / up, or down for both; swa0 / swa1 shared).  Activations: act
+// [ceil(K / 512)][act_rows] words -- the tokens x for gate/up (a routed
+// row's token is perm[row] / k), the hidden rows for down.  hq / hq_exp:
+// the first GEMM's outputs, H as codes [hq_rows, h] and its exponent words
+// [ceil(h / 512)][hq_rows].
+struct Fp8Blk {
+  const uint32_t *wa0, *wa1, *swa0, *swa1;
+  int wg;
+  const uint32_t* act;
+  int act_rows;
+  const int32_t* perm;
+  int k;
+  uint8_t* hq;
+  uint32_t* hq_exp;
+  int hq_rows;
+};
+
+// 4 x 4 byte transpose inside each group of 4 consecutive lanes: lane i
+// holds row i (byte j = column j) and ends up with column i.
+MOE_DEV uint32_t transpose4x4_b8(uint32_t w, int lane) {
+  uint32_t r = __shfl_xor_sync(0xffffffffu, w, 2);
+  w = (lane & 2) ? __byte_perm(w, r, 0x3276) : __byte_perm(w, r, 0x5410);
+  r = __shfl_xor_sync(0xffffffffu, w, 1);
+  return (lane & 1) ? __byte_perm(w, r, 0x3715) : __byte_perm(w, r, 0x6240);
 }
 // the weight operand is MN-major (the weights' transpose is multiplied)
 __host__ __device__ constexpr bool tc2_mn_a(int op) { return op == TC2_BWD_DH || op == TC2_BWD_DX; }
@@ -64,18 +109,24 @@ __host__ __device__ constexpr bool tc2_mn_a(int op) { return op == TC2_BWD_DH ||
 // MMAs of the next.
 // OUTB: output boxes staged per epilogue warp (0: the epilogue stores from
 // registers; 1 or 2: bf16 outputs go out by TMA store from shared memory).
-template <int SA, int SB, int NACC, int NBUF, int OUTB>
+template <int SA, int SB, int NACC, int NBUF, int OUTB, bool BLK = false>
 struct Tc2Cfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile
   static constexpr int A_STAGE = NACC * A_BYTES;
   static constexpr int B_STAGE = 128 * TC_BK * 2;    // half of a 256-token tile
   static constexpr int B_OFF = SA * A_STAGE;
   static constexpr int STG_OFF = B_OFF + SB * B_STAGE;
-  static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * OUTB * TC_BOX_BYTES;
+  // block-scaled products: two stages of scale words (four 32 x 16-byte
+  // copy sources each), then the H-amax exchange [2 halves][2][4 warps][32]
+  static constexpr int SF_STAGE = 2048;
+  static constexpr int SF_OFF = STG_OFF + TC_EPI_WARPS * OUTB * TC_BOX_BYTES;
+  static constexpr int XCH_OFF = SF_OFF + (BLK ? 2 * SF_STAGE : 0);
+  static constexpr int BAR_OFF = XCH_OFF + (BLK ? 2 * 2 * 4 * 32 * 4 : 0);
   // a_full, a_empty [SA]; b_full, b_empty [SB]; acc_full, acc_empty [2];
   // drain; tile_full, tile_empty [RING]
   // (+ one per epilogue warp: its staged input box, the SwiGLU gradient's dH)
-  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + TC_EPI_WARPS;
+  // (+ block-scaled: sf_full, sf_empty [2]; the exchange's [2 halves][2])
+  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + TC_EPI_WARPS + (BLK ? 8 : 0);
   static constexpr int MISC_BYTES = 4 * TC_TILE_RING + 4 * 5;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * N_BARS + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -132,9 +183,10 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   // down projection, the padded dY rows / dy (shared) for dH, the padded
   // dA|dB rows for dX
   int rb;
-  if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_FWD_UP_FP8)
+  if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_FWD_UP_FP8 || OP == TC2_FWD_UP_B8)
     rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
-  else if (OP == TC2_FWD_DOWN || OP == TC2_FWD_DOWN_FP8) rb = G.off[g] + t.tok0;
+  else if (OP == TC2_FWD_DOWN || OP == TC2_FWD_DOWN_FP8 || OP == TC2_FWD_DOWN_B8)
+    rb = G.off[g] + t.tok0;
   else if (OP == TC2_BWD_DH) rb = t.shared ? t.tok0 : G.poff[g] + t.tok0;
   else rb = G.poff[g] + t.tok0;
   t.row_b = rb + (int)rank * t.half;
@@ -144,16 +196,18 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
 }
 
 template <int SA, int SB, int NACC, int NBUF, int OUTB, int OP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC2_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc2_threads(OP), 1)
 k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
              int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
-             const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs) {
+             const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs, const Fp8Blk fb) {
   constexpr bool DOWN = tc2_down(OP);
   constexpr bool MNA = tc2_mn_a(OP);
   constexpr bool FP8U = OP == TC2_FWD_UP_FP8, FP8D = OP == TC2_FWD_DOWN_FP8;
-  constexpr bool FP8 = FP8U || FP8D;
-  constexpr int KB_ELEMS = FP8 ? 128 : TC_BK;  // elements per 128-byte K step
-  using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB>;
+  constexpr bool FP8 = FP8U || FP8D;  // per-row scales, applied in the epilogue
+  constexpr bool BLK = tc2_blk(OP);   // block scales, applied by the MMA
+  constexpr bool UPB = OP == TC2_FWD_UP_B8;
+  constexpr int KB_ELEMS = (FP8 || BLK) ? 128 : TC_BK;  // elements per 128-byte K step
+  using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB, BLK>;
   static_assert(OUTB >= 0 && OUTB <= 3, "staged boxes per epilogue warp");
   static_assert(OP != TC2_BWD_DAB || OUTB == 0 || OUTB == 3, "dH in, dA and dB out");
   // second GEMM with both 256-row blocks in one TMEM buffer: staggered blocks
@@ -167,9 +221,9 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const bool leader = rank == 0;
 
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
-  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8U) ? G.toff_a
+  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8U || UPB) ? G.toff_a
                         : (OP == TC2_BWD_DH ? G.toff_c : G.toff_b);
-  int* counter = G.next + (FP8U ? TC2_FWD_UP : FP8D ? TC2_FWD_DOWN : OP);
+  int* counter = G.next + ((FP8U || UPB) ? TC2_FWD_UP : (FP8D || BLK) ? TC2_FWD_DOWN : OP);
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
@@ -186,6 +240,10 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   auto tile_full = [&](int s) { return bar(2 * SA + 2 * SB + 5 + s); };
   auto tile_empty = [&](int s) { return bar(2 * SA + 2 * SB + 5 + TC_TILE_RING + s); };
   auto aux_full = [&](int w) { return bar(2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + w); };
+  constexpr int SFB0 = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + TC_EPI_WARPS;
+  auto sf_full = [&](int s) { return bar(SFB0 + s); };
+  auto sf_empty = [&](int s) { return bar(SFB0 + 2 + s); };
+  auto xch_bar = [&](int hf, int par) { return bar(SFB0 + 4 + 2 * hf + par); };
   uint8_t* misc = bar_base + 8 * C::N_BARS;
   volatile int* tile_id = reinterpret_cast<volatile int*>(misc);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc + 4 * TC_TILE_RING);
@@ -208,9 +266,16 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     mbar_init(drain_bar, 1);
     for (int s = 0; s < TC_TILE_RING; ++s) {
       mbar_init(tile_full(s), 1);
-      mbar_init(tile_empty(s), 2 * TC2_CONSUMERS);  // consumers of both CTAs
+      mbar_init(tile_empty(s), 2 * (TC2_CONSUMERS + (BLK ? 1 : 0)));  // consumers of both CTAs
     }
     for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(aux_full(w), 1);
+    if (BLK) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(sf_full(s), 2);   // the scale warps of both CTAs (leader's barrier)
+        mbar_init(sf_empty(s), 1);  // the leader's multicast commit
+      }
+      for (int i = 0; i < 4; ++i) mbar_init(xch_bar(i >> 1, i & 1), 4);  // the four lane quarters
+    }
     *abort_flag = 0;
     progress[0] = progress[1] = progress[2] = 0;
     fence_barrier_init();
@@ -319,7 +384,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         const int b = next_tile(i, true);
         if (b < 0) break;
         const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
-        const bool bs = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH || FP8U) && t.shared;
+        const bool bs =
+            (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH || FP8U || UPB) && t.shared;
         const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
         const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
         const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
@@ -352,6 +418,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       if (leader) {
         // ---------- MMA issuer (leader only) ----------
         int it = 0, tl = 0;
+        int qsf = 0;  // block-scaled: scale groups (4 K steps each) of the tiles before this one
         for (int i = 0;; ++i) {
           const int b = next_tile(i, true);
           if (b < 0) break;
@@ -359,6 +426,38 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, 0);
           const uint32_t idesc = FP8 ? umma_idesc_e4m3(2 * TC_BM, t.npad)
                                      : umma_idesc_bf16(2 * TC_BM, t.npad) | (MNA ? (1u << 15) : 0u);
+          // Block-scaled: the scale words of K steps 4 j .. 4 j + 3 (group
+          // j) are copied from the scale warps' stage into TMEM set (qsf + j)
+          // & 1 before the group's first MMA (the copy and the MMAs issued
+          // after it run in order), and the set and stage are released by a
+          // commit after the group's last MMA.  The copy into a set comes
+          // after the scale warp refilled its stage, which it does only after
+          // that commit: the MMAs of the group two back have completed.
+          int g_loaded = -1;
+          auto sf_col = [&](int kb) {
+            return tmem + (((qsf + (kb >> 2)) & 1) ? 496u : 240u);
+          };
+          auto ensure_sf = [&](int kb) -> bool {
+            if constexpr (BLK) {
+              while (g_loaded < (kb >> 2)) {
+                ++g_loaded;
+                const int q = qsf + g_loaded;
+                if (!mbar_wait_cluster(sf_full(q & 1), (q >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t col = tmem + ((q & 1) ? 496u : 240u);
+                const uint32_t src = smem_u32(smem + C::SF_OFF + (q & 1) * C::SF_STAGE);
+                tmem_cp_pair_32x128b(col, smem_desc_rows16(src));             // A rows, accumulator 0
+                tmem_cp_pair_32x128b(col + 4, smem_desc_rows16(src + 512));   // A rows, accumulator 1
+                tmem_cp_pair_32x128b(col + 8, smem_desc_rows16(src + 1024));  // tokens 0 .. 127
+                if (t.npad > 128) tmem_cp_pair_32x128b(col + 12, smem_desc_rows16(src + 1536));
+              }
+            }
+            return true;
+          };
+          auto release_sf = [&](int kb, int w) {
+            if (BLK && w == (t.mma1 ? 1 : 0) && ((kb & 3) == 3 || kb == nkb - 1))
+              umma_commit_pair(sf_empty((qsf + (kb >> 2)) & 1));
+          };
           const int u = tl % NBUF;  // TMEM buffer of this tile
           // k step kb of this tile uses ring stage it + kb
           auto stage_ready = [&](int kb) -> bool {
@@ -377,7 +476,11 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             const uint32_t d = tmem + (w ? 256u : (uint32_t)(u * 256));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {  // four 32-byte K slices
-              if (FP8)
+              if (BLK)
+                umma_mx_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32),
+                             umma_idesc_mx_e4m3(2 * TC_BM, t.npad, (uint32_t)(kb & 3)),
+                             sf_col(kb) + (w ? 4u : 0u), sf_col(kb) + 8u, (kb | kk) != 0);
+              else if (FP8)
                 umma_f8_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32), idesc,
                              (kb | kk) != 0);
               else
@@ -399,29 +502,41 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             // Second GEMM: block 0 runs S k steps ahead of block 1 at the
             // start of the tile and finishes S k steps before it, so the
             // drain of each block overlaps MMAs of the other.
-            const int S = min(min(SA, SB), nkb / 2);
+            // (block-scaled: S <= 4, so block 0 is never more than one scale
+            // group ahead of block 1 and two TMEM scale sets suffice)
+            const int S = min(min(min(SA, SB), nkb / 2), BLK ? 4 : 64);
             ok = tl == 0 || mbar_wait_cluster(acc_empty(0), (tl - 1) & 1);
             tc_fence_after();
             for (int kb = 0; ok && kb < S; ++kb)
-              if ((ok = stage_ready(kb))) issue(kb, 0);
+              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
+                issue(kb, 0);
+                release_sf(kb, 0);
+              }
             ok = ok && (tl == 0 || mbar_wait_cluster(acc_empty(1), (tl - 1) & 1));
             tc_fence_after();
             for (int kb = 0; ok && kb < S; ++kb) {
               if (t.mma1) issue(kb, 1);
+              release_sf(kb, 1);
               release(kb);
             }
             for (int kb = S; ok && kb < nkb - S; ++kb) {
-              if ((ok = stage_ready(kb))) {
+              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
                 issue(kb, 0);
+                release_sf(kb, 0);
                 if (t.mma1) issue(kb, 1);
+                release_sf(kb, 1);
                 release(kb);
               }
             }
             for (int kb = nkb - S; ok && kb < nkb; ++kb)
-              if ((ok = stage_ready(kb))) issue(kb, 0);
+              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
+                issue(kb, 0);
+                release_sf(kb, 0);
+              }
             if (ok) umma_commit_pair(acc_full(0));
             for (int kb = nkb - S; ok && kb < nkb; ++kb) {
               if (t.mma1) issue(kb, 1);
+              release_sf(kb, 1);
               release(kb);
             }
             if (ok) umma_commit_pair(acc_full(1));
@@ -429,9 +544,11 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             ok = tl < NBUF || mbar_wait_cluster(acc_empty(u), ((tl / NBUF) - 1) & 1);
             tc_fence_after();
             for (int kb = 0; ok && kb < nkb; ++kb) {
-              if ((ok = stage_ready(kb))) {
+              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
                 issue(kb, 0);
+                release_sf(kb, 0);
                 if (t.mma1) issue(kb, 1);
+                release_sf(kb, 1);
                 release(kb);
               }
             }
@@ -442,11 +559,68 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             continue;
           }
           it += nkb;
+          qsf += (nkb + 3) >> 2;
           ++tl;
         }
       }  // the peer has no MMA role
     }
     __syncwarp();
+  } else if (BLK && warp == TC2_SF_WARP) {
+    // ---------- block scales (both CTAs): the exponent words of each group
+    // of 4 K steps, in the layout tcgen05.cp .32x128b.warpx4 copies into
+    // TMEM -- 32 rows of 16 bytes, row r holding the words of rows (or
+    // tokens) r, r + 32, r + 64, r + 96.  This CTA's 128 weight rows of each
+    // accumulator share one block row, so their 32 x 4 words are all that
+    // block's word; every token column needs its own word, and both CTAs
+    // hold all the tile's tokens (each CTA's rows meet every token). ----------
+    const uint32_t F = 0xffffffffu;
+    const int ng = (nkb + 3) >> 2;
+    int q = 0;
+    for (int i = 0;; ++i) {  // after an abort, keep reading the tile ring until "none"
+      int b = 0;
+      if (lane == 0) b = next_tile(i, true);
+      b = __shfl_sync(F, b, 0);
+      if (b < 0) break;
+      const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
+      const uint32_t* wa0 = t.shared ? fb.swa0 : fb.wa0;
+      const uint32_t* wa1 = t.shared ? fb.swa1 : fb.wa1;
+      const int rb0 = t.row_a0 / TC_BM, rb1 = t.row_a1 / TC_BM;
+      int arow[8];  // activation row of token column lane + 32 j (-1: none)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int n = lane + 32 * j;
+        arow[j] = n >= t.ntok ? -1
+                  : !UPB      ? t.out_row0 + n
+                  : t.shared  ? t.tok0 + n
+                              : fb.perm[t.out_row0 + n] / fb.k;
+      }
+      for (int gi = 0; gi < ng; ++gi, ++q) {
+        const int s = q & 1;
+        int ok = 1;
+        if (lane == 0)
+          ok = !*abort_flag && (q < 2 || mbar_wait(sf_empty(s), ((q >> 1) - 1) & 1));
+        if (!__shfl_sync(F, ok, 0)) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + C::SF_OFF + s * C::SF_STAGE;
+        const uint32_t w0 = t.v0 ? wa0[(size_t)rb0 * fb.wg + gi] : 0x7f7f7f7fu;
+        const uint32_t w1 = (NACC == 2 && (UPB || t.v1)) ? wa1[(size_t)rb1 * fb.wg + gi] : 0x7f7f7f7fu;
+        uint32_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          v[j] = arow[j] >= 0 ? fb.act[(size_t)gi * fb.act_rows + arow[j]] : 0x7f7f7f7fu;
+        reinterpret_cast<uint4*>(st)[lane] = make_uint4(w0, w0, w0, w0);
+        reinterpret_cast<uint4*>(st + 512)[lane] = make_uint4(w1, w1, w1, w1);
+        reinterpret_cast<uint4*>(st + 1024)[lane] = make_uint4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<uint4*>(st + 1536)[lane] = make_uint4(v[4], v[5], v[6], v[7]);
+        fence_proxy_async_smem();  // visible to the tensor core's copy
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(sf_full(s)); else mbar_arrive_cluster(cluster_map(sf_full(s), 0));
+        }
+      }
+    }
   } else {
     // ---------- epilogue warps 2 .. 2+TC_EPI_WARPS-1 (both CTAs) ----------
     // Warp (q, half) drains TMEM lanes 32 q .. +31 (its 32 output rows),
@@ -455,11 +629,12 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     // it, then block 1.  bf16 outputs of 32 whole tokens go out through
     // shared memory by TMA store; the rest (a ragged last chunk, the shared
     // expert's fp32 rows, the SwiGLU gradient) from registers.
-    constexpr bool F32SH = OP == TC2_FWD_DOWN || OP == TC2_BWD_DX || FP8D;  // shared rows in fp32
+    constexpr bool F32SH = OP == TC2_FWD_DOWN || OP == TC2_BWD_DX || FP8D ||
+                           OP == TC2_FWD_DOWN_B8;  // shared rows in fp32
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
-    int tl = 0, nbox = 0, naux = 0;
+    int tl = 0, nbox = 0, naux = 0, nch = 0;
     for (int i = 0;; ++i) {
       const int b = next_tile(i, false);
       __syncwarp();
@@ -495,6 +670,59 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         }
         for (int c = 32 * half; c < t.npad; c += 64) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+          if (UPB) {
+            // H of 32 tokens x this warp's 32 hidden units, quantized: the
+            // CTA's 128 hidden units of a token are one 1 x 128 block, spread
+            // over the four lane quarters, so the four warps of this half
+            // exchange their per-token maxima (|h| as bits: NaN above inf
+            // above every finite value) through shared memory.  (valid is
+            // the same for the four warps: it depends only on the CTA.)
+            if (!valid) continue;
+            const uint32_t F = 0xffffffffu;
+            float va[32], vb[32];
+            tmem_load_2x32(ta + c, tb + c, va, vb);
+            uint32_t mine = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              va[j] = silu_fast(va[j]) * vb[j];
+              const uint32_t m = __reduce_max_sync(F, __float_as_uint(va[j]) & 0x7fffffffu);
+              if (lane == j) mine = m;
+            }
+            const int par = nch & 1;
+            volatile uint32_t* xch = reinterpret_cast<volatile uint32_t*>(smem + C::XCH_OFF) +
+                                     (size_t)((half * 2 + par) * 4) * 32;
+            xch[q * 32 + lane] = mine;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xch_bar(half, par));
+            const bool got = mbar_wait(xch_bar(half, par), (nch >> 1) & 1);
+            ++nch;
+            if (!__all_sync(F, got)) {
+              if (lane == 0) *abort_flag = 1;
+              break;
+            }
+            const uint32_t amax = max(max(xch[lane], xch[32 + lane]), max(xch[64 + lane], xch[96 + lane]));
+            const int e = block_exp_from_bits(amax);
+            const float inv = exp2_neg(e);
+            const int kbh = t.out_f0 / TC_BM;  // the block's index along h
+            if (q == 0 && c + lane < t.ntok)
+              reinterpret_cast<uint8_t*>(fb.hq_exp)[((size_t)(kbh >> 2) * fb.hq_rows + t.out_row0 + c +
+                                                     lane) * 4 + (kbh & 3)] = (uint8_t)(e + 127);
+            // codes: word p of this lane = tokens 4p .. 4p+3 of its hidden
+            // unit, then a 4 x 4 byte transpose per group of 4 lanes gives
+            // lane 4m + i token 4p + i's hidden units 4m .. 4m + 3
+            uint8_t* hq = fb.hq + (size_t)(t.out_row0 + c) * n_out + of + 4 * (lane >> 2);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const float i0 = __shfl_sync(F, inv, 4 * p), i1 = __shfl_sync(F, inv, 4 * p + 1);
+              const float i2 = __shfl_sync(F, inv, 4 * p + 2), i3 = __shfl_sync(F, inv, 4 * p + 3);
+              uint32_t w = (uint32_t)cvt_e4m3x2(va[4 * p] * i0, va[4 * p + 1] * i1) |
+                           ((uint32_t)cvt_e4m3x2(va[4 * p + 2] * i2, va[4 * p + 3] * i3) << 16);
+              w = transpose4x4_b8(w, lane);
+              const int tok = 4 * p + (lane & 3);
+              if (c + tok < t.ntok) *reinterpret_cast<uint32_t*>(hq + (size_t)tok * n_out) = w;
+            }
+            continue;
+          }
           if (OP == TC2_BWD_DAB && OUTB == 3 && c + 32 <= t.ntok) {
             // SwiGLU gradient of 32 whole tokens: dH box in by TMA, dA and dB
             // boxes out by TMA (one buffer of each)

@@ -85,6 +85,7 @@ struct Plan {
   bool training;  // the backward's buffers follow the forward's
   bool fp8;       // gate/up products on e4m3 codes (packed weights, tokens quantized here)
   bool fp8_down;  // down projection on e4m3 codes (packed W_down, H quantized here)
+  bool fp8_blk;   // both products on block-scaled e4m3 codes (packed block weights)
   int el;  // bytes per activation / weight element
   // router: CUDA-core tiles (r_bm x r_bn) or tensor-core pairs over E_pad
   // experts (rt_eb blocks of 256) x rt_tt token tiles x n_split K slices
@@ -106,11 +107,13 @@ struct Plan {
 int validate_desc(const moe_desc* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
-  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_EXPERTS))
+  if (d->flags &
+      ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_EXPERTS | MOE_FP8_BLOCK))
     return MOE_ERR_DTYPE;
-  if ((d->flags & MOE_FP8_EXPERTS) &&
+  if ((d->flags & (MOE_FP8_EXPERTS | MOE_FP8_BLOCK)) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY | MOE_TRAINING))))
     return MOE_ERR_DTYPE;
+  if ((d->flags & MOE_FP8_BLOCK) && (d->flags & MOE_FP8_EXPERTS)) return MOE_ERR_DTYPE;
   if ((d->flags & MOE_TRAINING) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY))))
     return MOE_ERR_DTYPE;
@@ -138,6 +141,7 @@ Plan make_plan(const moe_desc* d) {
   p.el = p.f32 ? 4 : 2;
   p.fp8 = d->flags & MOE_FP8_GATE_UP;
   p.fp8_down = d->flags & MOE_FP8_DOWN;
+  p.fp8_blk = d->flags & MOE_FP8_BLOCK;
 
   // router GEMM tiling and split of the model dimension
   p.big_router = p.E >= 96;
@@ -210,9 +214,11 @@ Plan make_plan(const moe_desc* d) {
       // (training: always the CTA-pair tiles, whose tile table the
       // backward's products share)
       // (fp8: the CTA-pair kernel alone has the e4m3 product)
-      p.big_tiles = per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_EXPERTS));
+      p.big_tiles =
+          per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_EXPERTS | MOE_FP8_BLOCK));
       if (p.big_tiles) {
-        p.bn = kPairBN;
+        // (block-scaled: TMEM also holds the scale sets, 240 tokens at most)
+        p.bn = p.fp8_blk ? TC2_BLK_BN : kPairBN;
         p.ft_a = MOE_PAIR_GEMM1 ? (p.h + 2 * TC_BM - 1) / (2 * TC_BM) : p.h / TC_BM;
         p.ft_b = MOE_PAIR_GEMM2 ? (p.d + 4 * TC_BM - 1) / (4 * TC_BM) : (p.d / TC_BM + 1) / 2;
       } else {
@@ -244,13 +250,20 @@ Plan make_plan(const moe_desc* d) {
   if (!p.route_only) {
     region((size_t)p.TK * 4, p.o_perm, p.b_perm);
     region((size_t)p.TK * 4, p.o_inv, p.b_inv);
-    region((size_t)p.TK * p.d * (p.fp8 ? 1 : p.el), p.o_xperm, p.b_xperm);
-    region((size_t)(p.TK + p.T) * p.h * p.el, p.o_h, p.b_h);
+    region((size_t)p.TK * p.d * ((p.fp8 || p.fp8_blk) ? 1 : p.el), p.o_xperm, p.b_xperm);
+    region(p.fp8_blk ? 0 : (size_t)(p.TK + p.T) * p.h * p.el, p.o_h, p.b_h);
     region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
     region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
-    region(p.fp8 ? e4m3_scale_offset(p.T, p.d) + (size_t)p.T * 4 : 0, p.o_xq, p.b_xq);
-    region(p.fp8_down ? e4m3_scale_offset((long long)p.TK + p.T, p.h) + (size_t)(p.TK + p.T) * 4
-                      : 0,
+    // x_q: codes [T, d], then fp32 row scales [T] (per row) or exponent
+    // words [ceil(d / 512)][T] (blocks); h_q likewise for the rows of H
+    region(p.fp8 ? e4m3_scale_offset(p.T, p.d) + (size_t)p.T * 4
+           : p.fp8_blk ? e4m3_scale_offset(p.T, p.d) + (size_t)e4m3_block_words(p.d) * p.T * 4
+                       : 0,
+           p.o_xq, p.b_xq);
+    const long long rows_h = (long long)p.TK + p.T;
+    region(p.fp8_down ? e4m3_scale_offset(rows_h, p.h) + (size_t)rows_h * 4
+           : p.fp8_blk ? e4m3_scale_offset(rows_h, p.h) + (size_t)e4m3_block_words(p.h) * rows_h * 4
+                       : 0,
            p.o_hq, p.b_hq);
   }
   p.training = d->flags & MOE_TRAINING;
@@ -417,7 +430,7 @@ bool make_rows_maps(CUtensorMap* m128, CUtensorMap* m64, CUtensorMap* m16, CUten
 bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
                   uint8_t* ws, TcMaps* m) {
   bool ok = true;
-  if (p.fp8) {
+  if (p.fp8 || p.fp8_blk) {
     // e4m3 codes: packed weights (codes first), X_perm codes, x codes
     const uint8_t* xq = ws + p.o_xq;
     ok &= make_map_u8(&m->up.a0, ex->w_gate, (long long)p.E * p.h, p.d, TC_BM);
@@ -440,7 +453,7 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
                          p.d);
     ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8, x, p.T, p.d);
   }
-  if (p.fp8_down) {
+  if (p.fp8_down || p.fp8_blk) {
     // e4m3 codes: packed W_down (codes first), rows of H quantized
     ok &= make_map_u8(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
     ok &= make_map_u8(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
@@ -469,12 +482,19 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
 // backward's two-block products (dH, dX) take the second GEMM's
 // configuration; the SwiGLU gradient stages three boxes per epilogue warp
 // (dH in, dA and dB out).
+// (block-scaled: the first GEMM writes H codes from registers, no staged
+// boxes; the second keeps one staged box per warp to leave room for the
+// scale stages)
 template <int OP> struct PairCfg {
-  static constexpr bool UP = OP == TC2_FWD_UP || OP == TC2_FWD_UP_FP8;
+  static constexpr bool UP = OP == TC2_FWD_UP || OP == TC2_FWD_UP_FP8 || OP == TC2_FWD_UP_B8;
   static constexpr int SA = OP == TC2_BWD_DAB ? 4 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
   static constexpr int SB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
-  static constexpr int OUTB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
+  static constexpr int OUTB = OP == TC2_BWD_DAB    ? 3
+                              : OP == TC2_FWD_UP_B8   ? 0
+                              : OP == TC2_FWD_DOWN_B8 ? 1
+                              : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
   static constexpr int NACC = 2, NBUF = 1;
+  using Cfg = Tc2Cfg<SA, SB, NACC, NBUF, OUTB, tc2_blk(OP)>;
 };
 
 template <int OP>
@@ -482,8 +502,7 @@ bool set_tc2_smem() {
   using P = PairCfg<OP>;
   return cudaFuncSetAttribute(k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, OP>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES) ==
-         cudaSuccess;
+                              P::Cfg::SMEM_BYTES) == cudaSuccess;
 }
 
 // One grouped product on CTA pairs, persistent: one pair per two SMs, at
@@ -491,13 +510,13 @@ bool set_tc2_smem() {
 template <int OP>
 void launch_pair(const Plan& p, const TcMapsDev& m, int max_tiles, int32_t* groups, int K,
                  int n_out, __nv_bfloat16* out, float* ysh, const __nv_bfloat16* aux,
-                 cudaStream_t s, const Fp8Scales& fs = Fp8Scales{}) {
+                 cudaStream_t s, const Fp8Scales& fs = Fp8Scales{}, const Fp8Blk& fb = Fp8Blk{}) {
   const int pairs = sm_count() / 2;
   const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
   using P = PairCfg<OP>;
   k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, OP>
-      <<<grid, TC2_THREADS, Tc2Cfg<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB>::SMEM_BYTES, s>>>(
-          m, groups, p.E, K, n_out, out, ysh, aux, fs);
+      <<<grid, tc2_threads(OP), P::Cfg::SMEM_BYTES, s>>>(m, groups, p.E, K, n_out, out, ysh, aux,
+                                                         fs, fb);
 }
 
 template <int BN, int SA, int SB, bool DOWN>
@@ -589,6 +608,7 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
   if (use_tc) {
     if (!make_tc_maps(p, x, experts, shared, ws, &maps)) return MOE_ERR_DEVICE;
     const bool ok =
+        p.fp8_blk ? (set_tc2_smem<TC2_FWD_UP_B8>() && set_tc2_smem<TC2_FWD_DOWN_B8>()) :
         p.big_tiles
             ? ((p.fp8 ? set_tc2_smem<TC2_FWD_UP_FP8>()
                       : MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
@@ -632,12 +652,17 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     int32_t* inv = reinterpret_cast<int32_t*>(ws + p.o_inv);
     uint8_t* xq = ws + p.o_xq;
     float* xs = reinterpret_cast<float*>(xq + e4m3_scale_offset(p.T, p.d));
+    uint32_t* xw = reinterpret_cast<uint32_t*>(xs);  // block-scaled: exponent words
     if (p.fp8)  // the tokens' codes and scales; the gather moves codes
       k_quant_rows<__nv_bfloat16><<<(p.T + 7) / 8, 256, 0, s>>>(
           static_cast<const __nv_bfloat16*>(x), p.T, p.d, xq, xs);
+    if (p.fp8_blk)
+      k_quant_ablocks<<<(p.T + 7) / 8, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), p.T,
+                                                     p.d, xq, xw);
+    const bool codes = p.fp8 || p.fp8_blk;
     k_permute_gather<<<(p.TK + 7) / 8, 256, 0, s>>>(
-        topk_idx, rank, hist, p.TK, p.E, p.k, p.fp8 ? xq : static_cast<const uint8_t*>(x),
-        ws + p.o_xperm, (size_t)p.d * (p.fp8 ? 1 : p.el), perm, inv);
+        topk_idx, rank, hist, p.TK, p.E, p.k, codes ? xq : static_cast<const uint8_t*>(x),
+        ws + p.o_xperm, (size_t)p.d * (codes ? 1 : p.el), perm, inv);
     mark(2);
     cudaEvent_t between = events ? static_cast<cudaEvent_t>(events[3]) : nullptr;
     if (p.f32) {
@@ -648,6 +673,31 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
       __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
       __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
       float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
+      if (p.fp8_blk) {
+        // both products on block-scaled codes: GEMM 1 writes H as codes and
+        // exponent words, GEMM 2 reads them (K counted in 64-element bf16
+        // steps of 128 bytes: d codes = d / 2)
+        const long long rows_h = (long long)p.TK + p.T;
+        uint8_t* hq = ws + p.o_hq;
+        uint32_t* hw = reinterpret_cast<uint32_t*>(hq + e4m3_scale_offset(rows_h, p.h));
+        auto words = [](const void* w, long long rows, long long cols) {
+          return reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(w) +
+                                                   e4m3_scale_offset(rows, cols));
+        };
+        const Fp8Blk f1{words(experts->w_gate, (long long)p.E * p.h, p.d),
+                        words(experts->w_up, (long long)p.E * p.h, p.d),
+                        words(shared->w_gate, p.h, p.d), words(shared->w_up, p.h, p.d),
+                        e4m3_block_words(p.d), xw, p.T, perm, p.k, hq, hw, (int)rows_h};
+        launch_pair<TC2_FWD_UP_B8>(p, maps.up, p.max_tiles_a, groups, p.d / 2, p.h, nullptr,
+                                   nullptr, nullptr, s, Fp8Scales{}, f1);
+        if (between) cudaEventRecord(between, s);
+        const uint32_t* wd = words(experts->w_down, (long long)p.E * p.d, p.h);
+        const uint32_t* swd = words(shared->w_down, p.d, p.h);
+        const Fp8Blk f2{wd, wd, swd, swd, e4m3_block_words(p.h), hw, (int)rows_h, nullptr, p.k,
+                        nullptr, nullptr, 0};
+        launch_pair<TC2_FWD_DOWN_B8>(p, maps.down, p.max_tiles_b, groups, p.h / 2, p.d, yperm,
+                                     ysh, nullptr, s, Fp8Scales{}, f2);
+      } else {
       if (p.fp8) {
         const size_t so = e4m3_scale_offset((long long)p.E * p.h, p.d),
                      ss = e4m3_scale_offset(p.h, p.d);
@@ -683,6 +733,7 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
       } else {
         launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b,
                           groups, yperm, ysh, s);
+      }
       }
     }
     mark(4);
@@ -793,6 +844,30 @@ int moe_quantize_rows_e4m3(const void* a, long long rows, int cols, void* packed
                                 static_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(a), rows, cols, q,
       reinterpret_cast<float*>(q + e4m3_scale_offset(rows, cols)));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+size_t moe_e4m3_block_packed_bytes(long long rows, int cols) {
+  if (rows < 0 || cols <= 0 || rows % 128 || cols % 128) return 0;
+  return e4m3_block_packed_bytes(rows, cols);
+}
+
+int moe_quantize_blocks_e4m3(const void* a, long long rows, int cols, void* packed,
+                             void* stream) {
+  if (rows < 0 || cols <= 0 || rows % 128 || cols % 128 || rows > (1LL << 40) / cols ||
+      rows / 128 > 65535)
+    return MOE_ERR_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!a || !packed) return MOE_ERR_NULL;
+  if (!aligned16(a) || !aligned16(packed)) return MOE_ERR_ALIGN;
+  int rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  cudaGetLastError();
+  uint8_t* q = static_cast<uint8_t*>(packed);
+  const dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
+  k_quant_wblocks<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(a), cols, q,
+      reinterpret_cast<uint32_t*>(q + e4m3_scale_offset(rows, cols)));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 

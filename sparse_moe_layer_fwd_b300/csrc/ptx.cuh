@@ -424,3 +424,75 @@ MOE_DEV void umma_commit_pair_local(uint32_t bar) {
                    bar)
                : "memory");
 }
+
+// Two fp32 values to e4m3 codes, nearest-even with saturation to +-448 (NaN
+// stays NaN): lo in the low byte.
+MOE_DEV uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ------------------------------------------------------------------ block-scaled MMA
+// tcgen05.mma kind::mxf8f6f4 with block scaling (scale_vec::1X: one UE8M0
+// scale byte, 2^(byte - 127), per row of A and per column of B for each
+// K = 32 slice), e4m3 A and B, fp32 accumulator.  The scales live in TMEM:
+// the scale of A row m (of this CTA's 128) is read from lane m, column
+// sfa + m / 32; the scale of B column n from lane n % 32 of the quarter that
+// computes the row, column sfb + n / 32, so every lane quarter holds a copy
+// (tcgen05.cp .32x128b.warpx4 writes exactly that).  Each 32-bit TMEM cell
+// holds four scale bytes; the instruction descriptor's scale-factor IDs pick
+// the byte (bits 29-30 for A, 4-5 for B).  Descriptor: B scale ID (4-5), A
+// and B format e4m3 = 0 (7-9, 10-12), K-major, N >> 3 (17-22), scale type
+// UE8M0 = 1 (23), M >> 4 (24-28), A scale ID (29-30).
+MOE_DEV uint32_t umma_idesc_mx_e4m3(int m, int n, uint32_t sf_id) {
+  return (sf_id << 4) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24) |
+         (sf_id << 29);
+}
+
+// D (+)= A * B^T with block scales, M = 256 over the CTA pair (leader only).
+MOE_DEV void umma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte matrix (no swizzle, rows of
+// 16 bytes stored densely: 8-row core groups 128 bytes apart), the source of
+// a .32x128b copy.
+MOE_DEV uint64_t smem_desc_rows16(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Copy 32 rows of 16 bytes from shared memory into TMEM columns taddr ..
+// taddr + 3 (row r -> lane r of every lane quarter, word w -> column w), in
+// both CTAs of the pair, each from its own shared memory; issued by the
+// leader's MMA thread, ordered before the MMAs it issues afterwards.
+MOE_DEV void tmem_cp_pair_32x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Exponent e of the power-of-two scale of a block whose largest magnitude
+// has the fp32 bit pattern `amax_bits` (sign cleared): the smallest integer
+// with amax <= 448 * 2^e, 0 for a block of zeros or one whose maximum is not
+// finite, clamped to [-127, 127].  With amax = m * 2^E, m in [1, 2): e = E - 8
+// when m <= 1.75 (448 = 1.75 * 2^8), else E - 7; subnormal maxima give
+// exponents below -127.
+MOE_DEV int block_exp_from_bits(uint32_t amax_bits) {
+  if (amax_bits == 0u || amax_bits >= 0x7f800000u) return 0;
+  const int ef = (int)(amax_bits >> 23);
+  if (ef == 0) return -127;
+  const int E = ef - 127;
+  const int e = (amax_bits & 0x7fffffu) <= 0x600000u ? E - 8 : E - 7;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as fp32 for the exponents block_exp_from_bits gives finite maxima
+// (-127 <= e <= 120).
+MOE_DEV float exp2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }

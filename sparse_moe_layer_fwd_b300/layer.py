@@ -34,6 +34,14 @@ class MoeLayer:
             self.packed.update({"w_down": self.quantize(w_down),
                                 "sh_down": self.quantize(sh_down)})
             w_down, sh_down = self.packed["w_down"], self.packed["sh_down"]
+        if have_w and flags & M.MOE_FP8_BLOCK:
+            qb = self.quantize_blocks
+            self.packed.update({"w_gate": qb(w_gate), "w_up": qb(w_up), "w_down": qb(w_down),
+                                "sh_gate": qb(sh_gate), "sh_up": qb(sh_up),
+                                "sh_down": qb(sh_down)})
+            w_gate, w_up, w_down = self.packed["w_gate"], self.packed["w_up"], self.packed["w_down"]
+            sh_gate, sh_up, sh_down = (self.packed["sh_gate"], self.packed["sh_up"],
+                                       self.packed["sh_down"])
         self.experts = M.make_experts(w_gate, w_up, w_down) if have_w else None
         self.shared = M.make_experts(sh_gate, sh_up, sh_down) if have_w else None
         tdt = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -62,6 +70,37 @@ class MoeLayer:
             stream = torch.cuda.current_stream(w.device)
         M.moe_quantize_rows_e4m3(w.contiguous(), rows, cols, out, stream)
         return out
+
+    @staticmethod
+    def quantize_blocks(w: torch.Tensor, stream=None) -> torch.Tensor:
+        """Packed block-scaled e4m3 copy (128 x 128 blocks) of a bf16 weight
+        tensor (rows = all but the last dimension): codes, then exponent
+        words from a 256-byte boundary."""
+        cols = w.shape[-1]
+        rows = w.numel() // cols
+        out = torch.empty(M.moe_e4m3_block_packed_bytes(rows, cols), dtype=torch.uint8,
+                          device=w.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(w.device)
+        M.moe_quantize_blocks_e4m3(w.contiguous(), rows, cols, out, stream)
+        return out
+
+    @staticmethod
+    def unpack_blocks(packed: torch.Tensor, rows: int, cols: int, act_rows: bool = False):
+        """(codes uint8 [rows, cols], exponents uint8 [row blocks, cols / 128])
+        of a packed block matrix; act_rows: an activation layout (one block
+        row per row, words [ceil(cols / 512)][rows])."""
+        so = M.e4m3_scale_offset(rows, cols)
+        wpr = M.e4m3_block_words(cols)
+        codes = packed[:rows * cols].view(rows, cols)
+        nb = cols // 128
+        if act_rows:
+            w = packed[so:so + 4 * wpr * rows].view(wpr, rows, 4)
+            ex = w.permute(1, 0, 2).reshape(rows, 4 * wpr)[:, :nb]
+        else:
+            w = packed[so:so + 4 * wpr * (rows // 128)].view(rows // 128, 4 * wpr)
+            ex = w[:, :nb]
+        return codes, ex
 
     @staticmethod
     def unpack(packed: torch.Tensor, rows: int, cols: int):

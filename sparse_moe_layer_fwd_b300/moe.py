@@ -21,6 +21,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS, MOE_TRAINING, MOE_FP8_GATE_UP, MOE_FP8_DOWN = 1, 2, 4, 8, 16
 MOE_FP8_EXPERTS = MOE_FP8_GATE_UP | MOE_FP8_DOWN
+MOE_FP8_BLOCK = 32
 MOE_OK = 0
 MOE_STATIC_SCRATCH_BYTES = 32 << 20
 ERRORS = {
@@ -89,6 +90,10 @@ def _load():
     lib.moe_e4m3_packed_bytes.restype = S
     lib.moe_quantize_rows_e4m3.argtypes = [P, ctypes.c_longlong, I, P, P]
     lib.moe_quantize_rows_e4m3.restype = I
+    lib.moe_e4m3_block_packed_bytes.argtypes = [ctypes.c_longlong, I]
+    lib.moe_e4m3_block_packed_bytes.restype = S
+    lib.moe_quantize_blocks_e4m3.argtypes = [P, ctypes.c_longlong, I, P, P]
+    lib.moe_quantize_blocks_e4m3.restype = I
     del U
     return lib
 
@@ -258,6 +263,27 @@ def moe_quantize_rows_e4m3(a, rows, cols, packed, stream=None, check=True) -> in
     rc = _lib.moe_quantize_rows_e4m3(_ptr(a), int(rows), int(cols), _ptr(packed),
                                      _stream(stream))
     return _check(rc, "moe_quantize_rows_e4m3") if check else rc
+
+
+def moe_e4m3_block_packed_bytes(rows: int, cols: int) -> int:
+    """Bytes of a block-quantized e4m3 matrix: codes [rows, cols], then the
+    exponent words [rows / 128][ceil(cols / 512)] from the next multiple of
+    256 bytes (0 unless rows and cols are multiples of 128)."""
+    return int(_lib.moe_e4m3_block_packed_bytes(int(rows), int(cols)))
+
+
+def e4m3_block_words(cols: int) -> int:
+    """Exponent words per block row (or per activation row): four 128-wide
+    blocks per word."""
+    return (cols // 128 + 3) // 4
+
+
+def moe_quantize_blocks_e4m3(a, rows, cols, packed, stream=None, check=True) -> int:
+    """Block-scaled e4m3 quantization (128 x 128 blocks) of the bf16 matrix
+    a [rows, cols] into the packed buffer (moe_e4m3_block_packed_bytes)."""
+    rc = _lib.moe_quantize_blocks_e4m3(_ptr(a), int(rows), int(cols), _ptr(packed),
+                                       _stream(stream))
+    return _check(rc, "moe_quantize_blocks_e4m3") if check else rc
 
 
 def moe_selftest_timeout(limit_ms: int, stream=None, check=True) -> int:

@@ -18,7 +18,8 @@ def test_library_exports_every_header_function():
         "moe_workspace_size", "moe_forward", "moe_host_io_extra_bytes", "moe_forward_host_io",
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
         "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward",
-        "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3", "moe_selftest_timeout"}
+        "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3", "moe_selftest_timeout",
+        "moe_e4m3_block_packed_bytes", "moe_quantize_blocks_e4m3"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
