@@ -88,8 +88,10 @@ def test_bias_step_moves_each_bias_by_at_most_gamma(E, k, seed):
     gamma = np.float32(1e-3)
     b2 = O.bias_update(b, load, 1e-3, T * k)
     step = np.abs(b2.astype(np.float64) - b.astype(np.float64))
-    # one fp32 step of gamma, rounded: at most gamma plus half an ulp of b
-    assert np.all(step <= float(gamma) + np.spacing(np.abs(b).astype(np.float32)).astype(np.float64))
+    # one fp32 step of gamma, rounded once: at most gamma plus half an ulp of
+    # the result (which can be larger than b's ulp when |b| is small)
+    mag = np.maximum(np.abs(b), np.abs(b2)).astype(np.float32)
+    assert np.all(step <= float(gamma) + np.spacing(mag).astype(np.float64))
     over = E * load > T * k
     assert np.all(b2[over] <= b[over]) and np.all(b2[E * load < T * k] >= b[E * load < T * k])
     assert np.array_equal(b2[E * load == T * k], b[E * load == T * k])
