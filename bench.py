@@ -191,14 +191,20 @@ def _working_set_bytes(wl, route_only):
     return b
 
 
-def _algorithmic(wl, load, fp8=False, fp8_down=False):
+def _algorithmic(wl, load, fp8=False, fp8_down=False, fp8_blk=False):
     """FLOPs and bytes of the two expert GEMMs for one launch each (fp8: a
-    GEMM reads one-byte codes of weights and tokens, plus row scales)."""
+    GEMM reads one-byte codes of weights and tokens, plus row scales, or
+    one exponent byte per 128 x 128 weight block and per 1 x 128 token or
+    hidden block)."""
     TK, T, d, h = wl.T * wl.k, wl.T, wl.d, wl.h
     rows = TK + T
     fl1 = 4.0 * rows * d * h
     fl2 = 2.0 * rows * d * h
     touched = int((load > 0).sum()) + 1  # + shared expert
+    if fp8_blk:
+        by1 = touched * 2 * h * d * (1 + 1 / 16384) + rows * d * (1 + 1 / 128) + rows * h * (1 + 1 / 128)
+        by2 = touched * d * h * (1 + 1 / 16384) + rows * h * (1 + 1 / 128) + TK * d * 2 + T * d * 4
+        return fl1, fl2, by1, by2, touched - 1
     if fp8:
         by1 = touched * 2 * h * (d + 4) + rows * (d + 4) + rows * h * 2
     else:
@@ -400,8 +406,10 @@ def run_ours(args, wl):
     route_only = args.route_only or wl.route_only
     inp = I.make_inputs(wl_rank, device="cuda", experts=not route_only)
     fp8 = bool(args.fp8) and not route_only
-    fp8_down = fp8 and args.fp8 == "experts"
-    base_flags = (M.MOE_FP8_EXPERTS if fp8_down else M.MOE_FP8_GATE_UP) if fp8 else 0
+    fp8_blk = fp8 and args.fp8 == "block"
+    fp8_down = fp8 and args.fp8 in ("experts", "block")
+    base_flags = (M.MOE_FP8_BLOCK if fp8_blk else M.MOE_FP8_EXPERTS if fp8_down
+                  else M.MOE_FP8_GATE_UP) if fp8 else 0
     layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else base_flags)
     stream = torch.cuda.current_stream()
     x = inp["x"]
@@ -558,11 +566,11 @@ def run_ours(args, wl):
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8, fp8_down)
+    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8, fp8_down, fp8_blk)
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
-    cap = NCU_TRAFFIC.get(wl.name + (":fp8" if fp8 else ""))  # GEMM 1 (gate/up)
+    cap = NCU_TRAFFIC.get(wl.name + (":fp8blk" if fp8_blk else ":fp8" if fp8 else ""))  # GEMM 1
     traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
     if prefill_like:
         ach = fl1 / g1_s / 1e12
@@ -613,7 +621,8 @@ def run_ours(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "ms_per_step_median": median_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 experts (per-row scales)" if fp8_down else
+        "dtype": ("e4m3 experts (128x128 weight / 1x128 activation block scales)" if fp8_blk else
+                  "e4m3 experts (per-row scales)" if fp8_down else
                   "e4m3 gate/up (per-row scales), bf16 down" if fp8 else "bf16"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
@@ -622,7 +631,8 @@ def run_ours(args, wl):
         "roofline": roof, "roofline_layer": layer_roof,
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
         "cpu_baseline": cpu, "e2e": e2e, **({"cuda_graph": graph} if graph else {}),
-        "gpu_launches": (kernels_per_step(wl, False, fp8) + int(fp8_down)) * args.steps,
+        "gpu_launches": (kernels_per_step(wl, False, fp8) + int(fp8_down and not fp8_blk))
+                        * args.steps,
         **({"decode": decode} if decode else {}),
         "clocks": clocks, "kernel_sha": sha, **meta,
     }
@@ -780,10 +790,11 @@ def main():
                     help="skip the V3 decode runs that follow the V3 prefill line")
     ap.add_argument("--train", action="store_true",
                     help="time a training step: forward and backward")
-    ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "experts"],
-                    help="expert products on per-row e4m3 codes: gate/up only "
-                         "(MOE_FP8_GATE_UP, the default) or gate/up and down "
-                         "(MOE_FP8_EXPERTS)")
+    ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "experts", "block"],
+                    help="expert products on e4m3 codes: gate/up only with per-row scales "
+                         "(MOE_FP8_GATE_UP, the default), gate/up and down with per-row "
+                         "scales (MOE_FP8_EXPERTS), or both with 128x128 / 1x128 block "
+                         "scales (MOE_FP8_BLOCK)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the forward replayed from a captured CUDA graph")
     ap.add_argument("--route-only", action="store_true",
