@@ -191,7 +191,7 @@ def _working_set_bytes(wl, route_only):
     return b
 
 
-def _algorithmic(wl, load, fp8=False, fp8_down=False, fp8_blk=False):
+def _algorithmic(wl, load, fp8=False, fp8_blk=False):
     """FLOPs and bytes of the two expert GEMMs for one launch each (fp8: a
     GEMM reads one-byte codes of weights and tokens, plus row scales, or
     one exponent byte per 128 x 128 weight block and per 1 x 128 token or
@@ -209,10 +209,7 @@ def _algorithmic(wl, load, fp8=False, fp8_down=False, fp8_blk=False):
         by1 = touched * 2 * h * (d + 4) + rows * (d + 4) + rows * h * 2
     else:
         by1 = touched * 2 * h * d * 2 + rows * d * 2 + rows * h * 2
-    if fp8_down:
-        by2 = touched * d * (h + 4) + rows * (h + 4) + TK * d * 2 + T * d * 4
-    else:
-        by2 = touched * d * h * 2 + rows * h * 2 + TK * d * 2 + T * d * 4
+    by2 = touched * d * h * 2 + rows * h * 2 + TK * d * 2 + T * d * 4
     return fl1, fl2, by1, by2, touched - 1
 
 
@@ -407,9 +404,7 @@ def run_ours(args, wl):
     inp = I.make_inputs(wl_rank, device="cuda", experts=not route_only)
     fp8 = bool(args.fp8) and not route_only
     fp8_blk = fp8 and args.fp8 == "block"
-    fp8_down = fp8 and args.fp8 in ("experts", "block")
-    base_flags = (M.MOE_FP8_BLOCK if fp8_blk else M.MOE_FP8_EXPERTS if fp8_down
-                  else M.MOE_FP8_GATE_UP) if fp8 else 0
+    base_flags = (M.MOE_FP8_BLOCK if fp8_blk else M.MOE_FP8_GATE_UP) if fp8 else 0
     layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_ROUTE_ONLY if route_only else base_flags)
     stream = torch.cuda.current_stream()
     x = inp["x"]
@@ -566,7 +561,7 @@ def run_ours(args, wl):
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8, fp8_down, fp8_blk)
+    fl1, fl2, by1, by2, touched = _algorithmic(wl, load, fp8, fp8_blk)
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
@@ -622,7 +617,6 @@ def run_ours(args, wl):
         "ms_per_step_median": median_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3 experts (128x128 weight / 1x128 activation block scales)" if fp8_blk else
-                  "e4m3 experts (per-row scales)" if fp8_down else
                   "e4m3 gate/up (per-row scales), bf16 down" if fp8 else "bf16"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
@@ -631,8 +625,7 @@ def run_ours(args, wl):
         "roofline": roof, "roofline_layer": layer_roof,
         "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
         "cpu_baseline": cpu, "e2e": e2e, **({"cuda_graph": graph} if graph else {}),
-        "gpu_launches": (kernels_per_step(wl, False, fp8) + int(fp8_down and not fp8_blk))
-                        * args.steps,
+        "gpu_launches": kernels_per_step(wl, False, fp8) * args.steps,
         **({"decode": decode} if decode else {}),
         "clocks": clocks, "kernel_sha": sha, **meta,
     }
@@ -790,11 +783,10 @@ def main():
                     help="skip the V3 decode runs that follow the V3 prefill line")
     ap.add_argument("--train", action="store_true",
                     help="time a training step: forward and backward")
-    ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "experts", "block"],
+    ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "block"],
                     help="expert products on e4m3 codes: gate/up only with per-row scales "
-                         "(MOE_FP8_GATE_UP, the default), gate/up and down with per-row "
-                         "scales (MOE_FP8_EXPERTS), or both with 128x128 / 1x128 block "
-                         "scales (MOE_FP8_BLOCK)")
+                         "(MOE_FP8_GATE_UP, the default), or both with 128x128 / 1x128 "
+                         "block scales (MOE_FP8_BLOCK)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the forward replayed from a captured CUDA graph")
     ap.add_argument("--route-only", action="store_true",

@@ -92,13 +92,9 @@ enum {
                                 w_gate and w_up of experts and shared then point at
                                 packed quantized matrices; w_down stays bf16; the
                                 tokens are quantized per row inside the call */
-#define MOE_FP8_DOWN    16u  /* as MOE_FP8_GATE_UP for the down projection: w_down
-                                of experts and shared point at packed quantized
-                                matrices, and the hidden rows H are quantized
-                                per row inside the call */
-#define MOE_FP8_EXPERTS (MOE_FP8_GATE_UP | MOE_FP8_DOWN)
+/* (flag 16 is not used) */
 #define MOE_FP8_BLOCK   32u  /* bf16 tensor-core path only, not with MOE_TRAINING or
-                                the per-row flags above: both expert products on
+                                MOE_FP8_GATE_UP: both expert products on
                                 block-scaled e4m3 codes (moe_quantize_blocks_e4m3);
                                 w_gate, w_up and w_down of experts and shared point
                                 at packed block-quantized matrices; the tokens and
@@ -114,27 +110,31 @@ typedef struct {
   int T, d, h, E, k;
   int dtype;        /* moe_dtype */
   unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING |
-                       MOE_FP8_GATE_UP | MOE_FP8_DOWN | MOE_FP8_BLOCK */
+                       MOE_FP8_GATE_UP | MOE_FP8_BLOCK */
 } moe_desc;
 
 /* Expert weights, element type desc->dtype.
  * Routed experts: w_gate [E, h, d], w_up [E, h, d], w_down [E, d, h].
  * Shared expert : w_gate [h, d],    w_up [h, d],    w_down [d, h].
  * (Each matrix is stored output-major: row i holds the weights of output i.)
- * With MOE_FP8_GATE_UP (w_gate, w_up) or MOE_FP8_DOWN (w_down) those
- * pointers instead hold the packed e4m3 form of the same matrices, written
- * by moe_quantize_rows_e4m3 (layout below). */
+ * With MOE_FP8_GATE_UP (w_gate, w_up) those pointers instead hold the packed
+ * per-row e4m3 form of the same matrices, written by moe_quantize_rows_e4m3;
+ * with MOE_FP8_BLOCK (all three) the packed block-scaled form written by
+ * moe_quantize_blocks_e4m3 (layouts below). */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
 } moe_expert_w;
 
-/* FP8 gate/up weights.  The official V3 model computes its expert products
- * in FP8 ("DeepSeek V3 viết lại bằng 190 dòng JAX thuần", section "Những gì
- * có trong 190 dòng code"); the re-creation leaves that out, and so does the
- * default path here.  With MOE_FP8_GATE_UP the first expert GEMM multiplies
- * e4m3 codes (tcgen05 kind::f8f6f4, fp32 accumulation) and applies the two
- * rows' scales to each product before SwiGLU.  Scaling unit: one row, with
- *   scale = amax(|row|) / 448 (1 for an all-zero row or a row with a NaN),
+/* FP8 gate/up weights with per-row scales.  The official V3 model computes
+ * its expert products in FP8 ("DeepSeek V3 viết lại bằng 190 dòng JAX thuần",
+ * section "Những gì đã được đơn giản hóa": the re-creation leaves FP8
+ * training out), and so does the default path here.  With MOE_FP8_GATE_UP the
+ * first expert GEMM multiplies e4m3 codes (tcgen05 kind::f8f6f4, fp32
+ * accumulation) and applies the two rows' scales to each product before
+ * SwiGLU.  Scaling unit: one row (a weight row, a token), with
+ *   scale = amax(|row|) / 448 (1 for an all-zero row or a row with a NaN:
+ *           the NaN stays in its own code and still makes that token's
+ *           output NaN),
  *   code  = e4m3(row / scale), nearest-even, saturating at +-448,
  * both fp32 operations.
  *
@@ -142,11 +142,8 @@ typedef struct {
  * moe_e4m3_packed_bytes(rows, cols) bytes:
  *   codes  [rows, cols] uint8 (e4m3 bit patterns) at byte 0,
  *   scales [rows]       fp32 at byte ceil(rows*cols / 256) * 256.
- * The routed gate (or up) weights are one matrix of E*h rows, the routed
- * down weights one of E*d rows (h columns); the shared expert's h rows (gate,
- * up) or d rows (down).  With MOE_FP8_DOWN the hidden row of each (token,
- * expert) pair and of the shared expert is quantized the same way before the
- * down projection. */
+ * The routed gate (or up) weights are one matrix of E*h rows; the shared
+ * expert's h rows. */
 MOE_API size_t moe_e4m3_packed_bytes(long long rows, int cols);
 
 /* Quantize a bf16 matrix a [rows, cols] (device, row-major, 16-byte aligned)
@@ -344,10 +341,9 @@ MOE_API const char* moe_error_string(int code);
  * "x_perm", "h", "y_perm", "y_shared", "x_q" (MOE_FP8_GATE_UP: the tokens
  * quantized, packed as above; MOE_FP8_BLOCK: the tokens' codes [T, d], then
  * their exponent words [ceil(d / 512)][T] from byte ceil(T*d / 256) * 256;
- * empty otherwise), "h_q" (MOE_FP8_DOWN: the rows of "h" quantized, packed;
- * MOE_FP8_BLOCK: the hidden rows' codes [T*k + T, h] and exponent words
- * [ceil(h / 512)][T*k + T], laid out as x_q; empty otherwise; with
- * MOE_FP8_BLOCK "h" is empty). */
+ * empty otherwise), "h_q" (MOE_FP8_BLOCK: the hidden rows' codes [T*k + T,
+ * h] and exponent words [ceil(h / 512)][T*k + T], laid out as x_q; empty
+ * otherwise; with MOE_FP8_BLOCK "h" is empty). */
 typedef struct {
   char name[16];
   size_t offset, bytes;

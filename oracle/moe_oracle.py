@@ -68,13 +68,7 @@ as a source, uses the same):
                a row holding a NaN),
                code = e4m3(row / scale) rounded to nearest even; the layer is
                then the same layer on the dequantized values code * scale
-               (routing on the unquantized tokens).
-               With the down projection in e4m3 as well, each row of W_down
-               and each hidden row H of a (token, expert) pair (and of the
-               shared expert) is quantized the same way before W_down is
-               applied; H is computed as above and held in bf16, the
-               layer's activation type (round to nearest even), before it
-               is quantized.
+               (routing on the unquantized tokens; W_down unquantized).
 
 11. fp8 block-scaled experts (the official model's tile granularity; a
                B300-native option, not on the pages): every expert weight
@@ -428,44 +422,6 @@ def quantize_rows_e4m3(a):
     q = (t / scale).to(torch.float8_e4m3fn)
     deq = q.to(torch.float64) * scale.to(torch.float64)
     return q.view(torch.uint8).numpy(), scale.squeeze(-1).numpy(), deq.numpy()
-
-
-def round_bf16(a):
-    """Nearest bf16 value (ties to even) of each element, as float64: the
-    storage of the hidden rows before they are quantized (reading 10)."""
-    import torch
-    return torch.as_tensor(np.asarray(a, dtype=F64)).to(torch.bfloat16).to(torch.float64).numpy()
-
-
-def fp8_swiglu_expert(x, w_gate, w_up, w_down, down: bool, gate_up: bool = True):
-    """One expert under reading 10: if ``gate_up``, gate/up on the
-    dequantized tokens and weights; if ``down``, H and W_down dequantized row
-    by row before the down projection."""
-    if gate_up:
-        xq = quantize_rows_e4m3(x)[2]
-        g = xq @ quantize_rows_e4m3(w_gate)[2].T
-        u = xq @ quantize_rows_e4m3(w_up)[2].T
-    else:
-        g, u = _f64(x) @ _f64(w_gate).T, _f64(x) @ _f64(w_up).T
-    hid = silu(g) * u
-    if down:
-        return quantize_rows_e4m3(round_bf16(hid))[2] @ quantize_rows_e4m3(w_down)[2].T
-    return hid @ _f64(w_down).T
-
-
-def fp8_expert_rows(x_rows, idx_rows, gate_rows, get_expert, shared, down: bool,
-                    gate_up: bool = True):
-    """Layer output for sampled rows under reading 10 (which products are in
-    e4m3: ``gate_up``, ``down``); arguments as expert_output_rows, the
-    selection and gates coming from the unquantized routing."""
-    x_rows = _f64(x_rows)
-    y = fp8_swiglu_expert(x_rows, *shared, down, gate_up)
-    idx_rows = np.asarray(idx_rows)
-    for e in np.unique(idx_rows):
-        tt, jj = np.nonzero(idx_rows == e)
-        ye = fp8_swiglu_expert(x_rows[tt], *get_expert(int(e)), down, gate_up)
-        y[tt] += gate_rows[tt, jj][:, None] * ye
-    return y
 
 
 def fp8_gate_up_rows(x_rows, idx_rows, gate_rows, get_expert, shared):

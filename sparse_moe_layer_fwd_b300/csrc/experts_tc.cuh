@@ -203,9 +203,10 @@ MOE_DEV void stage_box_bf16(uint32_t ta, uint32_t tb, uint32_t box, int lane) {
   }
 }
 
-// stage_box_bf16 for the fp8 products: the accumulators hold sums of code
-// products, so each value is first multiplied by its weight row's scale and
-// its token's scale (SWIGLU: gate and up, each with its own row scales).
+// stage_box_bf16 for the per-row fp8 products: the accumulators hold sums
+// of code products, so each value is first multiplied by its weight row's
+// scale and its token's scale (SWIGLU: gate and up, each with its own row
+// scales).
 // rsg / rsu: scales of the rows (lane >> 2) + 8 r, r = 0..3 of the warp's 32;
 // tsc[2 i + e]: scale of token column 8 i + 2 (lane & 3) + e.
 template <bool SWIGLU>
@@ -334,10 +335,9 @@ MOE_DEV TcTile tc_tile(const GroupTable& G, const int32_t* toff, int E, int b, i
   return t;
 }
 
-// Scales of the fp8 products.  Gate/up: per weight row (g, u routed [E*h];
-// sg, su shared [h]) and per token (tok [T]; a routed row's token is
-// perm[row] / k).  Down: per W_down row (g [E*d], sg [d]) and per row of H
-// (tok [T*k + T], numbered as the output rows); u, su, perm unused.
+// Scales of the per-row fp8 gate/up products: per weight row (g, u routed
+// [E*h]; sg, su shared [h]) and per token (tok [T]; a routed row's token is
+// perm[row] / k).
 struct Fp8Scales {
   const float *g, *u, *sg, *su, *tok;
   const int32_t* perm;

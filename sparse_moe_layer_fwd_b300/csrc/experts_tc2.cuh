@@ -46,15 +46,13 @@ enum : int {
   TC2_BWD_DX = 4,    // dX = dA W_gate + dB W_up (weights read transposed)      K = 2h
   TC2_FWD_UP_FP8 = 5,  // H as TC2_FWD_UP from e4m3 codes of weights and tokens
                        // with per-row scales (kind::f8f6f4)          K = d (bytes)
-  TC2_FWD_DOWN_FP8 = 6,  // Y as TC2_FWD_DOWN from e4m3 codes of W_down and H  K = h (bytes)
   TC2_FWD_UP_B8 = 7,     // H as TC2_FWD_UP from block-scaled e4m3 codes (kind::mxf8f6f4), H
                          // written as e4m3 codes with one scale per 1 x 128 block   K = d (bytes)
   TC2_FWD_DOWN_B8 = 8,   // Y as TC2_FWD_DOWN from block-scaled e4m3 codes of W_down and H
 };
 // two blocks of 256 rows of one matrix per tile (else gate and up rows)
 __host__ __device__ constexpr bool tc2_down(int op) {
-  return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX || op == TC2_FWD_DOWN_FP8 ||
-         op == TC2_FWD_DOWN_B8;
+  return op == TC2_FWD_DOWN || op == TC2_BWD_DH || op == TC2_BWD_DX || op == TC2_FWD_DOWN_B8;
 }
 // block-scaled e4m3 products: scales in TMEM, one more warp stages them
 __host__ __device__ constexpr bool tc2_blk(int op) {
@@ -185,7 +183,7 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   int rb;
   if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_FWD_UP_FP8 || OP == TC2_FWD_UP_B8)
     rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
-  else if (OP == TC2_FWD_DOWN || OP == TC2_FWD_DOWN_FP8 || OP == TC2_FWD_DOWN_B8)
+  else if (OP == TC2_FWD_DOWN || OP == TC2_FWD_DOWN_B8)
     rb = G.off[g] + t.tok0;
   else if (OP == TC2_BWD_DH) rb = t.shared ? t.tok0 : G.poff[g] + t.tok0;
   else rb = G.poff[g] + t.tok0;
@@ -202,8 +200,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
              const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs, const Fp8Blk fb) {
   constexpr bool DOWN = tc2_down(OP);
   constexpr bool MNA = tc2_mn_a(OP);
-  constexpr bool FP8U = OP == TC2_FWD_UP_FP8, FP8D = OP == TC2_FWD_DOWN_FP8;
-  constexpr bool FP8 = FP8U || FP8D;  // per-row scales, applied in the epilogue
+  constexpr bool FP8U = OP == TC2_FWD_UP_FP8;
+  constexpr bool FP8 = FP8U;  // per-row scales, applied in the epilogue
   constexpr bool BLK = tc2_blk(OP);   // block scales, applied by the MMA
   constexpr bool UPB = OP == TC2_FWD_UP_B8;
   constexpr int KB_ELEMS = (FP8 || BLK) ? 128 : TC_BK;  // elements per 128-byte K step
@@ -223,7 +221,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
   const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8U || UPB) ? G.toff_a
                         : (OP == TC2_BWD_DH ? G.toff_c : G.toff_b);
-  int* counter = G.next + ((FP8U || UPB) ? TC2_FWD_UP : (FP8D || BLK) ? TC2_FWD_DOWN : OP);
+  int* counter = G.next + ((FP8U || UPB) ? TC2_FWD_UP : BLK ? TC2_FWD_DOWN : OP);
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
@@ -629,8 +627,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     // it, then block 1.  bf16 outputs of 32 whole tokens go out through
     // shared memory by TMA store; the rest (a ragged last chunk, the shared
     // expert's fp32 rows, the SwiGLU gradient) from registers.
-    constexpr bool F32SH = OP == TC2_FWD_DOWN || OP == TC2_BWD_DX || FP8D ||
-                           OP == TC2_FWD_DOWN_B8;  // shared rows in fp32
+    constexpr bool F32SH =
+        OP == TC2_FWD_DOWN || OP == TC2_BWD_DX || OP == TC2_FWD_DOWN_B8;  // shared rows in fp32
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
@@ -658,15 +656,14 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         float rsg[4] = {1.f, 1.f, 1.f, 1.f}, rsu[4] = {1.f, 1.f, 1.f, 1.f}, rlg = 1.f, rlu = 1.f;
         if (FP8 && valid) {
           const float* sgp = t.shared ? fs.sg : fs.g + (size_t)t.g * n_out;
+          const float* sup = t.shared ? fs.su : fs.u + (size_t)t.g * n_out;
 #pragma unroll
-          for (int r = 0; r < 4; ++r) rsg[r] = sgp[of + (lane >> 2) + 8 * r];
-          rlg = sgp[of + lane];
-          if (FP8U) {
-            const float* sup = t.shared ? fs.su : fs.u + (size_t)t.g * n_out;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) rsu[r] = sup[of + (lane >> 2) + 8 * r];
-            rlu = sup[of + lane];
+          for (int r = 0; r < 4; ++r) {
+            rsg[r] = sgp[of + (lane >> 2) + 8 * r];
+            rsu[r] = sup[of + (lane >> 2) + 8 * r];
           }
+          rlg = sgp[of + lane];
+          rlu = sup[of + lane];
         }
         for (int c = 32 * half; c < t.npad; c += 64) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -752,12 +749,10 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             }
             continue;
           }
-          // fp8: scale of token column c + lane (gate/up: the token's row of
-          // x; down: the row of H, numbered as the output rows)
+          // fp8: scale of token column c + lane (the token's row of x)
           float tsl = 0.f;
           if (FP8 && c + lane < t.ntok)
-            tsl = FP8D ? fs.tok[t.out_row0 + c + lane]
-                       : fs.tok[t.shared ? t.tok0 + c + lane : fs.perm[t.out_row0 + c + lane] / fs.k];
+            tsl = fs.tok[t.shared ? t.tok0 + c + lane : fs.perm[t.out_row0 + c + lane] / fs.k];
           if (OUTB > 0 && OP != TC2_BWD_DAB && c + 32 <= t.ntok && !(F32SH && t.shared)) {
             // 32 whole tokens of bf16 output: stage the box in shared
             // memory and store it with TMA (boxes used round robin)
@@ -791,10 +786,6 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           else
             tmem_load_32(ta + c, va);
           if (!valid) continue;
-          if (FP8D) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) va[j] *= rlg * __shfl_sync(0xffffffffu, tsl, j);
-          }
           if (FP8U) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {

@@ -83,8 +83,7 @@ struct Plan {
   int T, d, h, E, k, TK;
   bool f32, route_only, simt, big_router, big_tiles, tc_router;
   bool training;  // the backward's buffers follow the forward's
-  bool fp8;       // gate/up products on e4m3 codes (packed weights, tokens quantized here)
-  bool fp8_down;  // down projection on e4m3 codes (packed W_down, H quantized here)
+  bool fp8;       // gate/up products on per-row e4m3 codes (packed weights, tokens quantized here)
   bool fp8_blk;   // both products on block-scaled e4m3 codes (packed block weights)
   int el;  // bytes per activation / weight element
   // router: CUDA-core tiles (r_bm x r_bn) or tensor-core pairs over E_pad
@@ -108,12 +107,12 @@ int validate_desc(const moe_desc* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
   if (d->flags &
-      ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_EXPERTS | MOE_FP8_BLOCK))
+      ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_GATE_UP | MOE_FP8_BLOCK))
     return MOE_ERR_DTYPE;
-  if ((d->flags & (MOE_FP8_EXPERTS | MOE_FP8_BLOCK)) &&
+  if ((d->flags & (MOE_FP8_GATE_UP | MOE_FP8_BLOCK)) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY | MOE_TRAINING))))
     return MOE_ERR_DTYPE;
-  if ((d->flags & MOE_FP8_BLOCK) && (d->flags & MOE_FP8_EXPERTS)) return MOE_ERR_DTYPE;
+  if ((d->flags & MOE_FP8_BLOCK) && (d->flags & MOE_FP8_GATE_UP)) return MOE_ERR_DTYPE;
   if ((d->flags & MOE_TRAINING) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY))))
     return MOE_ERR_DTYPE;
@@ -140,7 +139,6 @@ Plan make_plan(const moe_desc* d) {
   p.simt = p.f32 || (d->flags & MOE_SIMT_EXPERTS);
   p.el = p.f32 ? 4 : 2;
   p.fp8 = d->flags & MOE_FP8_GATE_UP;
-  p.fp8_down = d->flags & MOE_FP8_DOWN;
   p.fp8_blk = d->flags & MOE_FP8_BLOCK;
 
   // router GEMM tiling and split of the model dimension
@@ -215,7 +213,7 @@ Plan make_plan(const moe_desc* d) {
       // backward's products share)
       // (fp8: the CTA-pair kernel alone has the e4m3 product)
       p.big_tiles =
-          per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_EXPERTS | MOE_FP8_BLOCK));
+          per_expert >= 96.0 || (d->flags & (MOE_TRAINING | MOE_FP8_GATE_UP | MOE_FP8_BLOCK));
       if (p.big_tiles) {
         // (block-scaled: TMEM also holds the scale sets, 240 tokens at most)
         p.bn = p.fp8_blk ? TC2_BLK_BN : kPairBN;
@@ -255,15 +253,14 @@ Plan make_plan(const moe_desc* d) {
     region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
     region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
     // x_q: codes [T, d], then fp32 row scales [T] (per row) or exponent
-    // words [ceil(d / 512)][T] (blocks); h_q likewise for the rows of H
+    // words [ceil(d / 512)][T] (blocks); h_q: the block-quantized rows of H
     region(p.fp8 ? e4m3_scale_offset(p.T, p.d) + (size_t)p.T * 4
            : p.fp8_blk ? e4m3_scale_offset(p.T, p.d) + (size_t)e4m3_block_words(p.d) * p.T * 4
                        : 0,
            p.o_xq, p.b_xq);
     const long long rows_h = (long long)p.TK + p.T;
-    region(p.fp8_down ? e4m3_scale_offset(rows_h, p.h) + (size_t)rows_h * 4
-           : p.fp8_blk ? e4m3_scale_offset(rows_h, p.h) + (size_t)e4m3_block_words(p.h) * rows_h * 4
-                       : 0,
+    region(p.fp8_blk ? e4m3_scale_offset(rows_h, p.h) + (size_t)e4m3_block_words(p.h) * rows_h * 4
+                     : 0,
            p.o_hq, p.b_hq);
   }
   p.training = d->flags & MOE_TRAINING;
@@ -453,7 +450,7 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
                          p.d);
     ok &= make_rows_maps(&m->up.bs128, &m->up.bs64, &m->up.bs16, &m->up.bs8, x, p.T, p.d);
   }
-  if (p.fp8_down || p.fp8_blk) {
+  if (p.fp8_blk) {
     // e4m3 codes: packed W_down (codes first), rows of H quantized
     ok &= make_map_u8(&m->down.a0, ex->w_down, (long long)p.E * p.d, p.h, TC_BM);
     ok &= make_map_u8(&m->down.sa0, sh->w_down, p.d, p.h, TC_BM);
@@ -613,8 +610,7 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
             ? ((p.fp8 ? set_tc2_smem<TC2_FWD_UP_FP8>()
                       : MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
-               (p.fp8_down ? set_tc2_smem<TC2_FWD_DOWN_FP8>()
-                : MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
+               (MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, true>()))
             : (set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, false>() &&
                set_tc1_smem<kSmallBN, kSmallSA, kSmallSB, true>());
@@ -714,26 +710,8 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
                            groups, hbuf, nullptr, s);
       }
       if (between) cudaEventRecord(between, s);
-      if (p.fp8_down) {
-        // the rows of H to codes and scales, then the down projection on them
-        const long long rows_h = (long long)p.TK + p.T;
-        uint8_t* hq = ws + p.o_hq;
-        float* hs = reinterpret_cast<float*>(hq + e4m3_scale_offset(rows_h, p.h));
-        k_quant_rows<__nv_bfloat16><<<(unsigned)((rows_h + 7) / 8), 256, 0, s>>>(
-            hbuf, rows_h, p.h, hq, hs);
-        const size_t so = e4m3_scale_offset((long long)p.E * p.d, p.h),
-                     ss = e4m3_scale_offset(p.d, p.h);
-        auto scl = [](const void* w, size_t o) {
-          return reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) + o);
-        };
-        const Fp8Scales fs{scl(experts->w_down, so), nullptr, scl(shared->w_down, ss), nullptr,
-                           hs, nullptr, p.k};
-        launch_pair<TC2_FWD_DOWN_FP8>(p, maps.down, p.max_tiles_b, groups, p.h / 2, p.d, yperm,
-                                      ysh, nullptr, s, fs);
-      } else {
-        launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b,
-                          groups, yperm, ysh, s);
-      }
+      launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b, groups,
+                        yperm, ysh, s);
       }
     }
     mark(4);

@@ -23,17 +23,13 @@ class MoeLayer:
         self._keep = (w_gate, w_up, w_down, sh_gate, sh_up, sh_down)
         have_w = w_gate is not None
         # fp8 modes: the weights they name as packed e4m3 matrices (codes +
-        # row scales), quantized once here
+        # row scales, or codes + block exponents), quantized once here
         self.packed = {}
         if have_w and flags & M.MOE_FP8_GATE_UP:
             self.packed.update({"w_gate": self.quantize(w_gate), "w_up": self.quantize(w_up),
                                 "sh_gate": self.quantize(sh_gate), "sh_up": self.quantize(sh_up)})
             w_gate, w_up = self.packed["w_gate"], self.packed["w_up"]
             sh_gate, sh_up = self.packed["sh_gate"], self.packed["sh_up"]
-        if have_w and flags & M.MOE_FP8_DOWN:
-            self.packed.update({"w_down": self.quantize(w_down),
-                                "sh_down": self.quantize(sh_down)})
-            w_down, sh_down = self.packed["w_down"], self.packed["sh_down"]
         if have_w and flags & M.MOE_FP8_BLOCK:
             qb = self.quantize_blocks
             self.packed.update({"w_gate": qb(w_gate), "w_up": qb(w_up), "w_down": qb(w_down),

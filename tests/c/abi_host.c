@@ -19,7 +19,9 @@ int main(void) {
   size_t ws = moe_workspace_size(&d);
   CHECK(ws > 0);
   moe_desc fp8 = d;
-  fp8.flags = MOE_FP8_EXPERTS;
+  fp8.flags = MOE_FP8_BLOCK;
+  CHECK(moe_workspace_size(&fp8) > 0);
+  fp8.flags = MOE_FP8_GATE_UP;
   CHECK(moe_workspace_size(&fp8) > 0);
   moe_desc bad = d;
   bad.k = 33;
@@ -51,6 +53,14 @@ int main(void) {
                     (void*)0x10000, ws - 1, NULL) == MOE_ERR_WORKSPACE);
   CHECK(moe_bias_update(NULL, (float*)0x10000, 1e-3f, 256, 65536, NULL) == MOE_ERR_NULL);
   CHECK(moe_e4m3_packed_bytes(10, 24) == 256 + 40);
+  /* 128 x 640 codes, then 1 block row x 2 words of exponents */
+  CHECK(moe_e4m3_block_packed_bytes(128, 640) == 128 * 640 + 8);
+  CHECK(moe_e4m3_block_packed_bytes(100, 640) == 0);
+  CHECK(moe_quantize_blocks_e4m3((const void*)0x10000, 128, 100, (void*)0x10000, NULL) ==
+        MOE_ERR_SHAPE);
+  moe_desc both = d;
+  both.flags = MOE_FP8_BLOCK | MOE_FP8_GATE_UP;
+  CHECK(moe_workspace_size(&both) == 0);
   CHECK(moe_quantize_rows_e4m3((const void*)0x10000, 4, 100, (void*)0x10000, NULL) ==
         MOE_ERR_SHAPE);
   CHECK(moe_selftest_timeout(0, NULL) == MOE_ERR_SHAPE);

@@ -595,52 +595,6 @@ def pin_fp8_gate_up(O):
     assert np.allclose(got2, ref2, rtol=0, atol=1e-12 * np.abs(ref2).max())
 
 
-def pin_fp8_down(O):
-    """The fp8 down projection: without it the expert is the gate/up-only
-    layer; with it, the result factors into the e4m3 codes and the two rows'
-    scales, y = s_H[:, None] * (C_H C_W^T) * s_W[None, :], with H the
-    gate/up-only hidden rows; scaling W_down by a power of two scales y."""
-    x, idx, gates, ex, sh = _fp8_case(45, exact=False)
-    wg, wu, wd = ex[1]
-    xt = x[:3]
-    y0 = O.fp8_swiglu_expert(xt, wg, wu, wd, down=False)
-    assert np.allclose(y0, O.fp8_gate_up_rows(xt, np.full((3, 1), 0), np.ones((3, 1)),
-                                              lambda e: ex[1], (wg, wu, 0 * wd)), rtol=1e-12)
-    xq = O.quantize_rows_e4m3(xt)[2]
-    hid = O.silu(xq @ O.quantize_rows_e4m3(wg)[2].T) * (xq @ O.quantize_rows_e4m3(wu)[2].T)
-    # H held in bf16 before it is quantized: rounded by hand (8 significant
-    # bits, ties to even) for the finite normal values here
-    def bf16(v):
-        m, e = np.frexp(v)                      # v = m 2^e, 0.5 <= |m| < 1
-        return np.ldexp(np.round(m * 256.0), e - 8)  # numpy rounds half to even
-    assert np.array_equal(O.round_bf16(hid), bf16(hid))
-    assert O.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0  # a tie goes to the even neighbour
-    assert O.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
-    ch, shs, _ = O.quantize_rows_e4m3(bf16(hid))
-    cw, sw, _ = O.quantize_rows_e4m3(wd)
-    e4 = dict(_e4m3_values())
-    val = np.vectorize(lambda c: e4[int(c)])
-    y_codes = shs.astype(np.float64)[:, None] * (val(ch) @ val(cw).T) * sw.astype(np.float64)[None, :]
-    y1 = O.fp8_swiglu_expert(xt, wg, wu, wd, down=True)
-    assert np.allclose(y1, y_codes, rtol=1e-12, atol=1e-300)
-    assert not np.allclose(y1, y0, rtol=1e-6)
-    y2 = O.fp8_swiglu_expert(xt, wg, wu, wd * 2.0 ** -9, down=True)
-    assert np.array_equal(y2, y1 * 2.0 ** -9)
-    # neither product quantized: the textbook SwiGLU expert
-    assert np.array_equal(O.fp8_swiglu_expert(xt, wg, wu, wd, down=False, gate_up=False),
-                          O.swiglu_expert(xt, wg, wu, wd))
-    # down only: H from the unquantized tokens and weights
-    hid_b = O.silu(xt @ wg.T) * (xt @ wu.T)
-    chb, shb, _ = O.quantize_rows_e4m3(bf16(hid_b))
-    yb = shb.astype(np.float64)[:, None] * (val(chb) @ val(cw).T) * sw.astype(np.float64)[None, :]
-    assert np.allclose(O.fp8_swiglu_expert(xt, wg, wu, wd, down=True, gate_up=False), yb,
-                       rtol=1e-12, atol=1e-300)
-    rows = O.fp8_expert_rows(x, idx, gates, lambda e: ex[e], sh, down=True)
-    one = O.fp8_swiglu_expert(x[2:3], *sh, down=True) + sum(
-        gates[2, j] * O.fp8_swiglu_expert(x[2:3], *ex[idx[2, j]], down=True) for j in range(idx.shape[1]))
-    assert np.allclose(rows[2:3], one, rtol=1e-12)
-
-
 def pin_e4m3_round(O):
     """e4m3 rounding written from the format: every finite e4m3 value is kept
     with the format's own code; the midpoint of two neighbours goes to the
@@ -837,7 +791,6 @@ PINS = [
     pin_backward_rows_agree,
     pin_quantize_e4m3,
     pin_fp8_gate_up,
-    pin_fp8_down,
     pin_e4m3_round,
     pin_block_exponent,
     pin_quantize_blocks,

@@ -38,7 +38,7 @@ def test_error_strings():
 @pytest.mark.parametrize("bad", [
     dict(T=-1), dict(d=0), dict(h=0), dict(E=0), dict(E=1025), dict(k=0), dict(k=33, E=64),
     dict(k=9, E=8), dict(d=96), dict(h=100), dict(dtype=7), dict(flags=8), dict(flags=16),
-    dict(flags=32),
+    dict(flags=32), dict(flags=64),
 ])
 def test_invalid_desc_has_no_workspace(bad):
     kw = dict(T=64, d=256, h=128, E=16, k=4, dtype="f32", flags=0)
@@ -165,24 +165,47 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     assert M.moe_host_io_extra_bytes(desc) >= 2 * T * d * el
 
 
-@pytest.mark.parametrize("F", [M.MOE_FP8_GATE_UP, M.MOE_FP8_DOWN, M.MOE_FP8_EXPERTS])
+@pytest.mark.parametrize("F", [M.MOE_FP8_GATE_UP, M.MOE_FP8_BLOCK])
 def test_fp8_flags(F):
-    # bf16 tensor-core forward only
+    # bf16 tensor-core forward only; the two fp8 modes do not combine; flag
+    # 16 is not a flag
     for bad in (("f32", F), ("bf16", F | M.MOE_SIMT_EXPERTS), ("bf16", F | M.MOE_ROUTE_ONLY),
-                ("bf16", F | M.MOE_TRAINING)):
+                ("bf16", F | M.MOE_TRAINING), ("bf16", M.MOE_FP8_GATE_UP | M.MOE_FP8_BLOCK),
+                ("bf16", F | 16)):
         assert M.moe_workspace_size(M.make_desc(64, 256, 128, 16, 4, bad[0], bad[1])) == 0
     T, d, h, E, k = 300, 7168, 2048, 256, 8
     desc = M.make_desc(T, d, h, E, k, "bf16", F)
     regs = M.moe_workspace_regions(desc)
     assert len(regs) == 13
-    gu, dn = bool(F & M.MOE_FP8_GATE_UP), bool(F & M.MOE_FP8_DOWN)
-    # gate/up: the gathered token rows hold one-byte codes; x_q: the tokens'
-    # codes, then their row scales.  down: h_q holds H's codes and scales.
-    assert regs["x_perm"][1] == T * k * d * (1 if gu else 2)
-    assert regs["x_q"][1] == ((T * d + 255) // 256 * 256 + 4 * T if gu else 0)
     R = T * k + T
-    assert regs["h_q"][1] == ((R * h + 255) // 256 * 256 + 4 * R if dn else 0)
+    # the gathered token rows hold one-byte codes in both modes
+    assert regs["x_perm"][1] == T * k * d
+    if F == M.MOE_FP8_GATE_UP:
+        # x_q: the tokens' codes, then their row scales; H in bf16
+        assert regs["x_q"][1] == (T * d + 255) // 256 * 256 + 4 * T
+        assert regs["h_q"][1] == 0 and regs["h"][1] == R * h * 2
+    else:
+        # x_q: codes, then exponent words [ceil(d / 512)][T]; h_q likewise for
+        # the hidden rows, which are never held in bf16
+        assert regs["x_q"][1] == (T * d + 255) // 256 * 256 + 4 * T * ((d // 128 + 3) // 4)
+        assert regs["h_q"][1] == (R * h + 255) // 256 * 256 + 4 * R * ((h // 128 + 3) // 4)
+        assert regs["h"][1] == 0
     assert regs["x_q"][0] % 256 == 0 and regs["h_q"][0] % 256 == 0
+
+
+def test_block_packed_layout_and_argument_errors():
+    assert M.moe_e4m3_block_packed_bytes(128, 640) == 128 * 640 + 4 * 2
+    assert M.moe_e4m3_block_packed_bytes(256, 7168) == 256 * 7168 + 2 * 14 * 4
+    for rows, cols in ((100, 128), (128, 100), (0, 128), (-128, 128), (128, 0)):
+        expect = (256 * 0 + 0) if rows == 0 and cols == 128 else 0
+        assert M.moe_e4m3_block_packed_bytes(rows, cols) == expect
+    E = M.ERR_CODE
+    q = lambda a=FAKE, rows=128, cols=128, out=FAKE: M.moe_quantize_blocks_e4m3(  # noqa: E731
+        a, rows, cols, out, check=False)
+    assert q(cols=100) == E["MOE_ERR_SHAPE"] and q(rows=64) == E["MOE_ERR_SHAPE"]
+    assert q(a=None) == E["MOE_ERR_NULL"] and q(out=None) == E["MOE_ERR_NULL"]
+    assert q(out=FAKE + 8) == E["MOE_ERR_ALIGN"]
+    assert q(rows=0, a=None) == M.MOE_OK
 
 
 def test_e4m3_packed_layout_and_argument_errors():

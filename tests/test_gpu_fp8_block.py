@@ -156,6 +156,9 @@ LAYERS = [
     dict(T=513, d=384, h=256, E=12, k=3),    # ragged tiles
     dict(T=2048, d=256, h=256, E=4, k=2),    # five token tiles of <= 240 per expert
     dict(T=16, d=512, h=512, E=64, k=8),     # decode-like: tiles of 16 tokens
+    dict(T=1, d=1024, h=256, E=16, k=4),     # one token
+    dict(T=513, d=2048, h=512, E=8, k=8),    # k = E: every expert takes every token
+    dict(T=700, d=640, h=640, E=6, k=2),     # d, h = 5 blocks: a partial exponent word
 ]
 
 

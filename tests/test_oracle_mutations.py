@@ -295,43 +295,16 @@ def _fp8_codes_only(x_rows, idx_rows, gate_rows, get_expert, shared):
                                        q(shared))
 
 
-def _fp8_expert_down_ignored(x, w_gate, w_up, w_down, down, gate_up=True):
-    return _ORIG["fp8_swiglu_expert"](x, w_gate, w_up, w_down, False, gate_up)
 
 
-def _fp8_expert_always_gate_up(x, w_gate, w_up, w_down, down, gate_up=True):
-    return _ORIG["fp8_swiglu_expert"](x, w_gate, w_up, w_down, down, True)
 
 
-def _fp8_expert_h_per_column(x, w_gate, w_up, w_down, down, gate_up=True):
-    q = _ORIG["quantize_rows_e4m3"]
-    xq = q(x)[2] if gate_up else np.asarray(x, F64)
-    wq = (lambda w: q(w)[2]) if gate_up else (lambda w: np.asarray(w, F64))
-    hid = _ORIG["silu"](xq @ wq(w_gate).T) * (xq @ wq(w_up).T)
-    if down:
-        return q(_ORIG["round_bf16"](hid).T)[2].T @ q(w_down)[2].T
-    return hid @ np.asarray(w_down, F64).T
 
 
-def _fp8_expert_h_unrounded(x, w_gate, w_up, w_down, down, gate_up=True):
-    q = _ORIG["quantize_rows_e4m3"]
-    xq = q(x)[2] if gate_up else np.asarray(x, F64)
-    wq = (lambda w: q(w)[2]) if gate_up else (lambda w: np.asarray(w, F64))
-    hid = _ORIG["silu"](xq @ wq(w_gate).T) * (xq @ wq(w_up).T)
-    if down:
-        return q(hid)[2] @ q(w_down)[2].T
-    return hid @ np.asarray(w_down, F64).T
 
 
-def _round_bf16_truncates(a):
-    import torch
-    t = torch.as_tensor(np.asarray(a, dtype=np.float32))
-    return (t.view(torch.int32) & ~0xFFFF).view(torch.float32).double().numpy()
 
 
-def _fp8_rows_ungated(x_rows, idx_rows, gate_rows, get_expert, shared, down, gate_up=True):
-    return _ORIG["fp8_expert_rows"](x_rows, idx_rows, np.ones_like(gate_rows), get_expert,
-                                    shared, down, gate_up)
 
 
 def _e4m3_round_half_away(v):
@@ -419,7 +392,8 @@ def _fp8_block_h_rounded_bf16(x, w_gate, w_up, w_down, gate_up, down):
         g, u = xq @ q(w_gate, 128)[2].T, xq @ q(w_up, 128)[2].T
     else:
         g, u = x @ np.asarray(w_gate, F64).T, x @ np.asarray(w_up, F64).T
-    hid = _ORIG["round_bf16"](_ORIG["silu"](g) * u)
+    import torch
+    hid = torch.as_tensor(_ORIG["silu"](g) * u).to(torch.bfloat16).to(torch.float64).numpy()
     if down:
         return q(hid, 1)[2] @ q(w_down, 128)[2].T
     return hid @ np.asarray(w_down, F64).T
@@ -491,12 +465,6 @@ MUTATIONS = [
     ("fp8_gate_up_rows", _fp8_unquantized_tokens),
     ("fp8_gate_up_rows", _fp8_down_quantized),
     ("fp8_gate_up_rows", _fp8_codes_only),
-    ("fp8_swiglu_expert", _fp8_expert_down_ignored),
-    ("fp8_swiglu_expert", _fp8_expert_h_per_column),
-    ("fp8_swiglu_expert", _fp8_expert_always_gate_up),
-    ("fp8_swiglu_expert", _fp8_expert_h_unrounded),
-    ("round_bf16", _round_bf16_truncates),
-    ("fp8_expert_rows", _fp8_rows_ungated),
     ("e4m3_round", _e4m3_round_half_away),
     ("e4m3_round", _e4m3_round_truncate),
     ("e4m3_round", _e4m3_round_two_bits),
