@@ -14,6 +14,7 @@ v3_prefill         8192   7168  2048  256  8   bf16   3     b ~ U(-0.01, 0.01)
 v3_decode          128    7168  2048  256  8   bf16   4     b = 0, balanced
 v3_decode_zipf     128    7168  2048  256  8   bf16   4     Zipf(1.2) router skew
 v3_prefill_32exp.  1024   7168  2048  32   8   bf16   3     profiling-size prefill
+v3_decode_32exp.   16     7168  2048  32   8   bf16   4     profiling-size decode
 =================  =====  ====  ====  ===  ==  =====  ====  ======================
 
 Distributions: x ~ N(0,1); W_gate, W_up ~ N(0, 1/d); W_down ~ N(0, 1/h);
@@ -87,6 +88,9 @@ WORKLOADS = {
         # V3 expert shapes with 32 experts and ~256 tokens per expert: the
         # prefill GEMM regime on 2.9 GB of weights, for profiler captures
         Workload("v3_prefill_32experts", 1024, 7168, 2048, 32, 8, "bf16", 3, bias="uniform"),
+        # the decode regime (about 4 tokens per expert) on the same 32
+        # experts' weights, for profiler captures of the decode GEMMs
+        Workload("v3_decode_32experts", 16, 7168, 2048, 32, 8, "bf16", 4, bias="zero"),
     ]
 }
 
