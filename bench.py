@@ -653,7 +653,8 @@ def run_train(args, wl):
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
     inp = I.make_inputs(wl.with_(seed=wl.seed + 1000 * rank) if ws > 1 else wl, device="cuda")
-    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_TRAINING)
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype,
+                                 M.MOE_TRAINING | (M.MOE_GRAD_BF16 if args.grad_bf16 else 0))
     gen = torch.Generator(device="cuda").manual_seed(wl.seed + 7)
     dy = torch.randn((wl.T, wl.d), generator=gen, device="cuda").to(inp["x"].dtype)
     x = inp["x"]
@@ -694,7 +695,8 @@ def run_train(args, wl):
         "metric": METRIC + " [training step: forward + backward]", "value": value,
         "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 (fp32 weight gradients)",
+        "vs_baseline": None,
+        "dtype": "bf16 (bf16 weight gradients)" if args.grad_bf16 else "bf16 (fp32 weight gradients)",
         "data": "synthetic (seeded N(0,1) tokens and output gradient, N(0,1/fan_in) weights)",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "h": wl.h, "E": wl.E, "k": wl.k,
                    "l2": "inputs larger than L2"},
@@ -783,6 +785,8 @@ def main():
                     help="skip the V3 decode runs that follow the V3 prefill line")
     ap.add_argument("--train", action="store_true",
                     help="time a training step: forward and backward")
+    ap.add_argument("--grad-bf16", action="store_true",
+                    help="with --train: weight gradients written in bf16 (MOE_GRAD_BF16)")
     ap.add_argument("--fp8", nargs="?", const="gate_up", choices=["gate_up", "block"],
                     help="expert products on e4m3 codes: gate/up only with per-row scales "
                          "(MOE_FP8_GATE_UP, the default), or both with 128x128 / 1x128 "

@@ -93,6 +93,11 @@ enum {
                                 packed quantized matrices; w_down stays bf16; the
                                 tokens are quantized per row inside the call */
 /* (flag 16 is not used) */
+#define MOE_GRAD_BF16   64u  /* with MOE_TRAINING: moe_backward writes the expert
+                                weight gradients (d_gate, d_up, d_down of experts
+                                and shared) in bf16 -- fp32 sums rounded once --
+                                instead of fp32, half the bytes; the router
+                                gradient stays fp32 */
 #define MOE_FP8_BLOCK   32u  /* bf16 tensor-core path only, not with MOE_TRAINING or
                                 MOE_FP8_GATE_UP: both expert products on
                                 block-scaled e4m3 codes (moe_quantize_blocks_e4m3);
@@ -110,7 +115,7 @@ typedef struct {
   int T, d, h, E, k;
   int dtype;        /* moe_dtype */
   unsigned flags;   /* MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING |
-                       MOE_FP8_GATE_UP | MOE_FP8_BLOCK */
+                       MOE_FP8_GATE_UP | MOE_FP8_BLOCK | MOE_GRAD_BF16 */
 } moe_desc;
 
 /* Expert weights, element type desc->dtype.
@@ -281,9 +286,10 @@ MOE_API int moe_seq_balance_loss(const moe_desc* desc, int seq_len, float alpha,
                                  const int32_t* topk_idx, const void* workspace,
                                  size_t ws_bytes, float* loss, void* stream);
 
-/* Gradients of expert weights (device, fp32, written in full -- experts that
- * no token selected get zeros).  Routed: d_gate [E, h, d], d_up [E, h, d],
- * d_down [E, d, h]; shared: the same with E = 1. */
+/* Gradients of expert weights (device, fp32 -- or bf16 with MOE_GRAD_BF16,
+ * the pointers then holding bf16 arrays of the same shapes -- written in
+ * full: experts that no token selected get zeros).  Routed: d_gate [E, h, d],
+ * d_up [E, h, d], d_down [E, d, h]; shared: the same with E = 1. */
 typedef struct {
   float *d_gate, *d_up, *d_down;
 } moe_expert_grad;

@@ -111,6 +111,51 @@ k_bwd_zero_gaps(const int32_t* __restrict__ groups, int E, __nv_bfloat16* __rest
   }
 }
 
+// ---------------------------------------------------------------- SwiGLU gradient
+// dA = dH B silu'(A), dB = dH silu(A) from the pre-activations the training
+// forward stored (A|B rows [rows, 2h], bf16, the forward's row order) and dH
+// ([rows, h]); written to the padded dA|dB rows ([., 2h]).  One warp per
+// row, 8 columns per lane per step; silu'(a) = s (1 + a (1 - s)), s =
+// sigmoid(a).
+__global__ void __launch_bounds__(256)
+k_bwd_swiglu(const int32_t* __restrict__ groups, int E, int rows, int h,
+             const __nv_bfloat16* __restrict__ ab, const __nv_bfloat16* __restrict__ dh,
+             __nv_bfloat16* __restrict__ dab) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  GroupTable G = group_table(const_cast<int32_t*>(groups), E);
+  int lo = 0, hi = E;  // the group g with off[g] <= r < off[g + 1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (G.off[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  const int prow = G.poff[lo] + (r - G.off[lo]);
+  const uint4* pa = reinterpret_cast<const uint4*>(ab + (size_t)r * 2 * h);
+  const uint4* pb = reinterpret_cast<const uint4*>(ab + (size_t)r * 2 * h + h);
+  const uint4* pg = reinterpret_cast<const uint4*>(dh + (size_t)r * h);
+  uint4* qa = reinterpret_cast<uint4*>(dab + (size_t)prow * 2 * h);
+  uint4* qb = reinterpret_cast<uint4*>(dab + (size_t)prow * 2 * h + h);
+  for (int i = lane; i < h / 8; i += 32) {
+    const uint4 va = pa[i], vb = pb[i], vg = pg[i];
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w},
+                   wg[4] = {vg.x, vg.y, vg.z, vg.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[m]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[m]));
+      const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wg[m]));
+      const float s0 = 1.0f / (1.0f + __expf(-a.x)), s1 = 1.0f / (1.0f + __expf(-a.y));
+      oa[m] = pack_bf16x2(g.x * b.x * (s0 * (1.0f + a.x * (1.0f - s0))),
+                          g.y * b.y * (s1 * (1.0f + a.y * (1.0f - s1))));
+      ob[m] = pack_bf16x2(g.x * (a.x * s0), g.y * (a.y * s1));
+    }
+    qa[i] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    qb[i] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
 // ---------------------------------------------------------------- router
 // One warp per token: lane j < k takes slot j.  s_j = sigmoid(u_j) from the
 // router's partial logits (summed in slice order, as the top-k did), g_j =
@@ -280,6 +325,9 @@ MOE_DEV WgTile wg_tile(const GroupTable& G, int E, int b, int MB, int NB, int pc
 // of dA|dB); M, N: output rows / columns per group; `shared_p_from_ps`: the
 // shared group's P rows come from the map ps at row 0 (dy) rather than the
 // routed map at the shared group's padded row; same for Q.
+// BF16OUT: the fp32 sums are rounded once to bf16 and stored as 32 x 32 bf16
+// boxes (64-byte rows, 64-byte swizzle), half the bytes of the fp32 output.
+template <bool BF16OUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(WG_THREADS, 1)
 k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ groups, int E,
             int M, int N, int pcol0, int qcol0, int counter_slot, int shared_p_from_ps,
@@ -478,13 +526,28 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
         const uint32_t box = stg + (uint32_t)((nbox % WG_BOXES) * WG_BOX_BYTES);
         if (lane == 0) bulk_wait_read<WG_BOXES - 1>();  // the box's previous store has read it
         __syncwarp();
-        // row `lane` of the box, 16-byte chunk j at chunk j ^ (lane & 7)
+        if (BF16OUT) {
+          // row `lane` of the box: 32 bf16 in four 16-byte chunks, chunk j at
+          // j ^ ((lane >> 1) & 3)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t a = box + (uint32_t)(lane * 128 + 16 * (j ^ (lane & 7)));
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[4 * j]),
-                       "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
-                       : "memory");
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a = box + (uint32_t)(lane * 64 + 16 * (j ^ ((lane >> 1) & 3)));
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                         "r"(pack_bf16x2(v[8 * j], v[8 * j + 1])),
+                         "r"(pack_bf16x2(v[8 * j + 2], v[8 * j + 3])),
+                         "r"(pack_bf16x2(v[8 * j + 4], v[8 * j + 5])),
+                         "r"(pack_bf16x2(v[8 * j + 6], v[8 * j + 7]))
+                         : "memory");
+          }
+        } else {
+          // row `lane` of the box, 16-byte chunk j at chunk j ^ (lane & 7)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t a = box + (uint32_t)(lane * 128 + 16 * (j ^ (lane & 7)));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[4 * j]),
+                         "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                         : "memory");
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();

@@ -247,45 +247,6 @@ MOE_DEV void stage_box_scaled(uint32_t ta, uint32_t tb, uint32_t box, int lane,
   }
 }
 
-// SwiGLU gradient of 32 tokens x this warp's 32 hidden units, through shared
-// memory: `dh_box` holds dH (box row = token, as stage_box_bf16 writes
-// them); gate (ta) and up (tb) accumulators are read in the 16x256b shape,
-// dH in the same fragment layout by ldmatrix .trans; dA = dH up silu'(gate)
-// and dB = dH silu(gate) are written to `da_box` and `db_box` by stmatrix.
-MOE_DEV void stage_swiglu_grad(uint32_t ta, uint32_t tb, uint32_t dh_box, uint32_t da_box,
-                               uint32_t db_box, int lane) {
-  const int mm = lane >> 3, ii = lane & 7;
-#pragma unroll
-  for (int L = 0; L < 32; L += 16) {
-    uint32_t ra[16], rb[16];
-    tmem_load_16x256b_2(ta + ((uint32_t)L << 16), tb + ((uint32_t)L << 16), ra, rb);
-#pragma unroll
-    for (int ip = 0; ip < 2; ++ip) {
-      const int tok = 8 * (2 * ip + (mm >> 1)) + ii, chunk = (L >> 3) + (mm & 1);
-      const uint32_t off = (uint32_t)(tok * 64 + 16 * (chunk ^ ((tok >> 1) & 3)));
-      uint32_t g4[4], wa[4], wb[4];
-      ldmatrix_x4_trans(dh_box + off, g4[0], g4[1], g4[2], g4[3]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int m = 4 * ip + q;  // matrix: columns 8 i .., lanes L + 8 hf ..
-        const float2 gh = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g4[q]));
-        float da[2], db[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float a = __uint_as_float(ra[2 * m + e]), up = __uint_as_float(rb[2 * m + e]);
-          const float sg = 1.0f / (1.0f + __expf(-a)), g = e ? gh.y : gh.x;
-          da[e] = g * up * (sg * (1.0f + a * (1.0f - sg)));
-          db[e] = g * (a * sg);
-        }
-        wa[q] = pack_bf16x2(da[0], da[1]);
-        wb[q] = pack_bf16x2(db[0], db[1]);
-      }
-      stmatrix_x4_trans(da_box + off, wa[0], wa[1], wa[2], wa[3]);
-      stmatrix_x4_trans(db_box + off, wb[0], wb[1], wb[2], wb[3]);
-    }
-  }
-}
-
 template <int BN, int SA, int SB>
 struct TcCfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per weight sub-tile

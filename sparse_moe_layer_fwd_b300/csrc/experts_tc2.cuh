@@ -42,13 +42,16 @@ enum : int {
   TC2_FWD_UP = 0,    // H = silu(X W_gate^T) * (X W_up^T)                      K = d
   TC2_FWD_DOWN = 1,  // Y = H W_down^T                                          K = h
   TC2_BWD_DH = 2,    // dH = dY W_down (W_down read transposed)                 K = d
-  TC2_BWD_DAB = 3,   // gate/up recomputed: dA = dH up silu'(gate), dB = dH silu(gate)
+  // (3: unused -- the SwiGLU gradient is an elementwise kernel on the
+  //  pre-activations the training forward stores, TC2_FWD_UP_T)
   TC2_BWD_DX = 4,    // dX = dA W_gate + dB W_up (weights read transposed)      K = 2h
   TC2_FWD_UP_FP8 = 5,  // H as TC2_FWD_UP from e4m3 codes of weights and tokens
                        // with per-row scales (kind::f8f6f4)          K = d (bytes)
   TC2_FWD_UP_B8 = 7,     // H as TC2_FWD_UP from block-scaled e4m3 codes (kind::mxf8f6f4), H
                          // written as e4m3 codes with one scale per 1 x 128 block   K = d (bytes)
   TC2_FWD_DOWN_B8 = 8,   // Y as TC2_FWD_DOWN from block-scaled e4m3 codes of W_down and H
+  TC2_FWD_UP_T = 9,      // H as TC2_FWD_UP, and (for the backward) the pre-activations
+                         // A = X W_gate^T, B = X W_up^T as bf16 rows [rows, 2h]
 };
 // two blocks of 256 rows of one matrix per tile (else gate and up rows)
 __host__ __device__ constexpr bool tc2_down(int op) {
@@ -122,9 +125,8 @@ struct Tc2Cfg {
   static constexpr int BAR_OFF = XCH_OFF + (BLK ? 2 * 2 * 4 * 32 * 4 : 0);
   // a_full, a_empty [SA]; b_full, b_empty [SB]; acc_full, acc_empty [2];
   // drain; tile_full, tile_empty [RING]
-  // (+ one per epilogue warp: its staged input box, the SwiGLU gradient's dH)
   // (+ block-scaled: sf_full, sf_empty [2]; the exchange's [2 halves][2])
-  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + TC_EPI_WARPS + (BLK ? 8 : 0);
+  static constexpr int N_BARS = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + (BLK ? 8 : 0);
   static constexpr int MISC_BYTES = 4 * TC_TILE_RING + 4 * 5;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * N_BARS + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -181,7 +183,7 @@ MOE_DEV Tc2Tile tc2_tile(const GroupTable& G, const int32_t* toff, int E, int b,
   // down projection, the padded dY rows / dy (shared) for dH, the padded
   // dA|dB rows for dX
   int rb;
-  if (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_FWD_UP_FP8 || OP == TC2_FWD_UP_B8)
+  if (OP == TC2_FWD_UP || OP == TC2_FWD_UP_FP8 || OP == TC2_FWD_UP_B8 || OP == TC2_FWD_UP_T)
     rb = t.shared ? t.tok0 : G.off[g] + t.tok0;
   else if (OP == TC2_FWD_DOWN || OP == TC2_FWD_DOWN_B8)
     rb = G.off[g] + t.tok0;
@@ -197,17 +199,19 @@ template <int SA, int SB, int NACC, int NBUF, int OUTB, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc2_threads(OP), 1)
 k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
              int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh,
-             const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs, const Fp8Blk fb) {
+             const __nv_bfloat16* __restrict__ aux, const Fp8Scales fs, const Fp8Blk fb,
+             __nv_bfloat16* __restrict__ out2) {
   constexpr bool DOWN = tc2_down(OP);
   constexpr bool MNA = tc2_mn_a(OP);
   constexpr bool FP8U = OP == TC2_FWD_UP_FP8;
   constexpr bool FP8 = FP8U;  // per-row scales, applied in the epilogue
   constexpr bool BLK = tc2_blk(OP);   // block scales, applied by the MMA
   constexpr bool UPB = OP == TC2_FWD_UP_B8;
+  constexpr bool UPT = OP == TC2_FWD_UP_T;  // also A|B (out2; TMA stores through maps.aux)
   constexpr int KB_ELEMS = (FP8 || BLK) ? 128 : TC_BK;  // elements per 128-byte K step
   using C = Tc2Cfg<SA, SB, NACC, NBUF, OUTB, BLK>;
   static_assert(OUTB >= 0 && OUTB <= 3, "staged boxes per epilogue warp");
-  static_assert(OP != TC2_BWD_DAB || OUTB == 0 || OUTB == 3, "dH in, dA and dB out");
+  static_assert(OP != TC2_FWD_UP_T || OUTB == 0 || OUTB == 3, "H, A and B out");
   // second GEMM with both 256-row blocks in one TMEM buffer: staggered blocks
   constexpr bool STAG = DOWN && NACC == 2 && NBUF == 1;
   static_assert(!DOWN || STAG || NACC == 1, "second GEMM: two staggered blocks or one block");
@@ -219,9 +223,9 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const bool leader = rank == 0;
 
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
-  const int32_t* toff = (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || FP8U || UPB) ? G.toff_a
+  const int32_t* toff = (OP == TC2_FWD_UP || FP8U || UPB || UPT) ? G.toff_a
                         : (OP == TC2_BWD_DH ? G.toff_c : G.toff_b);
-  int* counter = G.next + ((FP8U || UPB) ? TC2_FWD_UP : BLK ? TC2_FWD_DOWN : OP);
+  int* counter = G.next + ((FP8U || UPB || UPT) ? TC2_FWD_UP : BLK ? TC2_FWD_DOWN : OP);
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
@@ -237,8 +241,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const uint32_t drain_bar = bar(2 * SA + 2 * SB + 4);
   auto tile_full = [&](int s) { return bar(2 * SA + 2 * SB + 5 + s); };
   auto tile_empty = [&](int s) { return bar(2 * SA + 2 * SB + 5 + TC_TILE_RING + s); };
-  auto aux_full = [&](int w) { return bar(2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + w); };
-  constexpr int SFB0 = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING + TC_EPI_WARPS;
+  constexpr int SFB0 = 2 * SA + 2 * SB + 5 + 2 * TC_TILE_RING;
   auto sf_full = [&](int s) { return bar(SFB0 + s); };
   auto sf_empty = [&](int s) { return bar(SFB0 + 2 + s); };
   auto xch_bar = [&](int hf, int par) { return bar(SFB0 + 4 + 2 * hf + par); };
@@ -266,7 +269,6 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       mbar_init(tile_full(s), 1);
       mbar_init(tile_empty(s), 2 * (TC2_CONSUMERS + (BLK ? 1 : 0)));  // consumers of both CTAs
     }
-    for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(aux_full(w), 1);
     if (BLK) {
       for (int s = 0; s < 2; ++s) {
         mbar_init(sf_full(s), 2);   // the scale warps of both CTAs (leader's barrier)
@@ -383,7 +385,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
         if (b < 0) break;
         const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
         const bool bs =
-            (OP == TC2_FWD_UP || OP == TC2_BWD_DAB || OP == TC2_BWD_DH || FP8U || UPB) && t.shared;
+            (OP == TC2_FWD_UP || OP == TC2_BWD_DH || FP8U || UPB || UPT) &&
+            t.shared;
         const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
         const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
         const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
@@ -632,7 +635,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
-    int tl = 0, nbox = 0, naux = 0, nch = 0;
+    int tl = 0, nbox = 0, nch = 0;
     for (int i = 0;; ++i) {
       const int b = next_tile(i, false);
       __syncwarp();
@@ -720,30 +723,22 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             }
             continue;
           }
-          if (OP == TC2_BWD_DAB && OUTB == 3 && c + 32 <= t.ntok) {
-            // SwiGLU gradient of 32 whole tokens: dH box in by TMA, dA and dB
-            // boxes out by TMA (one buffer of each)
-            const uint32_t dhb = stg, dab_a = stg + TC_BOX_BYTES, dab_b = stg + 2 * TC_BOX_BYTES;
-            const uint32_t ab = aux_full(warp - 2);
-            if (lane == 0) {
-              bulk_wait_read<0>();       // the last stores have read the dA, dB boxes
-              fence_proxy_async_smem();  // after this warp's reads of the last dH box
-              mbar_arrive_expect_tx(ab, TC_BOX_BYTES);
-              tma_load_2d(dhb, &maps.aux, ab, of, t.out_row0 + c, l2_policy_evict_first());
-            }
-            const bool got = mbar_wait(ab, naux & 1);
-            ++naux;
-            if (!__all_sync(0xffffffffu, got)) {
-              if (lane == 0) *abort_flag = 1;
-              break;
-            }
-            stage_swiglu_grad(ta + c, tb + c, dhb, dab_a, dab_b, lane);
+          if (UPT && OUTB == 3 && c + 32 <= t.ntok) {
+            // 32 whole tokens: H, and the pre-activations A (gate) and B
+            // (up) for the backward, staged as three boxes and stored by TMA
+            // (H rows of `out`; A|B rows [rows, 2h] through maps.aux)
+            if (lane == 0) bulk_wait_read<0>();  // the last chunk's stores have read the boxes
+            __syncwarp();
+            stage_box_bf16<true>(ta + c, tb + c, stg, lane);
+            stage_box_bf16<false>(ta + c, tb + c, stg + TC_BOX_BYTES, lane);
+            stage_box_bf16<false>(tb + c, tb + c, stg + 2 * TC_BOX_BYTES, lane);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               if (valid) {
-                tma_store_2d(&maps.out, dab_a, of, t.pout_row0 + c);
-                tma_store_2d(&maps.out, dab_b, n_out + of, t.pout_row0 + c);
+                tma_store_2d(&maps.out, stg, of, t.out_row0 + c);
+                tma_store_2d(&maps.aux, stg + TC_BOX_BYTES, of, t.out_row0 + c);
+                tma_store_2d(&maps.aux, stg + 2 * TC_BOX_BYTES, n_out + of, t.out_row0 + c);
               }
               bulk_commit();
             }
@@ -753,7 +748,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           float tsl = 0.f;
           if (FP8 && c + lane < t.ntok)
             tsl = fs.tok[t.shared ? t.tok0 + c + lane : fs.perm[t.out_row0 + c + lane] / fs.k];
-          if (OUTB > 0 && OP != TC2_BWD_DAB && c + 32 <= t.ntok && !(F32SH && t.shared)) {
+          if (OUTB > 0 && c + 32 <= t.ntok && !(F32SH && t.shared)) {
             // 32 whole tokens of bf16 output: stage the box in shared
             // memory and store it with TMA (boxes used round robin)
             const uint32_t box = stg + (uint32_t)((nbox % (OUTB > 0 ? OUTB : 1)) * TC_BOX_BYTES);
@@ -793,24 +788,15 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
               va[j] = silu_fast(va[j] * (rlg * ts)) * (vb[j] * (rlu * ts));
             }
             store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
-          } else if (OP == TC2_FWD_UP) {
+          } else if (OP == TC2_FWD_UP || UPT) {
+            if (UPT) {  // the pre-activations first, then H in place
+              __nv_bfloat16* ab = out2 + (size_t)(t.out_row0 + c) * (2 * n_out) + of;
+              store_rows_bf16(ab, 2 * n_out, va, c, t.ntok, lane);
+              store_rows_bf16(ab + n_out, 2 * n_out, vb, c, t.ntok, lane);
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
             store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
-          } else if (OP == TC2_BWD_DAB) {
-            // dH of (token c + j, this lane's hidden unit), rows as H's
-            float da[32], db[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float gh = c + j < t.ntok
-                  ? __bfloat162float(aux[(size_t)(t.out_row0 + c + j) * n_out + of + lane]) : 0.f;
-              const float a = va[j], sg = 1.0f / (1.0f + __expf(-a));
-              da[j] = gh * vb[j] * (sg * (1.0f + a * (1.0f - sg)));
-              db[j] = gh * (a * sg);
-            }
-            __nv_bfloat16* o = out + (size_t)(t.pout_row0 + c) * (2 * n_out) + of;
-            store_rows_bf16(o, 2 * n_out, da, c, t.ntok, lane);
-            store_rows_bf16(o + n_out, 2 * n_out, db, c, t.ntok, lane);
           } else if (F32SH && t.shared) {
             store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + of, n_out, va, c, t.ntok, lane);
           } else {

@@ -96,8 +96,9 @@ struct Plan {
   // workspace regions (byte offsets)
   size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh,
       o_xq, o_hq, total;
-  // backward: padded dY rows, dG, du, dH, padded dA|dB rows, dX rows, shared dX
-  size_t o_dyp, o_dg, o_du, o_dh, o_dab, o_dxp, o_dxs;
+  // backward: padded dY rows, dG, du, dH, padded dA|dB rows, dX rows, shared dX;
+  // the training forward's pre-activations A|B
+  size_t o_dyp, o_dg, o_du, o_dh, o_dab, o_dxp, o_dxs, o_ab;
   long long rows_dyp, rows_dab;  // allocated padded rows
   size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh,
       b_xq, b_hq;
@@ -106,9 +107,10 @@ struct Plan {
 int validate_desc(const moe_desc* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_DTYPE;
-  if (d->flags &
-      ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_GATE_UP | MOE_FP8_BLOCK))
+  if (d->flags & ~(MOE_ROUTE_ONLY | MOE_SIMT_EXPERTS | MOE_TRAINING | MOE_FP8_GATE_UP |
+                   MOE_FP8_BLOCK | MOE_GRAD_BF16))
     return MOE_ERR_DTYPE;
+  if ((d->flags & MOE_GRAD_BF16) && !(d->flags & MOE_TRAINING)) return MOE_ERR_DTYPE;
   if ((d->flags & (MOE_FP8_GATE_UP | MOE_FP8_BLOCK)) &&
       (d->dtype != MOE_BF16 || (d->flags & (MOE_SIMT_EXPERTS | MOE_ROUTE_ONLY | MOE_TRAINING))))
     return MOE_ERR_DTYPE;
@@ -276,6 +278,7 @@ Plan make_plan(const moe_desc* d) {
     region((size_t)p.rows_dab * 2 * p.h * 2, p.o_dab, b);
     region((size_t)p.TK * p.d * 2, p.o_dxp, b);
     region((size_t)p.T * p.d * 4, p.o_dxs, b);
+    region((size_t)(p.TK + p.T) * 2 * p.h * 2, p.o_ab, b);
   }
   p.total = off > 0 ? off : 256;
   return p;
@@ -471,22 +474,25 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   m->down.bs16 = m->down.b16;
   m->down.bs8 = m->down.b8;
   ok &= make_out_map(&m->up.out, ws + p.o_h, (long long)p.TK + p.T, p.h);
+  if (p.training)  // the pre-activations A|B rows, stored by the training forward
+    ok &= make_out_map(&m->up.aux, ws + p.o_ab, (long long)p.TK + p.T, 2LL * p.h);
   ok &= make_out_map(&m->down.out, ws + p.o_yperm, p.TK, p.d);
   return ok;
 }
 
 // The CTA-pair kernel of each operation: ring depths and staged boxes.  The
 // backward's two-block products (dH, dX) take the second GEMM's
-// configuration; the SwiGLU gradient stages three boxes per epilogue warp
-// (dH in, dA and dB out).
+// configuration; the training forward's gate/up product stages three boxes
+// per epilogue warp (H, A, B).
 // (block-scaled: the first GEMM writes H codes from registers, no staged
 // boxes; the second keeps one staged box per warp to leave room for the
 // scale stages)
 template <int OP> struct PairCfg {
   static constexpr bool UP = OP == TC2_FWD_UP || OP == TC2_FWD_UP_FP8 || OP == TC2_FWD_UP_B8;
-  static constexpr int SA = OP == TC2_BWD_DAB ? 4 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
-  static constexpr int SB = OP == TC2_BWD_DAB ? 3 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
-  static constexpr int OUTB = OP == TC2_BWD_DAB    ? 3
+  static constexpr bool B3 = OP == TC2_FWD_UP_T;  // three staged boxes per chunk (H, A, B)
+  static constexpr int SA = B3 ? 4 : (UP ? MOE_PAIR1_SA : MOE_PAIR2_SA);
+  static constexpr int SB = B3 ? 3 : (UP ? MOE_PAIR1_SB : MOE_PAIR2_SB);
+  static constexpr int OUTB = B3                      ? 3
                               : OP == TC2_FWD_UP_B8   ? 0
                               : OP == TC2_FWD_DOWN_B8 ? 1
                               : (UP ? MOE_PAIR1_OUTB : MOE_PAIR2_OUTB);
@@ -507,13 +513,14 @@ bool set_tc2_smem() {
 template <int OP>
 void launch_pair(const Plan& p, const TcMapsDev& m, int max_tiles, int32_t* groups, int K,
                  int n_out, __nv_bfloat16* out, float* ysh, const __nv_bfloat16* aux,
-                 cudaStream_t s, const Fp8Scales& fs = Fp8Scales{}, const Fp8Blk& fb = Fp8Blk{}) {
+                 cudaStream_t s, const Fp8Scales& fs = Fp8Scales{}, const Fp8Blk& fb = Fp8Blk{},
+                 __nv_bfloat16* out2 = nullptr) {
   const int pairs = sm_count() / 2;
   const int grid = 2 * (max_tiles < pairs ? max_tiles : pairs);
   using P = PairCfg<OP>;
   k_expert_tc2<P::SA, P::SB, P::NACC, P::NBUF, P::OUTB, OP>
       <<<grid, tc2_threads(OP), P::Cfg::SMEM_BYTES, s>>>(m, groups, p.E, K, n_out, out, ysh, aux,
-                                                         fs, fb);
+                                                         fs, fb, out2);
 }
 
 template <int BN, int SA, int SB, bool DOWN>
@@ -607,7 +614,8 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     const bool ok =
         p.fp8_blk ? (set_tc2_smem<TC2_FWD_UP_B8>() && set_tc2_smem<TC2_FWD_DOWN_B8>()) :
         p.big_tiles
-            ? ((p.fp8 ? set_tc2_smem<TC2_FWD_UP_FP8>()
+            ? ((p.fp8        ? set_tc2_smem<TC2_FWD_UP_FP8>()
+                : p.training ? set_tc2_smem<TC2_FWD_UP_T>()
                       : MOE_PAIR_GEMM1 ? set_tc2_smem<TC2_FWD_UP>()
                                : set_tc1_smem<kBigBN, kBigSA, kBigSB, false>()) &&
                (MOE_PAIR_GEMM2 ? set_tc2_smem<TC2_FWD_DOWN>()
@@ -705,6 +713,11 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
         // K in bf16 units of 128 bytes per step: d codes = d / 2 "elements"
         launch_pair<TC2_FWD_UP_FP8>(p, maps.up, p.max_tiles_a, groups, p.d / 2, p.h, hbuf,
                                     nullptr, nullptr, s, fs);
+      } else if (p.training) {
+        // the pre-activations A|B as well, for the backward's SwiGLU gradient
+        launch_pair<TC2_FWD_UP_T>(p, maps.up, p.max_tiles_a, groups, p.d, p.h, hbuf, nullptr,
+                                  nullptr, s, Fp8Scales{}, Fp8Blk{},
+                                  reinterpret_cast<__nv_bfloat16*>(ws + p.o_ab));
       } else {
         launch_gemm<false>(p, maps.up, p.big_tiles && MOE_PAIR_GEMM1, p.bn, p.max_tiles_a,
                            groups, hbuf, nullptr, s);
@@ -871,7 +884,11 @@ struct BwdMaps {
 
 bool make_bwd_maps(const Plan& p, const void* x, const moe_expert_w* ex, const moe_expert_w* sh,
                    const void* dy, uint8_t* ws, const moe_expert_grad* dex,
-                   const moe_expert_grad* dsh, BwdMaps* m) {
+                   const moe_expert_grad* dsh, bool grad_bf16, BwdMaps* m) {
+  // weight-gradient outputs: fp32, or bf16 with MOE_GRAD_BF16
+  auto out_map = [&](CUtensorMap* mm, const void* base, long long rows, long long cols) {
+    return grad_bf16 ? make_out_map(mm, base, rows, cols) : make_out_map_f32(mm, base, rows, cols);
+  };
   bool ok = make_tc_maps(p, x, ex, sh, ws, &m->fwd);
   const long long rows_h = (long long)p.TK + p.T;
   // dH: W_down [E*d rows, h cols] read as d-row x h-column boxes (MN-major)
@@ -896,24 +913,21 @@ bool make_bwd_maps(const Plan& p, const void* x, const moe_expert_w* ex, const m
   m->dx.bs8 = m->dx.b8;
   ok &= make_out_map(&m->dx.out, ws + p.o_dxp, p.TK, p.d);
   // weight gradients: both operands MN-major, 64-column x 64-row boxes
-  // the SwiGLU gradient reads dH boxes and writes dA|dB boxes
-  ok &= make_out_map(&m->fwd.up.out, ws + p.o_dab, p.rows_dab, 2LL * p.h);
-  ok &= make_out_map(&m->fwd.up.aux, ws + p.o_dh, rows_h, p.h);
   ok &= make_map(&m->wd.p, ws + p.o_dyp, p.rows_dyp, p.d, 64);
   ok &= make_map(&m->wd.ps, dy, p.T, p.d, 64);
   ok &= make_map(&m->wd.q, ws + p.o_h, rows_h, p.h, 64);
   m->wd.qs = m->wd.q;
-  ok &= make_out_map_f32(&m->wd.o, dex->d_down, (long long)p.E * p.d, p.h);
-  ok &= make_out_map_f32(&m->wd.os, dsh->d_down, p.d, p.h);
+  ok &= out_map(&m->wd.o, dex->d_down, (long long)p.E * p.d, p.h);
+  ok &= out_map(&m->wd.os, dsh->d_down, p.d, p.h);
   ok &= make_map(&m->wg.p, ws + p.o_dab, p.rows_dab, 2LL * p.h, 64);
   m->wg.ps = m->wg.p;
   ok &= make_map(&m->wg.q, ws + p.o_xperm, p.TK, p.d, 64);
   ok &= make_map(&m->wg.qs, x, p.T, p.d, 64);
   m->wu = m->wg;
-  ok &= make_out_map_f32(&m->wg.o, dex->d_gate, (long long)p.E * p.h, p.d);
-  ok &= make_out_map_f32(&m->wg.os, dsh->d_gate, p.h, p.d);
-  ok &= make_out_map_f32(&m->wu.o, dex->d_up, (long long)p.E * p.h, p.d);
-  ok &= make_out_map_f32(&m->wu.os, dsh->d_up, p.h, p.d);
+  ok &= out_map(&m->wg.o, dex->d_gate, (long long)p.E * p.h, p.d);
+  ok &= out_map(&m->wg.os, dsh->d_gate, p.h, p.d);
+  ok &= out_map(&m->wu.o, dex->d_up, (long long)p.E * p.h, p.d);
+  ok &= out_map(&m->wu.os, dsh->d_up, p.h, p.d);
   return ok;
 }
 
@@ -943,7 +957,9 @@ int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
   rc = device_ok();
   if (rc != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t e_hd = (size_t)p.E * p.h * p.d * 4, hd = (size_t)p.h * p.d * 4;
+  const bool gb = desc->flags & MOE_GRAD_BF16;
+  const size_t gel = gb ? 2 : 4;  // bytes per weight-gradient element
+  const size_t e_hd = (size_t)p.E * p.h * p.d * gel, hd = (size_t)p.h * p.d * gel;
   cudaGetLastError();
   if (p.T == 0) {  // no tokens: every gradient is zero
     const bool ok = cudaMemsetAsync(d_experts->d_gate, 0, e_hd, s) == cudaSuccess &&
@@ -957,11 +973,12 @@ int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdMaps maps;
-  if (!make_bwd_maps(p, x, experts, shared, dy, ws, d_experts, d_shared, &maps))
+  if (!make_bwd_maps(p, x, experts, shared, dy, ws, d_experts, d_shared, gb, &maps))
     return MOE_ERR_DEVICE;
-  if (!set_tc2_smem<TC2_BWD_DH>() || !set_tc2_smem<TC2_BWD_DAB>() ||
-      !set_tc2_smem<TC2_BWD_DX>() ||
-      cudaFuncSetAttribute(k_wgrad_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!set_tc2_smem<TC2_BWD_DH>() || !set_tc2_smem<TC2_BWD_DX>() ||
+      cudaFuncSetAttribute(k_wgrad_tc2<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           WG_SMEM_BYTES) != cudaSuccess ||
+      cudaFuncSetAttribute(k_wgrad_tc2<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            WG_SMEM_BYTES) != cudaSuccess)
     return MOE_ERR_LAUNCH;
 
@@ -986,15 +1003,21 @@ int moe_backward(const moe_desc* desc, const void* x, const float* w_router,
   k_bwd_router<<<(p.T + 7) / 8, 256, 0, s>>>(part, p.n_split, topk_idx, inv, dg, p.T, p.E, p.k,
                                                du);
   launch_pair<TC2_BWD_DH>(p, maps.dh, p.max_tiles_c, groups, p.d, p.h, dh, nullptr, nullptr, s);
-  launch_pair<TC2_BWD_DAB>(p, maps.fwd.up, p.max_tiles_a, groups, p.d, p.h, dab, nullptr, dh, s);
+  // SwiGLU gradient from the pre-activations the forward stored
+  k_bwd_swiglu<<<(unsigned)((p.TK + p.T + 7) / 8), 256, 0, s>>>(
+      groups, p.E, p.TK + p.T, p.h, reinterpret_cast<const __nv_bfloat16*>(ws + p.o_ab), dh, dab);
   launch_pair<TC2_BWD_DX>(p, maps.dx, p.max_tiles_b, groups, 2 * p.h, p.d, dxp, dxs, nullptr, s);
   const int pairs = sm_count() / 2;
   auto wgrad = [&](const WgMapsDev& m, int M, int N, int pcol0, int slot, int p_from_ps,
                    int q_from_qs) {
     const long long tiles = (long long)(p.E + 1) * ((M + 255) / 256) * ((N + 255) / 256);
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    k_wgrad_tc2<<<grid, WG_THREADS, WG_SMEM_BYTES, s>>>(m, groups, p.E, M, N, pcol0, 0, slot,
-                                                         p_from_ps, q_from_qs);
+    if (gb)
+      k_wgrad_tc2<true><<<grid, WG_THREADS, WG_SMEM_BYTES, s>>>(m, groups, p.E, M, N, pcol0, 0,
+                                                                slot, p_from_ps, q_from_qs);
+    else
+      k_wgrad_tc2<false><<<grid, WG_THREADS, WG_SMEM_BYTES, s>>>(m, groups, p.E, M, N, pcol0, 0,
+                                                                 slot, p_from_ps, q_from_qs);
   };
   wgrad(maps.wd, p.d, p.h, 0, 5, 1, 0);
   wgrad(maps.wg, p.h, p.d, 0, 6, 0, 1);

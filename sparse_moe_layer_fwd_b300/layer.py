@@ -137,15 +137,17 @@ class MoeLayer:
     def backward(self, x, dy, stream=None) -> dict:
         """Gradients for the output gradient dy, after forward(x) on this layer
         (built with MOE_TRAINING): dx, the expert and shared-expert weight
-        gradients (fp32) and the router's."""
+        gradients (fp32, or bf16 with MOE_GRAD_BF16) and the router's."""
         if stream is None:
             stream = torch.cuda.current_stream(self.workspace.device)
         wg, wu, wd, sg, su, sd = self._keep
         f32 = dict(dtype=torch.float32, device=self.workspace.device)
-        g = {"dx": torch.empty_like(dy), "dW_gate": torch.empty(wg.shape, **f32),
-             "dW_up": torch.empty(wu.shape, **f32), "dW_down": torch.empty(wd.shape, **f32),
-             "dsh_gate": torch.empty(sg.shape, **f32), "dsh_up": torch.empty(su.shape, **f32),
-             "dsh_down": torch.empty(sd.shape, **f32),
+        wdt = dict(dtype=torch.bfloat16 if self.flags & M.MOE_GRAD_BF16 else torch.float32,
+                   device=self.workspace.device)
+        g = {"dx": torch.empty_like(dy), "dW_gate": torch.empty(wg.shape, **wdt),
+             "dW_up": torch.empty(wu.shape, **wdt), "dW_down": torch.empty(wd.shape, **wdt),
+             "dsh_gate": torch.empty(sg.shape, **wdt), "dsh_up": torch.empty(su.shape, **wdt),
+             "dsh_down": torch.empty(sd.shape, **wdt),
              "dW_router": torch.empty(self.w_router.shape, **f32)}
         M.moe_backward(self.desc, x, self.w_router, self.experts, self.shared, self.topk_idx,
                        self.gates, dy, g["dx"],

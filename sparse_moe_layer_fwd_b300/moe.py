@@ -21,6 +21,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ROUTE_ONLY, MOE_SIMT_EXPERTS, MOE_TRAINING, MOE_FP8_GATE_UP = 1, 2, 4, 8
 MOE_FP8_BLOCK = 32
+MOE_GRAD_BF16 = 64
 MOE_OK = 0
 MOE_STATIC_SCRATCH_BYTES = 32 << 20
 ERRORS = {

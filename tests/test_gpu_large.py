@@ -110,12 +110,15 @@ def test_v3_largest_token_count():
     torch.cuda.empty_cache()
 
 
-def test_v3_prefill_backward_sampled():
+@pytest.mark.parametrize("grad_bf16", [False, True], ids=["fp32grad", "bf16grad"])
+def test_v3_prefill_backward_sampled(grad_bf16):
     """Full-size backward: every gradient finite, dx of 8 seeded tokens and
-    the weight gradients of the least-loaded expert against the oracle."""
+    the weight gradients of the least-loaded expert against the oracle (also
+    with the weight gradients written in bf16)."""
     wl = I.WORKLOADS["v3_prefill"]
     inp = I.make_inputs(wl, device="cuda")
-    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, M.MOE_TRAINING)
+    flags = M.MOE_TRAINING | (M.MOE_GRAD_BF16 if grad_bf16 else 0)
+    layer = MoeLayer.from_inputs(inp, wl.k, wl.dtype, flags)
     layer.forward(inp["x"])
     gen = torch.Generator(device="cuda").manual_seed(5)
     dy = torch.randn((wl.T, wl.d), generator=gen, device="cuda").to(torch.bfloat16)
