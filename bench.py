@@ -60,14 +60,31 @@ def kernels_per_step(wl, route_only, fp8=False):
     n = (2 if tc_router(wl) else 1) + 3
     return n if route_only else n + 4 + int(fp8)
 
-# DRAM traffic of expert GEMM 1 per launch from ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum, one capture of the full-size workload; both are
-# single-pass counters), keyed by workload, with the hash of the GEMM sources
-# at capture time; reported as null once those sources change.
+# DRAM traffic of expert GEMM 1 per launch (dram__bytes_read.sum +
+# dram__bytes_write.sum).  Counters beyond the kernel time are captured on
+# the 32-expert V3-width prefill case (2.9 GB of weights, one kernel, two
+# launches) and scaled to a full launch by the ratio of the two cases'
+# algorithmic bytes (weights of the touched experts plus token rows, which
+# the traffic follows); keyed to the hash of the GEMM sources at capture time
+# and reported as null once those sources change.
 NCU_TRAFFIC = {
-    "v3_prefill": {"sha": "7c7fabfbfd8ab89f", "bytes": 17.7129e9 + 0.29699e9},
-    "v3_prefill:fp8": {"sha": "7c7fabfbfd8ab89f", "bytes": 8.5332e9 + 0.29247e9},
+    # filled from profiles/k_expert_tc2_v3_prefill_32experts_full.md
 }
+
+
+def _scaled_traffic(cap, wl, load, fp8, fp8_blk):
+    """A small-case capture scaled to this workload's launch."""
+    if not cap:
+        return None
+    small = I_WORKLOADS()[cap["case"]]
+    sload = np.full(small.E, small.T * small.k // small.E)
+    return cap["bytes"] * (_algorithmic(wl, load, fp8, fp8_blk)[2] /
+                           _algorithmic(small, sload, fp8, fp8_blk)[2])
+
+
+def I_WORKLOADS():
+    from sparse_moe_layer_fwd_b300 import inputs as I
+    return I.WORKLOADS
 
 
 def _peaks():
@@ -565,8 +582,9 @@ def run_ours(args, wl):
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
-    cap = NCU_TRAFFIC.get(wl.name + (":fp8blk" if fp8_blk else ":fp8" if fp8 else ""))  # GEMM 1
-    traffic = cap["bytes"] if cap and cap.get("sha") == sha else None
+    cap = NCU_TRAFFIC.get(":fp8blk" if fp8_blk else ":fp8" if fp8 else "bf16")  # GEMM 1
+    traffic = (_scaled_traffic(cap, wl, load, fp8, fp8_blk)
+               if cap and cap.get("sha") == sha and wl.T * wl.k / wl.E >= 96 else None)
     if prefill_like:
         ach = fl1 / g1_s / 1e12
         peak, kind, scale = _tensor_peak(peaks, clocks, fp8)
