@@ -68,7 +68,12 @@ def kernels_per_step(wl, route_only, fp8=False):
 # the traffic follows); keyed to the hash of the GEMM sources at capture time
 # and reported as null once those sources change.
 NCU_TRAFFIC = {
-    # filled from profiles/k_expert_tc2_v3_prefill_32experts_full.md
+    # profiles/k_expert_tc2_v3_prefill_32experts_full.md ("DRAM counters of
+    # the current sources"): GEMM 1 read + written bytes on that case
+    "bf16": {"sha": "70e35cc962d72144", "case": "v3_prefill_32experts",
+             "bytes": 2.187689216e9 + 0.034349568e9},
+    ":fp8blk": {"sha": "70e35cc962d72144", "case": "v3_prefill_32experts",
+                "bytes": 1.045511168e9 + 0.018667008e9},
 }
 
 
