@@ -126,6 +126,16 @@ def _kernel_sha(read=None):
     return h.hexdigest()[:16]
 
 
+SMI_LAG_S = 0.15
+
+
+def _kernel_clocks(M, reset_first=False):
+    """Mean SM clock (MHz) of each tensor-core kernel class since the last
+    reset, from the kernels' own cycle and %globaltimer counters."""
+    rec = M.moe_sm_clock_record(reset=reset_first)
+    return {n: round(v["mhz"], 1) for n, v in rec.items() if v["mhz"]}
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a window."""
 
@@ -134,6 +144,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
+        self.rows = []
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         uuid = str(torch.cuda.get_device_properties(device_index).uuid)
         sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
@@ -164,7 +175,13 @@ class ClockSampler:
                     continue
                 rows.append((ts, parts))
         os.unlink(self.file.name)
-        inside = [p for ts, p in rows if t0 - 0.05 <= ts <= t1 + 0.05] or [p for _, p in rows[-5:]]
+        self.rows = rows
+        # nvidia-smi reports a clock change about 0.1 s after the kernels see
+        # it (a power-capped V3 prefill run: the step times rose at 58 ms of
+        # load, the first sample showing the lower clock came at 173 ms), so
+        # the window reaches SMI_LAG_S past the end of the timed region
+        inside = ([p for ts, p in rows if t0 - 0.05 <= ts <= t1 + SMI_LAG_S]
+                  or [p for _, p in rows[-5:]])
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         sm = []
@@ -316,11 +333,13 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
-def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None):
+def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None, trace=None):
     """`steps` forward passes back to back on `stream` with per-phase events
     (moe_forward_profiled); flush: a buffer written before every step
     (outside the per-step spans).  Returns (loop ms, per-step ms list, mean
-    phase ms array, clocks or None)."""
+    phase ms array, clocks or None).  trace: a dict that receives each
+    step's start (ms from the first) and phase times, and the raw clock
+    samples (s from the start)."""
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(M.N_PHASE_EVENTS)]
           for _ in range(steps)]
     for row in ev:  # torch creates the CUDA event on its first record
@@ -330,6 +349,7 @@ def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None):
     sampler = ClockSampler(sampler_index) if sampler_index is not None else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    M.moe_sm_clock_record(reset=True)
     t_host0 = time.time()
     start.record(stream)
     for i in range(steps):
@@ -342,6 +362,8 @@ def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None):
     torch.cuda.synchronize()
     t_host1 = time.time()
     clocks = sampler.stop(t_host0, t_host1) if sampler else None
+    if clocks is not None:
+        clocks["kernel_sm_mhz"] = _kernel_clocks(M)
     if M.moe_last_error() != M.MOE_OK:
         raise RuntimeError("device error word set during the timed region")
     per_step = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
@@ -350,24 +372,31 @@ def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None):
     for i in range(steps):
         for p in range(len(M.PHASES)):
             phase_ms[p] += ev[i][p].elapsed_time(ev[i][p + 1])
+    if trace is not None:
+        trace["phases"] = list(M.PHASES)
+        trace["steps"] = [[start.elapsed_time(ev[i][0])] +
+                          [ev[i][p].elapsed_time(ev[i][p + 1]) for p in range(len(M.PHASES))]
+                          for i in range(steps)]
+        if sampler is not None:
+            trace["smi_fields"] = ClockSampler.FIELDS
+            trace["smi"] = [[round(ts - t_host0, 3)] + p[1:] for ts, p in sampler.rows]
     return loop_ms, per_step, phase_ms / steps, clocks
 
 
-def _tensor_peak(peaks, clocks, fp8=False):
+def _tensor_peak(peaks, clocks, fp8=False, slot="gate_up"):
     """Denominator of a tensor-core roofline: the measured burst bf16 figure
-    (times the nominal fp8/bf16 ratio 2 for e4m3 products).  The step loop
-    runs for a fraction of a second, so the burst figure applies; where the
-    clock record of the timed window shows the power cap, the fraction at
-    the sampled clock (peak x median SM MHz / max SM MHz) is given beside
-    it, not in its place."""
+    (times the nominal fp8/bf16 ratio 2 for e4m3 products).  Beside it, not
+    in its place: the scale of the clock the kernel ran at, its in-band mean
+    SM clock over the timed region (kernel cycles / kernel ns) over the
+    maximum SM clock.  Back-to-back V3 prefill steps reach the board's power
+    cap within about 60 ms, after which the SM clock settles near 1.3 GHz."""
     mult = 2.0 if fp8 else 1.0
     peak = mult * peaks["bf16_tflops"]
     kind = (f"{'2 x ' if fp8 else ''}{peaks['source']} bf16 burst"
             + (" (nominal fp8/bf16 ratio)" if fp8 else ""))
     scale = None
-    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz") and \
-            "sw_power_cap" in clocks.get("reasons", []):
-        scale = clocks["sm_mhz"] / clocks["sm_max_mhz"]
+    if clocks and clocks.get("sm_max_mhz") and clocks.get("kernel_sm_mhz", {}).get(slot):
+        scale = min(1.0, clocks["kernel_sm_mhz"][slot] / clocks["sm_max_mhz"])
     return peak, kind, scale
 
 
@@ -457,8 +486,13 @@ def run_ours(args, wl):
 
     # timed region: per-step phase events on the launching stream
     barrier()
+    trace = {} if args.trace and rank == 0 else None
     local_ms, per_step, phase_ms, clocks = _timed_forward(
-        M, layer, x, stream, args.steps, flush, local if rank == 0 else None)
+        M, layer, x, stream, args.steps, flush, local if rank == 0 else None, trace)
+    if trace is not None:
+        with open(args.trace, "w") as f:
+            json.dump({"workload": wl.name, "kernel_sm_mhz": (clocks or {}).get("kernel_sm_mhz"),
+                       **trace}, f)
     barrier()
     elapsed_ms, value = aggregate(local_ms, wl.T * args.steps, ws, "cuda")
     median_ms = statistics.median(per_step)
@@ -600,13 +634,19 @@ def run_ours(args, wl):
                 "traffic": traffic, "peak_kind": kind,
                 "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
         if scale is not None:
-            roof["frac_at_sampled_clock"] = ach / (peak * scale)
+            roof["kernel_clock_scale"] = scale
+            roof["frac_at_kernel_clock"] = ach / (peak * scale)
         both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
         layer_roof = {"expert_gemms_tflops": both, "frac": both / peak,
                       "gemm2_tflops": fl2 / g2_s / 1e12, "gemm2_frac": fl2 / g2_s / 1e12 / peak,
                       "gemm2_gbs": by2 / g2_s / 1e9}
-        if scale is not None:
-            layer_roof["frac_at_sampled_clock"] = both / (peak * scale)
+        _, _, scale2 = _tensor_peak(peaks, clocks, fp8, "down")
+        if scale is not None and scale2 is not None:
+            # both products at their own clocks: FLOPs over the sum of each
+            # product's time scaled to the maximum clock
+            layer_roof["frac_at_kernel_clock"] = (fl1 + fl2) / (
+                g1_s * scale + g2_s * scale2) / 1e12 / peak
+            layer_roof["gemm2_frac_at_kernel_clock"] = fl2 / (g2_s * scale2) / 1e12 / peak
     else:
         ach = by1 / g1_s / 1e9
         roof = {"bound": "hbm",
@@ -692,6 +732,7 @@ def run_train(args, wl):
             e.record(stream)
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
+    M.moe_sm_clock_record(reset=True)
     t0 = time.time()
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -701,6 +742,8 @@ def run_train(args, wl):
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop(t0, time.time()) if sampler else None
+    if clocks is not None:
+        clocks["kernel_sm_mhz"] = _kernel_clocks(M)
     if M.moe_last_error() != M.MOE_OK:
         raise RuntimeError("device error word set")
     fwd = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
@@ -712,7 +755,7 @@ def run_train(args, wl):
     rows = wl.T * wl.k + wl.T
     bflops = 12.0 * rows * wl.d * wl.h
     bwd_ms = bwd / args.steps
-    peak, kind, scale = _tensor_peak(peaks, clocks)
+    peak, kind, scale = _tensor_peak(peaks, clocks, slot="backward")
     ach = bflops / (bwd_ms / 1e3) / 1e12
     line = {
         "metric": METRIC + " [training step: forward + backward]", "value": value,
@@ -731,7 +774,8 @@ def run_train(args, wl):
                      "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                      "traffic": None, "peak_kind": f"{kind}; 12 d h FLOP per row",
                      "flops_per_launch": bflops, "ms_per_launch": bwd_ms,
-                     **({"frac_at_sampled_clock": ach / (peak * scale)} if scale else {})},
+                     **({"kernel_clock_scale": scale, "frac_at_kernel_clock": ach / (peak * scale)}
+                        if scale else {})},
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -804,6 +848,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=512,
                     help="output rows the CPU oracle computes for cpu_baseline")
+    ap.add_argument("--trace", default=None,
+                    help="write the main workload's per-step phase times and raw clock "
+                         "samples to this JSON file")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the V3 decode runs that follow the V3 prefill line")
     ap.add_argument("--train", action="store_true",

@@ -321,6 +321,26 @@ MOE_API int moe_backward(const moe_desc* desc, const void* x, const float* w_rou
  * word cannot be read. */
 MOE_API int moe_last_error(void);
 
+/* In-band SM clock record of the tensor-core kernels.  Each CTA of those
+ * kernels adds, on exit, the SM clock cycles (%clock64) and the wall time
+ * (%globaltimer, ns) from its start to its end into one of MOE_CLOCK_SLOTS
+ * per-process counter pairs; cycles / ns is the mean SM clock (GHz) at which
+ * that kernel class ran -- under the board's power cap it falls below the
+ * maximum clock within tens of milliseconds of load, sooner than nvidia-smi
+ * reports it.  Slots: */
+#define MOE_CLOCK_GATE_UP 0 /* the forward gate/up products (expert GEMM 1) */
+#define MOE_CLOCK_DOWN    1 /* the forward down products (expert GEMM 2) */
+#define MOE_CLOCK_BWD     2 /* the backward's tensor-core products */
+#define MOE_CLOCK_ROUTER  3 /* the tensor-core router */
+#define MOE_CLOCK_SLOTS   4
+/* Copies the counters to out[2 * slot] (cycles) and out[2 * slot + 1] (ns)
+ * for every slot (host array of 2 * MOE_CLOCK_SLOTS values) and, if reset is
+ * non-zero, zeroes them.  Synchronous with respect to the device's legacy
+ * default stream: synchronise the caller's stream first.  Counting costs two
+ * atomic adds per CTA and launch.  Returns MOE_ERR_NULL for out == NULL,
+ * MOE_ERR_DEVICE if the counters cannot be read. */
+MOE_API int moe_sm_clock_record(unsigned long long* out, int reset);
+
 /* Self-test of the failure path.  Every wait of the library's kernels on a
  * pipeline barrier is bounded: when it runs out (4 s), the kernel sets the
  * device error word and returns, and moe_last_error then reports

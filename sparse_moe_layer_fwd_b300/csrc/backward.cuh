@@ -343,6 +343,7 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
   const int total = (E + 1) * MB * NB;
   int* counter = G.next + counter_slot;
   if ((int)(blockIdx.x >> 1) >= total) return;
+  const SmClockStart clk_start = sm_clock_start();
 
   uint8_t* bar_base = smem + WG_BAR_OFF;
   auto bar = [&](int i) { return smem_u32(bar_base + 8 * i); };
@@ -583,4 +584,5 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
   cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem, 512);
+  if (threadIdx.x == 0) sm_clock_add(2, clk_start);
 }

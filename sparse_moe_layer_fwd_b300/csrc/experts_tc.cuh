@@ -328,6 +328,7 @@ k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ 
   int* counter = G.next + (DOWN ? 1 : 0);
   const int total = toff[E + 1];
   if ((int)blockIdx.x >= total) return;
+  const SmClockStart clk_start = sm_clock_start();
   {
     // a CTA-uniform decision: one thread reads the error word
     __shared__ int s_skip;
@@ -586,4 +587,5 @@ k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ 
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (threadIdx.x == 0) sm_clock_add(DOWN ? 1 : 0, clk_start);
 }

@@ -229,6 +229,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   const int total = toff[E + 1];
   // the same decision in both CTAs of the pair (same cluster index)
   if ((int)(blockIdx.x >> 1) >= total) return;
+  const SmClockStart clk_start = sm_clock_start();
 
   uint8_t* bar_base = smem + C::BAR_OFF;
   auto bar = [&](int i) { return smem_u32(bar_base + 8 * i); };
@@ -836,4 +837,6 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   cluster_sync_all();  // neither CTA leaves while the other may still use its memory
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  if (threadIdx.x == 0)
+    sm_clock_add(MNA ? 2 : DOWN ? 1 : 0, clk_start);  // backward / down / gate-up
 }

@@ -1061,6 +1061,23 @@ int moe_seq_balance_loss(const moe_desc* desc, int seq_len, float alpha, const i
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
+static_assert(MOE_CLOCK_SLOTS == MOE_CLOCK_NSLOT, "clock slots");
+
+int moe_sm_clock_record(unsigned long long* out, int reset) {
+  if (!out) return MOE_ERR_NULL;
+  unsigned long long v[MOE_CLOCK_NSLOT][2];
+  if (cudaMemcpyFromSymbol(v, g_moe_clock, sizeof(v)) != cudaSuccess) return MOE_ERR_DEVICE;
+  for (int s = 0; s < MOE_CLOCK_NSLOT; ++s) {
+    out[2 * s] = v[s][0];
+    out[2 * s + 1] = v[s][1];
+  }
+  if (reset) {
+    const unsigned long long zero[MOE_CLOCK_NSLOT][2] = {};
+    if (cudaMemcpyToSymbol(g_moe_clock, zero, sizeof(zero)) != cudaSuccess) return MOE_ERR_DEVICE;
+  }
+  return MOE_OK;
+}
+
 int moe_last_error(void) {
   unsigned v = 0;
   if (cudaMemcpyFromSymbol(&v, g_moe_dev_error, sizeof(v)) != cudaSuccess) return MOE_ERR_DEVICE;

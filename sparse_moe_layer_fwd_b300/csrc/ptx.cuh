@@ -21,6 +21,12 @@ static __device__ unsigned int g_moe_dev_error;
 // something is genuinely stuck.
 #define MOE_WAIT_LIMIT_NS 4000000000ull
 
+// In-band SM clock record: per kernel class (slot), the sums over CTAs of
+// the SM clock cycles and of the %globaltimer ns from a CTA's start to its
+// end (read by moe_sm_clock_record).
+#define MOE_CLOCK_NSLOT 4
+static __device__ unsigned long long g_moe_clock[MOE_CLOCK_NSLOT][2];
+
 MOE_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -29,6 +35,16 @@ MOE_DEV uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+struct SmClockStart {
+  uint64_t clk, ns;
+};
+MOE_DEV SmClockStart sm_clock_start() { return {(uint64_t)clock64(), global_timer_ns()}; }
+MOE_DEV void sm_clock_add(int slot, SmClockStart s0) {
+  const uint64_t clk = (uint64_t)clock64() - s0.clk, ns = global_timer_ns() - s0.ns;
+  atomicAdd(&g_moe_clock[slot][0], (unsigned long long)clk);
+  atomicAdd(&g_moe_clock[slot][1], (unsigned long long)ns);
 }
 
 // ------------------------------------------------------------------ mbarrier

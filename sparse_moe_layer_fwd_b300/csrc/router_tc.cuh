@@ -92,6 +92,7 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
+  const SmClockStart clk_start = sm_clock_start();
 
   const int pid = blockIdx.x >> 1;  // the same unit in both CTAs of the pair
   const int eb = pid % n_eb, tt = (pid / n_eb) % n_tt, s = pid / (n_eb * n_tt);
@@ -273,4 +274,5 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
   cluster_sync_all();  // neither CTA leaves while the other may still use its memory
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem, RT_TMEM_COLS);
+  if (threadIdx.x == 0) sm_clock_add(3, clk_start);
 }

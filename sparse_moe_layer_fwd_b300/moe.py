@@ -80,6 +80,8 @@ def _load():
     lib.moe_seq_balance_loss.argtypes = [dp, I, ctypes.c_float, P, P, S, P, P]
     lib.moe_seq_balance_loss.restype = I
     lib.moe_last_error.argtypes, lib.moe_last_error.restype = [], I
+    lib.moe_sm_clock_record.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), I]
+    lib.moe_sm_clock_record.restype = I
     lib.moe_error_string.argtypes, lib.moe_error_string.restype = [I], ctypes.c_char_p
     lib.moe_workspace_regions.argtypes = [dp, ctypes.POINTER(MoeRegion), I]
     lib.moe_workspace_regions.restype = I
@@ -220,6 +222,25 @@ def moe_seq_balance_loss(desc, seq_len, alpha, topk_idx, workspace, ws_bytes, lo
 
 def moe_last_error() -> int:
     return int(_lib.moe_last_error())
+
+
+MOE_CLOCK_SLOTS = 4
+CLOCK_SLOT_NAMES = ("gate_up", "down", "backward", "router")
+
+
+def moe_sm_clock_record(reset: bool = False, check=True) -> dict:
+    """Mean SM clock (MHz) each tensor-core kernel class ran at since the
+    last reset, from the kernels' in-band cycle and wall-time counters:
+    {slot name: {"cycles", "ns", "mhz"}}.  Synchronise first."""
+    buf = (ctypes.c_ulonglong * (2 * MOE_CLOCK_SLOTS))()
+    rc = _lib.moe_sm_clock_record(buf, 1 if reset else 0)
+    if check:
+        _check(rc, "moe_sm_clock_record")
+    out = {}
+    for i, n in enumerate(CLOCK_SLOT_NAMES):
+        cyc, ns = int(buf[2 * i]), int(buf[2 * i + 1])
+        out[n] = {"cycles": cyc, "ns": ns, "mhz": (1e3 * cyc / ns) if ns else None}
+    return out
 
 
 def moe_error_string(code: int) -> str:

@@ -64,6 +64,8 @@ int main(void) {
   CHECK(moe_quantize_rows_e4m3((const void*)0x10000, 4, 100, (void*)0x10000, NULL) ==
         MOE_ERR_SHAPE);
   CHECK(moe_selftest_timeout(0, NULL) == MOE_ERR_SHAPE);
+  CHECK(moe_sm_clock_record(NULL, 0) == MOE_ERR_NULL);
+  CHECK(MOE_CLOCK_SLOTS == 4);
   /* routing with the static array: a problem whose scratch exceeds it is
    * refused before any device is touched */
   moe_desc big = {65536, 128, 128, 256, 1, MOE_BF16, MOE_ROUTE_ONLY};

@@ -19,7 +19,7 @@ def test_library_exports_every_header_function():
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
         "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward",
         "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3", "moe_selftest_timeout",
-        "moe_e4m3_block_packed_bytes", "moe_quantize_blocks_e4m3"}
+        "moe_e4m3_block_packed_bytes", "moe_quantize_blocks_e4m3", "moe_sm_clock_record"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -252,3 +252,20 @@ def test_noalloc_rejects_problems_larger_than_its_array():
     assert rc == M.ERR_CODE["MOE_ERR_WORKSPACE"]
     assert M.library().moe_route_noalloc(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                          None) == M.ERR_CODE["MOE_ERR_NULL"]
+
+
+def test_clock_record_slots_match_the_header():
+    """The binding's slot count and order are the header's MOE_CLOCK_*."""
+    import re
+    text = open(M.HEADER_PATH).read()
+    slots = {m.group(1): int(m.group(2))
+             for m in re.finditer(r"#define\s+MOE_CLOCK_(\w+)\s+(\d+)", text)}
+    assert slots.pop("SLOTS") == M.MOE_CLOCK_SLOTS == len(M.CLOCK_SLOT_NAMES)
+    assert sorted(slots.values()) == list(range(M.MOE_CLOCK_SLOTS))
+    for name, idx in slots.items():
+        assert M.CLOCK_SLOT_NAMES[idx] == {"GATE_UP": "gate_up", "DOWN": "down",
+                                           "BWD": "backward", "ROUTER": "router"}[name]
+
+
+def test_clock_record_arguments():
+    assert M.library().moe_sm_clock_record(None, 0) == M.ERR_CODE["MOE_ERR_NULL"]
