@@ -383,21 +383,30 @@ def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None, trace=
     return loop_ms, per_step, phase_ms / steps, clocks
 
 
+# Dense bf16 tensor-core rate per SM clock: 4096 multiply-adds per clock
+# per SM (a stand-alone CTA-pair MMA loop reaches it for N >= 128; the
+# nominal 2.25 PFLOP/s dense bf16 is this rate at about 1.86 GHz), 148 SMs.
+BF16_TFLOPS_PER_MHZ = 2 * 4096 * 148 / 1e6
+
+
 def _tensor_peak(peaks, clocks, fp8=False, slot="gate_up"):
     """Denominator of a tensor-core roofline: the measured burst bf16 figure
     (times the nominal fp8/bf16 ratio 2 for e4m3 products).  Beside it, not
-    in its place: the scale of the clock the kernel ran at, its in-band mean
-    SM clock over the timed region (kernel cycles / kernel ns) over the
-    maximum SM clock.  Back-to-back V3 prefill steps reach the board's power
-    cap within about 60 ms, after which the SM clock settles near 1.3 GHz."""
+    in its place: the tensor pipe's peak at the clock the kernel ran at --
+    its in-band mean SM clock over the timed region (kernel cycles / kernel
+    ns) times the per-clock rate.  Back-to-back V3 prefill steps reach the
+    board's power cap within about 60 ms, after which the SM clock settles
+    near 1.3 GHz; the burst figure itself (a single 8192^3 product) implies
+    at least 1808.6 / 1.212 = 1492 MHz."""
     mult = 2.0 if fp8 else 1.0
     peak = mult * peaks["bf16_tflops"]
     kind = (f"{'2 x ' if fp8 else ''}{peaks['source']} bf16 burst"
             + (" (nominal fp8/bf16 ratio)" if fp8 else ""))
-    scale = None
-    if clocks and clocks.get("sm_max_mhz") and clocks.get("kernel_sm_mhz", {}).get(slot):
-        scale = min(1.0, clocks["kernel_sm_mhz"][slot] / clocks["sm_max_mhz"])
-    return peak, kind, scale
+    at_clock = None
+    mhz = ((clocks or {}).get("kernel_sm_mhz") or {}).get(slot)
+    if mhz:
+        at_clock = {"sm_mhz": mhz, "peak_tflops": mult * BF16_TFLOPS_PER_MHZ * mhz}
+    return peak, kind, at_clock
 
 
 def _decode_line(M, I, MoeLayer, name, args, peaks, local):
@@ -626,27 +635,26 @@ def run_ours(args, wl):
                if cap and cap.get("sha") == sha and wl.T * wl.k / wl.E >= 96 else None)
     if prefill_like:
         ach = fl1 / g1_s / 1e12
-        peak, kind, scale = _tensor_peak(peaks, clocks, fp8)
+        peak, kind, clk1 = _tensor_peak(peaks, clocks, fp8)
         roof = {"bound": "tensor",
                 "kernel": ("k_expert_tc2 (GEMM 1 on e4m3 codes: gate/up + SwiGLU, CTA pairs)"
                            if fp8 else "k_expert_tc2 (GEMM 1: gate/up + SwiGLU, CTA pairs)"),
                 "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "traffic": traffic, "peak_kind": kind,
                 "flops_per_launch": fl1, "ms_per_launch": phase_ms[2]}
-        if scale is not None:
-            roof["kernel_clock_scale"] = scale
-            roof["frac_at_kernel_clock"] = ach / (peak * scale)
+        if clk1 is not None:
+            roof["at_kernel_clock"] = {**clk1, "frac": ach / clk1["peak_tflops"]}
         both = (fl1 + fl2) / (g1_s + g2_s) / 1e12
         layer_roof = {"expert_gemms_tflops": both, "frac": both / peak,
                       "gemm2_tflops": fl2 / g2_s / 1e12, "gemm2_frac": fl2 / g2_s / 1e12 / peak,
                       "gemm2_gbs": by2 / g2_s / 1e9}
-        _, _, scale2 = _tensor_peak(peaks, clocks, fp8, "down")
-        if scale is not None and scale2 is not None:
-            # both products at their own clocks: FLOPs over the sum of each
-            # product's time scaled to the maximum clock
-            layer_roof["frac_at_kernel_clock"] = (fl1 + fl2) / (
-                g1_s * scale + g2_s * scale2) / 1e12 / peak
-            layer_roof["gemm2_frac_at_kernel_clock"] = fl2 / (g2_s * scale2) / 1e12 / peak
+        _, _, clk2 = _tensor_peak(peaks, clocks, fp8, "down")
+        if clk1 is not None and clk2 is not None:
+            # both products at their own clocks: FLOPs over what the tensor
+            # pipe could do in each product's time at that product's clock
+            layer_roof["frac_at_kernel_clock"] = (fl1 + fl2) / 1e12 / (
+                g1_s * clk1["peak_tflops"] + g2_s * clk2["peak_tflops"])
+            layer_roof["gemm2_frac_at_kernel_clock"] = fl2 / 1e12 / (g2_s * clk2["peak_tflops"])
     else:
         ach = by1 / g1_s / 1e9
         roof = {"bound": "hbm",
@@ -755,7 +763,7 @@ def run_train(args, wl):
     rows = wl.T * wl.k + wl.T
     bflops = 12.0 * rows * wl.d * wl.h
     bwd_ms = bwd / args.steps
-    peak, kind, scale = _tensor_peak(peaks, clocks, slot="backward")
+    peak, kind, clkb = _tensor_peak(peaks, clocks, slot="backward")
     ach = bflops / (bwd_ms / 1e3) / 1e12
     line = {
         "metric": METRIC + " [training step: forward + backward]", "value": value,
@@ -774,8 +782,8 @@ def run_train(args, wl):
                      "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                      "traffic": None, "peak_kind": f"{kind}; 12 d h FLOP per row",
                      "flops_per_launch": bflops, "ms_per_launch": bwd_ms,
-                     **({"kernel_clock_scale": scale, "frac_at_kernel_clock": ach / (peak * scale)}
-                        if scale else {})},
+                     **({"at_kernel_clock": {**clkb, "frac": ach / clkb["peak_tflops"]}}
+                        if clkb else {})},
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
