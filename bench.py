@@ -136,6 +136,15 @@ def _kernel_clocks(M, reset_first=False):
     return {n: round(v["mhz"], 1) for n, v in rec.items() if v["mhz"]}
 
 
+def _note_inband_cap(clocks):
+    """Mark a window whose tensor-core kernels ran more than 5% below the
+    maximum SM clock by their own counters, whatever nvidia-smi showed."""
+    mhz = [v for v in (clocks.get("kernel_sm_mhz") or {}).values() if v]
+    if mhz and clocks.get("sm_max_mhz") and min(mhz) < 0.95 * clocks["sm_max_mhz"]:
+        clocks["inband_below_max"] = (f"tensor-core kernels at {min(mhz):.0f}-{max(mhz):.0f} MHz "
+                                      f"by their own cycle counters (board power cap)")
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a window."""
 
@@ -364,6 +373,7 @@ def _timed_forward(M, layer, x, stream, steps, flush, sampler_index=None, trace=
     clocks = sampler.stop(t_host0, t_host1) if sampler else None
     if clocks is not None:
         clocks["kernel_sm_mhz"] = _kernel_clocks(M)
+        _note_inband_cap(clocks)
     if M.moe_last_error() != M.MOE_OK:
         raise RuntimeError("device error word set during the timed region")
     per_step = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
@@ -752,6 +762,7 @@ def run_train(args, wl):
     clocks = sampler.stop(t0, time.time()) if sampler else None
     if clocks is not None:
         clocks["kernel_sm_mhz"] = _kernel_clocks(M)
+        _note_inband_cap(clocks)
     if M.moe_last_error() != M.MOE_OK:
         raise RuntimeError("device error word set")
     fwd = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))

@@ -364,7 +364,9 @@ MOE_API const char* moe_error_string(int code);
  * tensor-core router; empty otherwise), "blk_hist", "pair_rank", "groups"
  * (int32 group table),
  * "perm" (permuted row -> token*k+slot), "inv" (token*k+slot -> permuted row),
- * "x_perm", "h", "y_perm", "y_shared", "x_q" (MOE_FP8_GATE_UP: the tokens
+ * "x_perm", "h", "y_perm" (the T*k routed rows in expert order, then the
+ * shared expert's T rows in token order, in the element type), "x_q"
+ * (MOE_FP8_GATE_UP: the tokens
  * quantized, packed as above; MOE_FP8_BLOCK: the tokens' codes [T, d], then
  * their exponent words [ceil(d / 512)][T] from byte ceil(T*d / 256) * 256;
  * empty otherwise), "h_q" (MOE_FP8_BLOCK: the hidden rows' codes [T*k + T,

@@ -1,8 +1,9 @@
 // combine.cuh -- gated combine and the bias update.
 //
-// k_combine: y[t] = Y_sh[t] + sum_{j=0..k-1} g[t,j] * Y_perm[inv[t*k+j]],
-//   one fp32 fused multiply-add per slot in that fixed slot order, rounded
-//   once to the output type.  (The gate multiplies the expert's output row
+// k_combine: y[t] = Y_perm[TK + t] + sum_{j=0..k-1} g[t,j] * Y_perm[inv[t*k+j]]
+//   (row TK + t: the shared expert's output for token t), one fp32 fused
+//   multiply-add per slot in that fixed slot order, rounded once to the
+//   output type.  (The gate multiplies the expert's output row
 //   here rather than in the down-projection epilogue: the same product, and
 //   the tensor-core epilogue, which stalls the MMAs while it drains the
 //   accumulators, loses its per-token broadcasts.)  One CTA per token, 8
@@ -50,9 +51,8 @@ MOE_DEV void store8(__nv_bfloat16* p, const float* v) {
 
 template <typename TA>
 __global__ void __launch_bounds__(128)
-k_combine(const float* __restrict__ y_sh, const TA* __restrict__ y_perm,
-          const int32_t* __restrict__ inv, const float* __restrict__ gates, int T, int d, int k,
-          TA* __restrict__ y) {
+k_combine(const TA* __restrict__ y_perm, const int32_t* __restrict__ inv,
+          const float* __restrict__ gates, int T, int d, int k, TA* __restrict__ y) {
   __shared__ int rows[32];
   __shared__ float gs[32];
   const int t = blockIdx.x;
@@ -63,7 +63,7 @@ k_combine(const float* __restrict__ y_sh, const TA* __restrict__ y_perm,
   __syncthreads();
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float acc[8];
-    load8(y_sh + (size_t)t * d + c, acc);
+    load8(y_perm + ((size_t)T * k + t) * d + c, acc);
     for (int j = 0; j < k; ++j) {
       float v[8];
       load8(y_perm + (size_t)rows[j] * d + c, v);

@@ -9,9 +9,9 @@
 // shared expert over all T tokens.  Tile = SIMT_TM tokens x SIMT_TN outputs;
 // the group table (dispatch.cuh) lists each group's token tiles.
 //   first GEMM  (DOWN = false): H[row] = silu(X W_gate^T) * (X W_up^T)
-//   second GEMM (DOWN = true) : routed  Y_perm[row] = H[row] W_down^T (the
-//                               gate is applied in the combine)
-//                               shared  Y_sh[t]     = H[TK + t] W_down^T (fp32)
+//   second GEMM (DOWN = true) : Y_perm[row] = H[row] W_down^T for the routed
+//                               rows (the gate is applied in the combine) and
+//                               for the shared expert's rows TK + t
 #pragma once
 
 #include "dispatch.cuh"
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256)
 k_expert_simt(const T* __restrict__ wa0, const T* __restrict__ wa1, const T* __restrict__ sa0,
               const T* __restrict__ sa1, const T* __restrict__ b_routed,
               const T* __restrict__ b_shared, const int32_t* __restrict__ groups, int E, int K,
-              int n_out, T* __restrict__ out, float* __restrict__ y_sh) {
+              int n_out, T* __restrict__ out) {
   GroupTable G = group_table(const_cast<int32_t*>(groups), E);
   const int32_t* toff = DOWN ? G.toff_b : G.toff_a;
   const int b = blockIdx.x;
@@ -115,8 +115,6 @@ k_expert_simt(const T* __restrict__ wa0, const T* __restrict__ wa1, const T* __r
       const int f = f0 + tf * 4 + q;
       if (!DOWN) {
         out[(size_t)row * n_out + f] = from_f<T>(silu_f(acc0[i][q]) * acc1[i][q]);
-      } else if (shared) {
-        y_sh[(size_t)(tok0 + r) * n_out + f] = acc0[i][q];
       } else {
         out[(size_t)row * n_out + f] = from_f<T>(acc0[i][q]);
       }

@@ -17,7 +17,8 @@
 //   first GEMM (DOWN = false): acc0 = W_gate rows f0..f0+127, acc1 = W_up rows
 //       f0..f0+127 (same B tile) -> H[row, f] = bf16(silu(acc0) * acc1)
 //   second GEMM (DOWN = true): acc0 / acc1 = W_down rows f0..+127 / f0+128..+255
-//       -> routed: Y_perm[row, f] = bf16(g(row) * acc); shared: Y_sh[t, f] = acc
+//       -> Y_perm[row, f] = bf16(acc), for the routed rows and the shared
+//       expert's rows TK + t (the gates are applied in the combine)
 //
 // Pipeline: K steps of 64 elements (128-byte rows, 128-byte swizzle).  The
 // weights (A: 2 x 16 KB per step, streamed from DRAM, long latency) and the
@@ -316,7 +317,7 @@ struct TcMapsDev {
 template <int BN, int SA, int SB, bool DOWN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ groups, int E,
-            int K, int n_out, __nv_bfloat16* __restrict__ out, float* __restrict__ y_sh) {
+            int K, int n_out, __nv_bfloat16* __restrict__ out) {
   using C = TcCfg<BN, SA, SB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -547,11 +548,6 @@ k_expert_tc(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__ 
 #pragma unroll
           for (int j = 0; j < 32; ++j) va[j] = silu_fast(va[j]) * vb[j];
           store_rows_bf16(out + (size_t)(t.out_row0 + c) * n_out + fw, n_out, va, c, t.ntok, lane);
-        } else if (t.shared) {
-          store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + fw, n_out, va, c, t.ntok, lane);
-          if (t.has_a1)
-            store_rows_f32(y_sh + (size_t)(t.tok0 + c) * n_out + fw + TC_BM, n_out, vb, c, t.ntok,
-                           lane);
         } else {
           __nv_bfloat16* o = out + (size_t)(t.out_row0 + c) * n_out + fw;
           store_rows_bf16(o, n_out, va, c, t.ntok, lane);

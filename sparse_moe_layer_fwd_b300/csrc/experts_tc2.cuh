@@ -630,9 +630,8 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
     // at once (SwiGLU, or its gradient); two-block tiles drain block 0, free
     // it, then block 1.  bf16 outputs of 32 whole tokens go out through
     // shared memory by TMA store; the rest (a ragged last chunk, the shared
-    // expert's fp32 rows, the SwiGLU gradient) from registers.
-    constexpr bool F32SH =
-        OP == TC2_FWD_DOWN || OP == TC2_BWD_DX || OP == TC2_FWD_DOWN_B8;  // shared rows in fp32
+    // expert's fp32 dX rows of the backward) from registers.
+    constexpr bool F32SH = OP == TC2_BWD_DX;  // the shared expert's dX rows in fp32
     const int q = warp & 3, half = (warp - 2) >> 2;
     const uint32_t stg = smem_u32(smem + C::STG_OFF) + (uint32_t)((warp - 2) * OUTB * TC_BOX_BYTES);
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
@@ -775,7 +774,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             ++nbox;
             continue;
           }
-          // from registers: a ragged last chunk, or fp32 shared-expert rows
+          // from registers: a ragged last chunk, or the shared expert's fp32 dX rows
           float va[32], vb[32];
           if (!DOWN)
             tmem_load_2x32(ta + c, tb + c, va, vb);

@@ -94,13 +94,13 @@ struct Plan {
   // expert tiling
   int bn, ft_a, ft_b, ft_c, tile_round, max_tiles_a, max_tiles_b, max_tiles_c;
   // workspace regions (byte offsets)
-  size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm, o_ysh,
+  size_t o_part, o_w3, o_hist, o_rank, o_groups, o_perm, o_inv, o_xperm, o_h, o_yperm,
       o_xq, o_hq, total;
   // backward: padded dY rows, dG, du, dH, padded dA|dB rows, dX rows, shared dX;
   // the training forward's pre-activations A|B
   size_t o_dyp, o_dg, o_du, o_dh, o_dab, o_dxp, o_dxs, o_ab;
   long long rows_dyp, rows_dab;  // allocated padded rows
-  size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm, b_ysh,
+  size_t b_part, b_w3, b_hist, b_rank, b_groups, b_perm, b_inv, b_xperm, b_h, b_yperm,
       b_xq, b_hq;
 };
 
@@ -252,8 +252,9 @@ Plan make_plan(const moe_desc* d) {
     region((size_t)p.TK * 4, p.o_inv, p.b_inv);
     region((size_t)p.TK * p.d * ((p.fp8 || p.fp8_blk) ? 1 : p.el), p.o_xperm, p.b_xperm);
     region(p.fp8_blk ? 0 : (size_t)(p.TK + p.T) * p.h * p.el, p.o_h, p.b_h);
-    region((size_t)p.TK * p.d * p.el, p.o_yperm, p.b_yperm);
-    region((size_t)p.T * p.d * 4, p.o_ysh, p.b_ysh);
+    // Y_perm: the routed rows in expert order, then the shared expert's rows
+    // in token order (row TK + t)
+    region((size_t)(p.TK + p.T) * p.d * p.el, p.o_yperm, p.b_yperm);
     // x_q: codes [T, d], then fp32 row scales [T] (per row) or exponent
     // words [ceil(d / 512)][T] (blocks); h_q: the block-quantized rows of H
     region(p.fp8 ? e4m3_scale_offset(p.T, p.d) + (size_t)p.T * 4
@@ -476,7 +477,7 @@ bool make_tc_maps(const Plan& p, const void* x, const moe_expert_w* ex, const mo
   ok &= make_out_map(&m->up.out, ws + p.o_h, (long long)p.TK + p.T, p.h);
   if (p.training)  // the pre-activations A|B rows, stored by the training forward
     ok &= make_out_map(&m->up.aux, ws + p.o_ab, (long long)p.TK + p.T, 2LL * p.h);
-  ok &= make_out_map(&m->down.out, ws + p.o_yperm, p.TK, p.d);
+  ok &= make_out_map(&m->down.out, ws + p.o_yperm, (long long)p.TK + p.T, p.d);
   return ok;
 }
 
@@ -534,22 +535,22 @@ bool set_tc1_smem() {
 // CTA per SM), at most one CTA (pair) per tile.
 template <bool DOWN>
 void launch_gemm(const Plan& p, const TcMapsDev& m, bool pair, int BN, int max_tiles,
-                 int32_t* groups, __nv_bfloat16* out, float* ysh, cudaStream_t s) {
+                 int32_t* groups, __nv_bfloat16* out, cudaStream_t s) {
   const int sms = sm_count();
   const int K = DOWN ? p.h : p.d, n_out = DOWN ? p.d : p.h;
   if (pair) {
-    launch_pair<DOWN ? TC2_FWD_DOWN : TC2_FWD_UP>(p, m, max_tiles, groups, K, n_out, out, ysh,
-                                                  nullptr, s);
+    launch_pair<DOWN ? TC2_FWD_DOWN : TC2_FWD_UP>(p, m, max_tiles, groups, K, n_out, out,
+                                                  nullptr, nullptr, s);
   } else if (BN == kBigBN) {
     const int grid = max_tiles < sms ? max_tiles : sms;
     k_expert_tc<kBigBN, kBigSA, kBigSB, DOWN><<<grid, TC_THREADS,
                                                   TcCfg<kBigBN, kBigSA, kBigSB>::SMEM_BYTES, s>>>(
-        m, groups, p.E, K, n_out, out, ysh);
+        m, groups, p.E, K, n_out, out);
   } else {
     const int grid = max_tiles < sms ? max_tiles : sms;
     k_expert_tc<kSmallBN, kSmallSA, kSmallSB, DOWN>
         <<<grid, TC_THREADS, TcCfg<kSmallBN, kSmallSA, kSmallSB>::SMEM_BYTES, s>>>(
-            m, groups, p.E, K, n_out, out, ysh);
+            m, groups, p.E, K, n_out, out);
   }
 }
 
@@ -559,14 +560,13 @@ void launch_simt(const Plan& p, const void* x, const moe_expert_w* ex, const moe
   const T* xp = reinterpret_cast<const T*>(ws + p.o_xperm);
   T* hbuf = reinterpret_cast<T*>(ws + p.o_h);
   T* yperm = reinterpret_cast<T*>(ws + p.o_yperm);
-  float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
   k_expert_simt<T, false><<<p.max_tiles_a, 256, 0, s>>>(
       (const T*)ex->w_gate, (const T*)ex->w_up, (const T*)sh->w_gate, (const T*)sh->w_up, xp,
-      (const T*)x, groups, p.E, p.d, p.h, hbuf, nullptr);
+      (const T*)x, groups, p.E, p.d, p.h, hbuf);
   if (between) cudaEventRecord(between, s);
   k_expert_simt<T, true><<<p.max_tiles_b, 256, 0, s>>>(
       (const T*)ex->w_down, nullptr, (const T*)sh->w_down, nullptr, hbuf, hbuf, groups, p.E, p.h,
-      p.d, yperm, ysh);
+      p.d, yperm);
 }
 
 int forward_impl(const moe_desc* desc, const void* x, const float* w_router, const float* bias,
@@ -676,7 +676,6 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
     } else {
       __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(ws + p.o_h);
       __nv_bfloat16* yperm = reinterpret_cast<__nv_bfloat16*>(ws + p.o_yperm);
-      float* ysh = reinterpret_cast<float*>(ws + p.o_ysh);
       if (p.fp8_blk) {
         // both products on block-scaled codes: GEMM 1 writes H as codes and
         // exponent words, GEMM 2 reads them (K counted in 64-element bf16
@@ -700,7 +699,7 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
         const Fp8Blk f2{wd, wd, swd, swd, e4m3_block_words(p.h), hw, (int)rows_h, nullptr, p.k,
                         nullptr, nullptr, 0};
         launch_pair<TC2_FWD_DOWN_B8>(p, maps.down, p.max_tiles_b, groups, p.h / 2, p.d, yperm,
-                                     ysh, nullptr, s, Fp8Scales{}, f2);
+                                     nullptr, nullptr, s, Fp8Scales{}, f2);
       } else {
       if (p.fp8) {
         const size_t so = e4m3_scale_offset((long long)p.E * p.h, p.d),
@@ -720,22 +719,21 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
                                   reinterpret_cast<__nv_bfloat16*>(ws + p.o_ab));
       } else {
         launch_gemm<false>(p, maps.up, p.big_tiles && MOE_PAIR_GEMM1, p.bn, p.max_tiles_a,
-                           groups, hbuf, nullptr, s);
+                           groups, hbuf, s);
       }
       if (between) cudaEventRecord(between, s);
       launch_gemm<true>(p, maps.down, p.big_tiles && MOE_PAIR_GEMM2, p.bn, p.max_tiles_b, groups,
-                        yperm, ysh, s);
+                        yperm, s);
       }
     }
     mark(4);
-    const float* ysh = reinterpret_cast<const float*>(ws + p.o_ysh);
     if (p.f32)
-      k_combine<float><<<p.T, 128, 0, s>>>(ysh, reinterpret_cast<const float*>(ws + p.o_yperm),
-                                           inv, gates, p.T, p.d, p.k, static_cast<float*>(y));
+      k_combine<float><<<p.T, 128, 0, s>>>(reinterpret_cast<const float*>(ws + p.o_yperm), inv,
+                                           gates, p.T, p.d, p.k, static_cast<float*>(y));
     else
       k_combine<__nv_bfloat16><<<p.T, 128, 0, s>>>(
-          ysh, reinterpret_cast<const __nv_bfloat16*>(ws + p.o_yperm), inv, gates, p.T, p.d,
-          p.k, static_cast<__nv_bfloat16*>(y));
+          reinterpret_cast<const __nv_bfloat16*>(ws + p.o_yperm), inv, gates, p.T, p.d, p.k,
+          static_cast<__nv_bfloat16*>(y));
   } else {
     mark(2);
     mark(3);
@@ -1112,10 +1110,10 @@ int moe_workspace_regions(const moe_desc* desc, moe_region* regions, int cap) {
       {"pair_rank", p.o_rank, p.b_rank},   {"groups", p.o_groups, p.b_groups},
       {"perm", p.o_perm, p.b_perm},        {"inv", p.o_inv, p.b_inv},
       {"x_perm", p.o_xperm, p.b_xperm},    {"h", p.o_h, p.b_h},
-      {"y_perm", p.o_yperm, p.b_yperm},    {"y_shared", p.o_ysh, p.b_ysh},
+      {"y_perm", p.o_yperm, p.b_yperm},
       {"x_q", p.o_xq, p.b_xq},             {"h_q", p.o_hq, p.b_hq},
   };
-  const int n = p.route_only ? 5 : 13;
+  const int n = p.route_only ? 5 : (int)(sizeof(all) / sizeof(all[0]));
   for (int i = 0; i < n && i < cap && regions; ++i) {
     memset(regions[i].name, 0, sizeof(regions[i].name));
     strncpy(regions[i].name, all[i].n, sizeof(regions[i].name) - 1);

@@ -33,7 +33,7 @@ int main(void) {
 
   moe_region regs[16];
   int n = moe_workspace_regions(&d, regs, 16);
-  CHECK(n == 13);
+  CHECK(n == 12);
   CHECK(strcmp(regs[0].name, "router_part") == 0);
   for (int i = 1; i < n; ++i) CHECK(regs[i].offset % 256 == 0);
 

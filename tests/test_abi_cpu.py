@@ -146,7 +146,7 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     desc = M.make_desc(T, d, h, E, k, dt)
     total = M.moe_workspace_size(desc)
     regs = M.moe_workspace_regions(desc)
-    assert total > 0 and len(regs) == 13
+    assert total > 0 and len(regs) == 12
     spans = sorted(regs.values())
     for (o1, b1), (o2, _) in zip(spans, spans[1:]):
         assert o1 % 256 == 0 and o1 + b1 <= o2
@@ -154,7 +154,8 @@ def test_workspace_regions_are_disjoint_and_aligned(shape):
     el = 4 if dt == "f32" else 2
     assert regs["x_perm"][1] == T * k * d * el
     assert regs["h"][1] == (T * k + T) * h * el
-    assert regs["y_shared"][1] == T * d * 4
+    # the routed rows, then the shared expert's rows
+    assert regs["y_perm"][1] == (T * k + T) * d * el
     assert regs["x_q"][1] == 0 and regs["h_q"][1] == 0
     # the tensor-core router (bf16 tokens, 96 experts or more) keeps the
     # router weights as three bf16 terms, expert rows padded to 256
@@ -176,7 +177,7 @@ def test_fp8_flags(F):
     T, d, h, E, k = 300, 7168, 2048, 256, 8
     desc = M.make_desc(T, d, h, E, k, "bf16", F)
     regs = M.moe_workspace_regions(desc)
-    assert len(regs) == 13
+    assert len(regs) == 12
     R = T * k + T
     # the gathered token rows hold one-byte codes in both modes
     assert regs["x_perm"][1] == T * k * d
