@@ -270,3 +270,13 @@ def test_clock_record_slots_match_the_header():
 
 def test_clock_record_arguments():
     assert M.library().moe_sm_clock_record(None, 0) == M.ERR_CODE["MOE_ERR_NULL"]
+
+
+@pytest.mark.parametrize("E", [34, 98, 256])
+def test_group_table_holds_every_scheduler_counter(E):
+    """The group table: seven per-group arrays (7 E + 12 ints) and then the
+    schedulers' tile counters, of which the backward uses next[2..7] -- the
+    region must hold all of them even where its size is a multiple of the
+    256-byte region alignment (E = 34 mod 64 with the old size)."""
+    regs = M.moe_workspace_regions(M.make_desc(64, 128, 128, E, 2, "bf16", M.MOE_TRAINING))
+    assert regs["groups"][1] >= (7 * E + 12 + 8) * 4
