@@ -17,10 +17,8 @@
 //                  bases, the exclusive scan off[], and the GEMM tile table
 //                  (token tiles per group, tile prefix sums).  Group E is the
 //                  shared expert, whose rows are all T tokens.
-// k_permute_gather: one warp per token t; lane j < k handles pair
-//                  p = t*k + j: pos = base[block][e] + rank, perm[pos] = p,
-//                  inv[p] = pos; the warp reads x[t] once and writes it to
-//                  X_perm[pos] of all k pairs.
+// k_permute_gather: one warp per pair: pos = base[block][e] + rank,
+//                  perm[pos] = p, inv[p] = pos, X_perm[pos] = x[t].
 #pragma once
 
 #include "ptx.cuh"
@@ -185,43 +183,25 @@ k_scan_groups(int32_t* __restrict__ blk_hist, int n_blocks, int E, int T, int TK
   }
 }
 
-// One warp per token (k <= 32); row_bytes a multiple of 16.  Each lane
-// moves up to GATHER_VEC 16-byte vectors of the row per round, so that a
-// warp has that many loads in flight before its k stores of each.
-#define GATHER_VEC 4
+// One warp per pair; row_bytes a multiple of 16.
 __global__ void __launch_bounds__(256)
 k_permute_gather(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ pair_rank,
-                 const int32_t* __restrict__ blk_base, int T, int E, int k,
+                 const int32_t* __restrict__ blk_base, int TK, int E, int k,
                  const uint8_t* __restrict__ x, uint8_t* __restrict__ x_perm, size_t row_bytes,
                  int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  int pos = 0;
-  if (lane < k) {
-    const int p = t * k + lane;
-    const int e = topk_idx[p];
-    pos = blk_base[(size_t)(p / MOE_PAIRS_PER_BLOCK) * E + e] + pair_rank[p];
+  const int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (p >= TK) return;
+  const int e = topk_idx[p];
+  const int b = p / MOE_PAIRS_PER_BLOCK;
+  const int pos = blk_base[(size_t)b * E + e] + pair_rank[p];
+  if (lane == 0) {
     perm[pos] = p;
     inv[p] = pos;
   }
+  const int t = p / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+  uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)pos * row_bytes);
   const int nv = (int)(row_bytes / 16);
-  for (int i0 = 0; i0 < nv; i0 += 32 * GATHER_VEC) {
-    uint4 v[GATHER_VEC];
-#pragma unroll
-    for (int u = 0; u < GATHER_VEC; ++u) {
-      const int i = i0 + 32 * u + lane;
-      if (i < nv) v[u] = src[i];
-    }
-    for (int j = 0; j < k; ++j) {
-      uint4* dst = reinterpret_cast<uint4*>(
-          x_perm + (size_t)__shfl_sync(0xffffffffu, pos, j) * row_bytes);
-#pragma unroll
-      for (int u = 0; u < GATHER_VEC; ++u) {
-        const int i = i0 + 32 * u + lane;
-        if (i < nv) dst[i] = v[u];
-      }
-    }
-  }
+  for (int i = lane; i < nv; i += 32) dst[i] = src[i];
 }

@@ -664,8 +664,8 @@ int forward_impl(const moe_desc* desc, const void* x, const float* w_router, con
       k_quant_ablocks<<<(p.T + 7) / 8, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), p.T,
                                                      p.d, xq, xw);
     const bool codes = p.fp8 || p.fp8_blk;
-    k_permute_gather<<<(p.T + 7) / 8, 256, 0, s>>>(
-        topk_idx, rank, hist, p.T, p.E, p.k, codes ? xq : static_cast<const uint8_t*>(x),
+    k_permute_gather<<<(p.TK + 7) / 8, 256, 0, s>>>(
+        topk_idx, rank, hist, p.TK, p.E, p.k, codes ? xq : static_cast<const uint8_t*>(x),
         ws + p.o_xperm, (size_t)p.d * (codes ? 1 : p.el), perm, inv);
     mark(2);
     cudaEvent_t between = events ? static_cast<cudaEvent_t>(events[3]) : nullptr;
