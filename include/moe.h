@@ -353,6 +353,13 @@ MOE_API int moe_sm_clock_record(unsigned long long* out, int reset);
  * out of range, MOE_ERR_DEVICE / MOE_ERR_LAUNCH as moe_forward. */
 MOE_API int moe_selftest_timeout(unsigned limit_ms, void* stream);
 
+/* The expert epilogue's silu(z) = z / (1 + e^-z) (the gate/up products'
+ * SwiGLU), applied elementwise to n fp32 device values z -> out, for
+ * accuracy tests of the kernel's arithmetic.  Enqueued on `stream`.  Returns
+ * MOE_ERR_SHAPE for n < 0, MOE_ERR_NULL for a NULL pointer with n > 0,
+ * MOE_ERR_DEVICE / MOE_ERR_LAUNCH as moe_forward. */
+MOE_API int moe_selftest_silu(const float* z, float* out, int n, void* stream);
+
 /* Static string for a MOE_* code. */
 MOE_API const char* moe_error_string(int code);
 

@@ -63,6 +63,9 @@
 
 // silu(z) = z * sigmoid(z) with the fast exponential and division: their
 // relative error (~1e-6) is far below the bf16 rounding of the stored H.
+// Where 1 + e^-z exceeds 2^126 (z below about -87.3) the fast division
+// gives z * 0: -0, or NaN for z = -inf.  (moe_selftest_silu exposes it to
+// the accuracy tests.)
 MOE_DEV float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // 8 x 8 transpose of 16-bit values inside each group of 8 consecutive lanes:

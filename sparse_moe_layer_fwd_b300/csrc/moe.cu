@@ -815,6 +815,17 @@ int moe_selftest_timeout(unsigned limit_ms, void* stream) {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
+int moe_selftest_silu(const float* z, float* out, int n, void* stream) {
+  if (n < 0) return MOE_ERR_SHAPE;
+  if (n == 0) return MOE_OK;
+  if (!z || !out) return MOE_ERR_NULL;
+  int rc = device_ok();
+  if (rc != MOE_OK) return rc;
+  cudaGetLastError();
+  k_selftest_silu<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(z, out, n);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
 size_t moe_e4m3_packed_bytes(long long rows, int cols) {
   if (rows < 0 || cols <= 0) return 0;
   return e4m3_scale_offset(rows, cols) + (size_t)rows * 4;

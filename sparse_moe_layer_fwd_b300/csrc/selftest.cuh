@@ -1,4 +1,5 @@
-// selftest.cuh -- exercise the failure path of the bounded waits on the GPU.
+// selftest.cuh -- exercise the failure path of the bounded waits on the GPU,
+// and expose the expert epilogue's silu for accuracy tests.
 //
 // Every wait of the library's kernels on an mbarrier gives up after a time
 // limit, sets the device error word (MOE_DEV_ERR_TIMEOUT, read and reset by
@@ -9,7 +10,7 @@
 // context stays usable.
 #pragma once
 
-#include "ptx.cuh"
+#include "experts_tc.cuh"
 
 __global__ void __launch_bounds__(32) k_selftest_wait(uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -25,4 +26,11 @@ __global__ void __launch_bounds__(32) k_selftest_wait(uint64_t limit_ns) {
     if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) break;
   }
   if (!done) atomicOr(&g_moe_dev_error, MOE_DEV_ERR_TIMEOUT);
+}
+
+// The expert epilogue's silu, elementwise (moe_selftest_silu).
+__global__ void __launch_bounds__(256) k_selftest_silu(const float* __restrict__ z,
+                                                       float* __restrict__ out, int n) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i < n) out[i] = silu_fast(z[i]);
 }

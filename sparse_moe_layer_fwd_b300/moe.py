@@ -88,6 +88,7 @@ def _load():
     lib.moe_route_noalloc.argtypes = [dp, P, P, P, P, P, P, P]
     lib.moe_route_noalloc.restype = I
     lib.moe_selftest_timeout.argtypes, lib.moe_selftest_timeout.restype = [U, P], I
+    lib.moe_selftest_silu.argtypes, lib.moe_selftest_silu.restype = [P, P, I, P], I
     lib.moe_e4m3_packed_bytes.argtypes = [ctypes.c_longlong, I]
     lib.moe_e4m3_packed_bytes.restype = S
     lib.moe_quantize_rows_e4m3.argtypes = [P, ctypes.c_longlong, I, P, P]
@@ -312,3 +313,9 @@ def moe_selftest_timeout(limit_ms: int, stream=None, check=True) -> int:
     a synchronise, moe_last_error() reports MOE_ERR_DEVICE_TIMEOUT."""
     rc = _lib.moe_selftest_timeout(int(limit_ms), _stream(stream))
     return _check(rc, "moe_selftest_timeout") if check else rc
+
+
+def moe_selftest_silu(z, out, stream=None, check=True) -> int:
+    """The expert epilogue's silu applied to the fp32 device tensor z -> out."""
+    rc = _lib.moe_selftest_silu(_ptr(z), _ptr(out), int(z.numel()), _stream(stream))
+    return _check(rc, "moe_selftest_silu") if check else rc

@@ -65,6 +65,8 @@ int main(void) {
         MOE_ERR_SHAPE);
   CHECK(moe_selftest_timeout(0, NULL) == MOE_ERR_SHAPE);
   CHECK(moe_sm_clock_record(NULL, 0) == MOE_ERR_NULL);
+  CHECK(moe_selftest_silu(NULL, NULL, -1, NULL) == MOE_ERR_SHAPE);
+  CHECK(moe_selftest_silu(NULL, (float*)0x10000, 4, NULL) == MOE_ERR_NULL);
   CHECK(MOE_CLOCK_SLOTS == 4);
   /* routing with the static array: a problem whose scratch exceeds it is
    * refused before any device is touched */

@@ -19,7 +19,8 @@ def test_library_exports_every_header_function():
         "moe_bias_update", "moe_last_error", "moe_error_string", "moe_workspace_regions",
         "moe_forward_profiled", "moe_route_noalloc", "moe_seq_balance_loss", "moe_backward",
         "moe_e4m3_packed_bytes", "moe_quantize_rows_e4m3", "moe_selftest_timeout",
-        "moe_e4m3_block_packed_bytes", "moe_quantize_blocks_e4m3", "moe_sm_clock_record"}
+        "moe_e4m3_block_packed_bytes", "moe_quantize_blocks_e4m3", "moe_sm_clock_record",
+        "moe_selftest_silu"}
     lib = ctypes.CDLL(M.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -280,3 +281,13 @@ def test_group_table_holds_every_scheduler_counter(E):
     256-byte region alignment (E = 34 mod 64 with the old size)."""
     regs = M.moe_workspace_regions(M.make_desc(64, 128, 128, E, 2, "bf16", M.MOE_TRAINING))
     assert regs["groups"][1] >= (7 * E + 12 + 8) * 4
+
+
+def test_selftest_silu_arguments():
+    E = M.ERR_CODE
+    lib = M.library()
+    assert lib.moe_selftest_silu(None, None, -1, None) == E["MOE_ERR_SHAPE"]
+    assert lib.moe_selftest_silu(None, None, 0, None) == M.MOE_OK
+    assert lib.moe_selftest_silu(None, FAKE, 4, None) == E["MOE_ERR_NULL"]
+    if not torch.cuda.is_available():
+        assert lib.moe_selftest_silu(FAKE, FAKE, 4, None) == E["MOE_ERR_DEVICE"]
