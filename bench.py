@@ -70,10 +70,10 @@ def kernels_per_step(wl, route_only, fp8=False):
 NCU_TRAFFIC = {
     # profiles/k_expert_tc2_v3_prefill_32experts_full.md ("DRAM counters of
     # the current sources"): GEMM 1 read + written bytes on that case
-    "bf16": {"sha": "70e35cc962d72144", "case": "v3_prefill_32experts",
-             "bytes": 2.187689216e9 + 0.034349568e9},
-    ":fp8blk": {"sha": "70e35cc962d72144", "case": "v3_prefill_32experts",
-                "bytes": 1.045511168e9 + 0.018667008e9},
+    "bf16": {"sha": "eaefe0b9e0d65bb5", "case": "v3_prefill_32experts",
+             "bytes": 2.192738304e9 + 0.035043328e9},
+    ":fp8blk": {"sha": "eaefe0b9e0d65bb5", "case": "v3_prefill_32experts",
+                "bytes": 1.045634048e9 + 0.018684416e9},
 }
 
 
