@@ -416,156 +416,190 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      if (leader) {
-        // ---------- MMA issuer (leader only) ----------
-        int it = 0, tl = 0;
-        int qsf = 0;  // block-scaled: scale groups (4 K steps each) of the tiles before this one
-        for (int i = 0;; ++i) {
-          const int b = next_tile(i, true);
-          if (b < 0) break;
-          if (*abort_flag) continue;  // keep reading the tile ring until the scheduler says "none"
-          const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, 0);
-          const uint32_t idesc = FP8 ? umma_idesc_e4m3(2 * TC_BM, t.npad)
-                                     : umma_idesc_bf16(2 * TC_BM, t.npad) | (MNA ? (1u << 15) : 0u);
-          // Block-scaled: the scale words of K steps 4 j .. 4 j + 3 (group
-          // j) are copied from the scale warps' stage into TMEM set (qsf + j)
-          // & 1 before the group's first MMA (the copy and the MMAs issued
-          // after it run in order), and the set and stage are released by a
-          // commit after the group's last MMA.  The copy into a set comes
-          // after the scale warp refilled its stage, which it does only after
-          // that commit: the MMAs of the group two back have completed.
-          int g_loaded = -1;
-          auto sf_col = [&](int kb) {
-            return tmem + (((qsf + (kb >> 2)) & 1) ? 496u : 240u);
-          };
-          auto ensure_sf = [&](int kb) -> bool {
-            if constexpr (BLK) {
-              while (g_loaded < (kb >> 2)) {
-                ++g_loaded;
-                const int q = qsf + g_loaded;
-                if (!mbar_wait_cluster(sf_full(q & 1), (q >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t col = tmem + ((q & 1) ? 496u : 240u);
-                const uint32_t src = smem_u32(smem + C::SF_OFF + (q & 1) * C::SF_STAGE);
+    if (leader) {
+      // ---------- MMA issuer (leader only): the whole warp runs the loop
+      // (waits, tile geometry, descriptors), one elected lane issues the
+      // tcgen05 instructions; every wait's outcome is made warp-uniform ----------
+      const uint32_t F = 0xffffffffu;
+      int it = 0, tl = 0;
+      int qsf = 0;  // block-scaled: scale groups (4 K steps each) of the tiles before this one
+      for (int i = 0;; ++i) {
+        const int b = __shfl_sync(F, next_tile(i, false), 0);
+        __syncwarp();
+        if (lane == 0) release_tile(i % TC_TILE_RING);
+        if (b < 0) break;
+        if (__any_sync(F, *abort_flag != 0)) continue;  // keep reading the tile ring until "none"
+        const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, 0);
+        const uint32_t idesc = FP8 ? umma_idesc_e4m3(2 * TC_BM, t.npad)
+                                   : umma_idesc_bf16(2 * TC_BM, t.npad) | (MNA ? (1u << 15) : 0u);
+        // Block-scaled: the scale words of K steps 4 j .. 4 j + 3 (group
+        // j) are copied from the scale warps' stage into TMEM set (qsf + j)
+        // & 1 before the group's first MMA (the copy and the MMAs issued
+        // after it run in order), and the set and stage are released by a
+        // commit after the group's last MMA.  The copy into a set comes
+        // after the scale warp refilled its stage, which it does only after
+        // that commit: the MMAs of the group two back have completed.
+        int g_loaded = -1;
+        auto sf_col = [&](int kb) {
+          return tmem + (((qsf + (kb >> 2)) & 1) ? 496u : 240u);
+        };
+        auto ensure_sf = [&](int kb) -> bool {
+          if constexpr (BLK) {
+            while (g_loaded < (kb >> 2)) {
+              ++g_loaded;
+              const int q = qsf + g_loaded;
+              if (!__all_sync(F, mbar_wait_cluster(sf_full(q & 1), (q >> 1) & 1))) return false;
+              tc_fence_after();
+              const uint32_t col = tmem + ((q & 1) ? 496u : 240u);
+              const uint32_t src = smem_u32(smem + C::SF_OFF + (q & 1) * C::SF_STAGE);
+              if (elect_one()) {
                 tmem_cp_pair_32x128b(col, smem_desc_rows16(src));             // A rows, accumulator 0
                 tmem_cp_pair_32x128b(col + 4, smem_desc_rows16(src + 512));   // A rows, accumulator 1
                 tmem_cp_pair_32x128b(col + 8, smem_desc_rows16(src + 1024));  // tokens 0 .. 127
                 if (t.npad > 128) tmem_cp_pair_32x128b(col + 12, smem_desc_rows16(src + 1536));
               }
+              __syncwarp();
             }
-            return true;
-          };
-          auto release_sf = [&](int kb, int w) {
-            if (BLK && w == (t.mma1 ? 1 : 0) && ((kb & 3) == 3 || kb == nkb - 1))
-              umma_commit_pair(sf_empty((qsf + (kb >> 2)) & 1));
-          };
-          const int u = tl % NBUF;  // TMEM buffer of this tile
-          // k step kb of this tile uses ring stage it + kb
-          auto stage_ready = [&](int kb) -> bool {
-            const int st = it + kb;
-            if (!mbar_wait(a_full(st % SA), (st / SA) & 1) || !mbar_wait(b_full(st % SB), (st / SB) & 1))
-              return false;
-            tc_fence_after();
-            return true;
-          };
-          // the four K=16 MMAs of k step kb into accumulator w (0: columns
-          // 256 u, 1: columns 256)
-          auto issue = [&](int kb, int w) {
-            const int st = it + kb;
-            const uint32_t a = smem_u32(smem + (st % SA) * C::A_STAGE) + (uint32_t)(w * C::A_BYTES);
-            const uint32_t bb = smem_u32(smem + C::B_OFF + (st % SB) * C::B_STAGE);
-            const uint32_t d = tmem + (w ? 256u : (uint32_t)(u * 256));
+          }
+          return true;
+        };
+        auto release_sf = [&](int kb, int w) {
+          if (BLK && w == (t.mma1 ? 1 : 0) && ((kb & 3) == 3 || kb == nkb - 1)) {
+            if (elect_one()) umma_commit_pair(sf_empty((qsf + (kb >> 2)) & 1));
+            __syncwarp();
+          }
+        };
+        const int u = tl % NBUF;  // TMEM buffer of this tile
+        // k step kb of this tile uses ring stage it + kb
+        auto stage_ready = [&](int kb) -> bool {
+          const int st = it + kb;
+          const bool ok1 =
+              mbar_wait(a_full(st % SA), (st / SA) & 1) && mbar_wait(b_full(st % SB), (st / SB) & 1);
+          if (!__all_sync(F, ok1)) return false;
+          tc_fence_after();
+          return true;
+        };
+        auto acc_ready = [&](int ab, int parity) -> bool {
+          const bool ok1 = mbar_wait_cluster(acc_empty(ab), parity);
+          return __all_sync(F, ok1);
+        };
+        // the four K=16 MMAs of k step kb into accumulator w (0: columns
+        // 256 u, 1: columns 256).  Operand descriptors: one per operand and
+        // call, the four K slices as constant offsets in the start-address
+        // field (32 bytes = 2 units for K-major rows, 2048 bytes = 128 units
+        // for 16-row MN-major slices; the field stays below 2^14 for every
+        // shared-memory address).
+        auto issue = [&](int kb, int w) {
+          const int st = it + kb;
+          const uint32_t a = smem_u32(smem + (st % SA) * C::A_STAGE) + (uint32_t)(w * C::A_BYTES);
+          const uint32_t bb = smem_u32(smem + C::B_OFF + (st % SB) * C::B_STAGE);
+          const uint32_t d = tmem + (w ? 256u : (uint32_t)(u * 256));
+          const uint64_t ad = MNA ? umma_desc_sw128_mn(a, C::A_BYTES / 2) : umma_desc_sw128(a);
+          const uint64_t bd = umma_desc_sw128(bb);
+          constexpr uint64_t A_STEP = MNA ? (2048 >> 4) : (32 >> 4);
+          if (BLK) {
+            const uint32_t id = umma_idesc_mx_e4m3(2 * TC_BM, t.npad, (uint32_t)(kb & 3));
+            const uint32_t sfa = sf_col(kb) + (w ? 4u : 0u), sfb = sf_col(kb) + 8u;
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // four 32-byte K slices
-              if (BLK)
-                umma_mx_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32),
-                             umma_idesc_mx_e4m3(2 * TC_BM, t.npad, (uint32_t)(kb & 3)),
-                             sf_col(kb) + (w ? 4u : 0u), sf_col(kb) + 8u, (kb | kk) != 0);
-              else if (FP8)
-                umma_f8_pair(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(bb + kk * 32), idesc,
+              for (int kk = 0; kk < 4; ++kk)  // four 32-byte K slices
+                umma_mx_pair(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), id, sfa, sfb,
+                             (kb | kk) != 0);
+            }
+          } else if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              if (FP8)
+                umma_f8_pair(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
                              (kb | kk) != 0);
               else
-                umma_bf16_pair(d,
-                               MNA ? umma_desc_sw128_mn(a + kk * 2048, C::A_BYTES / 2)
-                                   : umma_desc_sw128(a + kk * 32),
-                               umma_desc_sw128(bb + kk * 32), idesc, (kb | kk) != 0);
+                umma_bf16_pair(d, ad + A_STEP * kk, bd + (uint64_t)(2 * kk), idesc,
+                               (kb | kk) != 0);
             }
-            mma_issued = true;
-          };
-          auto release = [&](int kb) {  // the stage is free once its MMAs complete
-            const int st = it + kb;
+          }
+          __syncwarp();
+          mma_issued = true;
+        };
+        auto release = [&](int kb) {  // the stage is free once its MMAs complete
+          const int st = it + kb;
+          if (elect_one()) {
             umma_commit_pair(a_empty(st % SA));
             umma_commit_pair(b_empty(st % SB));
             progress[2] = st + 1;
-          };
-          bool ok;
-          if (STAG) {
-            // Second GEMM: block 0 runs S k steps ahead of block 1 at the
-            // start of the tile and finishes S k steps before it, so the
-            // drain of each block overlaps MMAs of the other.
-            // (block-scaled: S <= 4, so block 0 is never more than one scale
-            // group ahead of block 1 and two TMEM scale sets suffice)
-            const int S = min(min(min(SA, SB), nkb / 2), BLK ? 4 : 64);
-            ok = tl == 0 || mbar_wait_cluster(acc_empty(0), (tl - 1) & 1);
-            tc_fence_after();
-            for (int kb = 0; ok && kb < S; ++kb)
-              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
-                issue(kb, 0);
-                release_sf(kb, 0);
-              }
-            ok = ok && (tl == 0 || mbar_wait_cluster(acc_empty(1), (tl - 1) & 1));
-            tc_fence_after();
-            for (int kb = 0; ok && kb < S; ++kb) {
+          }
+          __syncwarp();
+        };
+        auto commit_acc = [&](int ab) {
+          if (elect_one()) umma_commit_pair(acc_full(ab));
+          __syncwarp();
+        };
+        bool ok;
+        if (STAG) {
+          // Second GEMM: block 0 runs S k steps ahead of block 1 at the
+          // start of the tile and finishes S k steps before it, so the
+          // drain of each block overlaps MMAs of the other.
+          // (block-scaled: S <= 4, so block 0 is never more than one scale
+          // group ahead of block 1 and two TMEM scale sets suffice)
+          const int S = min(min(min(SA, SB), nkb / 2), BLK ? 4 : 64);
+          ok = tl == 0 || acc_ready(0, (tl - 1) & 1);
+          tc_fence_after();
+          for (int kb = 0; ok && kb < S; ++kb)
+            if ((ok = stage_ready(kb) && ensure_sf(kb))) {
+              issue(kb, 0);
+              release_sf(kb, 0);
+            }
+          ok = ok && (tl == 0 || acc_ready(1, (tl - 1) & 1));
+          tc_fence_after();
+          for (int kb = 0; ok && kb < S; ++kb) {
+            if (t.mma1) issue(kb, 1);
+            release_sf(kb, 1);
+            release(kb);
+          }
+          for (int kb = S; ok && kb < nkb - S; ++kb) {
+            if ((ok = stage_ready(kb) && ensure_sf(kb))) {
+              issue(kb, 0);
+              release_sf(kb, 0);
               if (t.mma1) issue(kb, 1);
               release_sf(kb, 1);
               release(kb);
             }
-            for (int kb = S; ok && kb < nkb - S; ++kb) {
-              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
-                issue(kb, 0);
-                release_sf(kb, 0);
-                if (t.mma1) issue(kb, 1);
-                release_sf(kb, 1);
-                release(kb);
-              }
+          }
+          for (int kb = nkb - S; ok && kb < nkb; ++kb)
+            if ((ok = stage_ready(kb) && ensure_sf(kb))) {
+              issue(kb, 0);
+              release_sf(kb, 0);
             }
-            for (int kb = nkb - S; ok && kb < nkb; ++kb)
-              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
-                issue(kb, 0);
-                release_sf(kb, 0);
-              }
-            if (ok) umma_commit_pair(acc_full(0));
-            for (int kb = nkb - S; ok && kb < nkb; ++kb) {
+          if (ok) commit_acc(0);
+          for (int kb = nkb - S; ok && kb < nkb; ++kb) {
+            if (t.mma1) issue(kb, 1);
+            release_sf(kb, 1);
+            release(kb);
+          }
+          if (ok) commit_acc(1);
+        } else {
+          ok = tl < NBUF || acc_ready(u, ((tl / NBUF) - 1) & 1);
+          tc_fence_after();
+          for (int kb = 0; ok && kb < nkb; ++kb) {
+            if ((ok = stage_ready(kb) && ensure_sf(kb))) {
+              issue(kb, 0);
+              release_sf(kb, 0);
               if (t.mma1) issue(kb, 1);
               release_sf(kb, 1);
               release(kb);
             }
-            if (ok) umma_commit_pair(acc_full(1));
-          } else {
-            ok = tl < NBUF || mbar_wait_cluster(acc_empty(u), ((tl / NBUF) - 1) & 1);
-            tc_fence_after();
-            for (int kb = 0; ok && kb < nkb; ++kb) {
-              if ((ok = stage_ready(kb) && ensure_sf(kb))) {
-                issue(kb, 0);
-                release_sf(kb, 0);
-                if (t.mma1) issue(kb, 1);
-                release_sf(kb, 1);
-                release(kb);
-              }
-            }
-            if (ok) umma_commit_pair(acc_full(u));
           }
-          if (!ok) {
-            *abort_flag = 1;
-            continue;
-          }
-          it += nkb;
-          qsf += (nkb + 3) >> 2;
-          ++tl;
+          if (ok) commit_acc(u);
         }
-      }  // the peer has no MMA role
-    }
+        if (!ok) {
+          if (lane == 0) *abort_flag = 1;
+          __syncwarp();
+          continue;
+        }
+        it += nkb;
+        qsf += (nkb + 3) >> 2;
+        ++tl;
+      }
+    }  // the peer has no MMA role
     __syncwarp();
   } else if (BLK && warp == TC2_SF_WARP) {
     // ---------- block scales (both CTAs): the exponent words of each group

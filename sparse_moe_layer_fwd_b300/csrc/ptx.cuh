@@ -47,6 +47,20 @@ MOE_DEV void sm_clock_add(int slot, SmClockStart s0) {
   atomicAdd(&g_moe_clock[slot][1], (unsigned long long)ns);
 }
 
+// true in one lane of the converged warp (elect.sync).  Single-thread
+// tcgen05 instructions are issued from such a lane inside loops that the
+// whole warp runs: their control flow and operands then stay warp-uniform.
+// (Issued from a loop that one lane runs alone, the same MMA sequence cost
+// its thread about 105 cycles per MMA instead of at most 66 -- less than the
+// MMA itself takes only for N above 200.)
+MOE_DEV bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}\n"
+      : "=r"(p));
+  return p != 0;
+}
+
 // ------------------------------------------------------------------ mbarrier
 MOE_DEV void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
