@@ -451,48 +451,58 @@ k_wgrad_tc2(const __grid_constant__ WgMapsDev maps, const int32_t* __restrict__ 
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      int it = 0, tl = 0;
-      for (int i = 0;; ++i) {
-        const int b = next_tile(i);
-        if (b >= 0) release_tile(i % TC_TILE_RING);
-        if (b < 0) break;
-        if (!leader) continue;  // the peer only keeps the tile ring in step
-        if (*abort_flag) continue;
-        // ---------- MMA issuer (leader) ----------
-        const WgTile t = wg_tile(G, E, b, MB, NB, pcol0, qcol0);
-        const int u = tl & 1;
-        if (tl >= 2 && !mbar_wait_cluster(acc_empty(u), ((tl >> 1) - 1) & 1)) {
-          *abort_flag = 1;
-          continue;
+    // The whole warp runs the loop (both CTAs keep the tile ring in step);
+    // in the leader one elected lane issues the tcgen05 instructions, with
+    // one descriptor per operand and stage (the 16-row K slices are constant
+    // offsets of 2048 bytes = 128 units in the start-address field).  Every
+    // wait's outcome is made warp-uniform.
+    const uint32_t F = 0xffffffffu;
+    int it = 0, tl = 0;
+    for (int i = 0;; ++i) {
+      const int b = __shfl_sync(F, next_tile(i), 0);
+      __syncwarp();
+      if (lane == 0 && b >= 0) release_tile(i % TC_TILE_RING);
+      if (b < 0) break;
+      if (!leader) continue;  // the peer only keeps the tile ring in step
+      if (__any_sync(F, *abort_flag != 0)) continue;
+      // ---------- MMA issuer (leader) ----------
+      const WgTile t = wg_tile(G, E, b, MB, NB, pcol0, qcol0);
+      const int u = tl & 1;
+      if (tl >= 2 && !__all_sync(F, mbar_wait_cluster(acc_empty(u), ((tl >> 1) - 1) & 1))) {
+        if (lane == 0) *abort_flag = 1;
+        continue;
+      }
+      tc_fence_after();
+      const uint32_t idesc = umma_idesc_bf16(256, 256) | (1u << 15) | (1u << 16);
+      const int ksteps = (t.rows + 15) / 16;  // rows rounded up to 16
+      bool ok = true;
+      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        const int st = it % WG_STAGES;
+        if (!__all_sync(F, mbar_wait(full(st), (it / WG_STAGES) & 1))) {
+          ok = false;
+          break;
         }
         tc_fence_after();
-        const uint32_t idesc = umma_idesc_bf16(256, 256) | (1u << 15) | (1u << 16);
-        const int ksteps = (t.rows + 15) / 16;  // rows rounded up to 16
-        bool ok = true;
-        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
-          const int st = it % WG_STAGES;
-          if (!mbar_wait(full(st), (it / WG_STAGES) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a = smem_u32(smem + st * WG_STAGE_BYTES), bq = a + WG_HALF_BYTES;
-          const int kk_n = min(4, ksteps - 4 * kb);
+        const uint32_t a = smem_u32(smem + st * WG_STAGE_BYTES), bq = a + WG_HALF_BYTES;
+        const uint64_t ad = umma_desc_sw128_mn(a, 8192), bd = umma_desc_sw128_mn(bq, 8192);
+        const int kk_n = min(4, ksteps - 4 * kb);
+        if (elect_one()) {
           for (int kk = 0; kk < kk_n; ++kk)
-            umma_bf16_pair(tmem + (uint32_t)(u * 256), umma_desc_sw128_mn(a + kk * 2048, 8192),
-                           umma_desc_sw128_mn(bq + kk * 2048, 8192), idesc, (kb | kk) != 0);
-          mma_issued = true;
+            umma_bf16_pair(tmem + (uint32_t)(u * 256), ad + (uint64_t)(128 * kk),
+                           bd + (uint64_t)(128 * kk), idesc, (kb | kk) != 0);
           umma_commit_pair(empty(st));
           progress[1] = it + 1;
         }
-        if (!ok) {
-          *abort_flag = 1;
-          continue;
-        }
-        umma_commit_pair(acc_full(u));
-        ++tl;
+        __syncwarp();
+        mma_issued = true;
       }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        continue;
+      }
+      if (elect_one()) umma_commit_pair(acc_full(u));
+      __syncwarp();
+      ++tl;
     }
     __syncwarp();
   } else {

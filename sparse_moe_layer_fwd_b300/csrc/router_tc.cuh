@@ -170,23 +170,31 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
       }
     }
   } else if (warp == 1) {
-    if (leader && lane == 0) {
+    if (leader) {
       // ---------- MMA issuer: per stage and token half, 3 split terms x 4 ----------
       // ---------- K=16 steps into a fresh accumulator (2 kb + h) mod 4   ----------
+      // The whole warp runs the loop and one elected lane issues (the issue
+      // costs a lone thread more than an N = 128 MMA takes); descriptors are
+      // built once per stage, the terms, slices and token halves are
+      // constant offsets (16-byte units) in their start-address fields.
+      const uint32_t F = 0xffffffffu;
       const uint32_t idesc = umma_idesc_bf16(256, 128);
       bool ok = true;
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const int st = kb % RT_STAGES;
-        if (*abort_flag || !mbar_wait(full(st), (kb / RT_STAGES) & 1)) {
+        const bool got = !*abort_flag && mbar_wait(full(st), (kb / RT_STAGES) & 1);
+        if (!__all_sync(F, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t a = smem_u32(smem + st * RT_STAGE), b = a + RT_A_STAGE;
+        const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(b);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int n = 2 * kb + h, u = n % RT_N_ACC;  // n-th use of the accumulators
-          if (n >= RT_N_ACC && !mbar_wait(acc_empty(u), ((n / RT_N_ACC) - 1) & 1)) {
+          if (n >= RT_N_ACC &&
+              !__all_sync(F, mbar_wait(acc_empty(u), ((n / RT_N_ACC) - 1) & 1))) {
             ok = false;
             break;
           }
@@ -194,22 +202,28 @@ k_router_tc(const __grid_constant__ RouterMapsDev maps, int T, int E, int E_pad,
           // smallest term first: while W3 and W2 products accumulate, the sum
           // is 2^8 to 2^16 times smaller than u, so only the four W1 MMAs add
           // at full magnitude.  B: token rows 64 h .. +63 of each CTA's half.
+          if (elect_one()) {
 #pragma unroll
-          for (int jj = 0; jj < 3; ++jj)
+            for (int jj = 0; jj < 3; ++jj)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_pair(tmem + (uint32_t)(u * 128),
-                             umma_desc_sw128(a + (2 - jj) * RT_A_BYTES + kk * 32),
-                             umma_desc_sw128(b + (uint32_t)(h * 64 * 128) + kk * 32), idesc,
-                             (jj | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16_pair(tmem + (uint32_t)(u * 128),
+                               ad + (uint64_t)(((2 - jj) * RT_A_BYTES) / 16 + 2 * kk),
+                               bd + (uint64_t)((h * 64 * 128) / 16 + 2 * kk), idesc,
+                               (jj | kk) != 0);
+            umma_commit_pair(acc_full(u));
+          }
+          __syncwarp();
           mma_issued = true;
-          umma_commit_pair(acc_full(u));
         }
         if (!ok) break;
-        umma_commit_pair(empty(st));
-        progress[1] = kb + 1;
+        if (elect_one()) {
+          umma_commit_pair(empty(st));
+          progress[1] = kb + 1;
+        }
+        __syncwarp();
       }
-      if (!ok) *abort_flag = 1;
+      if (!ok && lane == 0) *abort_flag = 1;
     }
     __syncwarp();
   } else {
