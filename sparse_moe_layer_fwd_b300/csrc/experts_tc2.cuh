@@ -310,44 +310,54 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
   };
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------- weight (A) producer; in the leader also the scheduler ----------
-      // weight rows read by one token tile: evict first; rows that the
-      // group's other token tiles (taken at about the same time by other
-      // pairs) read again: normal priority, so that they meet in L2
-      const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
-      int it = 0;
-      for (int i = 0;; ++i) {
-        int b;
-        if (leader) {
-          const int s = i % TC_TILE_RING;
-          if (i >= TC_TILE_RING &&
-              !mbar_wait_cluster(tile_empty(s), ((i / TC_TILE_RING) & 1) ^ 1)) {
-            *abort_flag = 1;
-            break;
-          }
-          b = *abort_flag ? total : atomicAdd(counter, 1);
-          if (b >= total) b = -1;
-          tile_id[s] = b;
-          st_cluster_u32(cluster_map(smem_u32(const_cast<int*>(&tile_id[s])), 1), (uint32_t)b);
+    // ---------- weight (A) producer; in the leader also the scheduler.  The
+    // whole warp runs the loop (waits and tile geometry warp-uniform); lane 0
+    // takes tiles and publishes them, one elected lane issues the copies ----------
+    const uint32_t F = 0xffffffffu;
+    // weight rows read by one token tile: evict first; rows that the group's
+    // other token tiles (taken at about the same time by other pairs) read
+    // again: normal priority, so that they meet in L2
+    const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
+    int it = 0;
+    for (int i = 0;; ++i) {
+      int b;
+      if (leader) {
+        const int s = i % TC_TILE_RING;
+        if (i >= TC_TILE_RING &&
+            !__all_sync(F, mbar_wait_cluster(tile_empty(s), ((i / TC_TILE_RING) & 1) ^ 1))) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        int bl = 0;
+        if (lane == 0) {
+          bl = *abort_flag ? total : atomicAdd(counter, 1);
+          if (bl >= total) bl = -1;
+          tile_id[s] = bl;
+          st_cluster_u32(cluster_map(smem_u32(const_cast<int*>(&tile_id[s])), 1), (uint32_t)bl);
           mbar_arrive(tile_full(s));
           mbar_arrive_cluster(cluster_map(tile_full(s), 1));
-        } else {
-          b = next_tile(i, true);
         }
-        if (b < 0) break;
-        const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
-        const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
-        const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
-        const uint64_t pol_w = t.reread ? pol_again : pol_once;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int sa = it % SA, r = it / SA;
-          if (*abort_flag || (it >= SA && !mbar_wait(a_empty(sa), (r & 1) ^ 1))) {
-            *abort_flag = 1;
-            break;
-          }
-          uint8_t* st = smem + sa * C::A_STAGE;
-          const uint32_t fb = lead(a_full(sa));
+        b = __shfl_sync(F, bl, 0);
+      } else {
+        b = __shfl_sync(F, next_tile(i, false), 0);
+        __syncwarp();
+        if (lane == 0) release_tile(i % TC_TILE_RING);
+      }
+      if (b < 0) break;
+      const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
+      const CUtensorMap* mA0 = t.shared ? &maps.sa0 : &maps.a0;
+      const CUtensorMap* mA1 = DOWN ? mA0 : (t.shared ? &maps.sa1 : &maps.a1);
+      const uint64_t pol_w = t.reread ? pol_again : pol_once;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int sa = it % SA, r = it / SA;
+        const bool ok1 = !*abort_flag && (it < SA || mbar_wait(a_empty(sa), (r & 1) ^ 1));
+        if (!__all_sync(F, ok1)) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + sa * C::A_STAGE;
+        const uint32_t fb = lead(a_full(sa));
+        if (elect_one()) {
           if (leader) mbar_arrive_expect_tx(a_full(sa), t.bytes_a);
           if (MNA) {
             // rows kb*64 .. +63 of the K dimension of the transposed weights,
@@ -374,33 +384,40 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
           }
           progress[0] = it + 1;
         }
+        __syncwarp();
       }
     }
+    __syncwarp();
   } else if (warp == TC_TOKEN_WARP) {
-    if (lane == 0) {
-      // ---------- token-row (B) producer: this CTA's half of the tile ----------
-      const uint64_t pol_x = l2_policy_evict_last();
-      int it = 0;
-      for (int i = 0;; ++i) {
-        const int b = next_tile(i, true);
-        if (b < 0) break;
-        const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
-        const bool bs =
-            (OP == TC2_FWD_UP || OP == TC2_BWD_DH || FP8U || UPB || UPT) &&
-            t.shared;
-        const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
-        const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
-        const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
-        const CUtensorMap* m8 = bs ? &maps.bs8 : &maps.b8;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int sb = it % SB, r = it / SB;
-          if (*abort_flag || (it >= SB && !mbar_wait(b_empty(sb), (r & 1) ^ 1))) {
-            *abort_flag = 1;
-            break;
-          }
-          uint8_t* st = smem + C::B_OFF + sb * C::B_STAGE;
-          const uint32_t fb = lead(b_full(sb));
-          const int kx = kb * KB_ELEMS;
+    // ---------- token-row (B) producer: this CTA's half of the tile (the
+    // whole warp runs the loop, one elected lane issues the copies) ----------
+    const uint32_t F = 0xffffffffu;
+    const uint64_t pol_x = l2_policy_evict_last();
+    int it = 0;
+    for (int i = 0;; ++i) {
+      const int b = __shfl_sync(F, next_tile(i, false), 0);
+      __syncwarp();
+      if (lane == 0) release_tile(i % TC_TILE_RING);
+      if (b < 0) break;
+      const Tc2Tile t = tc2_tile<OP, NACC>(G, toff, E, b, n_out, rank);
+      const bool bs =
+          (OP == TC2_FWD_UP || OP == TC2_BWD_DH || FP8U || UPB || UPT) &&
+          t.shared;
+      const CUtensorMap* m128 = bs ? &maps.bs128 : &maps.b128;
+      const CUtensorMap* m64 = bs ? &maps.bs64 : &maps.b64;
+      const CUtensorMap* m16 = bs ? &maps.bs16 : &maps.b16;
+      const CUtensorMap* m8 = bs ? &maps.bs8 : &maps.b8;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int sb = it % SB, r = it / SB;
+        const bool ok1 = !*abort_flag && (it < SB || mbar_wait(b_empty(sb), (r & 1) ^ 1));
+        if (!__all_sync(F, ok1)) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + C::B_OFF + sb * C::B_STAGE;
+        const uint32_t fb = lead(b_full(sb));
+        const int kx = kb * KB_ELEMS;
+        if (elect_one()) {
           if (leader) mbar_arrive_expect_tx(b_full(sb), (uint32_t)t.npad * (TC_BK * 2));
           int j = 0;
           for (; j + 128 <= t.half; j += 128)
@@ -413,8 +430,10 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             tma_load_2d_pair(smem_u32(st + j * (TC_BK * 2)), m8, fb, kx, t.row_b + j, pol_x);
           progress[1] = it + 1;
         }
+        __syncwarp();
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (leader) {
       // ---------- MMA issuer (leader only): the whole warp runs the loop
@@ -768,7 +787,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             stage_box_bf16<false>(tb + c, tb + c, stg + 2 * TC_BOX_BYTES, lane);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
+            if (elect_one()) {  // lane 0 of the converged warp, as for the waits
               if (valid) {
                 tma_store_2d(&maps.out, stg, of, t.out_row0 + c);
                 tma_store_2d(&maps.aux, stg + TC_BOX_BYTES, of, t.out_row0 + c);
@@ -776,6 +795,7 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
               }
               bulk_commit();
             }
+            __syncwarp();
             continue;
           }
           // fp8: scale of token column c + lane (the token's row of x)
@@ -801,10 +821,11 @@ k_expert_tc2(const __grid_constant__ TcMapsDev maps, const int32_t* __restrict__
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
+            if (elect_one()) {  // lane 0 of the converged warp, as for the waits
               if (valid) tma_store_2d(&maps.out, box, of, t.out_row0 + c);
               bulk_commit();
             }
+            __syncwarp();
             ++nbox;
             continue;
           }
