@@ -70,10 +70,10 @@ def kernels_per_step(wl, route_only, fp8=False):
 NCU_TRAFFIC = {
     # profiles/k_expert_tc2_v3_prefill_32experts_full.md ("DRAM counters of
     # the current sources"): GEMM 1 read + written bytes on that case
-    "bf16": {"sha": "09cc655c3726420c", "case": "v3_prefill_32experts",
-             "bytes": 2.175521280e9 + 0.033825024e9},
-    ":fp8blk": {"sha": "09cc655c3726420c", "case": "v3_prefill_32experts",
-                "bytes": 1.043354880e9 + 0.018547200e9},
+    "bf16": {"sha": "dd10e8a46ce0f545", "case": "v3_prefill_32experts",
+             "bytes": 2.176548352e9 + 0.033965824e9},
+    ":fp8blk": {"sha": "dd10e8a46ce0f545", "case": "v3_prefill_32experts",
+                "bytes": 1.043218432e9 + 0.018627072e9},
 }
 
 
