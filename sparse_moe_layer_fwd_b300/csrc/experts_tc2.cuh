@@ -22,7 +22,11 @@
 //
 // Roles per CTA as in the 1-SM kernel (warp 0: weights [+ tile scheduler in
 // the leader], warp 1: MMA in the leader, warps 2-9: epilogue, warp 10:
-// token rows).  Only the leader (cluster rank 0) issues MMAs; both CTAs'
+// token rows).  The weight, MMA and token-row warps run their loops as whole
+// warps and issue the TMA copies and tcgen05 instructions from one elected
+// lane (the issue then keeps up with an MMA of N >= 128; from a loop that
+// one lane runs alone it did not).  Only the leader (cluster rank 0) issues
+// MMAs; both CTAs'
 // TMA loads complete on the leader's "full" barriers (.cta_group::2 TMA), the
 // leader's commits arrive on both CTAs' "empty" and "acc_full" barriers
 // (multicast), and the peer's roles arrive remotely on the leader's
