@@ -406,7 +406,7 @@ def _tensor_peak(peaks, clocks, fp8=False, slot="gate_up"):
     its in-band mean SM clock over the timed region (kernel cycles / kernel
     ns) times the per-clock rate.  Back-to-back V3 prefill steps reach the
     board's power cap within about 60 ms, after which the SM clock settles
-    near 1.3 GHz; the burst figure itself (a single 8192^3 product) implies
+    near 1.1-1.3 GHz; the burst figure itself (a single 8192^3 product) implies
     at least 1808.6 / 1.212 = 1492 MHz."""
     mult = 2.0 if fp8 else 1.0
     peak = mult * peaks["bf16_tflops"]
