@@ -716,7 +716,7 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
-# The five configurations of the layer's specification by their short names.
+# Short names of the five benchmark workloads (--config C3 is --workload v3_prefill).
 CONFIGS = {"C0": "tiny_fp32", "C1": "mini_bf16", "C2": "bias_dynamics", "C3": "v3_prefill",
            "C4": "v3_decode", "C4z": "v3_decode_zipf"}
 
