@@ -62,11 +62,12 @@ def kernels_per_step(wl, route_only, fp8=False):
 
 # DRAM traffic of expert GEMM 1 per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum).  Counters beyond the kernel time are captured on
-# the 32-expert V3-width prefill case (2.9 GB of weights, one kernel, two
-# launches) and scaled to a full launch by the ratio of the two cases'
-# algorithmic bytes (weights of the touched experts plus token rows, which
-# the traffic follows); keyed to the hash of the GEMM sources at capture time
-# and reported as null once those sources change.
+# the 32-expert V3-width cases (2.9 GB of weights, one kernel, two launches;
+# prefill: 256 tokens per expert, decode: 4) and scaled to a full launch of
+# the same regime by the ratio of the two cases' algorithmic bytes (weights
+# of the touched experts plus token rows, which the traffic follows); keyed
+# to the hash of the GEMM sources at capture time and reported as null once
+# those sources change.
 NCU_TRAFFIC = {
     # profiles/k_expert_tc2_v3_prefill_32experts_full.md ("DRAM counters of
     # the current sources"): GEMM 1 read + written bytes on that case
@@ -74,7 +75,20 @@ NCU_TRAFFIC = {
              "bytes": 2.176548352e9 + 0.033965824e9},
     ":fp8blk": {"sha": "dd10e8a46ce0f545", "case": "v3_prefill_32experts",
                 "bytes": 1.043218432e9 + 0.018627072e9},
+    # profiles/k_expert_tc_v3_decode_32experts_full.md: the one-SM kernel
+    "bf16:decode": {"sha": "dd10e8a46ce0f545", "case": "v3_decode_32experts",
+                    "bytes": 1.939902e9 + 0.003503104e9},
 }
+
+
+def _traffic_for(wl, load, fp8=False, fp8_blk=False):
+    """GEMM 1's DRAM bytes per launch of this workload, from the capture of
+    its regime (null if none matches the current sources)."""
+    regime = "" if wl.T * wl.k / wl.E >= 96 else ":decode"
+    cap = NCU_TRAFFIC.get((":fp8blk" if fp8_blk else ":fp8" if fp8 else "bf16") + regime)
+    if not cap or cap.get("sha") != _kernel_sha():
+        return None
+    return _scaled_traffic(cap, wl, load, fp8, fp8_blk)
 
 
 def _scaled_traffic(cap, wl, load, fp8, fp8_blk):
@@ -450,6 +464,7 @@ def _decode_line(M, I, MoeLayer, name, args, peaks, local):
            "layer_bytes_per_step": layer_bytes, "layer_gbs": layer_gbs,
            "frac": layer_gbs / peaks["hbm_gbs"],
            "gemm1_gbs": g1, "gemm1_frac": g1 / peaks["hbm_gbs"],
+           "gemm1_traffic": _traffic_for(wl, load), "gemm1_bytes": by1,
            "peak": peaks["hbm_gbs"], "peak_kind": f"{peaks['source']} HBM copy bandwidth",
            "phase_ms": {n: float(v) for n, v in zip(M.PHASES, phase_ms)},
            "gpu_launches": kernels_per_step(wl, False) * args.steps,
@@ -640,9 +655,7 @@ def run_ours(args, wl):
     g1_s, g2_s = phase_ms[2] / 1e3, phase_ms[3] / 1e3
     prefill_like = wl.T * wl.k / wl.E >= 96
     sha = _kernel_sha()
-    cap = NCU_TRAFFIC.get(":fp8blk" if fp8_blk else ":fp8" if fp8 else "bf16")  # GEMM 1
-    traffic = (_scaled_traffic(cap, wl, load, fp8, fp8_blk)
-               if cap and cap.get("sha") == sha and wl.T * wl.k / wl.E >= 96 else None)
+    traffic = _traffic_for(wl, load, fp8, fp8_blk)  # GEMM 1
     if prefill_like:
         ach = fl1 / g1_s / 1e12
         peak, kind, clk1 = _tensor_peak(peaks, clocks, fp8)
