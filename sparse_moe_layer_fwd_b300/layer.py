@@ -11,6 +11,22 @@ import torch
 from . import moe as M
 
 
+def _check(name, t, shape, dtype, device):
+    """Raise unless t is a contiguous tensor of exactly this shape and dtype
+    on this device: the library reads and writes exactly that many elements
+    from its data pointer, so anything else would be read past its end (or,
+    off the GPU, not be device memory at all)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    shape = tuple(int(n) for n in shape)
+    if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous {dtype} tensor of shape {shape}, got "
+                         f"{t.dtype} {tuple(t.shape)}"
+                         + ("" if t.is_contiguous() else " (not contiguous)"))
+    if t.device != device:
+        raise ValueError(f"{name}: expected a tensor on {device}, got one on {t.device}")
+
+
 class MoeLayer:
     def __init__(self, w_router, bias, w_gate, w_up, w_down, sh_gate, sh_up, sh_down, *,
                  T: int, k: int, dtype: str, flags: int = 0, host_io: bool = False):
@@ -18,6 +34,17 @@ class MoeLayer:
         self.h = w_gate.shape[1] if w_gate is not None else 128
         self.T, self.k, self.dtype, self.flags = T, k, dtype, flags
         dev = w_router.device
+        if dev.type != "cuda":
+            raise ValueError(f"w_router: expected a CUDA tensor, got one on {dev}")
+        E, d, h = self.E, self.d, self.h
+        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        _check("w_router", w_router, (E, d), torch.float32, dev)
+        _check("bias", bias, (E,), torch.float32, dev)
+        if w_gate is not None:
+            for name, t, shape in (("w_gate", w_gate, (E, h, d)), ("w_up", w_up, (E, h, d)),
+                                   ("w_down", w_down, (E, d, h)), ("sh_gate", sh_gate, (h, d)),
+                                   ("sh_up", sh_up, (h, d)), ("sh_down", sh_down, (d, h))):
+                _check(name, t, shape, tdt, dev)
         self.desc = M.make_desc(T, self.d, self.h, self.E, k, dtype, flags)
         self.w_router, self.bias = w_router, bias
         self._keep = (w_gate, w_up, w_down, sh_gate, sh_up, sh_down)
@@ -40,7 +67,7 @@ class MoeLayer:
                                        self.packed["sh_down"])
         self.experts = M.make_experts(w_gate, w_up, w_down) if have_w else None
         self.shared = M.make_experts(sh_gate, sh_up, sh_down) if have_w else None
-        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        self._tdt = tdt
         self.ws_bytes = M.moe_workspace_size(self.desc)
         if self.ws_bytes == 0:
             raise M.MoeError(M.ERR_CODE["MOE_ERR_SHAPE"], "moe_workspace_size")
@@ -114,6 +141,7 @@ class MoeLayer:
                    T=T, k=k, dtype=dtype, flags=flags, host_io=host_io)
 
     def forward(self, x, stream=None):
+        _check("x", x, (self.T, self.d), self._tdt, self.workspace.device)
         if stream is None:
             stream = torch.cuda.current_stream(x.device)
         M.moe_forward(self.desc, x, self.w_router, self.bias, self.experts, self.shared, self.y,
@@ -122,6 +150,9 @@ class MoeLayer:
         return self.y
 
     def forward_host_io(self, x_host, y_host, stream=None):
+        cpu = torch.device("cpu")
+        _check("x_host", x_host, (self.T, self.d), self._tdt, cpu)
+        _check("y_host", y_host, (self.T, self.d), self._tdt, cpu)
         if stream is None:
             stream = torch.cuda.current_stream(self.workspace.device)
         M.moe_forward_host_io(self.desc, x_host, self.w_router, self.bias, self.experts,
@@ -138,6 +169,8 @@ class MoeLayer:
         """Gradients for the output gradient dy, after forward(x) on this layer
         (built with MOE_TRAINING): dx, the expert and shared-expert weight
         gradients (fp32, or bf16 with MOE_GRAD_BF16) and the router's."""
+        _check("x", x, (self.T, self.d), self._tdt, self.workspace.device)
+        _check("dy", dy, (self.T, self.d), self._tdt, self.workspace.device)
         if stream is None:
             stream = torch.cuda.current_stream(self.workspace.device)
         wg, wu, wd, sg, su, sd = self._keep
