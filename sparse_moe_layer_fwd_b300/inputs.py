@@ -91,6 +91,11 @@ WORKLOADS = {
         # the decode regime (about 4 tokens per expert) on the same 32
         # experts' weights, for profiler captures of the decode GEMMs
         Workload("v3_decode_32experts", 16, 7168, 2048, 32, 8, "bf16", 4, bias="zero"),
+        # V3 prefill's token volume (8192 tokens, top-8, 940 MB of permuted
+        # rows, more than L2 holds) on 16 experts' weights (1.5 GB): the
+        # dispatch and combine at full size with a few GB on the device, for
+        # profiler captures of those kernels
+        Workload("v3_prefill_16experts", 8192, 7168, 2048, 16, 8, "bf16", 3, bias="uniform"),
     ]
 }
 
