@@ -83,10 +83,16 @@ NCU_TRAFFIC = {
 
 def _traffic_for(wl, load, fp8=False, fp8_blk=False):
     """GEMM 1's DRAM bytes per launch of this workload, from the capture of
-    its regime (null if none matches the current sources)."""
+    its regime: null if none matches the current sources, or if the
+    workload's tokens per expert are more than twice or less than half the
+    captured case's (the share of weight rows re-read from L2 would differ)."""
     regime = "" if wl.T * wl.k / wl.E >= 96 else ":decode"
     cap = NCU_TRAFFIC.get((":fp8blk" if fp8_blk else ":fp8" if fp8 else "bf16") + regime)
     if not cap or cap.get("sha") != _kernel_sha():
+        return None
+    small = I_WORKLOADS()[cap["case"]]
+    ratio = (wl.T * wl.k / wl.E) / (small.T * small.k / small.E)
+    if not 0.5 <= ratio <= 2.0:
         return None
     return _scaled_traffic(cap, wl, load, fp8, fp8_blk)
 

@@ -47,3 +47,9 @@ def test_stale_capture_reports_null(monkeypatch):
     # no capture of the per-row FP8 mode: null whatever the sources
     wl = I.WORKLOADS["v3_prefill"]
     assert bench._traffic_for(wl, _balanced(wl), fp8=True) is None
+
+
+def test_other_tokens_per_expert_reports_null():
+    # 4096 tokens per expert against the capture's 256: L2 reuse differs
+    wl = I.WORKLOADS["v3_prefill_16experts"]
+    assert bench._traffic_for(wl, _balanced(wl)) is None
